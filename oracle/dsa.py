@@ -1,0 +1,103 @@
+"""fp64 oracle of the DSA-style indexed sparse decode step.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Page [P4] "딥시크 희소 어텐션 DSA 원리: 라이트닝 인덱서와 상위 2048 토큰 선택 구조 해설",
+section "쉽게 이해하기" (easy explanation):
+  * the lightning indexer scores every past token with a weighted sum over a
+    few small heads of ReLU dot products, the keys being shared by all
+    indexer heads:  I[s] = sum_h w_h * max(0, qI_h . kI_s);
+  * the selector keeps the 2048 best positions and drops the rest
+    (reading: ties go to the lower position; the decision is taken in fp32,
+    the precision of the kernels);
+  * attention then runs at full precision over the selected tokens only,
+    with the softmax denominator summed over the selected set only
+    (scale 1/sqrt(dk));
+  * selection is made independently for each query position.
+Key-message list of the same page: 2048 tokens are 1.6% of a 128k context.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, Iterable, Optional
+
+import numpy as np
+import torch
+
+from .nsa import to_f64
+
+__all__ = ["dsa_indexer_scores", "topk_positions", "topk_alternatives",
+           "dsa_attention", "dsa_decode_reference"]
+
+
+def dsa_indexer_scores(qI: np.ndarray, wI: np.ndarray, kI: np.ndarray) -> np.ndarray:
+    """I[s] = sum_h w_h * ReLU(qI_h . kI_s) for every position s.
+
+    qI [HI, dI], wI [HI], kI [T, dI] -> I [T] (fp64).
+    """
+    relu = np.maximum(kI @ qI.T, 0.0)          # [T, HI]
+    return relu @ wI
+
+
+def topk_positions(I32: np.ndarray, k: int) -> np.ndarray:
+    """The k positions of largest fp32 score, ties to the lower position,
+    returned ascending.  k >= T keeps every position."""
+    T = I32.shape[0]
+    if k >= T:
+        return np.arange(T, dtype=np.int64)
+    pos = np.arange(T)
+    order = np.lexsort((pos, -I32.astype(np.float32)))
+    return np.sort(order[:k])
+
+
+def topk_alternatives(I32: np.ndarray, k: int, rel_tol: float):
+    """(gap_rel, definite, band, need) for one row, as in the NSA selector:
+    positions clearly above the cut must be kept, ``need`` more come from the
+    band of positions within ``rel_tol`` of the cut."""
+    T = I32.shape[0]
+    if k >= T:
+        return float("inf"), np.arange(T), np.zeros(0, dtype=np.int64), 0
+    s = I32.astype(np.float64)
+    order = np.lexsort((np.arange(T), -I32.astype(np.float32)))
+    last_in, first_out = s[order[k - 1]], s[order[k]]
+    cut = 0.5 * (last_in + first_out)
+    scale = max(abs(last_in), abs(first_out), 1e-30)
+    tol = rel_tol * scale
+    above = np.nonzero(s > cut + tol)[0]
+    band = np.nonzero(np.abs(s - cut) <= tol)[0]
+    return (last_in - first_out) / scale, above, band, k - above.size
+
+
+def dsa_attention(q: np.ndarray, Ksel: np.ndarray, Vsel: np.ndarray, scale: float) -> np.ndarray:
+    """Softmax attention of q [H, dk] over the selected keys only."""
+    logits = (q @ Ksel.T) * scale
+    logits = logits - logits.max(axis=-1, keepdims=True)
+    e = np.exp(logits)
+    return (e / e.sum(axis=-1, keepdims=True)) @ Vsel
+
+
+def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
+                         batches: Optional[Iterable[int]] = None) -> Dict[str, np.ndarray]:
+    """One DSA decode step for the batch rows ``batches`` (default all).
+
+    inp: bf16 tensors of ``workloads.make_dsa``.  Returns out [S,H,dv],
+    idx [S,min(k,T)] (ascending), I [S,T] fp64 and I32 [S,T] fp32 scores.
+    """
+    qI, wI, kI, q, k, v = (inp[n] for n in ("qI", "wI", "kI", "q", "k", "v"))
+    B, T, dk = k.shape
+    H, dv = q.shape[1], v.shape[2]
+    scale = 1.0 / math.sqrt(dk)
+    batches = list(range(B)) if batches is None else list(batches)
+    kk = min(topk, T)
+    res = dict(out=np.zeros((len(batches), H, dv)),
+               idx=np.zeros((len(batches), kk), dtype=np.int64),
+               I=np.zeros((len(batches), T)), I32=np.zeros((len(batches), T), dtype=np.float32))
+    for si, b in enumerate(batches):
+        I = dsa_indexer_scores(to_f64(qI[b]), to_f64(wI[b]), to_f64(kI[b]))
+        I32 = I.astype(np.float32)
+        sel = topk_positions(I32, topk)
+        ti = torch.as_tensor(sel)
+        res["out"][si] = dsa_attention(to_f64(q[b]), to_f64(k[b, ti]), to_f64(v[b, ti]), scale)
+        res["idx"][si], res["I"][si], res["I32"][si] = sel, I, I32
+    res["batches"] = np.array(batches)
+    return res

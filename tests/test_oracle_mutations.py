@@ -1,0 +1,73 @@
+"""The pins must catch plausible mistakes: each case plants one mistake in the
+oracle (on the CPU, through monkeypatching) and checks that a pin test fails."""
+import numpy as np
+import pytest
+
+from oracle import nsa as O
+from oracle import dsa as D
+import tests.test_oracle_pins as P
+
+
+def _fails(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_shifted_overlap_is_caught(monkeypatch):
+    real = O.overlap_matrix
+
+    def shifted(Nc, nb, l, d, lsel):       # block j fed by compressed blocks 4j-4..4j
+        Om = real(Nc + 3, nb, l, d, lsel)
+        return Om[3:]
+    monkeypatch.setattr(O, "overlap_matrix", shifted)
+    _fails(P.test_block_scores_one_hot_and_conservation)
+
+
+def test_partial_block_visibility_is_caught(monkeypatch):
+    def early(t, l, d, Nc):                # a block counted visible once it starts
+        t = np.asarray(t, dtype=np.int64)
+        return np.minimum(t // d + 1, Nc)
+    monkeypatch.setattr(O, "num_visible_compressed", early)
+    _fails(P.test_cmp_attention_causality_and_empty)
+
+
+def test_dropped_position_embedding_is_caught(monkeypatch):
+    real = O.compress
+    monkeypatch.setattr(O, "compress", lambda X, PE, W, l, d: real(X, 0 * PE, W, l, d))
+    _fails(P.test_compress_matches_torch_unfold_matmul)
+
+
+def test_reversed_tie_break_is_caught(monkeypatch):
+    def rev(S32, t, n, lsel):
+        jt = t // lsel
+        out = np.full(n, -1, dtype=np.int32)
+        if jt + 1 <= n:
+            out[: jt + 1] = np.arange(jt + 1)
+            return out
+        forced = np.array(sorted({0, jt, jt - 1}))
+        cand = np.setdiff1d(np.arange(jt + 1), forced)
+        order = np.lexsort((-cand, -S32[cand]))
+        out[:] = np.sort(np.concatenate([forced, cand[order[: n - forced.size]]]))
+        return out
+    monkeypatch.setattr(O, "select_blocks", rev)
+    _fails(P.test_select_blocks_brute_force, 1)
+
+
+def test_wrong_scale_is_caught(monkeypatch):
+    real = O._attend
+    monkeypatch.setattr(O, "_attend", lambda q, K, V, keys, scale: real(q, K, V, keys, 2 * scale))
+    _fails(P.test_selection_only_equals_full_attention_when_all_blocks_fit)
+
+
+def test_window_off_by_one_is_caught(monkeypatch):
+    real = O._attend
+
+    def win(q, t, K, V, w, scale):         # (t-w-1, t]: one token too many
+        return real(q, K, V, np.arange(max(0, t - w), t + 1), scale)
+    monkeypatch.setattr(O, "win_attention", win)
+    _fails(P.test_uniform_attention_gives_plain_means)
+
+
+def test_missing_relu_is_caught(monkeypatch):
+    monkeypatch.setattr(D, "dsa_indexer_scores", lambda qI, wI, kI: (kI @ qI.T) @ wI)
+    _fails(P.test_dsa_indexer_brute_force)
