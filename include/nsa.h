@@ -1,0 +1,196 @@
+/*
+ * nsa.h -- C ABI of libnsa.so: the forward hot path of Native Sparse Attention
+ * (NSA) and of a DSA-style indexed sparse decode on one NVIDIA B300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *  [P2] "AI 모델의 '긴 문장 처리' 한계 돌파, 딥시크의 새 어텐션 기술 화제", section II:
+ *       three parallel attention paths (compressed coarse tokens, selected fine
+ *       tokens, sliding window); l=32, d=16, l'=64, n=16 (1 initial + 2 local
+ *       blocks included), w=512.  Section III.3: a 64k decode step reads 5,632
+ *       tokens instead of 65,536.
+ *  [P3] deepdaiv newsletter no. 82, paragraphs on token compression, token
+ *       selection (block importance from the compressed tokens, blockwise
+ *       selection for contiguous memory access) and the sliding window.
+ *  [P4] "딥시크 희소 어텐션 DSA 원리: 라이트닝 인덱서와 상위 2048 토큰 선택 구조 해설",
+ *       "쉽게 이해하기": ReLU-weighted indexer with keys shared by its heads,
+ *       top-2048 selection, softmax over the selected set only.
+ *
+ * Conventions for every call
+ *  - All tensors are bf16, row-major, dense, in device memory of the current
+ *    CUDA device; base pointers must be 16-byte aligned.  Index outputs are
+ *    int32.  Query head h uses KV head floor(h / (H/G)).
+ *  - The caller owns every buffer and the stream.  The library never
+ *    allocates, frees or synchronises; scratch memory is the caller's
+ *    workspace ``ws`` of at least the size the matching *_workspace_size()
+ *    call returns (256-byte aligned).
+ *  - Calls are asynchronous on ``stream`` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream).  Host-side validation runs first: on any
+ *    invalid argument the call returns an error and launches nothing.
+ *  - Kernels never trap.  Every device-side wait is bounded; a wait that
+ *    runs out records NSA_ERR_DEVICE_TIMEOUT in the workspace status word,
+ *    which nsa_device_status() reads back.
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef NSA_H_
+#define NSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+enum nsa_status_code {
+  NSA_OK = 0,
+  NSA_ERR_INVALID_ARG = 1,     /* null pointer, non-positive size, bad enum  */
+  NSA_ERR_UNSUPPORTED = 2,     /* shape outside what the kernels implement   */
+  NSA_ERR_MISALIGNED = 3,      /* a pointer not 16-byte (ws: 256-byte) aligned */
+  NSA_ERR_WORKSPACE = 4,       /* ws_bytes smaller than the required size    */
+  NSA_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed          */
+  NSA_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait ran out         */
+  NSA_ERR_NO_DEVICE = 7        /* no usable sm_100-family device             */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nsa_status_string(int status);
+
+/* ABI version of this header (major*100 + minor). */
+int nsa_version(void);
+
+/* ---------------------------------------------------------------- NSA config */
+/* Flags for nsa_cfg.flags */
+#define NSA_FLAG_KC_GIVEN 1u   /* nsa_prefill_fwd: kc/vc already hold the compressed
+                                  cache; skip the compression step */
+
+typedef struct nsa_cfg {
+  int B;        /* sequences                                            */
+  int T;        /* tokens per sequence (decode: cache length; query at T-1) */
+  int H;        /* query heads                                          */
+  int G;        /* KV heads (GQA groups); H % G == 0                    */
+  int dk;       /* query/key head dim                                   */
+  int dv;       /* value head dim                                       */
+  int l;        /* compression block length        (pages: 32)          */
+  int d;        /* compression stride              (pages: 16)          */
+  int lsel;     /* selection block length l'       (pages: 64)          */
+  int n;        /* selected blocks per query       (pages: 16)          */
+  int w;        /* sliding-window length           (pages: 512)         */
+  float scale;  /* softmax scale of all three branches; <= 0 -> 1/sqrt(dk) */
+  unsigned flags;
+  /* compression map phi [P2 II.1, P3]: block i of one KV head is
+     flatten(X[d*i : d*i+l] + PE) @ W.  Device pointers, bf16:           */
+  const void* pe_k;  /* [l, dk]                                          */
+  const void* pe_v;  /* [l, dv]                                          */
+  const void* w_k;   /* [l*dk, dk]                                       */
+  const void* w_v;   /* [l*dv, dv]                                       */
+} nsa_cfg;
+
+/* Supported by this build: l=32, d=16, lsel=64, 3 <= n <= 32, 1 <= w,
+   dk and dv multiples of 64 with dk <= 256 and dv <= 256, H/G a power of two
+   between 1 and 128, T >= 1, B >= 1.  Anything else -> NSA_ERR_UNSUPPORTED. */
+
+/* Layout of the K/V tensors handed to nsa_compress_kv */
+#define NSA_LAYOUT_BTGD 0   /* [B, T, G, d]  (prefill inputs)        */
+#define NSA_LAYOUT_BGTD 1   /* [B, G, T, d]  (head-major decode cache) */
+
+/* Number of compressed blocks per KV head: floor((T-l)/d)+1, or 0 if T < l. */
+int nsa_num_compressed(const nsa_cfg* cfg);
+
+/* Workspace bytes needed by nsa_compress_kv / nsa_prefill_fwd /
+   nsa_decode_step for this cfg (0 on an invalid cfg). */
+size_t nsa_compress_workspace_size(const nsa_cfg* cfg);
+size_t nsa_prefill_workspace_size(const nsa_cfg* cfg);
+size_t nsa_decode_workspace_size(const nsa_cfg* cfg);
+
+/*
+ * nsa_compress_kv -- token compression [P2 II.1; P3, token compression]
+ *   kc[b,g,i,:] = bf16( flatten(k[b, d*i : d*i+l, g, :] + pe_k) @ w_k )
+ *   vc[b,g,i,:] = bf16( flatten(v[b, d*i : d*i+l, g, :] + pe_v) @ w_v )
+ * for i < Nc = nsa_num_compressed(cfg).  Accumulation is fp32; each output
+ * is rounded once to bf16.
+ *   k, v    : layout NSA_LAYOUT_BTGD ([B,T,G,dk] / [B,T,G,dv]) or
+ *             NSA_LAYOUT_BGTD ([B,G,T,dk] / [B,G,T,dv])
+ *   kc, vc  : out, [B, G, Nc, dk] / [B, G, Nc, dv]
+ *   phi parameters come from cfg (pe_k, pe_v, w_k, w_v).
+ */
+int nsa_compress_kv(const nsa_cfg* cfg, int layout, const void* k, const void* v,
+                    void* kc, void* vc, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * nsa_prefill_fwd -- NSA forward over whole sequences [P2 II; P3].
+ * For every sequence b, query position t and head h (group g):
+ *   compressed : softmax over the complete compressed blocks i (d*i+l-1 <= t)
+ *   scores     : S[t,g,j] = sum_{h in g} sum_i w(i,j) p_cmp[t,h,i], w = shared
+ *                d-chunks of compressed block i and selection block j
+ *   selection  : blocks 0, j_t, j_t-1 (j_t = t/lsel) plus the top n-3 other
+ *                causal blocks by S, ties to the lower index (all blocks if
+ *                j_t < n); attention over their tokens s <= t
+ *   window     : attention over s in (t-w, t]
+ *   out[b,t,h,:] = g_cmp*O_cmp + g_slc*O_slc + g_win*O_win
+ *   q     : [B,T,H,dk]     k : [B,T,G,dk]     v : [B,T,G,dv]
+ *   gates : [B,T,H,3] (cmp, slc, win)
+ *   kc,vc : [B,G,Nc,dk] / [B,G,Nc,dv]; written by this call (compression
+ *           step) unless cfg->flags has NSA_FLAG_KC_GIVEN, then read only
+ *   out   : [B,T,H,dv]
+ *   idx_out (nullable): [B,T,G,n] int32, the kept blocks ascending, -1 padded
+ */
+int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v,
+                    const void* gates, void* kc, void* vc, void* out, int32_t* idx_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * nsa_decode_step -- one new token per sequence [P2 II, III.3]: row t = T-1
+ * of the prefill definition, read from the caches (the cache already holds
+ * the new token).  Per KV head it reads the Nc compressed entries, the n
+ * selected blocks and the w-token window.
+ *   q      : [B,H,dk]        gates : [B,H,3]
+ *   kcache : [B,G,T,dk]      vcache : [B,G,T,dv]   (head-major)
+ *   kc, vc : [B,G,Nc,dk] / [B,G,Nc,dv] compressed caches (nsa_compress_kv
+ *            with NSA_LAYOUT_BGTD)
+ *   out    : [B,H,dv]
+ *   idx_out (nullable): [B,G,n] int32
+ */
+int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const void* vcache,
+                    const void* kc, const void* vc, const void* gates, void* out,
+                    int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- DSA */
+typedef struct dsa_cfg {
+  int B;       /* batch rows (one query token each, at position T-1)  */
+  int T;       /* context length                                      */
+  int HI;      /* indexer heads                                       */
+  int dI;      /* indexer head dim                                    */
+  int H;       /* attention query heads (one shared KV)               */
+  int dk;      /* key dim                                             */
+  int dv;      /* value dim                                           */
+  int topk;    /* positions kept per query (pages: 2048)              */
+  float scale; /* <= 0 -> 1/sqrt(dk)                                  */
+} dsa_cfg;
+/* Supported: HI <= 16, dI a multiple of 8 up to 256, dk and dv multiples of 8
+   up to 1024, 1 <= topk, H <= 32. */
+
+size_t dsa_decode_workspace_size(const dsa_cfg* cfg);
+
+/*
+ * dsa_decode_step -- indexed sparse decode [P4, "쉽게 이해하기"]:
+ *   I[b,s]   = sum_h wI[b,h] * max(0, qI[b,h,:] . kI[b,s,:])    for s < T
+ *   keep     = the min(topk,T) positions of largest fp32 I, ties to the lower s
+ *   out[b,h] = softmax_{s in keep}(q[b,h,:] . k[b,s,:] * scale) @ v[b,keep,:]
+ *   qI [B,HI,dI]   wI [B,HI]   kI [B,T,dI]   q [B,H,dk]   k [B,T,dk]
+ *   v [B,T,dv]     out [B,H,dv]
+ *   idx_out (nullable): [B, min(topk,T)] int32, ascending
+ */
+int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI,
+                    const void* q, const void* k, const void* v, void* out, int32_t* idx_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- status word */
+/* Synchronises ``stream``, returns the status word the kernels of the last
+   call on ``ws`` recorded (NSA_OK if none) and clears it. */
+int nsa_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NSA_H_ */

@@ -86,19 +86,22 @@ def num_visible_compressed(t, l: int, d: int, Nc: int):
     return np.minimum(n, Nc)
 
 
-def compress(X: np.ndarray, PE: np.ndarray, W: np.ndarray, l: int, d: int) -> np.ndarray:
+def compress(X: np.ndarray, PE: np.ndarray, W: np.ndarray, l: int, d: int,
+             round_bf16: bool = True) -> np.ndarray:
     """Token compression [P2 II.1, P3].
 
     X [T, dX] keys (or values) of one KV head, PE [l, dX] intra-block position
     embedding, W [l*dX, dout].  Block i = flatten(X[d*i : d*i+l] + PE) @ W,
-    rounded once to bf16 (the compressed cache is stored in bf16).
+    rounded once to bf16 (the compressed cache is stored in bf16);
+    ``round_bf16=False`` returns the exact fp64 value before that rounding.
     """
     T, dX = X.shape
     Nc = num_compressed(T, l, d)
     if Nc == 0:
         return np.zeros((0, W.shape[1]))
     flat = np.stack([(X[d * i: d * i + l] + PE).reshape(l * dX) for i in range(Nc)])
-    return bf16_round(flat @ W)
+    exact = flat @ W
+    return bf16_round(exact) if round_bf16 else exact
 
 
 def _softmax_masked(logits: np.ndarray, valid: np.ndarray) -> np.ndarray:

@@ -1,0 +1,194 @@
+"""Python binding of libnsa.so (include/nsa.h): argument marshalling only.
+
+Every step of the NSA / DSA hot path runs in the library's CUDA kernels.  The
+functions here take torch tensors (device memory, owned by the caller), pass
+their raw pointers and the current CUDA stream through ctypes, and raise
+``NsaError`` on a non-zero status.  There is no CPU fallback: importing this
+package fails loudly if libnsa.so has not been built
+(``python -m sparse_attention_long_10_b300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "NsaError", "NsaCfg", "DsaCfg", "LIB_PATH", "lib", "make_cfg", "make_dsa_cfg",
+    "NSA_LAYOUT_BTGD", "NSA_LAYOUT_BGTD", "NSA_FLAG_KC_GIVEN",
+    "nsa_status_string", "nsa_version", "nsa_num_compressed",
+    "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
+    "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_prefill_fwd", "nsa_decode_step",
+    "dsa_decode_step", "nsa_device_status", "workspace",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnsa.so")
+
+NSA_LAYOUT_BTGD = 0
+NSA_LAYOUT_BGTD = 1
+NSA_FLAG_KC_GIVEN = 1
+
+_c_int, _c_float, _c_uint, _c_vp, _c_size = (ctypes.c_int, ctypes.c_float, ctypes.c_uint,
+                                             ctypes.c_void_p, ctypes.c_size_t)
+
+
+class NsaCfg(ctypes.Structure):
+    """Mirror of ``nsa_cfg`` (include/nsa.h)."""
+    _fields_ = [("B", _c_int), ("T", _c_int), ("H", _c_int), ("G", _c_int), ("dk", _c_int),
+                ("dv", _c_int), ("l", _c_int), ("d", _c_int), ("lsel", _c_int), ("n", _c_int),
+                ("w", _c_int), ("scale", _c_float), ("flags", _c_uint), ("pe_k", _c_vp),
+                ("pe_v", _c_vp), ("w_k", _c_vp), ("w_v", _c_vp)]
+
+
+class DsaCfg(ctypes.Structure):
+    """Mirror of ``dsa_cfg`` (include/nsa.h)."""
+    _fields_ = [("B", _c_int), ("T", _c_int), ("HI", _c_int), ("dI", _c_int), ("H", _c_int),
+                ("dk", _c_int), ("dv", _c_int), ("topk", _c_int), ("scale", _c_float)]
+
+
+class NsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {nsa_status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libnsa.so is not built ({LIB_PATH}); run "
+                          "`python -m sparse_attention_long_10_b300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER
+    sig = {
+        "nsa_status_string": (ctypes.c_char_p, [_c_int]),
+        "nsa_version": (_c_int, []),
+        "nsa_num_compressed": (_c_int, [P(NsaCfg)]),
+        "nsa_compress_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_prefill_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_decode_workspace_size": (_c_size, [P(NsaCfg)]),
+        "dsa_decode_workspace_size": (_c_size, [P(DsaCfg)]),
+        "nsa_compress_kv": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_size,
+                                     _c_vp]),
+        "nsa_prefill_fwd": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     _c_vp, _c_vp, _c_size, _c_vp]),
+        "nsa_decode_step": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     _c_vp, _c_vp, _c_size, _c_vp]),
+        "dsa_decode_step": (_c_int, [P(DsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     _c_vp, _c_vp, _c_size, _c_vp]),
+        "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name, None)
+        if f is None:
+            continue
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------ helpers
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libnsa must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise NsaError(rc, where)
+
+
+def make_cfg(B, T, H, G, dk, dv, phi=None, l=32, d=16, lsel=64, n=16, w=512, scale=0.0,
+             flags=0) -> NsaCfg:
+    """Build an ``nsa_cfg``.  ``phi`` = dict(pe_k, pe_v, w_k, w_v) of device tensors."""
+    c = NsaCfg(B, T, H, G, dk, dv, l, d, lsel, n, w, float(scale), flags, None, None, None, None)
+    if phi is not None:
+        c.pe_k, c.pe_v = _ptr(phi["pe_k"]), _ptr(phi["pe_v"])
+        c.w_k, c.w_v = _ptr(phi["w_k"]), _ptr(phi["w_v"])
+    return c
+
+
+def make_dsa_cfg(B, T, HI, dI, H, dk, dv, topk, scale=0.0) -> DsaCfg:
+    return DsaCfg(B, T, HI, dI, H, dk, dv, topk, float(scale))
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Caller-owned workspace (uint8, 256-byte aligned by the caching allocator)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ ABI wrappers
+def nsa_status_string(code: int) -> str:
+    return lib.nsa_status_string(code).decode()
+
+
+def nsa_version() -> int:
+    return lib.nsa_version()
+
+
+def nsa_num_compressed(cfg: NsaCfg) -> int:
+    return lib.nsa_num_compressed(ctypes.byref(cfg))
+
+
+def nsa_compress_workspace_size(cfg: NsaCfg) -> int:
+    return lib.nsa_compress_workspace_size(ctypes.byref(cfg))
+
+
+def nsa_prefill_workspace_size(cfg: NsaCfg) -> int:
+    return lib.nsa_prefill_workspace_size(ctypes.byref(cfg))
+
+
+def nsa_decode_workspace_size(cfg: NsaCfg) -> int:
+    return lib.nsa_decode_workspace_size(ctypes.byref(cfg))
+
+
+def dsa_decode_workspace_size(cfg: DsaCfg) -> int:
+    return lib.dsa_decode_workspace_size(ctypes.byref(cfg))
+
+
+def nsa_compress_kv(cfg: NsaCfg, layout: int, k, v, kc, vc, ws, stream=None):
+    _check(lib.nsa_compress_kv(ctypes.byref(cfg), layout, _ptr(k), _ptr(v), _ptr(kc), _ptr(vc),
+                               _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+           "nsa_compress_kv")
+
+
+def nsa_prefill_fwd(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, ws, stream=None):
+    _check(lib.nsa_prefill_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates),
+                               _ptr(kc), _ptr(vc), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               ws.numel() if ws is not None else 0, _stream(stream)),
+           "nsa_prefill_fwd")
+
+
+def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None):
+    _check(lib.nsa_decode_step(ctypes.byref(cfg), _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kc),
+                               _ptr(vc), _ptr(gates), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               ws.numel() if ws is not None else 0, _stream(stream)),
+           "nsa_decode_step")
+
+
+def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=None):
+    _check(lib.dsa_decode_step(ctypes.byref(cfg), _ptr(qI), _ptr(wI), _ptr(kI), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               ws.numel() if ws is not None else 0, _stream(stream)),
+           "dsa_decode_step")
+
+
+def nsa_device_status(ws, stream=None) -> int:
+    return lib.nsa_device_status(_ptr(ws), _stream(stream))

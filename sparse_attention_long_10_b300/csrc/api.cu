@@ -1,0 +1,207 @@
+// api.cu -- the extern "C" surface of libnsa.so (declared in include/nsa.h):
+// argument validation, workspace carving, launch sequencing.  No allocation,
+// no synchronisation except in nsa_device_status().
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.hpp"
+#include "nsa.h"
+
+using namespace nsa;
+
+namespace {
+
+constexpr size_t kHeader = sizeof(DeviceStatus);
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Device check, cached per device id: needs an sm_100-family GPU (tcgen05).
+int check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NSA_ERR_NO_DEVICE;
+  static int cached[64];  // 0 unknown, 1 ok, 2 bad
+  if (dev < 0 || dev >= 64) return NSA_ERR_NO_DEVICE;
+  if (cached[dev] == 0) {
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return NSA_ERR_NO_DEVICE;
+    cached[dev] = (major == 10) ? 1 : 2;
+  }
+  return cached[dev] == 1 ? NSA_OK : NSA_ERR_NO_DEVICE;
+}
+
+int validate_cfg(const nsa_cfg* c) {
+  if (c == nullptr) return NSA_ERR_INVALID_ARG;
+  if (c->B < 1 || c->T < 1 || c->H < 1 || c->G < 1 || c->dk < 1 || c->dv < 1) return NSA_ERR_INVALID_ARG;
+  if (c->l < 1 || c->d < 1 || c->lsel < 1 || c->n < 1 || c->w < 1) return NSA_ERR_INVALID_ARG;
+  if (c->H % c->G != 0) return NSA_ERR_INVALID_ARG;
+  const int hpg = c->H / c->G;
+  if (!is_pow2(hpg) || hpg > 128) return NSA_ERR_UNSUPPORTED;
+  if (c->l != 32 || c->d != 16 || c->lsel != 64) return NSA_ERR_UNSUPPORTED;
+  if (c->n < 3 || c->n > 32) return NSA_ERR_UNSUPPORTED;
+  if (c->dk % 64 != 0 || c->dv % 64 != 0 || c->dk > 256 || c->dv > 256) return NSA_ERR_UNSUPPORTED;
+  if ((long long)c->T > (1ll << 24) || (long long)c->B * c->T > (1ll << 26)) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
+int validate_phi(const nsa_cfg* c) {
+  const void* p[4] = {c->pe_k, c->pe_v, c->w_k, c->w_v};
+  for (const void* x : p) {
+    if (x == nullptr) return NSA_ERR_INVALID_ARG;
+    if (!aligned16(x)) return NSA_ERR_MISALIGNED;
+  }
+  return NSA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* x : ps) {
+    if (x == nullptr) return NSA_ERR_INVALID_ARG;
+    if (!aligned16(x)) return NSA_ERR_MISALIGNED;
+  }
+  return NSA_OK;
+}
+
+int num_compressed(const nsa_cfg& c) { return c.T < c.l ? 0 : (c.T - c.l) / c.d + 1; }
+
+// ---- workspace layout -------------------------------------------------------
+struct CompressWs {
+  size_t bias_k, bias_v, end;
+};
+CompressWs compress_ws(const nsa_cfg& c) {
+  CompressWs w;
+  w.bias_k = kHeader;
+  w.bias_v = align_up(w.bias_k + sizeof(float) * c.dk, 256);
+  w.end = align_up(w.bias_v + sizeof(float) * c.dv, 256);
+  return w;
+}
+
+struct PrefillWs {
+  CompressWs cw;
+  size_t part, idx, end;
+};
+PrefillWs prefill_ws(const nsa_cfg& c) {
+  PrefillWs w;
+  w.cw = compress_ws(c);
+  w.part = w.cw.end;
+  w.idx = align_up(w.part + sizeof(uint16_t) * (size_t)c.B * c.T * c.H * c.dv, 256);
+  w.end = align_up(w.idx + sizeof(int32_t) * (size_t)c.B * c.T * c.G * c.n, 256);
+  return w;
+}
+
+// shapes the prefill kernels implement (beyond validate_cfg)
+int prefill_supported(const nsa_cfg& c) {
+  const int hpg = c.H / c.G;
+  if (hpg > 16 || c.n > 16 || (c.dv != 64 && c.dv != 128) || c.T > 65536) return NSA_ERR_UNSUPPORTED;
+  if (cmp_win_smem_bytes(c) > smem_max() || sel_smem_bytes(c) > smem_max()) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr) return NSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NSA_ERR_MISALIGNED;
+  if (ws_bytes < need) return NSA_ERR_WORKSPACE;
+  return NSA_OK;
+}
+
+int run_compress(const nsa_cfg& c, int layout, const void* k, const void* v, void* kc, void* vc, uint8_t* ws,
+                 cudaStream_t s) {
+  const CompressWs w = compress_ws(c);
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(ws);
+  int rc = launch_compress_one(c, layout, k, c.dk, c.pe_k, c.w_k, kc, reinterpret_cast<float*>(ws + w.bias_k), st, s);
+  if (rc != NSA_OK) return rc;
+  return launch_compress_one(c, layout, v, c.dv, c.pe_v, c.w_v, vc, reinterpret_cast<float*>(ws + w.bias_v), st, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nsa_status_string(int status) {
+  switch (status) {
+    case NSA_OK: return "NSA_OK";
+    case NSA_ERR_INVALID_ARG: return "NSA_ERR_INVALID_ARG";
+    case NSA_ERR_UNSUPPORTED: return "NSA_ERR_UNSUPPORTED";
+    case NSA_ERR_MISALIGNED: return "NSA_ERR_MISALIGNED";
+    case NSA_ERR_WORKSPACE: return "NSA_ERR_WORKSPACE";
+    case NSA_ERR_CUDA: return "NSA_ERR_CUDA";
+    case NSA_ERR_DEVICE_TIMEOUT: return "NSA_ERR_DEVICE_TIMEOUT";
+    case NSA_ERR_NO_DEVICE: return "NSA_ERR_NO_DEVICE";
+    default: return "NSA_ERR_UNKNOWN";
+  }
+}
+
+int nsa_version(void) { return 100; }
+
+int nsa_num_compressed(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK) return -1;
+  return num_compressed(*cfg);
+}
+
+size_t nsa_compress_workspace_size(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK) return 0;
+  return compress_ws(*cfg).end;
+}
+
+int nsa_compress_kv(const nsa_cfg* cfg, int layout, const void* k, const void* v, void* kc, void* vc, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  if (layout != NSA_LAYOUT_BTGD && layout != NSA_LAYOUT_BGTD) return NSA_ERR_INVALID_ARG;
+  if ((rc = validate_phi(cfg)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({k, v})) != NSA_OK) return rc;
+  if (num_compressed(*cfg) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  if ((rc = check_ws(ws, ws_bytes, compress_ws(*cfg).end)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (num_compressed(*cfg) == 0) return NSA_OK;
+  return run_compress(*cfg, layout, k, v, kc, vc, static_cast<uint8_t*>(ws), s);
+}
+
+size_t nsa_prefill_workspace_size(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK) return 0;
+  return prefill_ws(*cfg).end;
+}
+
+int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, const void* gates, void* kc,
+                    void* vc, void* out, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  const nsa_cfg& c = *cfg;
+  if ((rc = prefill_supported(c)) != NSA_OK) return rc;
+  const bool given = (c.flags & NSA_FLAG_KC_GIVEN) != 0;
+  const int Nc = num_compressed(c);
+  if (!given && (rc = validate_phi(cfg)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, k, v, gates, out})) != NSA_OK) return rc;
+  if (Nc > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  const PrefillWs w = prefill_ws(c);
+  if ((rc = check_ws(ws, ws_bytes, w.end)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(wsb);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (!given && Nc > 0 && (rc = run_compress(c, NSA_LAYOUT_BTGD, k, v, kc, vc, wsb, s)) != NSA_OK) return rc;
+  void* part = wsb + w.part;
+  int32_t* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int32_t*>(wsb + w.idx);
+  if ((rc = launch_cmp_win(c, q, k, v, kc, vc, gates, part, idx, st, s)) != NSA_OK) return rc;
+  return launch_sel(c, q, k, v, gates, idx, part, out, st, s);
+}
+
+int nsa_device_status(void* ws, void* stream) {
+  if (ws == nullptr) return NSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DeviceStatus h;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(h), s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
+  return h.code;
+}
+
+}  // extern "C"

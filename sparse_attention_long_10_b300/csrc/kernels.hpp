@@ -1,0 +1,38 @@
+// kernels.hpp -- host-side launchers of the NSA / DSA kernels (internal to
+// libnsa.so; the public surface is include/nsa.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "nsa.h"
+
+namespace nsa {
+
+struct DeviceStatus;
+
+// Largest dynamic shared memory any kernel of the library asks for (bytes).
+constexpr size_t smem_max() { return 232448; }  // 227 KB
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- compression (compress.cu)
+size_t compress_smem_bytes(int N);
+// One of K or V: X in ``layout``, dX = head dim = output dim.
+int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, const void* pe, const void* W,
+                        void* out, float* bias_ws, DeviceStatus* st, cudaStream_t stream);
+
+// ---- prefill (prefill_cmp_win.cu, prefill_sel.cu)
+size_t cmp_win_smem_bytes(const nsa_cfg& c);
+size_t sel_smem_bytes(const nsa_cfg& c);
+// compressed attention + block scores + top-n + window; writes
+// part = g_cmp*O_cmp + g_win*O_win (bf16 [B,T,H,dv]) and idx [B,T,G,n]
+int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s);
+// selected attention; out = part + g_slc*O_slc
+int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
+               const void* part, void* out, DeviceStatus* st, cudaStream_t s);
+
+}  // namespace nsa

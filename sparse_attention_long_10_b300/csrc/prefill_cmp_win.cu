@@ -1,0 +1,667 @@
+// prefill_cmp_win.cu -- NSA prefill, per (sequence, KV group, tile of queries):
+//   1. compressed attention [P2 II.1; P3 token compression], two passes over
+//      the compressed keys: pass 1 finds each row's softmax max and sum, pass 2
+//      recomputes the scores, forms the exactly normalised probabilities p,
+//      accumulates O_cmp and the block importance scores
+//          S[t,j] = sum_{h in group} sum_i w(i,j) p[t,h,i]
+//      (w = d-token chunks shared by compressed block i and selection block j);
+//   2. top-n block selection [P2 II: n blocks incl. block 0 and the 2 local
+//      blocks; P3 token selection], ties to the lower block index;
+//   3. sliding-window attention over (t-w, t] [P2 II.3; P3], again two
+//      passes so the probabilities are exactly normalised.
+// The gates are folded into the probabilities (P' = g * p), so one TMEM
+// accumulator holds g_cmp*O_cmp + g_win*O_win; that partial sum is written in
+// bf16 and the selected-attention kernel adds g_slc*O_slc to it.
+//
+// Rows of the MMA are (query, head) pairs of ONE GQA group: 128/HPG queries x
+// HPG heads share every K/V tile (group-centric loading).  Warp roles:
+//   warps 0-3  softmax / scores / top-k (thread = one row = one TMEM lane)
+//   warp  4    TMA producer (Q once, then a ring of 16 KB K/V chunks)
+//   warp  5    tcgen05 MMA issuer (single thread)
+// TMEM: S double buffer (2 x 128 columns) + O (dv columns).
+#include "common.cuh"
+#include "kernels.hpp"
+#include "tmap.hpp"
+
+namespace nsa {
+
+namespace {
+
+constexpr int kRing = 6;
+constexpr int kSlot = 16384;   // 128 rows x 128 bytes
+constexpr int kThreads = 192;
+constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
+
+struct CmpWinArgs {
+  int T, H, G, dk, dv, n, w, Nc, QT, nbs;
+  float sc2;                       // softmax scale * log2(e)
+  const __nv_bfloat16* gates;      // [B,T,H,3]
+  __nv_bfloat16* part;             // [B,T,H,dv]
+  int32_t* idx;                    // [B,T,G,n]
+  DeviceStatus* st;
+  uint32_t off_ring, off_p, off_scores, off_bar;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t ring_full[kRing];
+  uint64_t ring_empty[kRing];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t p_free;
+  uint64_t o_full;
+  uint64_t wg;          // softmax-warpgroup rendezvous (count 4)
+  uint32_t tmem;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ int visible_cmp(int t, int Nc) {
+  // compressed block i is visible once its last token 16*i+31 <= t
+  if (t < 31) return 0;
+  const int nv = (t - 31) / 16 + 1;
+  return nv < Nc ? nv : Nc;
+}
+
+// Butterfly reduce-scatter of 32 values over groups of HPG lanes (HPG <= 32):
+// afterwards lane holds 32/HPG group sums in v[0..], original indices base+k.
+template <int HPG>
+__device__ __forceinline__ int reduce_scatter32(float (&v)[33], int lane) {
+  int base = 0;
+#pragma unroll
+  for (int m = HPG / 2, n = 16; m >= 1; m >>= 1, n >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      const float send = up ? v[k] : v[k + n];
+      const float keep = up ? v[k + n] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+    if (up) base += n;
+  }
+  return base;
+}
+
+template <int HPG>
+__device__ __forceinline__ float allreduce_group(float x) {
+#pragma unroll
+  for (int m = HPG / 2; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+
+// Write one row's 128 bf16 probabilities into the 128B-swizzled K-major P tile.
+__device__ __forceinline__ void store_p_row(uint8_t* ps, int r, const float (&p)[kTile], float gate) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+      const int i = q * 64 + cc * 8;
+      uint4 pk;
+      pk.x = pack_bf16x2(p[i + 0] * gate, p[i + 1] * gate);
+      pk.y = pack_bf16x2(p[i + 2] * gate, p[i + 3] * gate);
+      pk.z = pack_bf16x2(p[i + 4] * gate, p[i + 5] * gate);
+      pk.w = pack_bf16x2(p[i + 6] * gate, p[i + 7] * gate);
+      *reinterpret_cast<uint4*>(ps + q * kSlot + sw128_offset(r, cc)) = pk;
+    }
+  }
+}
+
+template <int HPG>
+__global__ void __launch_bounds__(kThreads, 1)
+    cmp_win_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapKc,
+                   const __grid_constant__ CUtensorMap mapVc, const __grid_constant__ CUtensorMap mapK,
+                   const __grid_constant__ CUtensorMap mapV, const CmpWinArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* qs = smem;
+  uint8_t* ring = smem + a.off_ring;
+  uint8_t* ps = smem + a.off_p;
+  float* scores = reinterpret_cast<float*>(smem + a.off_scores);
+  Bars* bars = reinterpret_cast<Bars*>(smem + a.off_bar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int QT = a.QT;
+  const int t0 = blockIdx.x * QT;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int kcs = a.dk / 64;   // 64-column chunks of a key row
+  const int vcs = a.dv / 64;
+
+  // per-CTA schedule (identical in every role)
+  const int t_last = min(t0 + QT - 1, a.T - 1);
+  const int nmax = visible_cmp(t_last, a.Nc);
+  const int ntc = (nmax + kTile - 1) / kTile;
+  const int s_lo = max(0, t0 - a.w + 1);
+  const int ntw = (t_last - s_lo) / kTile + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&bars->ring_full[s], 1);
+      mbar_init(&bars->ring_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 4);
+    }
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->wg, 4);
+    bars->abort_flag = prior_error(a.st);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tmem_s = tmem;          // S buffers at columns 0 and 128
+  const uint32_t tmem_o = tmem + 256;    // O at columns 256 .. 256+dv
+
+  if (*abort_flag) {
+    // an earlier CTA failed: do nothing
+  } else if (warp == 4) {
+    // =============================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapKc);
+      tma_prefetch_desc(&mapVc);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * kSlot));
+      for (int c = 0; c < kcs; ++c) tma_load_4d(qs + c * kSlot, &mapQ, &bars->q_full, c * 64, g * HPG, t0, b);
+      int v = 0;
+      bool ok = true;
+      auto push = [&](const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+        if (!ok) return;
+        const int slot = v % kRing;
+        const uint32_t round = (uint32_t)(v / kRing);
+        if (!mbar_wait(&bars->ring_empty[slot], (round & 1) ^ 1, abort_flag, a.st, 201)) {
+          ok = false;
+          return;
+        }
+        mbar_arrive_expect_tx(&bars->ring_full[slot], kSlot);
+        tma_load_4d(ring + slot * kSlot, map, &bars->ring_full[slot], c0, c1, c2, c3);
+        ++v;
+      };
+      auto push_kc = [&](int j) { for (int c = 0; c < kcs; ++c) push(&mapKc, c * 64, j * kTile, g, b); };
+      auto push_vc = [&](int j) { for (int c = 0; c < vcs; ++c) push(&mapVc, c * 64, j * kTile, g, b); };
+      auto push_k = [&](int j) { for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b); };
+      auto push_v = [&](int j) { for (int c = 0; c < vcs; ++c) push(&mapV, c * 64, g, s_lo + j * kTile, b); };
+      // phase 1: compressed keys; phase 2: compressed keys + values
+      for (int j = 0; j < ntc; ++j) push_kc(j);
+      if (ntc > 0) {
+        push_kc(0);
+        for (int j = 0; j < ntc; ++j) {
+          if (j + 1 < ntc) push_kc(j + 1);
+          push_vc(j);
+        }
+      }
+      // phase 3: window keys; phase 4: window keys + values
+      for (int j = 0; j < ntw; ++j) push_k(j);
+      push_k(0);
+      for (int j = 0; j < ntw; ++j) {
+        if (j + 1 < ntw) push_k(j + 1);
+        push_v(j);
+      }
+      if (!ok || *abort_flag) {
+        mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
+        for (int x = (v > kRing ? v - kRing : 0); x < v; ++x)
+          mbar_wait_plain(&bars->ring_full[x % kRing], (uint32_t)((x / kRing) & 1), kWaitLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    // =============================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 64, false, true);
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 211);
+      int u = 0, v = 0, pv = 0;
+      bool first_pv = true;
+      const uint32_t qs_a = smem_u32(qs);
+      const uint32_t ring_a = smem_u32(ring);
+      const uint32_t ps_a = smem_u32(ps);
+      auto take_slot = [&](uint32_t& addr) -> bool {
+        const int slot = v % kRing;
+        const uint32_t round = (uint32_t)(v / kRing);
+        if (!mbar_wait(&bars->ring_full[slot], round & 1, abort_flag, a.st, 212)) return false;
+        tc_fence_after();
+        addr = ring_a + slot * kSlot;
+        return true;
+      };
+      auto release_slot = [&]() {
+        umma_commit(&bars->ring_empty[v % kRing]);
+        ++v;
+      };
+      auto issue_qk = [&]() {
+        if (!ok) return;
+        const int sb = u & 1;
+        const uint32_t use = (uint32_t)(u >> 1);
+        if (!mbar_wait(&bars->s_free[sb], (use & 1) ^ 1, abort_flag, a.st, 213)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        for (int c = 0; c < kcs; ++c) {
+          uint32_t kaddr;
+          if (!take_slot(kaddr)) {
+            ok = false;
+            return;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_sw128(qs_a + c * kSlot + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(kaddr + k * 32, 16, 1024);
+            umma_bf16(tmem_s + sb * kTile, ad, bd, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+          }
+          release_slot();
+        }
+        umma_commit(&bars->s_full[sb]);
+        ++u;
+      };
+      auto issue_pv = [&]() {
+        if (!ok) return;
+        if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214)) {
+          ok = false;
+          return;
+        }
+        tc_fence_after();
+        for (int c = 0; c < vcs; ++c) {
+          uint32_t vaddr;
+          if (!take_slot(vaddr)) {
+            ok = false;
+            return;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t ad = sdesc_sw128(ps_a + (k >> 2) * kSlot + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(vaddr + k * 2048, kSlot, 1024);
+            umma_bf16(tmem_o + c * 64, ad, bd, idesc_pv, (first_pv && k == 0) ? 0u : 1u);
+          }
+          release_slot();
+        }
+        first_pv = false;
+        umma_commit(&bars->p_free);
+        ++pv;
+      };
+      for (int j = 0; j < ntc; ++j) issue_qk();
+      if (ntc > 0) {
+        issue_qk();
+        for (int j = 0; j < ntc; ++j) {
+          if (j + 1 < ntc) issue_qk();
+          issue_pv();
+        }
+      }
+      for (int j = 0; j < ntw; ++j) issue_qk();
+      issue_qk();
+      for (int j = 0; j < ntw; ++j) {
+        if (j + 1 < ntw) issue_qk();
+        issue_pv();
+      }
+      umma_commit(&bars->o_full);
+      if (!ok || *abort_flag) mbar_wait_plain(&bars->o_full, 0, kWaitLimitNs);
+    }
+  } else {
+    // =============================================================== softmax warpgroup
+    const int r = threadIdx.x;               // row = TMEM lane
+    const int qi = r / HPG;
+    const int h = r % HPG;
+    const int t = t0 + qi;
+    const bool row_ok = t < a.T;
+    const int head = g * HPG + h;
+    const int n_t = row_ok ? visible_cmp(t, a.Nc) : 0;
+    float g_c = 0.f, g_w = 0.f;
+    if (row_ok) {
+      const __nv_bfloat16* gp = a.gates + (((size_t)b * a.T + t) * a.H + head) * 3;
+      g_c = __bfloat162float(gp[0]);
+      g_w = __bfloat162float(gp[2]);
+    }
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    int u = 0, pv = 0;
+    uint32_t wg_phase = 0;
+
+    auto wg_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->wg);
+      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 221)) ok = false;
+      ++wg_phase;
+    };
+    // loads the next S tile (128 fp32 per row) and releases its TMEM buffer
+    auto consume_s = [&](float (&x)[kTile]) -> bool {
+      const int sb = u & 1;
+      const uint32_t use = (uint32_t)(u >> 1);
+      ++u;
+      if (!mbar_wait(&bars->s_full[sb], use & 1, abort_flag, a.st, 222)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < kTile / 16; ++c) {
+        uint32_t rr[16];
+        tmem_ld16(tmem_s + lane_base + sb * kTile + c * 16, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+      return true;
+    };
+    auto put_p = [&](const float (&p)[kTile], float gate) -> bool {
+      if (!mbar_wait(&bars->p_free, (uint32_t)((pv & 1) ^ 1), abort_flag, a.st, 223)) return false;
+      ++pv;
+      tc_fence_after();
+      store_p_row(ps, r, p, gate);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      return true;
+    };
+
+    // zero the block-score rows
+    for (int i = r; i < QT * a.nbs; i += 128) scores[i] = 0.f;
+    wg_sync();
+
+    float x[kTile];
+    // ---------------- phase 1: compressed max / sum
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < ntc && ok; ++j) {
+      if (!consume_s(x)) { ok = false; break; }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) {
+        x[i] = (j * kTile + i < n_t) ? x[i] * a.sc2 : -INFINITY;
+        mt = fmaxf(mt, x[i]);
+      }
+      const float mn = fmaxf(m, mt);
+      if (mn == -INFINITY) continue;
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) s += fast_exp2(x[i] - mn);
+      l = l * fast_exp2(m - mn) + s;
+      m = mn;
+    }
+    float inv_l = l > 0.f ? 1.f / l : 0.f;
+    // ---------------- phase 2: exact p, O_cmp, block scores
+    float* srow = scores + (size_t)qi * a.nbs;
+    const bool lead = (lane % (HPG < 32 ? HPG : 32)) == 0;
+    for (int j = 0; j < ntc && ok; ++j) {
+      if (!consume_s(x)) { ok = false; break; }
+#pragma unroll
+      for (int i = 0; i < kTile; ++i)
+        x[i] = (j * kTile + i < n_t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
+      // block importance: selection block 32j+u collects compressed blocks
+      // 4u-1 (one chunk), 4u..4u+2 (two chunks each), 4u+3 (one chunk)
+      float vsum[33];
+#pragma unroll
+      for (int uu = 0; uu < 32; ++uu)
+        vsum[uu] = (uu > 0 ? x[4 * uu - 1] : 0.f) + 2.f * (x[4 * uu] + x[4 * uu + 1] + x[4 * uu + 2]) +
+                   x[4 * uu + 3];
+      vsum[32] = x[kTile - 1];
+      if (HPG <= 32) {
+        const int base = reduce_scatter32<(HPG <= 32 ? HPG : 32)>(vsum, lane);
+        const float v32 = allreduce_group<(HPG <= 32 ? HPG : 32)>(vsum[32]);
+        if (row_ok) {
+#pragma unroll
+          for (int k = 0; k < 32 / (HPG <= 32 ? HPG : 32); ++k) srow[32 * j + base + k] += vsum[k];
+          if (lead) srow[32 * j + 32] += v32;
+        }
+      } else {
+        const int base = reduce_scatter32<32>(vsum, lane);
+        const float v32 = allreduce_group<32>(vsum[32]);
+        if (row_ok) {
+          atomicAdd(&srow[32 * j + base], vsum[0]);
+          if (lane == 0) atomicAdd(&srow[32 * j + 32], v32);
+        }
+      }
+      if (!put_p(x, g_c)) { ok = false; break; }
+    }
+    // ---------------- top-n selection (one warp per query)
+    wg_sync();
+    if (ok) {
+      for (int qq = warp; qq < QT; qq += 4) {
+        const int tq = t0 + qq;
+        if (tq >= a.T) continue;
+        const int jt = tq / 64;
+        int32_t* out = a.idx + (((size_t)b * a.T + tq) * a.G + g) * a.n;
+        if (jt + 1 <= a.n) {
+          if (lane < a.n) out[lane] = lane <= jt ? lane : -1;
+          continue;
+        }
+        const float* sq = scores + (size_t)qq * a.nbs;
+        // candidates 1 .. jt-2 (blocks 0, jt-1, jt are forced)
+        float cv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int j = 1 + lane + 32 * k;
+          cv[k] = (j <= jt - 2) ? sq[j] : -INFINITY;
+        }
+        int mine = -1;
+        const int nfree = a.n - 3;
+        for (int rnd = 0; rnd < nfree; ++rnd) {
+          float best = -INFINITY;
+          int bk = 0;
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (cv[k] > best) {  // strict: lower k (lower index) wins ties
+              best = cv[k];
+              bk = k;
+            }
+          int bj = (best == -INFINITY) ? 0x7fffffff : 1 + lane + 32 * bk;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+            if (ob > best || (ob == best && oj < bj)) {
+              best = ob;
+              bj = oj;
+            }
+          }
+          if (lane == rnd) mine = bj;
+          if (((bj - 1) & 31) == lane) {
+            const int kk = (bj - 1) >> 5;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (k == kk) cv[k] = -INFINITY;
+          }
+        }
+        if (lane == nfree) mine = 0;
+        if (lane == nfree + 1) mine = jt - 1;
+        if (lane == nfree + 2) mine = jt;
+        int rank = 0;
+        for (int k = 0; k < a.n; ++k) {
+          const int o = __shfl_sync(0xffffffffu, mine, k);
+          rank += (o < mine) ? 1 : 0;
+        }
+        if (lane < a.n) out[rank] = mine;
+      }
+    }
+    // ---------------- phase 3: window max / sum
+    m = -INFINITY;
+    l = 0.f;
+    const int w_lo = t - a.w + 1;
+    for (int j = 0; j < ntw && ok; ++j) {
+      if (!consume_s(x)) { ok = false; break; }
+      float mt = -INFINITY;
+      const int s0 = s_lo + j * kTile;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) {
+        const int s = s0 + i;
+        x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] * a.sc2 : -INFINITY;
+        mt = fmaxf(mt, x[i]);
+      }
+      const float mn = fmaxf(m, mt);
+      if (mn == -INFINITY) continue;
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) s += fast_exp2(x[i] - mn);
+      l = l * fast_exp2(m - mn) + s;
+      m = mn;
+    }
+    inv_l = l > 0.f ? 1.f / l : 0.f;
+    // ---------------- phase 4: exact window p, accumulate g_w * O_win
+    for (int j = 0; j < ntw && ok; ++j) {
+      if (!consume_s(x)) { ok = false; break; }
+      const int s0 = s_lo + j * kTile;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) {
+        const int s = s0 + i;
+        x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
+      }
+      if (!put_p(x, g_w)) { ok = false; break; }
+    }
+    // ---------------- epilogue: O -> bf16 partial output
+    if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 224)) {
+      tc_fence_after();
+      __nv_bfloat16* dst = a.part + (((size_t)b * a.T + t) * a.H + head) * a.dv;
+      for (int c0 = 0; c0 < a.dv; c0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tmem_o + lane_base + c0, rr);
+        tmem_ld_wait(rr);
+        if (row_ok) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(__uint_as_float(rr[2 * k]), __uint_as_float(rr[2 * k + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+struct Layout {
+  uint32_t off_ring, off_p, off_scores, off_bar, total;
+};
+
+Layout layout_for(int dk, int QT, int nbs) {
+  Layout L;
+  L.off_ring = (uint32_t)(dk / 64) * kSlot;
+  L.off_p = L.off_ring + kRing * kSlot;
+  L.off_scores = L.off_p + 2 * kSlot;
+  L.off_bar = (uint32_t)align_up(L.off_scores + (size_t)QT * nbs * sizeof(float), 1024);
+  L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;  // + alignment slack
+  return L;
+}
+
+int scores_stride(int T, int Nc) {
+  const int ntc = (Nc + kTile - 1) / kTile;
+  const int nb = (T + 63) / 64;
+  const int s = (32 * ntc + 1 > nb ? 32 * ntc + 1 : nb) + 1;
+  return (s + 3) & ~3;
+}
+
+template <int HPG>
+int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(cmp_win_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()) !=
+        cudaSuccess)
+      return NSA_ERR_CUDA;
+    attr = true;
+  }
+  dim3 grid((a0.T + a0.QT - 1) / a0.QT, a0.G, B);
+  cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
+  return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t cmp_win_smem_bytes(const nsa_cfg& c) {
+  const int hpg = c.H / c.G;
+  const int QT = 128 / hpg;
+  const int Nc = c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
+  return layout_for(c.dk, QT, scores_stride(c.T, Nc)).total;
+}
+
+int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
+                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s) {
+  const int hpg = c.H / c.G;
+  const int QT = 128 / hpg;
+  const int Nc = c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
+  const int nbs = scores_stride(c.T, Nc);
+  const Layout L = layout_for(c.dk, QT, nbs);
+  if (L.total > smem_max()) return NSA_ERR_UNSUPPORTED;
+  const uint64_t e = 2;
+  CUtensorMap maps[5];
+  {  // q [B,T,H,dk]: box (64, hpg heads, QT queries)
+    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)c.T, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dk * e, (uint64_t)c.H * c.dk * e, (uint64_t)c.T * c.H * c.dk * e};
+    const uint32_t box[4] = {64, (uint32_t)hpg, (uint32_t)QT, 1};
+    if (!make_tmap_bf16(&maps[0], q, 4, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  const int Ncm = Nc > 0 ? Nc : 1;
+  {  // kc [B,G,Nc,dk]
+    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)Ncm, (uint64_t)c.G, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dk * e, (uint64_t)Ncm * c.dk * e, (uint64_t)c.G * Ncm * c.dk * e};
+    const uint32_t box[4] = {64, 128, 1, 1};
+    if (!make_tmap_bf16(&maps[1], Nc > 0 ? kc : k, 4, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  {  // vc [B,G,Nc,dv]
+    const uint64_t dims[4] = {(uint64_t)c.dv, (uint64_t)Ncm, (uint64_t)c.G, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dv * e, (uint64_t)Ncm * c.dv * e, (uint64_t)c.G * Ncm * c.dv * e};
+    const uint32_t box[4] = {64, 128, 1, 1};
+    if (!make_tmap_bf16(&maps[2], Nc > 0 ? vc : v, 4, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  {  // k [B,T,G,dk]: box (64, 1 group, 128 tokens)
+    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dk * e, (uint64_t)c.G * c.dk * e, (uint64_t)c.T * c.G * c.dk * e};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    if (!make_tmap_bf16(&maps[3], k, 4, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  {  // v [B,T,G,dv]
+    const uint64_t dims[4] = {(uint64_t)c.dv, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dv * e, (uint64_t)c.G * c.dv * e, (uint64_t)c.T * c.G * c.dv * e};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    if (!make_tmap_bf16(&maps[4], v, 4, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  CmpWinArgs a;
+  a.T = c.T;
+  a.H = c.H;
+  a.G = c.G;
+  a.dk = c.dk;
+  a.dv = c.dv;
+  a.n = c.n;
+  a.w = c.w;
+  a.Nc = Nc;
+  a.QT = QT;
+  a.nbs = nbs;
+  const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
+  a.sc2 = scale * 1.4426950408889634f;
+  a.gates = static_cast<const __nv_bfloat16*>(gates);
+  a.part = static_cast<__nv_bfloat16*>(part);
+  a.idx = idx;
+  a.st = st;
+  a.off_ring = L.off_ring;
+  a.off_p = L.off_p;
+  a.off_scores = L.off_scores;
+  a.off_bar = L.off_bar;
+  switch (hpg) {
+    case 1: return launch_hpg<1>(a, c.B, maps, L.total, s);
+    case 2: return launch_hpg<2>(a, c.B, maps, L.total, s);
+    case 4: return launch_hpg<4>(a, c.B, maps, L.total, s);
+    case 8: return launch_hpg<8>(a, c.B, maps, L.total, s);
+    case 16: return launch_hpg<16>(a, c.B, maps, L.total, s);
+    case 32: return launch_hpg<32>(a, c.B, maps, L.total, s);
+    case 64: return launch_hpg<64>(a, c.B, maps, L.total, s);
+    case 128: return launch_hpg<128>(a, c.B, maps, L.total, s);
+    default: return NSA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace nsa
