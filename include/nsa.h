@@ -185,6 +185,17 @@ int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const vo
                     const void* q, const void* k, const void* v, void* out, int32_t* idx_out,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- profiling */
+/* No counterpart on the pages: measurement support.  When enabled, every
+   kernel launch of the library is bracketed by two CUDA events on its
+   stream.  nsa_profile_read() synchronises them and, for up to max_kernels
+   distinct kernel names (comma-joined into ``names``, at most name_cap
+   bytes including the terminator), stores the launch count and the summed
+   device time in ms, then forgets the records.  Returns the number of names
+   (or a negative status on a CUDA error: -NSA_ERR_CUDA). */
+int nsa_profile_enable(int on);
+int nsa_profile_read(int max_kernels, char* names, size_t name_cap, int* launches, float* total_ms);
+
 /* ---------------------------------------------------------------- status word */
 /* Synchronises ``stream``, returns the status word the kernels of the last
    call on ``ws`` recorded (NSA_OK if none) and clears it. */

@@ -22,7 +22,7 @@ __all__ = [
     "nsa_status_string", "nsa_version", "nsa_num_compressed",
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_prefill_fwd", "nsa_decode_step",
-    "dsa_decode_step", "nsa_device_status", "workspace",
+    "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnsa.so")
@@ -78,6 +78,9 @@ def _load() -> ctypes.CDLL:
         "dsa_decode_step": (_c_int, [P(DsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
+        "nsa_profile_enable": (_c_int, [_c_int]),
+        "nsa_profile_read": (_c_int, [_c_int, ctypes.c_char_p, _c_size, ctypes.POINTER(_c_int),
+                                      ctypes.POINTER(_c_float)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name, None)
@@ -192,3 +195,19 @@ def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=N
 
 def nsa_device_status(ws, stream=None) -> int:
     return lib.nsa_device_status(_ptr(ws), _stream(stream))
+
+
+def nsa_profile_enable(on: bool = True) -> None:
+    lib.nsa_profile_enable(1 if on else 0)
+
+
+def nsa_profile_read(max_kernels: int = 32):
+    """{kernel name: (launches, total device ms)} since the last read."""
+    names = ctypes.create_string_buffer(4096)
+    cnt = (_c_int * max_kernels)()
+    tot = (_c_float * max_kernels)()
+    n = lib.nsa_profile_read(max_kernels, names, 4096, cnt, tot)
+    if n < 0:
+        raise NsaError(-n, "nsa_profile_read")
+    keys = names.value.decode().split(",") if n else []
+    return {k: (cnt[i], tot[i]) for i, k in enumerate(keys)}

@@ -193,6 +193,28 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
   return launch_sel(c, q, k, v, gates, idx, part, out, st, s);
 }
 
+size_t nsa_decode_workspace_size(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK) return 0;
+  return kHeader;
+}
+
+int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const void* vcache, const void* kc,
+                    const void* vc, const void* gates, void* out, int32_t* idx_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  return NSA_ERR_UNSUPPORTED;
+}
+
+size_t dsa_decode_workspace_size(const dsa_cfg* cfg) { return cfg == nullptr ? 0 : kHeader; }
+
+int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI, const void* q,
+                    const void* k, const void* v, void* out, int32_t* idx_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (cfg == nullptr) return NSA_ERR_INVALID_ARG;
+  return NSA_ERR_UNSUPPORTED;
+}
+
 int nsa_device_status(void* ws, void* stream) {
   if (ws == nullptr) return NSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

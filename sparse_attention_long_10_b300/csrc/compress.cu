@@ -13,6 +13,7 @@
 //   fp32 accumulator in TMEM, bias + bf16 epilogue from TMEM.
 #include "common.cuh"
 #include "kernels.hpp"
+#include "profiler.hpp"
 #include "tmap.hpp"
 
 namespace nsa {
@@ -190,8 +191,10 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
   // bias = flatten(PE) @ W
   {
     dim3 grid((N + 31) / 32), block(32, 8);
+    prof::begin("phi_bias", stream);
     phi_bias_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(pe),
                                                 static_cast<const __nv_bfloat16*>(W), c.l * dX, N, bias_ws);
+    prof::end(stream);
   }
   CUtensorMap mapA, mapB;
   const uint64_t T16 = (uint64_t)c.T / 16;
@@ -232,7 +235,9 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
     attr_set = true;
   }
   dim3 grid((Nc + kTileM - 1) / kTileM, c.G, c.B);
+  prof::begin("compress_gemm", stream);
   compress_gemm_kernel<<<grid, 128, smem, stream>>>(mapA, mapB, a);
+  prof::end(stream);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 

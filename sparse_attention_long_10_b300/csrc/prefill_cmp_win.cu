@@ -21,6 +21,7 @@
 // TMEM: S double buffer (2 x 128 columns) + O (dv columns).
 #include "common.cuh"
 #include "kernels.hpp"
+#include "profiler.hpp"
 #include "tmap.hpp"
 
 namespace nsa {
@@ -576,7 +577,9 @@ int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem
     attr = true;
   }
   dim3 grid((a0.T + a0.QT - 1) / a0.QT, a0.G, B);
+  prof::begin("cmp_win", s);
   cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
+  prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 

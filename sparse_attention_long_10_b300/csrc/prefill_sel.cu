@@ -18,6 +18,7 @@
 // a pair, or one value dimension), warp 4 TMA producer, warp 5 MMA issuer.
 #include "common.cuh"
 #include "kernels.hpp"
+#include "profiler.hpp"
 #include "tmap.hpp"
 
 namespace nsa {
@@ -509,7 +510,9 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
     attr = true;
   }
   dim3 grid((c.T + a.QPC - 1) / a.QPC, c.G, c.B);
+  prof::begin("sel", s);
   sel_kernel<<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+  prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
