@@ -3,9 +3,9 @@
 Every step of the NSA / DSA hot path runs in the library's CUDA kernels.  The
 functions here take torch tensors (device memory, owned by the caller), pass
 their raw pointers and the current CUDA stream through ctypes, and raise
-``NsaError`` on a non-zero status.  There is no CPU fallback: importing this
-package fails loudly if libnsa.so has not been built
-(``python -m sparse_attention_long_10_b300.build``).
+``NsaError`` on a non-zero status.  There is no CPU fallback: the first use of
+the library (any call, or the ``lib`` attribute) raises ImportError if
+libnsa.so has not been built (``python -m sparse_attention_long_10_b300.build``).
 """
 from __future__ import annotations
 
@@ -91,7 +91,20 @@ def _load() -> ctypes.CDLL:
     return L
 
 
-lib = _load()
+_LIB = None
+
+
+def _lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
 
 
 # ------------------------------------------------------------------ helpers
@@ -139,66 +152,66 @@ def workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 # ------------------------------------------------------------------ ABI wrappers
 def nsa_status_string(code: int) -> str:
-    return lib.nsa_status_string(code).decode()
+    return _lib().nsa_status_string(code).decode()
 
 
 def nsa_version() -> int:
-    return lib.nsa_version()
+    return _lib().nsa_version()
 
 
 def nsa_num_compressed(cfg: NsaCfg) -> int:
-    return lib.nsa_num_compressed(ctypes.byref(cfg))
+    return _lib().nsa_num_compressed(ctypes.byref(cfg))
 
 
 def nsa_compress_workspace_size(cfg: NsaCfg) -> int:
-    return lib.nsa_compress_workspace_size(ctypes.byref(cfg))
+    return _lib().nsa_compress_workspace_size(ctypes.byref(cfg))
 
 
 def nsa_prefill_workspace_size(cfg: NsaCfg) -> int:
-    return lib.nsa_prefill_workspace_size(ctypes.byref(cfg))
+    return _lib().nsa_prefill_workspace_size(ctypes.byref(cfg))
 
 
 def nsa_decode_workspace_size(cfg: NsaCfg) -> int:
-    return lib.nsa_decode_workspace_size(ctypes.byref(cfg))
+    return _lib().nsa_decode_workspace_size(ctypes.byref(cfg))
 
 
 def dsa_decode_workspace_size(cfg: DsaCfg) -> int:
-    return lib.dsa_decode_workspace_size(ctypes.byref(cfg))
+    return _lib().dsa_decode_workspace_size(ctypes.byref(cfg))
 
 
 def nsa_compress_kv(cfg: NsaCfg, layout: int, k, v, kc, vc, ws, stream=None):
-    _check(lib.nsa_compress_kv(ctypes.byref(cfg), layout, _ptr(k), _ptr(v), _ptr(kc), _ptr(vc),
+    _check(_lib().nsa_compress_kv(ctypes.byref(cfg), layout, _ptr(k), _ptr(v), _ptr(kc), _ptr(vc),
                                _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_compress_kv")
 
 
 def nsa_prefill_fwd(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, ws, stream=None):
-    _check(lib.nsa_prefill_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates),
+    _check(_lib().nsa_prefill_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates),
                                _ptr(kc), _ptr(vc), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_prefill_fwd")
 
 
 def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None):
-    _check(lib.nsa_decode_step(ctypes.byref(cfg), _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kc),
+    _check(_lib().nsa_decode_step(ctypes.byref(cfg), _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kc),
                                _ptr(vc), _ptr(gates), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_decode_step")
 
 
 def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=None):
-    _check(lib.dsa_decode_step(ctypes.byref(cfg), _ptr(qI), _ptr(wI), _ptr(kI), _ptr(q), _ptr(k),
+    _check(_lib().dsa_decode_step(ctypes.byref(cfg), _ptr(qI), _ptr(wI), _ptr(kI), _ptr(q), _ptr(k),
                                _ptr(v), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "dsa_decode_step")
 
 
 def nsa_device_status(ws, stream=None) -> int:
-    return lib.nsa_device_status(_ptr(ws), _stream(stream))
+    return _lib().nsa_device_status(_ptr(ws), _stream(stream))
 
 
 def nsa_profile_enable(on: bool = True) -> None:
-    lib.nsa_profile_enable(1 if on else 0)
+    _lib().nsa_profile_enable(1 if on else 0)
 
 
 def nsa_profile_read(max_kernels: int = 32):
@@ -206,7 +219,7 @@ def nsa_profile_read(max_kernels: int = 32):
     names = ctypes.create_string_buffer(4096)
     cnt = (_c_int * max_kernels)()
     tot = (_c_float * max_kernels)()
-    n = lib.nsa_profile_read(max_kernels, names, 4096, cnt, tot)
+    n = _lib().nsa_profile_read(max_kernels, names, 4096, cnt, tot)
     if n < 0:
         raise NsaError(-n, "nsa_profile_read")
     keys = names.value.decode().split(",") if n else []
