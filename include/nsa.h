@@ -118,6 +118,28 @@ int nsa_compress_kv(const nsa_cfg* cfg, int layout, const void* k, const void* v
                     void* kc, void* vc, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * nsa_compress_kv_noalloc -- the same computation as nsa_compress_kv, for
+ * callers that cannot allocate device memory when they compress: a serving
+ * loop whose device memory is planned once and never grows, or an embedding
+ * program that is handed tensor pointers but owns no device allocator (and
+ * avoids cudaMalloc, which can synchronise the device).  It takes no
+ * workspace and allocates nothing: its scratch (status word + the two fp32
+ * flatten(PE) @ W bias vectors, at most 2304 bytes) lives in a fixed static
+ * device array of the library, held by every GPU that loads it until exit.
+ * The pages have no counterpart of this entry point.
+ *   - The first call on a device resolves that array's device address (with
+ *     the device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: calls that can overlap on the GPU
+ *     (different streams without ordering) race on it.  Each call clears the
+ *     status word before it launches.
+ *   - Arguments and outputs as nsa_compress_kv; a cfg whose biases do not fit
+ *     the array returns NSA_ERR_WORKSPACE.
+ */
+int nsa_compress_kv_noalloc(const nsa_cfg* cfg, int layout, const void* k, const void* v,
+                            void* kc, void* vc, void* stream);
+
+/*
  * nsa_prefill_fwd -- NSA forward over whole sequences [P2 II; P3].
  * For every sequence b, query position t and head h (group g):
  *   compressed : softmax over the complete compressed blocks i (d*i+l-1 <= t)
