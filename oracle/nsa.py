@@ -122,6 +122,8 @@ def cmp_attention(q: np.ndarray, t: np.ndarray, Kc: np.ndarray, Vc: np.ndarray,
     Returns (O [R, hh, dv], p [R, hh, Nc]) with p = 0 on invisible blocks.
     """
     Nc = Kc.shape[0]
+    if Nc == 0:                      # no complete block anywhere: empty branch -> 0
+        return np.zeros(q.shape[:2] + (Vc.shape[1],)), np.zeros(q.shape[:2] + (0,))
     n_t = num_visible_compressed(t, l, d, Nc)
     logits = (q @ Kc.T) * scale                             # [R, hh, Nc]
     valid = (np.arange(Nc)[None, :] < n_t[:, None])[:, None, :]

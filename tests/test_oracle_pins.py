@@ -147,6 +147,14 @@ def test_cmp_attention_causality_and_empty():
     np.testing.assert_array_equal(o, o2)
 
 
+def test_cmp_attention_no_complete_block():
+    # T < l: no compressed block exists, the branch output is 0
+    rng = np.random.default_rng(5)
+    o, p = O.cmp_attention(rng.standard_normal((3, 2, 8)), np.array([0, 10, 30]), np.zeros((0, 8)),
+                           np.zeros((0, 4)), 0.3, 32, 16)
+    assert o.shape == (3, 2, 4) and np.all(o == 0) and p.shape == (3, 2, 0)
+
+
 # ----------------------------------------------------------------- block scores
 def test_overlap_matrix_brute_force():
     l, d, lsel = 32, 16, 64
