@@ -309,6 +309,122 @@ def run_ours(args, ws, rank):
     return res, inp
 
 
+# ---------------------------------------------------------------- decode leg
+def time_graph_steps(graph, steps, flush):
+    """Device time of ``steps`` replays of ``graph`` (ms each), with the L2
+    flushed (``flush`` is larger than L2) before every replay and outside the
+    timed interval."""
+    times = []
+    for _ in range(steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+def run_decode_leg(args, ws):
+    """One NSA decode step for 16 sequences with 65,536-token caches: the
+    query at t = T-1 reads 4095 compressed entries, 16 kept blocks and the
+    512-token window per KV head.  The compressed caches are precomputed once
+    (they are decode-time state, like the KV cache)."""
+    import sparse_attention_long_10_b300 as nsa
+    wl = decode_config()
+    B, T, H, G, dk, dv = wl.B, wl.T, wl.H, wl.G, wl.dk, wl.dv
+    inp = make_decode(wl)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    cfg = nsa.make_cfg(B, T, H, G, dk, dv, phi=dev)
+    Nc = nsa.nsa_num_compressed(cfg)
+    kc = torch.empty(B, G, Nc, dk, dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty(B, G, Nc, dv, dtype=torch.bfloat16, device="cuda")
+    cws = nsa.workspace(nsa.nsa_compress_workspace_size(cfg))
+    nsa.nsa_compress_kv(cfg, nsa.NSA_LAYOUT_BGTD, dev["kcache"], dev["vcache"], kc, vc, cws)
+    out = torch.empty(B, H, dv, dtype=torch.bfloat16, device="cuda")
+    wsp = nsa.workspace(nsa.nsa_decode_workspace_size(cfg))
+
+    def step(stream=None):
+        nsa.nsa_decode_step(cfg, dev["q"], dev["kcache"], dev["vcache"], kc, vc, dev["gates"], out, None,
+                            wsp, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("decode: device status set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = statistics.mean(time_graph_steps(graph, args.steps, flush))
+    ms = max_over_ranks(ms, ws)
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("decode: device status set in the timed region")
+    # per-kernel split (eager launches bracketed by events, L2 flushed between steps)
+    nsa.nsa_profile_enable(True)
+    for _ in range(args.steps):
+        flush.add_(1)
+        step()
+    torch.cuda.synchronize()
+    prof = nsa.nsa_profile_read()
+    nsa.nsa_profile_enable(False)
+    # end to end: the new token's q, gates and K/V row copied in, out copied back
+    host_q = inp["q"].pin_memory()
+    host_g = inp["gates"].pin_memory()
+    host_k = inp["kcache"][:, :, T - 1].contiguous().pin_memory()
+    host_v = inp["vcache"][:, :, T - 1].contiguous().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_g, host_k, host_v))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step_e2e():
+        dev["q"].copy_(host_q, non_blocking=True)
+        dev["gates"].copy_(host_g, non_blocking=True)
+        dev["kcache"][:, :, T - 1].copy_(host_k, non_blocking=True)
+        dev["vcache"][:, :, T - 1].copy_(host_v, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    e_times = []
+    for _ in range(args.steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step_e2e()
+        e1.record()
+        e_times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_times), ws)
+    nbytes = decode_bytes(B, G, T, dk, dv)
+    pk = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    kern = {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
+            for k, (c, t) in prof.items()}
+    return {
+        "metric": "NSA decode step latency (16 seqs x 65,536-token caches)",
+        "value": ms * 1e3, "unit": "us", "higher_is_better": False,
+        "workload": wl.name, "steps": args.steps,
+        "bytes_per_step": nbytes,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})",
+                     "frac_of_8TBs": gbs / 8000.0, "traffic": None,
+                     "note": "whole step (memset + 2 kernels, CUDA graph replay), L2 flushed before each step"},
+        "kernels": kern,
+        "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
+        "e2e": {"value": ms_e2e * 1e3, "unit": "us", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -316,6 +432,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step leg")
     ap.add_argument("--workload", default="prefill_64k", choices=sorted(PREFILL_CONFIGS),
                     help="prefill workload; the headline is prefill_64k, smaller ones serve profiling")
     args = ap.parse_args()
@@ -345,6 +462,9 @@ def main():
         return
 
     res, inp = run_ours(args, ws, rank)
+    if not args.no_decode:
+        res["decode"] = run_decode_leg(args, ws)
+        res["gpu_launches"] += res["decode"]["gpu_launches_per_step"] * args.steps
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         blas, ncpu = cpu_cores()
         rate, info = oracle_prefill_rate(inp, rows_per_step=16, steps=2)

@@ -194,8 +194,8 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
 }
 
 size_t nsa_decode_workspace_size(const nsa_cfg* cfg) {
-  if (validate_cfg(cfg) != NSA_OK) return 0;
-  return kHeader;
+  if (validate_cfg(cfg) != NSA_OK || decode_supported(*cfg) != NSA_OK) return 0;
+  return decode_ws_bytes(*cfg);
 }
 
 int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const void* vcache, const void* kc,
@@ -203,7 +203,16 @@ int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const
                     void* stream) {
   int rc = validate_cfg(cfg);
   if (rc != NSA_OK) return rc;
-  return NSA_ERR_UNSUPPORTED;
+  const nsa_cfg& c = *cfg;
+  if ((rc = decode_supported(c)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, kcache, vcache, gates, out})) != NSA_OK) return rc;
+  if (num_compressed(c) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  if ((rc = check_ws(ws, ws_bytes, decode_ws_bytes(c))) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, decode_zero_bytes(c), s) != cudaSuccess) return NSA_ERR_CUDA;
+  return launch_decode(c, q, kcache, vcache, kc, vc, gates, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
 size_t dsa_decode_workspace_size(const dsa_cfg* cfg) { return cfg == nullptr ? 0 : kHeader; }

@@ -35,4 +35,13 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
                const void* part, void* out, DeviceStatus* st, cudaStream_t s);
 
+// ---- decode (decode.cu)
+int decode_supported(const nsa_cfg& c);
+size_t decode_ws_bytes(const nsa_cfg& c);
+// bytes at the start of the decode workspace (status word + counters) that
+// must be zero when the step starts
+size_t decode_zero_bytes(const nsa_cfg& c);
+int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const void* vcache, const void* kc,
+                  const void* vc, const void* gates, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
+
 }  // namespace nsa
