@@ -425,6 +425,89 @@ def run_decode_leg(args, ws):
     }
 
 
+# ---------------------------------------------------------------- DSA decode leg
+def run_dsa_leg(args, ws):
+    """One DSA-style decode step: batch 8, 131,072-token context, indexer of 4
+    heads x 64 dims, top-2048 positions, attention of 16 heads (dk=576,
+    dv=512) over the kept positions only."""
+    import sparse_attention_long_10_b300 as nsa
+    wl = dsa_config()
+    inp = make_dsa(wl)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    cfg = nsa.make_dsa_cfg(wl.B, wl.T, wl.HI, wl.dI, wl.H, wl.dk, wl.dv, wl.topk)
+    out = torch.empty(wl.B, wl.H, wl.dv, dtype=torch.bfloat16, device="cuda")
+    wsp = nsa.workspace(nsa.dsa_decode_workspace_size(cfg))
+
+    def step():
+        nsa.dsa_decode_step(cfg, dev["qI"], dev["wI"], dev["kI"], dev["q"], dev["k"], dev["v"], out, None, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("dsa: device status set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(statistics.mean(time_graph_steps(graph, args.steps, flush)), ws)
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("dsa: device status set in the timed region")
+    nsa.nsa_profile_enable(True)
+    for _ in range(args.steps):
+        flush.add_(1)
+        step()
+    torch.cuda.synchronize()
+    prof = nsa.nsa_profile_read()
+    nsa.nsa_profile_enable(False)
+    # end to end: the new token's queries and indexer weights in, out back
+    host = {k: inp[k].pin_memory() for k in ("qI", "wI", "q")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step_e2e():
+        for k, t in host.items():
+            dev[k].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    e_times = []
+    for _ in range(args.steps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step_e2e()
+        e1.record()
+        e_times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_times), ws)
+    kk = min(wl.topk, wl.T)
+    nbytes = wl.B * wl.T * wl.dI * 2 + wl.B * kk * (wl.dk + wl.dv) * 2
+    pk = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {
+        "metric": "DSA decode step latency (8 rows x 131,072-token context, top-2048)",
+        "value": ms * 1e3, "unit": "us", "higher_is_better": False,
+        "workload": wl.name, "steps": args.steps, "bytes_per_step": nbytes,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})", "traffic": None,
+                     "note": "whole step (memset + 4 kernels, CUDA graph replay), L2 flushed before each step"},
+        "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
+                    for k, (c, t) in prof.items()},
+        "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
+        "e2e": {"value": ms_e2e * 1e3, "unit": "us", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,9 +515,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode-step leg")
-    ap.add_argument("--workload", default="prefill_64k", choices=sorted(PREFILL_CONFIGS),
-                    help="prefill workload; the headline is prefill_64k, smaller ones serve profiling")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode and DSA decode legs")
+    ap.add_argument("--workload", default="prefill_64k", choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k"],
+                    help="prefill workload (the headline is prefill_64k; smaller ones serve profiling) or "
+                         "decode_64k / dsa_128k: one decode leg alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, _ = dist_setup()
@@ -461,10 +545,17 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
+    if args.workload in ("decode_64k", "dsa_128k"):
+        res = (run_decode_leg if args.workload == "decode_64k" else run_dsa_leg)(args, ws)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     res, inp = run_ours(args, ws, rank)
     if not args.no_decode:
         res["decode"] = run_decode_leg(args, ws)
         res["gpu_launches"] += res["decode"]["gpu_launches_per_step"] * args.steps
+        res["dsa"] = run_dsa_leg(args, ws)
+        res["gpu_launches"] += res["dsa"]["gpu_launches_per_step"] * args.steps
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         blas, ncpu = cpu_cores()
         rate, info = oracle_prefill_rate(inp, rows_per_step=16, steps=2)

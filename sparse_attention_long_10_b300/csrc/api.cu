@@ -215,13 +215,30 @@ int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const
   return launch_decode(c, q, kcache, vcache, kc, vc, gates, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
-size_t dsa_decode_workspace_size(const dsa_cfg* cfg) { return cfg == nullptr ? 0 : kHeader; }
+int validate_dsa(const dsa_cfg* c) {
+  if (c == nullptr) return NSA_ERR_INVALID_ARG;
+  if (c->B < 1 || c->T < 1 || c->HI < 1 || c->dI < 1 || c->H < 1 || c->dk < 1 || c->dv < 1 || c->topk < 1)
+    return NSA_ERR_INVALID_ARG;
+  return dsa_supported(*c);
+}
+
+size_t dsa_decode_workspace_size(const dsa_cfg* cfg) {
+  if (validate_dsa(cfg) != NSA_OK) return 0;
+  return dsa_ws_bytes(*cfg);
+}
 
 int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI, const void* q,
                     const void* k, const void* v, void* out, int32_t* idx_out, void* ws, size_t ws_bytes,
                     void* stream) {
-  if (cfg == nullptr) return NSA_ERR_INVALID_ARG;
-  return NSA_ERR_UNSUPPORTED;
+  int rc = validate_dsa(cfg);
+  if (rc != NSA_OK) return rc;
+  if ((rc = check_ptrs({qI, wI, kI, q, k, v, out})) != NSA_OK) return rc;
+  if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  if ((rc = check_ws(ws, ws_bytes, dsa_ws_bytes(*cfg))) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, dsa_zero_bytes(*cfg), s) != cudaSuccess) return NSA_ERR_CUDA;
+  return launch_dsa(*cfg, qI, wI, kI, q, k, v, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
 int nsa_device_status(void* ws, void* stream) {

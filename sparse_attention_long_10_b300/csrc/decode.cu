@@ -60,10 +60,10 @@ struct DecArgs {
   float* pm;                         // [BG][NS][16]
   float* pl;                         // [BG][NS][16]
   float* po;                         // [BG][NS][16][dv]
-  float* u;                          // [BG][16][4*nq]
-  float* cc;                         // [BG][16][nq+1]
+  float* u;                          // [BG][4*nq][16]
+  float* cc;                         // [BG][nq+1][16]
   float* mref;                       // [BG][nq][16]
-  float* ocmp;                       // [BG][16][dv]
+  float* stats;                      // [BG][32]: compressed-branch max (log2 units) and 1/sum per head
   int32_t* idx;                      // [BG][n]
   int* cnt;                          // [2][BG]
   DeviceStatus* st;
@@ -84,7 +84,9 @@ __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
 
 // Block-score partials of one head for the warp's 16 entries (quarter qd):
 // group k (entries 4k..4k+3) feeds block 4qd+k with 2*sum - last + prev_last,
-// and its last entry's second chunk feeds block 4qd+4 (the carry c).
+// and its last entry's second chunk feeds block 4qd+4 (the carry c).  All 16
+// head slots are written (heads past hpg see a zero query and stay finite);
+// the selection step weights them by zero.
 __device__ __forceinline__ void block_partials(const float (&p)[2][4], int eo, int head, int qd, float mref_val,
                                                int tq, int bg, const DecArgs& a) {
   float last[2], gs[2];
@@ -102,61 +104,57 @@ __device__ __forceinline__ void block_partials(const float (&p)[2][4], int eo, i
   const float prev1 = hi ? sx1 : sx0;
   const float u0 = 2.f * gs[0] - last[0] + prev0;
   const float u1 = 2.f * gs[1] - last[1] + prev1;
-  if (head < a.hpg) {
-    float* ub = a.u + ((size_t)bg * 16 + head) * (size_t)(4 * a.nq) + 4 * qd;
-    if ((tq & 1) == 0) {
-      ub[tq >> 1] = u0;
-      ub[2 + (tq >> 1)] = u1;
-    }
-    if (tq == 2) a.cc[((size_t)bg * 16 + head) * (size_t)(a.nq + 1) + qd + 1] = last[1];
-    if (tq == 0) a.mref[((size_t)bg * a.nq + qd) * 16 + head] = mref_val;
+  float* ub = a.u + ((size_t)bg * (4 * a.nq) + 4 * qd) * 16 + head;
+  if ((tq & 1) == 0) {
+    ub[(tq >> 1) * 16] = u0;
+    ub[(2 + (tq >> 1)) * 16] = u1;
   }
+  if (tq == 2) a.cc[((size_t)bg * (a.nq + 1) + qd + 1) * 16 + head] = last[1];
+  if (tq == 0) a.mref[((size_t)bg * a.nq + qd) * 16 + head] = mref_val;
 }
 
+__device__ __forceinline__ float dot16(const float* f, const float4* v) {
+  const float4 a = v[0], b = v[1], c = v[2], d = v[3];
+  return f[0] * a.x + f[1] * a.y + f[2] * a.z + f[3] * a.w + f[4] * b.x + f[5] * b.y + f[6] * b.z + f[7] * b.w +
+         f[8] * c.x + f[9] * c.y + f[10] * c.z + f[11] * c.w + f[12] * d.x + f[13] * d.y + f[14] * d.z +
+         f[15] * d.w;
+}
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
 // Selection step, run by the last CTA of a group after every compressed and
-// window split has left its partial: exact softmax statistics, O_cmp, block
-// scores, top-n.
-template <int DV>
+// window split has left its partial: exact softmax statistics of the
+// compressed branch (kept in ``stats`` for the final combine), block
+// importance S[j] for every causal block, top-n.
 __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int warp = warp_id(), lane = lane_id();
+  const int NSc = a.splits;
   float* Mh = reinterpret_cast<float*>(smem);      // 16
   float* iL = Mh + 16;                              // 16
   float* wv = iL + 16;                              // [4][32] winner scores
   int* wj = reinterpret_cast<int*>(wv + 128);       // [4][32] winner blocks
-  float* fsm = reinterpret_cast<float*>(wj + 128);  // [nq][16]
+  float* sp = reinterpret_cast<float*>(wj + 128);   // [NSc][2][16] partial m, l
+  float* fsm = sp + 32 * NSc;                       // [nq][16]
   float* Ssm = fsm + (size_t)a.nq * 16;             // [jt+1]
-  const int hpg = a.hpg;
-  const int NSc = a.splits;
+  for (int e = tid; e < NSc * 16; e += kThreads) {
+    const size_t o = ((size_t)bg * a.NS + e / 16) * 16 + (e & 15);
+    sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
+    sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
+  }
+  __syncthreads();
   if (tid < 16) {
     float M = -INFINITY;
-    for (int s = 0; s < NSc; ++s) M = fmaxf(M, ldcg_f(a.pm + ((size_t)bg * a.NS + s) * 16 + tid));
+    for (int s = 0; s < NSc; ++s) M = fmaxf(M, sp[s * 32 + tid]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f;
-    for (int s = 0; s < NSc; ++s) {
-      const size_t o = ((size_t)bg * a.NS + s) * 16 + tid;
-      L += ldcg_f(a.pl + o) * fast_exp2(ldcg_f(a.pm + o) - Mu);
-    }
+    for (int s = 0; s < NSc; ++s) L += sp[s * 32 + 16 + tid] * fast_exp2(sp[s * 32 + tid] - Mu);
+    const float il = (L > 0.f && tid < a.hpg) ? 1.f / L : 0.f;
     Mh[tid] = Mu;
-    iL[tid] = (L > 0.f && tid < hpg) ? 1.f / L : 0.f;
+    iL[tid] = il;
+    a.stats[(size_t)bg * 32 + tid] = Mu;
+    a.stats[(size_t)bg * 32 + 16 + tid] = il;
   }
-  __syncthreads();
-  // normalised compressed-branch output
-  for (int e = tid; e < 16 * DV; e += kThreads) {
-    const int h = e / DV, d = e % DV;
-    float acc = 0.f;
-    for (int s = 0; s < NSc; ++s) {
-      const size_t o = ((size_t)bg * a.NS + s) * 16 + h;
-      acc += fast_exp2(ldcg_f(a.pm + o) - Mh[h]) * ldcg_f(a.po + o * DV + d);
-    }
-    a.ocmp[((size_t)bg * 16 + h) * DV + d] = acc * iL[h];
-  }
-  // per-quarter normalisation factors exp(mref - M) / L
-  for (int e = tid; e < a.nq * 16; e += kThreads) {
-    const int h = e & 15;
-    fsm[e] = (h < hpg) ? fast_exp2(ldcg_f(a.mref + (size_t)bg * a.nq * 16 + e) - Mh[h]) * iL[h] : 0.f;
-  }
-  __syncthreads();
   const int jt = (a.T - 1) / 64;
   const int n = a.n;
   int32_t* idx = a.idx + (size_t)bg * n;
@@ -169,19 +167,43 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
     }
     return;
   }
+  __syncthreads();
+  // per-quarter normalisation factors exp(mref - M) / L
+  {
+    const float* mr = a.mref + (size_t)bg * a.nq * 16;
+    for (int e4 = tid; e4 < a.nq * 4; e4 += kThreads) {
+      const float4 m4 = ldcg4(mr + 4 * e4);
+      const int h = (4 * e4) & 15;
+      float4 f;
+      f.x = fast_exp2(m4.x - Mh[h + 0]) * iL[h + 0];
+      f.y = fast_exp2(m4.y - Mh[h + 1]) * iL[h + 1];
+      f.z = fast_exp2(m4.z - Mh[h + 2]) * iL[h + 2];
+      f.w = fast_exp2(m4.w - Mh[h + 3]) * iL[h + 3];
+      reinterpret_cast<float4*>(fsm)[e4] = f;
+    }
+  }
+  __syncthreads();
   // block importance S[j], j <= jt
-  const int U = 4 * a.nq;
-  for (int j = tid; j <= jt; j += kThreads) {
-    const int qq = j >> 2;
-    float s = 0.f;
-    if (qq < a.nq) {
-      for (int h = 0; h < hpg; ++h) s += fsm[qq * 16 + h] * ldcg_f(a.u + ((size_t)bg * 16 + h) * U + j);
+  {
+    const float* ub = a.u + (size_t)bg * (4 * a.nq) * 16;
+    const float* cb = a.cc + (size_t)bg * (a.nq + 1) * 16;
+    for (int j = tid; j <= jt; j += kThreads) {
+      const int qq = j >> 2;
+      float s = 0.f;
+      if (qq < a.nq) {
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = ldcg4(ub + (size_t)j * 16 + 4 * k);
+        s = dot16(fsm + qq * 16, v);
+      }
+      if ((j & 3) == 0 && qq >= 1 && qq <= a.nq) {
+        float4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = ldcg4(cb + (size_t)qq * 16 + 4 * k);
+        s += dot16(fsm + (qq - 1) * 16, v);
+      }
+      Ssm[j] = s;
     }
-    if ((j & 3) == 0 && qq >= 1 && qq <= a.nq) {
-      for (int h = 0; h < hpg; ++h)
-        s += fsm[(qq - 1) * 16 + h] * ldcg_f(a.cc + ((size_t)bg * 16 + h) * (a.nq + 1) + qq);
-    }
-    Ssm[j] = s;
   }
   __syncthreads();
   // top-(n-3) among the free blocks 1 .. jt-2: each of 4 warps finds the best
@@ -222,7 +244,7 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   }
   __syncthreads();
   if (warp == 0) {
-    // lane holds candidates c = lane and lane + 32 of the 4*kfree winners
+    // lane holds candidates c = lane + 32k of the 4*kfree winners
     float cv[4];
     int cj[4];
 #pragma unroll
@@ -275,48 +297,80 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   }
 }
 
-// Final combine, run by the last selection CTA of a group.
+// Final combine, run by the last selection CTA of a group:
+//   out = g_cmp * O_cmp + g_slc * O_slc + g_win * O_win
+// with each branch's partials weighted by exp(m_split - M) / L.
 template <int DV>
 __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int b = bg / a.G, g = bg % a.G;
-  float* fs = reinterpret_cast<float*>(smem);    // [sel_splits][16]
-  float* fw = fs + a.sel_splits * 16;            // [16]
-  float* gt = fw + 16;                           // [16][3]
-  const int s0 = a.splits + 1;
-  if (tid < 16) {
-    const int h = tid;
-    float M = -INFINITY;
-    for (int s = 0; s < a.sel_splits; ++s) M = fmaxf(M, ldcg_f(a.pm + ((size_t)bg * a.NS + s0 + s) * 16 + h));
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = 0; s < a.sel_splits; ++s) {
-      const size_t o = ((size_t)bg * a.NS + s0 + s) * 16 + h;
-      const float f = fast_exp2(ldcg_f(a.pm + o) - Mu);
-      fs[s * 16 + h] = f;
-      L += ldcg_f(a.pl + o) * f;
-    }
-    const float iL = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < a.sel_splits; ++s) fs[s * 16 + h] *= iL;
-    const float lw = ldcg_f(a.pl + ((size_t)bg * a.NS + a.splits) * 16 + h);
-    fw[h] = lw > 0.f ? 1.f / lw : 0.f;
-    if (h < a.hpg) {
-      const __nv_bfloat16* gp = a.gates + ((size_t)b * a.H + g * a.hpg + h) * 3;
-      gt[h * 3 + 0] = __bfloat162float(gp[0]);
-      gt[h * 3 + 1] = __bfloat162float(gp[1]);
-      gt[h * 3 + 2] = __bfloat162float(gp[2]);
-    }
+  const int NS = a.NS;
+  const int win = a.splits, s0 = a.splits + 1;
+  float* sp = reinterpret_cast<float*>(smem);    // [NS][2][16] partial m, l
+  float* fac = sp + 32 * NS;                     // [NS][16] weight of each partial
+  float* gt = fac + 16 * NS;                     // [16][3]
+  for (int e = tid; e < NS * 16; e += kThreads) {
+    const size_t o = ((size_t)bg * NS + e / 16) * 16 + (e & 15);
+    sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
+    sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
+  }
+  if (tid < 16 && tid < a.hpg) {
+    const __nv_bfloat16* gp = a.gates + ((size_t)b * a.H + g * a.hpg + tid) * 3;
+    gt[tid * 3 + 0] = __bfloat162float(gp[0]);
+    gt[tid * 3 + 1] = __bfloat162float(gp[1]);
+    gt[tid * 3 + 2] = __bfloat162float(gp[2]);
   }
   __syncthreads();
-  for (int e = tid; e < a.hpg * DV; e += kThreads) {
-    const int h = e / DV, d = e % DV;
-    float slc = 0.f;
-    for (int s = 0; s < a.sel_splits; ++s)
-      slc += fs[s * 16 + h] * ldcg_f(a.po + (((size_t)bg * a.NS + s0 + s) * 16 + h) * DV + d);
-    const float win = fw[h] * ldcg_f(a.po + (((size_t)bg * a.NS + a.splits) * 16 + h) * DV + d);
-    const float cmp = ldcg_f(a.ocmp + ((size_t)bg * 16 + h) * DV + d);
-    const float o = gt[h * 3 + 0] * cmp + gt[h * 3 + 1] * slc + gt[h * 3 + 2] * win;
-    a.out[((size_t)b * a.H + g * a.hpg + h) * DV + d] = __float2bfloat16_rn(o);
+  if (tid < 16) {
+    const int h = tid;
+    // compressed: statistics from the selection step, folded with g_cmp
+    const float Mc = ldcg_f(a.stats + (size_t)bg * 32 + h);
+    const float iLc = ldcg_f(a.stats + (size_t)bg * 32 + 16 + h);
+    const float gc = h < a.hpg ? gt[h * 3 + 0] : 0.f;
+    const float gs = h < a.hpg ? gt[h * 3 + 1] : 0.f;
+    const float gw = h < a.hpg ? gt[h * 3 + 2] : 0.f;
+    for (int s = 0; s < a.splits; ++s) fac[s * 16 + h] = gc * fast_exp2(sp[s * 32 + h] - Mc) * iLc;
+    const float lw = sp[win * 32 + 16 + h];
+    fac[win * 16 + h] = lw > 0.f ? gw / lw : 0.f;
+    float M = -INFINITY;
+    for (int s = s0; s < NS; ++s) M = fmaxf(M, sp[s * 32 + h]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    for (int s = s0; s < NS; ++s) L += sp[s * 32 + 16 + h] * fast_exp2(sp[s * 32 + h] - Mu);
+    const float il = L > 0.f ? gs / L : 0.f;
+    for (int s = s0; s < NS; ++s) fac[s * 16 + h] = fast_exp2(sp[s * 32 + h] - Mu) * il;
+  }
+  __syncthreads();
+  const float* po = a.po + (size_t)bg * NS * 16 * DV;
+  for (int e4 = tid; e4 < a.hpg * DV / 4; e4 += kThreads) {
+    const int h = (4 * e4) / DV;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= NS; s += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = ldcg4(po + ((size_t)(s + k) * 16) * DV + 4 * e4);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float f = fac[(s + k) * 16 + h];
+        acc.x += f * v[k].x;
+        acc.y += f * v[k].y;
+        acc.z += f * v[k].z;
+        acc.w += f * v[k].w;
+      }
+    }
+    for (; s < NS; ++s) {
+      const float4 v = ldcg4(po + ((size_t)s * 16) * DV + 4 * e4);
+      const float f = fac[s * 16 + h];
+      acc.x += f * v.x;
+      acc.y += f * v.y;
+      acc.z += f * v.z;
+      acc.w += f * v.w;
+    }
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x, acc.y);
+    pk.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(a.out + ((size_t)b * a.H + g * a.hpg) * DV + 4 * e4) = pk;
   }
 }
 
@@ -582,14 +636,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!bars->last) return;
   __threadfence();
   if (MODE == 0)
-    select_step<DV>(a, bg, smem);
+    select_step(a, bg, smem);
   else
     combine_step<DV>(a, bg, smem);
 }
 
 // ------------------------------------------------------------------ host side
 struct DecWs {
-  size_t cnt, pm, pl, po, u, cc, mref, ocmp, idx, end;
+  size_t cnt, pm, pl, po, u, cc, mref, stats, idx, end;
 };
 
 struct DecShape {
@@ -619,8 +673,8 @@ DecWs dec_ws(const nsa_cfg& c) {
   w.u = align_up(w.po + sizeof(float) * BG * s.NS * 16 * c.dv, 256);
   w.cc = align_up(w.u + sizeof(float) * BG * 16 * 4 * (size_t)s.nq, 256);
   w.mref = align_up(w.cc + sizeof(float) * BG * 16 * (size_t)(s.nq + 1), 256);
-  w.ocmp = align_up(w.mref + sizeof(float) * BG * (size_t)s.nq * 16, 256);
-  w.idx = align_up(w.ocmp + sizeof(float) * BG * 16 * c.dv, 256);
+  w.stats = align_up(w.mref + sizeof(float) * BG * (size_t)s.nq * 16, 256);
+  w.idx = align_up(w.stats + sizeof(float) * BG * 32, 256);
   w.end = align_up(w.idx + sizeof(int32_t) * BG * c.n, 256);
   return w;
 }
@@ -634,8 +688,8 @@ DecSmem dec_smem(const nsa_cfg& c) {
   const size_t ring = (size_t)kStages * (c.dk / 64 + c.dv / 64) * kBox;
   const size_t merge = sizeof(float) * (3 * 64 + 4 * 16 * (size_t)c.dv);
   const size_t jt1 = (size_t)(c.T - 1) / 64 + 1;
-  const size_t select = sizeof(float) * (32 + 256 + 16 * (size_t)s.nq + jt1);
-  const size_t combine = sizeof(float) * (16 * (size_t)s.sel_splits + 16 + 48);
+  const size_t select = sizeof(float) * (32 + 256 + 32 * (size_t)s.splits + 16 * (size_t)s.nq + jt1);
+  const size_t combine = sizeof(float) * (48 * (size_t)s.NS + 48);
   size_t body = ring;
   if (merge > body) body = merge;
   if (select > body) body = select;
@@ -739,7 +793,7 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
   a.u = reinterpret_cast<float*>(ws + w.u);
   a.cc = reinterpret_cast<float*>(ws + w.cc);
   a.mref = reinterpret_cast<float*>(ws + w.mref);
-  a.ocmp = reinterpret_cast<float*>(ws + w.ocmp);
+  a.stats = reinterpret_cast<float*>(ws + w.stats);
   a.idx = reinterpret_cast<int32_t*>(ws + w.idx);
   a.cnt = reinterpret_cast<int*>(ws + w.cnt);
   a.st = reinterpret_cast<DeviceStatus*>(ws);

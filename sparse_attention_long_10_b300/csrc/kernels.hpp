@@ -44,4 +44,11 @@ size_t decode_zero_bytes(const nsa_cfg& c);
 int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const void* vcache, const void* kc,
                   const void* vc, const void* gates, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
 
+// ---- DSA decode (dsa.cu)
+int dsa_supported(const dsa_cfg& c);
+size_t dsa_ws_bytes(const dsa_cfg& c);
+size_t dsa_zero_bytes(const dsa_cfg& c);
+int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
+               const void* v, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
+
 }  // namespace nsa
