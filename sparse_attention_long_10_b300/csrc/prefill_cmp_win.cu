@@ -345,14 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++u;
       if (!mbar_wait(&bars->s_full[sb], use & 1, abort_flag, a.st, 222)) return false;
       tc_fence_after();
+      uint32_t rs[kTile / 16][16];
 #pragma unroll
-      for (int c = 0; c < kTile / 16; ++c) {
-        uint32_t rr[16];
-        tmem_ld16(tmem_s + lane_base + sb * kTile + c * 16, rr);
-        tmem_ld_wait(rr);
+      for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem_s + lane_base + sb * kTile + c * 16, rs[c]);
+      tmem_ld_wait(rs[0]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rr[i]);
-      }
+      for (int c = 1; c < kTile / 16; ++c) tmem_reg_fence(rs[c]);
+#pragma unroll
+      for (int c = 0; c < kTile / 16; ++c)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rs[c][i]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[sb]);

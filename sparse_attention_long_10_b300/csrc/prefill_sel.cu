@@ -10,12 +10,19 @@
 //     S^T[key, head] = K_pair[key, :] . Q_t[head, :]        (M=128, N=NP)
 //     O^T[dv, head] += V_pair^T[dv, key] . P^T[key, head]    (M=128, N=NP)
 // All n*l' scores of the item sit in TMEM at once, so the softmax over the
-// kept keys is exact (one max, one sum), and the slc gate is folded into P.
-// The epilogue adds the cmp+win partial sum from prefill_cmp_win.cu:
+// kept keys is exact: one pass over TMEM finds each head's max, a second forms
+// p = exp(s - max) (unnormalised, bf16) and the sums.  The epilogue applies
+// g_slc / sum and adds the cmp+win partial sum from prefill_cmp_win.cu:
 //     out = part + g_slc * O_slc          (bf16)
 //
-// Warp roles: warps 0-3 softmax + epilogue (thread = TMEM lane = one key of
-// a pair, or one value dimension), warp 4 TMA producer, warp 5 MMA issuer.
+// Warp roles (12 warps):
+//   warps 0-3, 4-7  two softmax + epilogue warpgroups, taking alternate items
+//                   (thread = TMEM lane = one key of a pair, or one value dim)
+//   warp 8          TMA producer of Q and the key chunks
+//   warp 9          QK^T MMA issuer
+//   warp 10         TMA producer of the value pairs
+//   warp 11         PV MMA issuer
+// TMEM: S^T double buffer (2 x 8 pairs x NP columns), O^T in 4 buffers.
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -25,13 +32,15 @@ namespace nsa {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr int NP = 16;           // MMA N: heads of the group, padded to 16
-constexpr int kRingK = 6;        // 16 KB: one 64-column chunk of a block pair
+constexpr int kRingK = 5;        // 16 KB: one 64-column chunk of a block pair
 constexpr int kRingV = 2;        // 32 KB: both 64-column chunks of a value pair
 constexpr int kSlotK = 16384;
 constexpr int kSlotV = 32768;
 constexpr int kQBuf = 2048;      // one 64-column chunk of NP query rows
+constexpr int kPBuf = 32768;     // P^T of one item: 8 pairs x 2 chunks x 2 KB
+constexpr int kItemsPerCta = 32;
 
 struct SelArgs {
   int T, H, G, dk, dv, n, hpg, QPC;
@@ -49,10 +58,10 @@ struct Bars {
   uint64_t k_full[kRingK], k_empty[kRingK];
   uint64_t v_full[kRingV], v_empty[kRingV];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, p_free;
-  uint64_t o_full[2], o_free[2];
-  uint64_t wg;
-  uint64_t drain;
+  uint64_t p_full[2], p_free[2];
+  uint64_t o_full[4], o_free[4];
+  uint64_t wg[2];
+  uint64_t drain[2];
   uint32_t tmem;
   int abort_flag;
 };
@@ -65,6 +74,50 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // zeros from a negative coordinate
 __device__ __forceinline__ int block_token(int blk) { return blk >= 0 ? blk * 64 : -128; }
 
+// The n (<= 16) kept blocks of one item, -1 past n: issued as independent
+// loads (four 16-byte loads when n == 16) so they cost one memory round trip.
+__device__ __forceinline__ void load_blocks(const int32_t* blk, int n, int (&bk)[16]) {
+  if (n == 16 && (reinterpret_cast<uintptr_t>(blk) & 15u) == 0) {
+    const int4* p4 = reinterpret_cast<const int4*>(blk);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int4 v = __ldg(p4 + k);
+      bk[4 * k + 0] = v.x;
+      bk[4 * k + 1] = v.y;
+      bk[4 * k + 2] = v.z;
+      bk[4 * k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) bk[k] = k < n ? __ldg(blk + k) : -1;
+  }
+}
+
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Warp sums of 16 per-lane values: afterwards lane holds the sum over the warp
+// of v[h] for h = head_of_lane(lane) (butterfly reduce-scatter, 16 shuffles).
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      const float send = up ? v[k] : v[k + n];
+      const float keep = up ? v[k + n] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ int head_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     sel_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const SelArgs a) {
@@ -73,8 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* qbuf = smem;                        // 2 items x kcs chunks x 2 KB
   uint8_t* kring = smem + a.off_kring;
   uint8_t* vring = smem + a.off_vring;
-  uint8_t* pt = smem + a.off_pt;               // P^T: npairs*2 chunks x 2 KB
-  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2][4][NP]
+  uint8_t* pt = smem + a.off_pt;               // P^T: 2 buffers x 8 pairs x 2 chunks x 2 KB
+  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2 wg][2 max/sum][4 warps][NP]
   Bars* bars = reinterpret_cast<Bars*>(smem + a.off_bar);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -95,6 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);
+      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->p_free[i], 1);
+      mbar_init(&bars->wg[i], 4);
+      mbar_init(&bars->drain[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->o_full[i], 1);
       mbar_init(&bars->o_free[i], 4);
     }
@@ -106,10 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
     }
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->p_free, 1);
-    mbar_init(&bars->wg, 4);
-    mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
   }
@@ -126,12 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
   const uint32_t tmem_s = tmem;                   // 2 x SC columns
-  const uint32_t tmem_o = tmem + 2 * SC;          // 2 x NP columns
+  const uint32_t tmem_o = tmem + 2 * SC;          // 4 x NP columns
 
   if (*abort_flag) {
     // an earlier CTA failed: do nothing
-  } else if (warp == 4) {
-    // =============================================================== producer
+  } else if (warp == 8 || warp == 10) {
+    // =============================================================== producers
+    // warp 8 streams Q and the key chunks, warp 10 the value pairs, so both
+    // rings stay in flight at once
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(&mapK);
@@ -151,10 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
       };
       auto load_k = [&](int i) {
-        const int32_t* blk = a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n;
-        for (int p = 0; p < npairs && ok; ++p) {
-          const int tk0 = block_token(__ldg(blk + 2 * p));
-          const int tk1 = block_token(2 * p + 1 < a.n ? __ldg(blk + 2 * p + 1) : -1);
+        int bks[16];
+        load_blocks(a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n, a.n, bks);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          if (p >= npairs || !ok) break;
+          const int tk0 = block_token(bks[2 * p]);
+          const int tk1 = block_token(bks[2 * p + 1]);
           for (int c = 0; c < kcs; ++c) {
             const int slot = kv % kRingK;
             if (!mbar_wait(&bars->k_empty[slot], (uint32_t)(((kv / kRingK) & 1) ^ 1), abort_flag, a.st, 302)) {
@@ -170,10 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto load_v = [&](int i) {
-        const int32_t* blk = a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n;
-        for (int p = 0; p < npairs && ok; ++p) {
-          const int tk0 = block_token(__ldg(blk + 2 * p));
-          const int tk1 = block_token(2 * p + 1 < a.n ? __ldg(blk + 2 * p + 1) : -1);
+        int bks[16];
+        load_blocks(a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n, a.n, bks);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          if (p >= npairs || !ok) break;
+          const int tk0 = block_token(bks[2 * p]);
+          const int tk1 = block_token(bks[2 * p + 1]);
           const int slot = vv % kRingV;
           if (!mbar_wait(&bars->v_empty[slot], (uint32_t)(((vv / kRingV) & 1) ^ 1), abort_flag, a.st, 303)) {
             ok = false;
@@ -188,14 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++vv;
         }
       };
-      load_q(0);
-      load_k(0);
-      for (int i = 0; i < nitems && ok; ++i) {
-        if (i + 1 < nitems) {
-          load_q(i + 1);
-          load_k(i + 1);
+      if (warp == 8) {
+        for (int i = 0; i < nitems && ok; ++i) {
+          load_q(i);
+          load_k(i);
         }
-        load_v(i);
+      } else {
+        for (int i = 0; i < nitems && ok; ++i) load_v(i);
       }
       if (!ok || *abort_flag) {
         for (int x = (nq > 2 ? nq - 2 : 0); x < nq; ++x)
@@ -206,8 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_plain(&bars->v_full[x % kRingV], (uint32_t)((x / kRingV) & 1), kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
-    // =============================================================== MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // =============================================================== MMA issuers
+    // warp 9 issues QK^T of every item, warp 11 PV; they use separate TMEM
+    // accumulators, so the key and value streams are consumed concurrently
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, NP, false, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, NP, true, false);
@@ -247,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int i) {
         if (!ok) return;
-        const int ob = i & 1;
-        if (!mbar_wait(&bars->o_free[ob], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag, a.st, 314) ||
-            !mbar_wait(&bars->p_full, (uint32_t)(i & 1), abort_flag, a.st, 315)) {
+        const int pb = i & 1, ob = i & 3;
+        if (!mbar_wait(&bars->o_free[ob], (uint32_t)(((i >> 2) & 1) ^ 1), abort_flag, a.st, 314) ||
+            !mbar_wait(&bars->p_full[pb], (uint32_t)((i >> 1) & 1), abort_flag, a.st, 315)) {
           ok = false;
           return;
         }
@@ -265,142 +329,153 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             // A = V^T (dv-major rows of keys), B = P^T (head rows, keys along K)
             const uint64_t ad = sdesc_sw128(v_a + slot * kSlotV + k * 2048, 16384, 1024);
-            const uint64_t bd = sdesc_sw128(p_a + (p * 2 + (k >> 2)) * kQBuf + (k & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                sdesc_sw128(p_a + pb * kPBuf + (p * 2 + (k >> 2)) * kQBuf + (k & 3) * 32, 16, 1024);
             umma_bf16(tmem_o + ob * NP, ad, bd, idesc_pv, (p > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&bars->v_empty[slot]);
           ++vv;
         }
-        umma_commit(&bars->p_free);
+        umma_commit(&bars->p_free[pb]);
         umma_commit(&bars->o_full[ob]);
       };
-      issue_qk(0);
-      for (int i = 0; i < nitems; ++i) {
-        if (i + 1 < nitems) issue_qk(i + 1);
-        issue_pv(i);
+      if (warp == 9) {
+        for (int i = 0; i < nitems; ++i) issue_qk(i);
+      } else {
+        for (int i = 0; i < nitems; ++i) issue_pv(i);
       }
       if (!ok || *abort_flag) {
-        // wait for every MMA issued so far before the CTA releases TMEM
-        umma_commit(&bars->drain);
-        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
+        // wait for every MMA this thread issued before the CTA releases TMEM
+        umma_commit(&bars->drain[warp == 9 ? 0 : 1]);
+        mbar_wait_plain(&bars->drain[warp == 9 ? 0 : 1], 0, kWaitLimitNs);
       }
     }
-  } else {
+  } else if (warp < 8) {
     // =============================================================== softmax + epilogue
-    const int r = threadIdx.x;          // key lane within a pair / value dim
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int wg = warp >> 2;                 // warpgroup: items i with i % 2 == wg
+    const int lw = warp & 3;
+    const int r = lw * 32 + lane;             // TMEM lane: key of a pair / value dim
+    const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
+    const bool hi_half = (r >> 6) != 0;
+    const int kk = r & 63;
+    uint8_t* my_pt = pt + wg * kPBuf;
+    float* red_m = red + wg * 2 * 4 * NP;     // [4][NP]
+    float* red_l = red_m + 4 * NP;            // [4][NP]
     bool ok = true;
     uint32_t wg_phase = 0;
     auto wg_sync = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->wg);
-      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 321)) ok = false;
+      if (lane == 0) mbar_arrive(&bars->wg[wg]);
+      if (!mbar_wait(&bars->wg[wg], wg_phase & 1, abort_flag, a.st, 321)) ok = false;
       ++wg_phase;
     };
-    float x[8][NP];    // [pair][head] (n <= 16 -> at most 8 pairs)
+    float coef[NP];   // g_slc / sum of the item whose epilogue is pending
 
+    // softmax of item i: P^T (unnormalised) into this warpgroup's buffer and
+    // coef[h] = g_slc[h] / sum[h]
     auto softmax = [&](int i) {
       if (!ok) return;
       const int t = t0 + i;
       const int sb = i & 1;
       const uint32_t par = (uint32_t)((i >> 1) & 1);
+      int bks[16];
+      load_blocks(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
+      float gsl[NP];
+      {
+        const __nv_bfloat16* gp = a.gates + (((size_t)b * a.T + t) * a.H + g * a.hpg) * 3 + 1;
+#pragma unroll
+        for (int h = 0; h < NP; ++h) gsl[h] = h < a.hpg ? __bfloat162float(gp[3 * h]) : 0.f;
+      }
       if (!mbar_wait(&bars->s_full[sb], par, abort_flag, a.st, 322)) {
         ok = false;
         return;
       }
       tc_fence_after();
-      const int32_t* blk = a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n;
+      // pass 1: per-head max of the raw scores over the valid kept keys
+      float mx[NP];
+#pragma unroll
+      for (int h = 0; h < NP; ++h) mx[h] = -INFINITY;
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
         if (p < npairs) {
           uint32_t rr[16];
           tmem_ld16(tmem_s + lane_base + sb * SC + p * NP, rr);
           tmem_ld_wait(rr);
-          const int bi = 2 * p + (r >> 6);
-          const int bk = bi < a.n ? __ldg(blk + bi) : -1;
-          const int s = bk * 64 + (r & 63);
-          const bool valid = bk >= 0 && s <= t;
+          const int bk = hi_half ? bks[2 * p + 1] : bks[2 * p];
+          const bool valid = bk >= 0 && bk * 64 + kk <= t;
 #pragma unroll
-          for (int h = 0; h < NP; ++h) x[p][h] = valid ? __uint_as_float(rr[h]) * a.sc2 : -INFINITY;
+          for (int h = 0; h < NP; ++h) mx[h] = fmaxf(mx[h], valid ? __uint_as_float(rr[h]) : -INFINITY);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
-      // max over the kept keys, per head
-      float mh[NP], lh[NP];
 #pragma unroll
-      for (int h = 0; h < NP; ++h) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int p = 0; p < 8; ++p)
-          if (p < npairs) m = fmaxf(m, x[p][h]);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        mh[h] = m;
-      }
-      float* rd = red + (wg_phase & 1) * 4 * NP;
+      for (int h = 0; h < NP; ++h) mx[h] = warp_max_f32(mx[h]);
       if (lane == 0)
 #pragma unroll
-        for (int h = 0; h < NP; ++h) rd[warp * NP + h] = mh[h];
+        for (int h = 0; h < NP; ++h) red_m[lw * NP + h] = mx[h];
       wg_sync();
-#pragma unroll
-      for (int h = 0; h < NP; ++h) mh[h] = fmaxf(fmaxf(rd[h], rd[NP + h]), fmaxf(rd[2 * NP + h], rd[3 * NP + h]));
-      // sum
+      if (!ok) return;
 #pragma unroll
       for (int h = 0; h < NP; ++h) {
-        float s = 0.f;
-#pragma unroll
-        for (int p = 0; p < 8; ++p)
-          if (p < npairs) {
-            x[p][h] = (mh[h] == -INFINITY) ? 0.f : fast_exp2(x[p][h] - mh[h]);
-            s += x[p][h];
-          }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        lh[h] = s;
+        const float m = fmaxf(fmaxf(red_m[h], red_m[NP + h]), fmaxf(red_m[2 * NP + h], red_m[3 * NP + h]));
+        mx[h] = (m == -INFINITY) ? 0.f : m * a.sc2;
       }
-      rd = red + (wg_phase & 1) * 4 * NP;
-      if (lane == 0)
-#pragma unroll
-        for (int h = 0; h < NP; ++h) rd[warp * NP + h] = lh[h];
-      wg_sync();
-      float coef[NP];
-#pragma unroll
-      for (int h = 0; h < NP; ++h) {
-        const float l = rd[h] + rd[NP + h] + rd[2 * NP + h] + rd[3 * NP + h];
-        float gs = 0.f;
-        if (h < a.hpg) gs = __bfloat162float(a.gates[(((size_t)b * a.T + t) * a.H + g * a.hpg + h) * 3 + 1]);
-        coef[h] = (l > 0.f) ? gs / l : 0.f;
-      }
-      // P^T (K-major: row = head, keys along K) for the PV MMA
-      if (!mbar_wait(&bars->p_free, (uint32_t)((i & 1) ^ 1), abort_flag, a.st, 323)) {
+      // pass 2: p = exp(s*scale - max), sums, P^T (bf16) for the PV MMA
+      if (!mbar_wait(&bars->p_free[sb], par ^ 1, abort_flag, a.st, 323)) {
         ok = false;
         return;
       }
       tc_fence_after();
-      const int kk = r & 63;
+      float ls[NP];
+#pragma unroll
+      for (int h = 0; h < NP; ++h) ls[h] = 0.f;
 #pragma unroll
       for (int p = 0; p < 8; ++p) {
         if (p < npairs) {
-          uint8_t* chunk = pt + (p * 2 + (r >> 6)) * kQBuf;
+          uint32_t rr[16];
+          tmem_ld16(tmem_s + lane_base + sb * SC + p * NP, rr);
+          tmem_ld_wait(rr);
+          const int bk = hi_half ? bks[2 * p + 1] : bks[2 * p];
+          const bool valid = bk >= 0 && bk * 64 + kk <= t;
+          uint8_t* chunk = my_pt + (p * 2 + (hi_half ? 1 : 0)) * kQBuf + (kk & 7) * 2;
 #pragma unroll
           for (int h = 0; h < NP; ++h) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(x[p][h] * coef[h]);
-            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, kk >> 3) + (kk & 7) * 2) = v;
+            const float e = valid ? fast_exp2(fmaf(__uint_as_float(rr[h]), a.sc2, -mx[h])) : 0.f;
+            ls[h] += e;
+            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, kk >> 3)) = __float2bfloat16_rn(e);
           }
         }
       }
+      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) {
+        mbar_arrive(&bars->s_free[sb]);
+        mbar_arrive(&bars->p_full[sb]);
+      }
+      // sums per head over the warpgroup (off the MMA's critical path)
+      const float ws = warp_sum16(ls, lane);
+      if ((lane & 1) == 0) red_l[lw * NP + head_of_lane(lane)] = ws;
+      wg_sync();
+      if (!ok) return;
+#pragma unroll
+      for (int h = 0; h < NP; ++h) {
+        const float l = red_l[h] + red_l[NP + h] + red_l[2 * NP + h] + red_l[3 * NP + h];
+        coef[h] = (l > 0.f) ? __fdividef(gsl[h], l) : 0.f;
+      }
     };
 
-    auto epilogue = [&](int i) {
+    auto epilogue = [&](int i, const float (&cf)[NP]) {
       if (!ok) return;
       const int t = t0 + i;
-      const int ob = i & 1;
-      if (!mbar_wait(&bars->o_full[ob], (uint32_t)((i >> 1) & 1), abort_flag, a.st, 324)) {
+      const int ob = i & 3;
+      const int d = r;
+      const size_t rowbase = ((size_t)b * a.T + t) * a.H + g * a.hpg;
+      // the cmp+win partial sum of this item, read before waiting for O
+      float prt[NP];
+#pragma unroll
+      for (int h = 0; h < NP; ++h)
+        prt[h] = (h < a.hpg && d < a.dv) ? __bfloat162float(a.part[(rowbase + h) * a.dv + d]) : 0.f;
+      if (!mbar_wait(&bars->o_full[ob], (uint32_t)((i >> 2) & 1), abort_flag, a.st, 324)) {
         ok = false;
         return;
       }
@@ -411,23 +486,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_free[ob]);
-      const int d = r;
       if (d < a.dv) {
-        const size_t rowbase = ((size_t)b * a.T + t) * a.H + g * a.hpg;
 #pragma unroll
         for (int h = 0; h < NP; ++h) {
-          if (h < a.hpg) {
-            const size_t o = (rowbase + h) * a.dv + d;
-            a.out[o] = __float2bfloat16_rn(__bfloat162float(a.part[o]) + __uint_as_float(rr[h]));
-          }
+          if (h < a.hpg)
+            a.out[(rowbase + h) * a.dv + d] = __float2bfloat16_rn(fmaf(cf[h], __uint_as_float(rr[h]), prt[h]));
         }
       }
     };
 
-    softmax(0);
-    for (int i = 0; i < nitems; ++i) {
-      if (i + 1 < nitems) softmax(i + 1);
-      epilogue(i);
+    // items wg, wg+2, ...: softmax(next) overlaps the PV of the current item,
+    // whose epilogue follows
+    float cprev[NP];
+    if (wg < nitems) {
+      softmax(wg);
+#pragma unroll
+      for (int h = 0; h < NP; ++h) cprev[h] = coef[h];
+    }
+    for (int i = wg; i < nitems; i += 2) {
+      if (i + 2 < nitems) softmax(i + 2);
+      epilogue(i, cprev);
+#pragma unroll
+      for (int h = 0; h < NP; ++h) cprev[h] = coef[h];
     }
   }
   tc_fence_before();
@@ -442,12 +522,12 @@ struct Layout {
 
 Layout layout_for(int dk, int n) {
   Layout L;
-  const int npairs = (n + 1) / 2;
+  (void)n;
   L.off_kring = (uint32_t)align_up((size_t)2 * (dk / 64) * kQBuf, 1024);
   L.off_vring = L.off_kring + kRingK * kSlotK;
   L.off_pt = L.off_vring + kRingV * kSlotV;
-  L.off_red = L.off_pt + (uint32_t)(npairs * 2 * kQBuf);
-  L.off_bar = (uint32_t)align_up(L.off_red + 2 * 4 * NP * sizeof(float), 256);
+  L.off_red = L.off_pt + 2 * kPBuf;
+  L.off_bar = (uint32_t)align_up(L.off_red + 2 * 2 * 4 * NP * sizeof(float), 256);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;
   return L;
 }
@@ -490,7 +570,7 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.dv = c.dv;
   a.n = c.n;
   a.hpg = hpg;
-  a.QPC = 16;
+  a.QPC = kItemsPerCta;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
   a.idx = idx;
