@@ -5,7 +5,7 @@
 // are kept, independently per query; attention runs over the kept tokens only,
 // its softmax normalised over that set].
 //
-// One query token per batch row b at position T-1.  Four launches:
+// One query token per batch row b at position T-1.  Five launches:
 //   dsa_index   I[s] = sum_h w_h * max(0, qI_h . kI_s) for every s (warp MMA,
 //               kI streamed by TMA); writes an order-preserving 32-bit key of
 //               the fp32 score and a 4096-bin histogram of the key's top 12
@@ -18,7 +18,10 @@
 //   dsa_compact ordered compaction of the kept positions (ascending).
 //   dsa_attn    softmax(q K_sel^T * scale) V_sel over the kept positions:
 //               rows gathered by untiled bulk copies, warp MMA, split over
-//               CTAs; the last CTA of a row merges the splits.
+//               CTAs of 64 kept positions, each leaving (max, sum, O);
+//   dsa_merge   merges a row's splits, one CTA per (head, row).
+// The last indexer CTA of a row finds the first radix cut from the row's
+// histogram.
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -39,7 +42,7 @@ constexpr int kSelPart = 2048;      // positions per threshold / compaction CTA
 constexpr int kCandCap = 8192;      // boundary-bin candidates kept per row
 constexpr int kAttnThreads = 160;   // 4 compute warps + 1 gather warp
 constexpr int kAttnTile = 32;       // kept tokens per attention tile
-constexpr int kAttnTilesPerCta = 4;
+constexpr int kAttnTilesPerCta = 2;
 constexpr int kAttnStages = 2;
 
 struct DsaArgs {
@@ -62,11 +65,12 @@ struct DsaArgs {
   uint32_t* gtcnt;                  // [B,nparts] keys above the boundary bin
   uint32_t* offs;                   // [B,nparts] output offset of each part
   uint32_t* thr;                    // [B,2] (K*, I*): the kk-th kept pair
+  uint32_t* cut1;                   // [B,2] first-level cut: boundary bin B1, count above it
   int32_t* idx;                     // [B,kk] kept positions, ascending
   float* pm;                        // [B,attn_ctas,16]
   float* pl;                        // [B,attn_ctas,16]
   float* po;                        // [B,attn_ctas,16,dv]
-  int* cnt;                         // [2,B]
+  int* cnt;                         // [3,B] last-CTA counters (threshold, indexer, unused)
   DeviceStatus* st;
 };
 
@@ -171,18 +175,19 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
         float sb = w0 * fmaxf(c[2], 0.f) + w1 * fmaxf(c[3], 0.f);
         sa = quad_sum(sa);
         sb = quad_sum(sb);
-        if (tq == 0) {
-          const int pa = s0 + i * kIdxTile + r0 + gq, pb = pa + 8;
-          if (pa < a.T) {
-            const uint32_t ka = order_key(sa);
-            a.keys[(size_t)b * a.T + pa] = ka;
-            atomicAdd(&hs[ka >> 20], 1u);
-          }
-          if (pb < a.T) {
-            const uint32_t kb = order_key(sb);
-            a.keys[(size_t)b * a.T + pb] = kb;
-            atomicAdd(&hs[kb >> 20], 1u);
-          }
+        // lanes with tq == 0 own keys r0+gq and r0+gq+8; equal bins within the
+        // warp are counted with one shared-memory atomic
+        const int pa = s0 + i * kIdxTile + r0 + gq, pb = pa + 8;
+        const uint32_t ka = order_key(sa), kb = order_key(sb);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pos = e ? pb : pa;
+          const uint32_t key = e ? kb : ka;
+          const bool mine = tq == 0 && pos < a.T;
+          if (mine) a.keys[(size_t)b * a.T + pos] = key;
+          const uint32_t bin = mine ? (key >> 20) : 0xffffffffu;
+          const unsigned same = __match_any_sync(0xffffffffu, bin);
+          if (mine && (__ffs(same) - 1) == lane) atomicAdd(&hs[bin], (uint32_t)__popc(same));
         }
       }
       __syncwarp();
@@ -193,6 +198,63 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   if (*abort_flag) return;
   for (int i = threadIdx.x; i < kBins; i += kIdxThreads)
     if (hs[i]) atomicAdd(&a.hist[(size_t)b * kBins + i], hs[i]);
+  // the last CTA of the row finds the boundary bin of the first radix level
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (threadIdx.x == 0) s_last = (atomicAdd(&a.cnt[a.B + b], 1) == (int)gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // suffix counts over the bins, 16 per thread for the first 256 threads' worth
+  uint32_t* hg = hs;   // reuse: copy of the row's histogram
+  {
+    constexpr int kPer = (kBins + kIdxThreads - 1) / kIdxThreads;
+    uint32_t v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kIdxThreads;
+      v[k] = i < kBins ? __ldcg(a.hist + (size_t)b * kBins + i) : 0u;
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kIdxThreads;
+      if (i < kBins) hg[i] = v[k];
+    }
+  }
+  __syncthreads();
+  // 128 threads, 32 bins each from the top: warp scans, then the thread whose
+  // range holds the kk-th best key walks its bins
+  __shared__ uint32_t wtot[4];
+  const int t = threadIdx.x;
+  uint32_t sum = 0, incl = 0;
+  if (t < 128) {
+    for (int i = 0; i < 32; ++i) sum += hg[kBins - 32 * t - 1 - i];
+    incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wtot[warp] = incl;
+  }
+  __syncthreads();
+  if (t < 128) {
+    for (int k = 0; k < warp; ++k) incl += wtot[k];
+    const uint32_t excl = incl - sum;
+    if (excl < (uint32_t)a.kk && incl >= (uint32_t)a.kk) {
+      uint32_t cum = excl;
+      for (int i = 0; i < 32; ++i) {
+        const int bin = kBins - 32 * t - 1 - i;
+        if (cum + hg[bin] >= (uint32_t)a.kk) {
+          a.cut1[(size_t)b * 2] = (uint32_t)bin;
+          a.cut1[(size_t)b * 2 + 1] = cum;
+          break;
+        }
+        cum += hg[bin];
+      }
+    }
+  }
 }
 
 // ============================================================ threshold
@@ -203,21 +265,24 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
 template <class Get>
 __device__ void block_cut(Get get, int nbins, uint32_t need, bool from_top, uint32_t* scan, uint32_t& bin,
                           uint32_t& before) {
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int per = nbins / 256;
   auto bin_of = [&](int i) { return from_top ? nbins - per * t - 1 - i : per * t + i; };
   uint32_t sum = 0;
   for (int i = 0; i < per; ++i) sum += get(bin_of(i));
-  scan[t] = sum;
-  __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    const uint32_t v = t >= off ? scan[t - off] : 0u;
-    __syncthreads();
-    scan[t] += v;
-    __syncthreads();
+  // inclusive scan over the 256 threads: within warps by shuffles, then warp totals
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
   }
-  const uint32_t incl = scan[t], excl = incl - sum;
+  if (lane == 31) scan[w] = incl;
   __syncthreads();
+  uint32_t wbase = 0;
+  for (int k = 0; k < w; ++k) wbase += scan[k];
+  incl += wbase;
+  const uint32_t excl = incl - sum;
   if (excl < need && incl >= need) {
     uint32_t cum = excl;
     for (int i = 0; i < per; ++i) {
@@ -297,18 +362,24 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
   if (s_last) return;
   __syncthreads();
   const uint32_t* hist = a.hist + (size_t)b * kBins;
-  uint32_t B1, above;
-  block_cut([&](int i) { return __ldcg(hist + i); }, kBins, (uint32_t)a.kk, true, scan, B1, above);
+  const uint32_t B1 = __ldcg(a.cut1 + (size_t)b * 2), above = __ldcg(a.cut1 + (size_t)b * 2 + 1);
   // this part's keys: count those above the boundary bin, collect the boundary bin
   const int p0 = part * kSelPart, p1 = min(a.T, p0 + kSelPart);
   const uint32_t* keys = a.keys + (size_t)b * a.T;
   uint32_t gt = 0;
-  for (int base = p0; base < p1; base += kSelThreads) {
-    const int pos = base + t;
-    uint32_t key = 0;
+  constexpr int kChunks = kSelPart / kSelThreads;
+  uint32_t kv[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int pos = p0 + c * kSelThreads + t;
+    kv[c] = pos < p1 ? __ldcg(keys + pos) : 0u;
+  }
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int pos = p0 + c * kSelThreads + t;
+    const uint32_t key = kv[c];
     bool cand = false;
     if (pos < p1) {
-      key = __ldcg(keys + pos);
       const uint32_t bin = key >> 20;
       gt += bin > B1 ? 1u : 0u;
       cand = bin == B1;
@@ -406,10 +477,18 @@ __global__ void __launch_bounds__(kSelThreads) dsa_compact_kernel(const DsaArgs 
   const uint32_t* keys = a.keys + (size_t)b * a.T;
   int32_t* dst = a.idx + (size_t)b * a.kk;
   int32_t* dst2 = a.idx_out != nullptr ? a.idx_out + (size_t)b * a.kk : nullptr;
-  for (int base = p0; base < p1; base += kSelThreads) {
+  constexpr int kChunks = kSelPart / kSelThreads;
+  bool selv[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int pos = p0 + c * kSelThreads + t;
+    selv[c] = pos < p1 && (a.all || kept(__ldcg(keys + pos), (uint32_t)pos, Ks, Is));
+  }
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int base = p0 + c * kSelThreads;
     const int pos = base + t;
-    bool sel = false;
-    if (pos < p1) sel = a.all ? true : kept(__ldcg(keys + pos), (uint32_t)pos, Ks, Is);
+    const bool sel = selv[c];
     const unsigned m = __ballot_sync(0xffffffffu, sel);
     if (lane == 0) wc[warp] = (uint32_t)__popc(m);
     __syncthreads();
@@ -633,72 +712,84 @@ __global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs
       r[8 * DV + 1] = o[j][3];
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) bars->last = (atomicAdd(&a.cnt[a.B + b], 1) == (int)gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (!bars->last) return;
-  __threadfence();
-  // ---------------------------------------------------------------- merge the row's splits
-  float* Mh = red_m;   // [16]
-  float* iLh = red_l;  // [16]
+}
+
+// Merge of a row's attention splits: out[b,h,:] = sum_c w_c O_c / sum_c w_c l_c,
+// w_c = exp(m_c - max m).  One CTA per (head, row), one thread per 4 columns.
+constexpr int kMergeGroups = 4;   // partial subsets summed in parallel per column
+
+template <int DV>
+__global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const DsaArgs a) {
+  constexpr int C4 = DV / 4;            // float4 columns
+  const int h = blockIdx.x, b = blockIdx.y;
   const int NC = a.attn_ctas;
-  if (threadIdx.x < 16) {
-    const int h = threadIdx.x;
+  __shared__ float Ms, iLs;
+  __shared__ int s_abort;
+  __shared__ float4 part[kMergeGroups - 1][C4];
+  if (threadIdx.x == 0) s_abort = prior_error(a.st);
+  __syncthreads();
+  if (s_abort) return;
+  const float* pm = a.pm + (size_t)b * NC * 16 + h;
+  const float* pl = a.pl + (size_t)b * NC * 16 + h;
+  if (threadIdx.x < 32) {
     float M = -INFINITY;
-    for (int c = 0; c < NC; ++c) M = fmaxf(M, __ldcg(a.pm + ((size_t)b * NC + c) * 16 + h));
+    for (int c = threadIdx.x; c < NC; c += 32) M = fmaxf(M, __ldcg(pm + (size_t)c * 16));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -INFINITY ? 0.f : M;
-    float Lsum = 0.f;
-    for (int c = 0; c < NC; ++c) {
-      const size_t o2 = ((size_t)b * NC + c) * 16 + h;
-      Lsum += __ldcg(a.pl + o2) * fast_exp2(__ldcg(a.pm + o2) - Mu);
+    float L = 0.f;
+    for (int c = threadIdx.x; c < NC; c += 32)
+      L += __ldcg(pl + (size_t)c * 16) * fast_exp2(__ldcg(pm + (size_t)c * 16) - Mu);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (threadIdx.x == 0) {
+      Ms = Mu;
+      iLs = L > 0.f ? 1.f / L : 0.f;
     }
-    Mh[h] = Mu;
-    iLh[h] = Lsum > 0.f ? 1.f / Lsum : 0.f;
   }
   __syncthreads();
-  const float* po = a.po + (size_t)b * NC * 16 * DV;
-  const float* pmr = a.pm + (size_t)b * NC * 16;
-  for (int e4 = threadIdx.x; e4 < a.H * DV / 4; e4 += kAttnThreads) {
-    const int h = (4 * e4) / DV;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int c = 0;
-    for (; c + 4 <= NC; c += 4) {
-      float4 v[4];
-      float f[4];
+  const int col = threadIdx.x % C4, grp = threadIdx.x / C4;
+  const float* po = a.po + ((size_t)b * NC * 16 + h) * DV + 4 * col;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = grp * 8; c0 < NC; c0 += 8 * kMergeGroups) {
+    float4 v[8];
+    float f[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[k] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)(c + k) * 16 * DV) + e4);
-        f[k] = __ldcg(pmr + (c + k) * 16 + h);
-      }
+    for (int k = 0; k < 8; ++k) {
+      const int c = c0 + k;
+      v[k] = c < NC ? __ldcg(reinterpret_cast<const float4*>(po + (size_t)c * 16 * DV)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      f[k] = c < NC ? __ldcg(pm + (size_t)c * 16) : -INFINITY;
+    }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float ff = fast_exp2(f[k] - Mh[h]);
-        acc.x += ff * v[k].x;
-        acc.y += ff * v[k].y;
-        acc.z += ff * v[k].z;
-        acc.w += ff * v[k].w;
-      }
+    for (int k = 0; k < 8; ++k) {
+      const float ff = fast_exp2(f[k] - Ms);
+      acc.x += ff * v[k].x;
+      acc.y += ff * v[k].y;
+      acc.z += ff * v[k].z;
+      acc.w += ff * v[k].w;
     }
-    for (; c < NC; ++c) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(po + (size_t)c * 16 * DV) + e4);
-      const float ff = fast_exp2(__ldcg(pmr + c * 16 + h) - Mh[h]);
-      acc.x += ff * v.x;
-      acc.y += ff * v.y;
-      acc.z += ff * v.z;
-      acc.w += ff * v.w;
+  }
+  if (grp > 0) part[grp - 1][col] = acc;
+  __syncthreads();
+  if (grp == 0) {
+#pragma unroll
+    for (int k = 0; k < kMergeGroups - 1; ++k) {
+      const float4 p2 = part[k][col];
+      acc.x += p2.x;
+      acc.y += p2.y;
+      acc.z += p2.z;
+      acc.w += p2.w;
     }
-    const float il = iLh[h];
     uint2 pk;
-    pk.x = pack_bf16x2(acc.x * il, acc.y * il);
-    pk.y = pack_bf16x2(acc.z * il, acc.w * il);
-    *reinterpret_cast<uint2*>(a.out + (size_t)b * a.H * DV + 4 * e4) = pk;
+    pk.x = pack_bf16x2(acc.x * iLs, acc.y * iLs);
+    pk.y = pack_bf16x2(acc.z * iLs, acc.w * iLs);
+    *reinterpret_cast<uint2*>(a.out + ((size_t)b * a.H + h) * DV + 4 * col) = pk;
   }
 }
 
 // ============================================================ host side
 struct DsaWs {
-  size_t cnt, hist, cand_n, zero_end, keys, cand, gtcnt, offs, thr, idx, pm, pl, po, end;
+  size_t cnt, hist, cand_n, zero_end, keys, cand, gtcnt, offs, thr, cut1, idx, pm, pl, po, end;
 };
 
 struct DsaShape {
@@ -719,7 +810,7 @@ DsaWs dsa_ws(const dsa_cfg& c) {
   const size_t B = (size_t)c.B;
   DsaWs w;
   w.cnt = sizeof(DeviceStatus);
-  w.cand_n = align_up(w.cnt + sizeof(int) * 2 * B, 256);
+  w.cand_n = align_up(w.cnt + sizeof(int) * 3 * B, 256);
   w.hist = align_up(w.cand_n + sizeof(uint32_t) * B, 256);
   w.zero_end = align_up(w.hist + sizeof(uint32_t) * B * kBins, 256);
   w.keys = w.zero_end;
@@ -727,7 +818,8 @@ DsaWs dsa_ws(const dsa_cfg& c) {
   w.gtcnt = align_up(w.cand + sizeof(uint32_t) * B * kCandCap * 2, 256);
   w.offs = align_up(w.gtcnt + sizeof(uint32_t) * B * s.nparts, 256);
   w.thr = align_up(w.offs + sizeof(uint32_t) * B * s.nparts, 256);
-  w.idx = align_up(w.thr + sizeof(uint32_t) * B * 2, 256);
+  w.cut1 = align_up(w.thr + sizeof(uint32_t) * B * 2, 256);
+  w.idx = align_up(w.cut1 + sizeof(uint32_t) * B * 2, 256);
   w.pm = align_up(w.idx + sizeof(int32_t) * B * (size_t)s.kk, 256);
   w.pl = align_up(w.pm + sizeof(float) * B * s.attn_ctas * 16, 256);
   w.po = align_up(w.pl + sizeof(float) * B * s.attn_ctas * 16, 256);
@@ -767,6 +859,10 @@ int launch_attn(const DsaArgs& a, cudaStream_t s) {
   }
   prof::begin("dsa_attn", s);
   dsa_attn_kernel<DV><<<dim3(a.attn_ctas, a.B), kAttnThreads, L.total, s>>>(a);
+  prof::end(s);
+  if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  prof::begin("dsa_merge", s);
+  dsa_merge_kernel<DV><<<dim3(a.H, a.B), DV / 4 * kMergeGroups, 0, s>>>(a);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
@@ -821,6 +917,7 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.gtcnt = reinterpret_cast<uint32_t*>(ws + w.gtcnt);
   a.offs = reinterpret_cast<uint32_t*>(ws + w.offs);
   a.thr = reinterpret_cast<uint32_t*>(ws + w.thr);
+  a.cut1 = reinterpret_cast<uint32_t*>(ws + w.cut1);
   a.idx = reinterpret_cast<int32_t*>(ws + w.idx);
   a.pm = reinterpret_cast<float*>(ws + w.pm);
   a.pl = reinterpret_cast<float*>(ws + w.pl);
