@@ -9,69 +9,71 @@
 // blocks and the w-token window once, for all hpg <= 16 query heads of the
 // group at the same time (group-centric loading).
 //
-// Two launches, split-KV:
-//   dec_kernel<MODE 0>  grid (cmp splits + 1, B*G)
-//       split x < splits: compressed attention over 8 tiles of 64 entries;
-//       split x = splits: window attention over (T-w, T-1].
-//       Each CTA leaves a partial (running max m, sum l, unnormalised O) per
-//       head, and the cmp splits also leave the per-quarter (16 entries)
-//       block-score partials u/c with their reference max.  The last CTA of
-//       a group (atomic counter, no waiting) merges the cmp partials into the
-//       exact softmax, normalises O_cmp, forms the block importance
-//           S[j] = sum_h sum_i w(i,j) p[h,i]
-//       (w = 16-token chunks shared by compressed entry i and block j) and
-//       picks blocks 0, j_t, j_t-1 plus the top n-3 others, ties to the lower
-//       index.
-//   dec_kernel<MODE 1>  grid (ceil(n/4), B*G)
-//       each CTA attends over 4 kept blocks; the last CTA of the group merges
-//       them, adds the window and compressed outputs with the gates and
-//       writes out = g_cmp*O_cmp + g_slc*O_slc + g_win*O_win (bf16).
-//
-// Data movement: 64-row x 64-column 128B-swizzled TMA boxes (one 16-byte
-// aligned row of 128 B per key), a 2-stage ring per CTA, two CTAs per SM.
-// Math: one warp takes 16 keys of each 64-key tile; QK^T and PV are
-// mma.sync m16n8k16 with the 16 heads as the M side (fp32 accumulation),
-// online softmax in registers.
+// Work is cut into units of up to 4 pairs of 64-row key/value blocks (512
+// keys) of one group; one CTA takes one unit, two CTAs share an SM:
+//     S^T[key, head] = K_pair[key, :] . q[head, :]         (tcgen05, M=128, N=16)
+//     exact softmax over the unit's keys (max pass, then exp pass over TMEM)
+//     O^T[dv, head] += V_pair^T[dv, key] . P^T[key, head]  (tcgen05, M=128, N=16)
+// and leaves the unit's (max, sum, unnormalised O) per head in the workspace.
+// Two launches:
+//   dec_kernel<MODE 0>  grid (compressed units + window units, B*G)
+//       compressed units also leave block-importance partials: for every
+//       selection block j the sum over its compressed entries i of
+//       w(i,j) p[h,i] (w = 16-token chunks shared), relative to the unit's
+//       max; the last CTA of a group (atomic counter, no waiting) normalises
+//       them, forms S[j] = sum_h ..., and keeps blocks 0, j_t, j_t-1 plus the
+//       top n-3 others, ties to the lower index.
+//   dec_kernel<MODE 1>  grid (selected units, B*G)
+//       the kept blocks; the last CTA of a group merges every unit and writes
+//       out = g_cmp*O_cmp + g_slc*O_slc + g_win*O_win (bf16).
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
 #include "tmap.hpp"
-#include "warp_mma.cuh"
 
 namespace nsa {
 
 namespace {
 
-constexpr int kThreads = 160;        // warps 0-3 compute, warp 4 TMA producer
-constexpr int kStages = 2;
-constexpr int kBox = 8192;           // 64 rows x 128 bytes
-constexpr int kTilesPerSplit = 8;    // 64-entry tiles per compressed split
-constexpr int kBlocksPerSelCta = 4;  // kept blocks per selection CTA
+constexpr int kThreads = 192;        // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
+constexpr int NP = 16;               // MMA N: heads of the group, padded to 16
+constexpr int kPairs = 4;            // block pairs per unit (512 keys)
+constexpr int kUnitKeys = 128 * kPairs;
+constexpr int kRingK = 3;            // 16 KB: one 64-column chunk of a pair
+constexpr int kRingV = 1;            // 32 KB: both 64-column chunks of a value pair
+constexpr int kSlotK = 16384;
+constexpr int kSlotV = 32768;
+constexpr int kQBuf = 2048;          // one 64-column chunk of NP query rows
+constexpr int kPBuf = kPairs * 2 * kQBuf;
 
 struct DecArgs {
   int B, T, H, G, BG, hpg, n, w;
-  int Nc, nq, ntc;                   // compressed entries, 16-entry quarters, 64-entry tiles
-  int splits, tps, sel_splits, bps, NS;
+  int Nc, ncu, nwu, nsu, NS;         // compressed / window / selected units per group, slots
+  int win0, win_len;                 // first window token, window length
   float sc2;                         // softmax scale * log2(e)
-  const __nv_bfloat16* q;            // [B,H,dk]
   const __nv_bfloat16* gates;        // [B,H,3]
   __nv_bfloat16* out;                // [B,H,dv]
   int32_t* idx_out;                  // nullable [B,G,n]
-  float* pm;                         // [BG][NS][16]
-  float* pl;                         // [BG][NS][16]
-  float* po;                         // [BG][NS][16][dv]
-  float* u;                          // [BG][4*nq][16]
-  float* cc;                         // [BG][nq+1][16]
-  float* mref;                       // [BG][nq][16]
-  float* stats;                      // [BG][32]: compressed-branch max (log2 units) and 1/sum per head
+  float* pm;                         // [BG][NS][16] unit max (log2 units, -inf if empty)
+  float* pl;                         // [BG][NS][16] unit sum
+  float* po;                         // [BG][NS][16][dv] unit O (unnormalised)
+  float* u;                          // [BG][ncu*128][16] block partials within a 32-entry chunk
+  float* cc;                         // [BG][ncu*16][16] carry of each chunk's last entry
+  float* stats;                      // [BG][32] compressed-branch max and 1/sum per head
   int32_t* idx;                      // [BG][n]
   int* cnt;                          // [2][BG]
   DeviceStatus* st;
+  uint32_t off_kring, off_vring, off_pt, off_red, off_bar;
 };
 
-struct DecBars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[kRingK], k_empty[kRingK];
+  uint64_t v_full[kRingV], v_empty[kRingV];
+  uint64_t s_full, p_full, o_full;
+  uint64_t wg;
+  uint64_t drain;
+  uint32_t tmem;
   int abort_flag;
   int last;
 };
@@ -81,36 +83,31 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
-// Block-score partials of one head for the warp's 16 entries (quarter qd):
-// group k (entries 4k..4k+3) feeds block 4qd+k with 2*sum - last + prev_last,
-// and its last entry's second chunk feeds block 4qd+4 (the carry c).  All 16
-// head slots are written (heads past hpg see a zero query and stay finite);
-// the selection step weights them by zero.
-__device__ __forceinline__ void block_partials(const float (&p)[2][4], int eo, int head, int qd, float mref_val,
-                                               int tq, int bg, const DecArgs& a) {
-  float last[2], gs[2];
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Warp sums of 16 per-lane values: afterwards lane holds the warp sum of
+// v[head_of_lane(lane)] (butterfly reduce-scatter, 16 shuffles).
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const float pair = p[nt][eo] + p[nt][eo + 1];
-    gs[nt] = pair + __shfl_xor_sync(0xffffffffu, pair, 1);
-    const float y = __shfl_xor_sync(0xffffffffu, p[nt][eo + 1], 1);
-    last[nt] = (tq & 1) ? p[nt][eo + 1] : y;
+  for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < n; ++k) {
+      const float send = up ? v[k] : v[k + n];
+      const float keep = up ? v[k + n] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
   }
-  const float sx0 = __shfl_xor_sync(0xffffffffu, last[0], 2);
-  const float sx1 = __shfl_xor_sync(0xffffffffu, last[1], 2);
-  const bool hi = (tq >> 1) != 0;
-  const float prev0 = hi ? sx0 : 0.f;
-  const float prev1 = hi ? sx1 : sx0;
-  const float u0 = 2.f * gs[0] - last[0] + prev0;
-  const float u1 = 2.f * gs[1] - last[1] + prev1;
-  float* ub = a.u + ((size_t)bg * (4 * a.nq) + 4 * qd) * 16 + head;
-  if ((tq & 1) == 0) {
-    ub[(tq >> 1) * 16] = u0;
-    ub[(2 + (tq >> 1)) * 16] = u1;
-  }
-  if (tq == 2) a.cc[((size_t)bg * (a.nq + 1) + qd + 1) * 16 + head] = last[1];
-  if (tq == 0) a.mref[((size_t)bg * a.nq + qd) * 16 + head] = mref_val;
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ int head_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
 __device__ __forceinline__ float dot16(const float* f, const float4* v) {
@@ -120,24 +117,21 @@ __device__ __forceinline__ float dot16(const float* f, const float4* v) {
          f[15] * d.w;
 }
 
-__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
-
-// Selection step, run by the last CTA of a group after every compressed and
-// window split has left its partial: exact softmax statistics of the
-// compressed branch (kept in ``stats`` for the final combine), block
-// importance S[j] for every causal block, top-n.
+// Selection step, run by the last compressed/window CTA of a group: exact
+// softmax statistics of the compressed branch (kept in ``stats`` for the
+// final combine), block importance S[j] for every causal block, top-n.
 __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int warp = warp_id(), lane = lane_id();
-  const int NSc = a.splits;
+  const int ncu = a.ncu;
   float* Mh = reinterpret_cast<float*>(smem);      // 16
   float* iL = Mh + 16;                              // 16
   float* wv = iL + 16;                              // [4][32] winner scores
   int* wj = reinterpret_cast<int*>(wv + 128);       // [4][32] winner blocks
-  float* sp = reinterpret_cast<float*>(wj + 128);   // [NSc][2][16] partial m, l
-  float* fsm = sp + 32 * NSc;                       // [nq][16]
-  float* Ssm = fsm + (size_t)a.nq * 16;             // [jt+1]
-  for (int e = tid; e < NSc * 16; e += kThreads) {
+  float* sp = reinterpret_cast<float*>(wj + 128);   // [ncu][2][16] unit max, sum
+  float* fsm = sp + 32 * ncu;                       // [ncu][16] factors exp(m_unit - M) / L
+  float* Ssm = fsm + 16 * ncu;                      // [jt+1]
+  for (int e = tid; e < ncu * 16; e += kThreads) {
     const size_t o = ((size_t)bg * a.NS + e / 16) * 16 + (e & 15);
     sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
     sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
@@ -145,15 +139,16 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   __syncthreads();
   if (tid < 16) {
     float M = -INFINITY;
-    for (int s = 0; s < NSc; ++s) M = fmaxf(M, sp[s * 32 + tid]);
+    for (int s = 0; s < ncu; ++s) M = fmaxf(M, sp[s * 32 + tid]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f;
-    for (int s = 0; s < NSc; ++s) L += sp[s * 32 + 16 + tid] * fast_exp2(sp[s * 32 + tid] - Mu);
+    for (int s = 0; s < ncu; ++s) L += sp[s * 32 + 16 + tid] * fast_exp2(sp[s * 32 + tid] - Mu);
     const float il = (L > 0.f && tid < a.hpg) ? 1.f / L : 0.f;
     Mh[tid] = Mu;
     iL[tid] = il;
     a.stats[(size_t)bg * 32 + tid] = Mu;
     a.stats[(size_t)bg * 32 + 16 + tid] = il;
+    for (int s = 0; s < ncu; ++s) fsm[s * 16 + tid] = fast_exp2(sp[s * 32 + tid] - Mu) * il;
   }
   const int jt = (a.T - 1) / 64;
   const int n = a.n;
@@ -168,39 +163,24 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
     return;
   }
   __syncthreads();
-  // per-quarter normalisation factors exp(mref - M) / L
+  // block importance S[j], j <= jt: unit j/128; blocks 8k+8 also take the
+  // carry of chunk k (entry 32k+31), which belongs to unit k/16
   {
-    const float* mr = a.mref + (size_t)bg * a.nq * 16;
-    for (int e4 = tid; e4 < a.nq * 4; e4 += kThreads) {
-      const float4 m4 = ldcg4(mr + 4 * e4);
-      const int h = (4 * e4) & 15;
-      float4 f;
-      f.x = fast_exp2(m4.x - Mh[h + 0]) * iL[h + 0];
-      f.y = fast_exp2(m4.y - Mh[h + 1]) * iL[h + 1];
-      f.z = fast_exp2(m4.z - Mh[h + 2]) * iL[h + 2];
-      f.w = fast_exp2(m4.w - Mh[h + 3]) * iL[h + 3];
-      reinterpret_cast<float4*>(fsm)[e4] = f;
-    }
-  }
-  __syncthreads();
-  // block importance S[j], j <= jt
-  {
-    const float* ub = a.u + (size_t)bg * (4 * a.nq) * 16;
-    const float* cb = a.cc + (size_t)bg * (a.nq + 1) * 16;
+    const float* ub = a.u + (size_t)bg * ncu * 128 * 16;
+    const float* cb = a.cc + (size_t)bg * ncu * 16 * 16;
     for (int j = tid; j <= jt; j += kThreads) {
-      const int qq = j >> 2;
+      float4 v[4];
       float s = 0.f;
-      if (qq < a.nq) {
-        float4 v[4];
+      if (4 * j < a.Nc) {   // block j holds compressed entries (its partials were written)
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[k] = ldcg4(ub + (size_t)j * 16 + 4 * k);
-        s = dot16(fsm + qq * 16, v);
+        s = dot16(fsm + (j >> 7) * 16, v);
       }
-      if ((j & 3) == 0 && qq >= 1 && qq <= a.nq) {
-        float4 v[4];
+      const int ch = (j >> 3) - 1;
+      if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = ldcg4(cb + (size_t)qq * 16 + 4 * k);
-        s += dot16(fsm + (qq - 1) * 16, v);
+        for (int k = 0; k < 4; ++k) v[k] = ldcg4(cb + (size_t)ch * 16 + 4 * k);
+        s += dot16(fsm + (ch >> 4) * 16, v);
       }
       Ssm[j] = s;
     }
@@ -299,14 +279,13 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
 
 // Final combine, run by the last selection CTA of a group:
 //   out = g_cmp * O_cmp + g_slc * O_slc + g_win * O_win
-// with each branch's partials weighted by exp(m_split - M) / L.
+// with each branch's unit partials weighted by exp(m_unit - M) / L.
 template <int DV>
 __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int b = bg / a.G, g = bg % a.G;
   const int NS = a.NS;
-  const int win = a.splits, s0 = a.splits + 1;
-  float* sp = reinterpret_cast<float*>(smem);    // [NS][2][16] partial m, l
+  float* sp = reinterpret_cast<float*>(smem);    // [NS][2][16] unit max, sum
   float* fac = sp + 32 * NS;                     // [NS][16] weight of each partial
   float* gt = fac + 16 * NS;                     // [16][3]
   for (int e = tid; e < NS * 16; e += kThreads) {
@@ -314,11 +293,12 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
     sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
     sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
   }
-  if (tid < 16 && tid < a.hpg) {
-    const __nv_bfloat16* gp = a.gates + ((size_t)b * a.H + g * a.hpg + tid) * 3;
-    gt[tid * 3 + 0] = __bfloat162float(gp[0]);
-    gt[tid * 3 + 1] = __bfloat162float(gp[1]);
-    gt[tid * 3 + 2] = __bfloat162float(gp[2]);
+  if (tid < 16) {
+    const bool hv = tid < a.hpg;
+    const __nv_bfloat16* gp = a.gates + ((size_t)b * a.H + g * a.hpg + (hv ? tid : 0)) * 3;
+    gt[tid * 3 + 0] = hv ? __bfloat162float(gp[0]) : 0.f;
+    gt[tid * 3 + 1] = hv ? __bfloat162float(gp[1]) : 0.f;
+    gt[tid * 3 + 2] = hv ? __bfloat162float(gp[2]) : 0.f;
   }
   __syncthreads();
   if (tid < 16) {
@@ -326,19 +306,19 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
     // compressed: statistics from the selection step, folded with g_cmp
     const float Mc = ldcg_f(a.stats + (size_t)bg * 32 + h);
     const float iLc = ldcg_f(a.stats + (size_t)bg * 32 + 16 + h);
-    const float gc = h < a.hpg ? gt[h * 3 + 0] : 0.f;
-    const float gs = h < a.hpg ? gt[h * 3 + 1] : 0.f;
-    const float gw = h < a.hpg ? gt[h * 3 + 2] : 0.f;
-    for (int s = 0; s < a.splits; ++s) fac[s * 16 + h] = gc * fast_exp2(sp[s * 32 + h] - Mc) * iLc;
-    const float lw = sp[win * 32 + 16 + h];
-    fac[win * 16 + h] = lw > 0.f ? gw / lw : 0.f;
-    float M = -INFINITY;
-    for (int s = s0; s < NS; ++s) M = fmaxf(M, sp[s * 32 + h]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = s0; s < NS; ++s) L += sp[s * 32 + 16 + h] * fast_exp2(sp[s * 32 + h] - Mu);
-    const float il = L > 0.f ? gs / L : 0.f;
-    for (int s = s0; s < NS; ++s) fac[s * 16 + h] = fast_exp2(sp[s * 32 + h] - Mu) * il;
+    for (int s = 0; s < a.ncu; ++s) fac[s * 16 + h] = gt[h * 3 + 0] * fast_exp2(sp[s * 32 + h] - Mc) * iLc;
+    // window and selected: merge their units here
+    auto branch = [&](int s0, int s1, float gate) {
+      float M = -INFINITY;
+      for (int s = s0; s < s1; ++s) M = fmaxf(M, sp[s * 32 + h]);
+      const float Mu = (M == -INFINITY) ? 0.f : M;
+      float L = 0.f;
+      for (int s = s0; s < s1; ++s) L += sp[s * 32 + 16 + h] * fast_exp2(sp[s * 32 + h] - Mu);
+      const float il = L > 0.f ? gate / L : 0.f;
+      for (int s = s0; s < s1; ++s) fac[s * 16 + h] = fast_exp2(sp[s * 32 + h] - Mu) * il;
+    };
+    branch(a.ncu, a.ncu + a.nwu, gt[h * 3 + 2]);
+    branch(a.ncu + a.nwu, NS, gt[h * 3 + 1]);
   }
   __syncthreads();
   const float* po = a.po + (size_t)bg * NS * 16 * DV;
@@ -374,256 +354,326 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
   }
 }
 
+// One unit: up to kPairs pairs of 64-row blocks of one group against the
+// group's query heads.
+//   MODE 0: x < ncu     compressed entries [512x, 512x+512) (limit Nc)
+//           x >= ncu    window tokens win0 + 512(x-ncu) + [0, 512) (limit T)
+//   MODE 1: x           kept blocks idx[8x .. 8x+7] (token rows 64*blk)
 template <int DK, int DV, int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
-    dec_kernel(const __grid_constant__ CUtensorMap mK0, const __grid_constant__ CUtensorMap mV0,
-               const __grid_constant__ CUtensorMap mK1, const __grid_constant__ CUtensorMap mV1,
-               const DecArgs a, uint32_t off_bars) {
-  constexpr int KB = DK / 64, VB = DV / 64;
-  constexpr int kStageBytes = (KB + VB) * kBox;
+    dec_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mK0,
+               const __grid_constant__ CUtensorMap mV0, const __grid_constant__ CUtensorMap mK1,
+               const __grid_constant__ CUtensorMap mV1, const DecArgs a) {
+  constexpr int kcs = DK / 64, vcs = DV / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  DecBars* bars = reinterpret_cast<DecBars*>(smem + off_bars);
+  uint8_t* qbuf = smem;                        // kcs chunks x 2 KB
+  uint8_t* kring = smem + a.off_kring;
+  uint8_t* vring = smem + a.off_vring;
+  uint8_t* pt = smem + a.off_pt;               // P^T: kPairs x 2 chunks x 2 KB
+  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2 max/sum][4 warps][NP]
+  Bars* bars = reinterpret_cast<Bars*>(smem + a.off_bar);
   volatile int* abort_flag = &bars->abort_flag;
   const int x = blockIdx.x, bg = blockIdx.y;
   const int b = bg / a.G, g = bg % a.G;
   const int warp = warp_id(), lane = lane_id();
 
-  // this CTA's tiles: kind 0 compressed entries, 1 window tokens, 2 kept blocks
-  int kind, first, ntiles;
+  // ------------------------------------------------------------ unit geometry
+  const bool cmp_unit = MODE == 0 && x < a.ncu;
+  int base = 0, limit = a.T, npairs = kPairs, sel0 = 0;
   if (MODE == 0) {
-    if (x < a.splits) {
-      kind = 0;
-      first = x * a.tps;
-      ntiles = min(a.tps, a.ntc - first);
+    if (cmp_unit) {
+      base = kUnitKeys * x;
+      limit = a.Nc;
+      npairs = min(kPairs, (a.Nc - base + 127) / 128);
     } else {
-      kind = 1;
-      first = max(0, a.T - a.w);
-      ntiles = (a.T - first + 63) / 64;
+      base = a.win0 + kUnitKeys * (x - a.ncu);
+      limit = a.T;
+      npairs = min(kPairs, (a.T - base + 127) / 128);
     }
   } else {
-    kind = 2;
-    first = x * a.bps;
-    ntiles = min(a.bps, a.n - first);
+    sel0 = 2 * kPairs * x;
+    npairs = min(kPairs, (a.n - sel0 + 1) / 2);
   }
-  const CUtensorMap* mapK = (kind == 1) ? &mK1 : &mK0;
-  const CUtensorMap* mapV = (kind == 1) ? &mV1 : &mV0;
-  const int limit = (kind == 0) ? a.Nc : a.T;
-  auto tile_row = [&](int i) -> int {  // first map row of tile i, -1 = absent
-    if (kind == 0) return 64 * (first + i);
-    if (kind == 1) return first + 64 * i;
-    const int blk = a.idx[(size_t)bg * a.n + first + i];
+  const CUtensorMap* mapK = cmp_unit ? &mK0 : &mK1;
+  const CUtensorMap* mapV = cmp_unit ? &mV0 : &mV1;
+  // first map row of block 2p+hb of this unit; -1 if absent (reads zeros)
+  auto block_row = [&](int p, int hb) -> int {
+    if (MODE == 0) return base + 128 * p + 64 * hb;
+    const int e = sel0 + 2 * p + hb;
+    const int blk = e < a.n ? a.idx[(size_t)bg * a.n + e] : -1;
     return blk >= 0 ? 64 * blk : -1;
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 4);
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < kRingK; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
     }
+    for (int i = 0; i < kRingV; ++i) {
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->wg, 4);
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
     bars->last = 0;
     fence_barrier_init();
   }
+  // query rows hpg..NP-1 are never loaded: keep them finite (zero)
+  for (int i = threadIdx.x; i < kcs * kQBuf / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tmem_s = tmem;                 // kPairs x NP columns
+  const uint32_t tmem_o = tmem + kPairs * NP;   // NP columns
 
-  const int gq = lane >> 2, tq = lane & 3;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[DV / 8][4];
-#pragma unroll
-  for (int i = 0; i < DV / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   bool ok = *abort_flag == 0;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && ok) {
+  if (!ok) {
+    // an earlier CTA failed: do nothing
+  } else if (warp == 4) {
+    // =============================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
       tma_prefetch_desc(mapK);
       tma_prefetch_desc(mapV);
-      int v = 0;
-      for (int i = 0; i < ntiles && ok; ++i) {
-        const int row = tile_row(i);
-        if (row < 0) continue;
-        const int slot = v % kStages;
-        if (!mbar_wait(&bars->empty[slot], (uint32_t)(((v / kStages) & 1) ^ 1), abort_flag, a.st, 401)) {
+      int kv = 0, vv = 0;
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * a.hpg * 128));
+      for (int c = 0; c < kcs; ++c) tma_load_3d(qbuf + c * kQBuf, &mapQ, &bars->q_full, c * 64, g * a.hpg, b);
+      for (int p = 0; p < npairs && ok; ++p) {
+        const int r0 = block_row(p, 0), r1 = block_row(p, 1);
+        for (int c = 0; c < kcs; ++c) {
+          const int slot = kv % kRingK;
+          if (!mbar_wait(&bars->k_empty[slot], (uint32_t)(((kv / kRingK) & 1) ^ 1), abort_flag, a.st, 401)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = kring + slot * kSlotK;
+          mbar_arrive_expect_tx(&bars->k_full[slot], kSlotK);
+          tma_load_3d(dst, mapK, &bars->k_full[slot], c * 64, r0 >= 0 ? r0 : -128, bg);
+          tma_load_3d(dst + 8192, mapK, &bars->k_full[slot], c * 64, r1 >= 0 ? r1 : -128, bg);
+          ++kv;
+        }
+      }
+      for (int p = 0; p < npairs && ok; ++p) {
+        const int r0 = block_row(p, 0), r1 = block_row(p, 1);
+        const int slot = vv % kRingV;
+        if (!mbar_wait(&bars->v_empty[slot], (uint32_t)(((vv / kRingV) & 1) ^ 1), abort_flag, a.st, 402)) {
           ok = false;
           break;
         }
-        uint8_t* dst = smem + slot * kStageBytes;
-        mbar_arrive_expect_tx(&bars->full[slot], kStageBytes);
-#pragma unroll
-        for (int c = 0; c < KB; ++c) tma_load_3d(dst + c * kBox, mapK, &bars->full[slot], c * 64, row, bg);
-#pragma unroll
-        for (int c = 0; c < VB; ++c) tma_load_3d(dst + (KB + c) * kBox, mapV, &bars->full[slot], c * 64, row, bg);
-        ++v;
+        uint8_t* dst = vring + slot * kSlotV;
+        mbar_arrive_expect_tx(&bars->v_full[slot], (uint32_t)(vcs * 16384));
+        for (int c = 0; c < vcs; ++c) {
+          tma_load_3d(dst + c * 16384, mapV, &bars->v_full[slot], c * 64, r0 >= 0 ? r0 : -128, bg);
+          tma_load_3d(dst + c * 16384 + 8192, mapV, &bars->v_full[slot], c * 64, r1 >= 0 ? r1 : -128, bg);
+        }
+        ++vv;
       }
       if (!ok || *abort_flag) {
-        for (int y = (v > kStages ? v - kStages : 0); y < v; ++y)
-          mbar_wait_plain(&bars->full[y % kStages], (uint32_t)((y / kStages) & 1), kWaitLimitNs);
+        mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
+        for (int y = (kv > kRingK ? kv - kRingK : 0); y < kv; ++y)
+          mbar_wait_plain(&bars->k_full[y % kRingK], (uint32_t)((y / kRingK) & 1), kWaitLimitNs);
+        for (int y = (vv > kRingV ? vv - kRingV : 0); y < vv; ++y)
+          mbar_wait_plain(&bars->v_full[y % kRingV], (uint32_t)((y / kRingV) & 1), kWaitLimitNs);
       }
     }
-  } else if (ok) {
-    // ------------------------------------------------------------ compute warps
-    uint32_t qa[DK / 16][4];
-    {
-      const __nv_bfloat16* qb = a.q + ((size_t)b * a.H + (size_t)g * a.hpg) * DK;
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int row = gq + 8 * hf;
-          uint32_t lo = 0, hi = 0;
-          if (row < a.hpg) {
-            lo = *reinterpret_cast<const uint32_t*>(qb + (size_t)row * DK + 16 * ks + 2 * tq);
-            hi = *reinterpret_cast<const uint32_t*>(qb + (size_t)row * DK + 16 * ks + 8 + 2 * tq);
+  } else if (warp == 5) {
+    // =============================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, NP, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, NP, true, false);
+      const uint32_t q_a = smem_u32(qbuf), k_a = smem_u32(kring), v_a = smem_u32(vring), p_a = smem_u32(pt);
+      int kv = 0, vv = 0;
+      if (!mbar_wait(&bars->q_full, 0, abort_flag, a.st, 411)) ok = false;
+      tc_fence_after();
+      for (int p = 0; p < npairs && ok; ++p) {
+        for (int c = 0; c < kcs; ++c) {
+          const int slot = kv % kRingK;
+          if (!mbar_wait(&bars->k_full[slot], (uint32_t)((kv / kRingK) & 1), abort_flag, a.st, 412)) {
+            ok = false;
+            break;
           }
-          qa[ks][hf] = lo;
-          qa[ks][2 + hf] = hi;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = sdesc_sw128(k_a + slot * kSlotK + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(q_a + c * kQBuf + k * 32, 16, 1024);
+            umma_bf16(tmem_s + p * NP, ad, bd, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars->k_empty[slot]);
+          ++kv;
         }
+      }
+      if (ok) umma_commit(&bars->s_full);
+      if (ok && !mbar_wait(&bars->p_full, 0, abort_flag, a.st, 413)) ok = false;
+      tc_fence_after();
+      for (int p = 0; p < npairs && ok; ++p) {
+        const int slot = vv % kRingV;
+        if (!mbar_wait(&bars->v_full[slot], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 414)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          // A = V^T (dv-major rows of keys), B = P^T (head rows, keys along K)
+          const uint64_t ad = sdesc_sw128(v_a + slot * kSlotV + k * 2048, 16384, 1024);
+          const uint64_t bd = sdesc_sw128(p_a + (p * 2 + (k >> 2)) * kQBuf + (k & 3) * 32, 16, 1024);
+          umma_bf16(tmem_o, ad, bd, idesc_pv, (p > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars->v_empty[slot]);
+        ++vv;
+      }
+      if (ok) umma_commit(&bars->o_full);
+      if (!ok || *abort_flag) {
+        umma_commit(&bars->drain);
+        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
       }
     }
-    const int r0 = warp * 16;
-    int v = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int row = tile_row(i);
-      if (row < 0) continue;
-      const int slot = v % kStages;
-      if (!mbar_wait(&bars->full[slot], (uint32_t)((v / kStages) & 1), abort_flag, a.st, 402)) {
-        ok = false;
-        break;
-      }
-      const uint32_t kbase = smem_u32(smem + slot * kStageBytes);
-      const uint32_t vbase = kbase + KB * kBox;
-      float s[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        const int rr = r0 + (lane & 7) + ((lane >> 4) << 3);
-        const int unit = (ks & 3) * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sw128_addr(kbase + (ks >> 2) * kBox, rr, unit), b0, b1, b2, b3);
-        mma_16816(s[0], qa[ks], b0, b1);
-        mma_16816(s[1], qa[ks], b2, b3);
-      }
-      // mask + online softmax (rows gq and gq+8 = two heads)
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool valid = row + r0 + 8 * nt + 2 * tq + e < limit;
-          s[nt][e] = valid ? s[nt][e] * a.sc2 : -INFINITY;
-          s[nt][2 + e] = valid ? s[nt][2 + e] * a.sc2 : -INFINITY;
-          mx0 = fmaxf(mx0, s[nt][e]);
-          mx1 = fmaxf(mx1, s[nt][2 + e]);
-        }
-      mx0 = quad_max(mx0);
-      mx1 = quad_max(mx1);
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float us0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float us1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float al0 = fast_exp2(m0 - us0), al1 = fast_exp2(m1 - us1);
-      float p[2][4];
-      float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          p[nt][e] = fast_exp2(s[nt][e] - us0);
-          p[nt][2 + e] = fast_exp2(s[nt][2 + e] - us1);
-          rs0 += p[nt][e];
-          rs1 += p[nt][2 + e];
-        }
-      l0 = l0 * al0 + rs0;
-      l1 = l1 * al1 + rs1;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int k = 0; k < DV / 8; ++k) {
-        o[k][0] *= al0;
-        o[k][1] *= al0;
-        o[k][2] *= al1;
-        o[k][3] *= al1;
-      }
-      if (MODE == 0 && kind == 0) {
-        const int qd = 4 * (first + i) + warp;
-        if (qd < a.nq) {
-          block_partials(p, 0, gq, qd, mn0, tq, bg, a);
-          block_partials(p, 2, gq + 8, qd, mn1, tq, bg, a);
-        }
-      }
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(p[0][0], p[0][1]);
-      pa[1] = pack_bf16x2(p[0][2], p[0][3]);
-      pa[2] = pack_bf16x2(p[1][0], p[1][1]);
-      pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-#pragma unroll
-      for (int np = 0; np < DV / 16; ++np) {
-        const int rr = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int unit = (np & 3) * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sw128_addr(vbase + (np >> 2) * kBox, rr, unit), b0, b1, b2, b3);
-        mma_16816(o[2 * np], pa, b0, b1);
-        mma_16816(o[2 * np + 1], pa, b2, b3);
-      }
+  } else {
+    // =============================================================== softmax (warps 0-3)
+    const int r = warp * 32 + lane;       // TMEM lane: key of a pair / value dim
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const bool hi_half = (r >> 6) != 0;
+    const int kk = r & 63;
+    float* red_m = red;                    // [4][NP]
+    float* red_l = red + 4 * NP;           // [4][NP]
+    uint32_t wg_phase = 0;
+    auto wg_sync = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[slot]);
-      ++v;
+      if (lane == 0) mbar_arrive(&bars->wg);
+      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 421)) ok = false;
+      ++wg_phase;
+    };
+    // first map row of this lane's block in each pair (-1 if absent)
+    int rows[kPairs];
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) rows[p] = p < npairs ? block_row(p, hi_half ? 1 : 0) : -1;
+    if (!mbar_wait(&bars->s_full, 0, abort_flag, a.st, 422)) ok = false;
+    tc_fence_after();
+    // pass 1: per-head max of the raw scores over the valid keys
+    float mrow[NP];
+#pragma unroll
+    for (int h = 0; h < NP; ++h) mrow[h] = -INFINITY;
+    if (ok) {
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        if (p < npairs) {
+          uint32_t rr[16];
+          tmem_ld16(tmem_s + lane_base + p * NP, rr);
+          tmem_ld_wait(rr);
+          const bool v = rows[p] >= 0 && rows[p] + kk < limit;
+#pragma unroll
+          for (int h = 0; h < NP; ++h) mrow[h] = fmaxf(mrow[h], v ? __uint_as_float(rr[h]) : -INFINITY);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < NP; ++h) mrow[h] = warp_max_f32(mrow[h]);
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < NP; ++h) red_m[warp * NP + h] = mrow[h];
     }
-    l0 = quad_sum(l0);
-    l1 = quad_sum(l1);
+    wg_sync();
+    float mu[NP];
+#pragma unroll
+    for (int h = 0; h < NP; ++h) {
+      const float m = fmaxf(fmaxf(red_m[h], red_m[NP + h]), fmaxf(red_m[2 * NP + h], red_m[3 * NP + h]));
+      mrow[h] = (m == -INFINITY) ? -INFINITY : m * a.sc2;
+      mu[h] = (m == -INFINITY) ? 0.f : m * a.sc2;
+    }
+    // pass 2: p = exp(s*scale - max), sums, P^T, block-score partials
+    float lrow[NP];
+#pragma unroll
+    for (int h = 0; h < NP; ++h) lrow[h] = 0.f;
+    if (ok) {
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        if (p < npairs) {
+          uint32_t rr[16];
+          tmem_ld16(tmem_s + lane_base + p * NP, rr);
+          tmem_ld_wait(rr);
+          const bool v = rows[p] >= 0 && rows[p] + kk < limit;
+          float e[NP];
+          uint8_t* chunk = pt + (p * 2 + (hi_half ? 1 : 0)) * kQBuf + (kk & 7) * 2;
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            e[h] = v ? fast_exp2(fmaf(__uint_as_float(rr[h]), a.sc2, -mu[h])) : 0.f;
+            lrow[h] += e[h];
+            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, kk >> 3)) = __float2bfloat16_rn(e[h]);
+          }
+          if (cmp_unit) {
+            // entries 4q..4q+3 of this warp's 32 feed block (entry/4) with
+            // 2*sum - last + last of the previous group; the warp's last entry
+            // carries one chunk into the block of the next 32 entries
+            float uq[NP];
+#pragma unroll
+            for (int h = 0; h < NP; ++h) {
+              float gsum = e[h] + __shfl_xor_sync(0xffffffffu, e[h], 1);
+              gsum += __shfl_xor_sync(0xffffffffu, gsum, 2);
+              const float last = __shfl_sync(0xffffffffu, e[h], lane | 3);
+              const float prev = __shfl_up_sync(0xffffffffu, last, 4);
+              uq[h] = 2.f * gsum - last + (lane >= 4 ? prev : 0.f);
+            }
+            const int entry0 = base + 128 * p + 32 * warp;   // first entry of this warp
+            if ((lane & 3) == 0) {
+              float4* dst =
+                  reinterpret_cast<float4*>(a.u + ((size_t)bg * a.ncu * 128 + (entry0 + lane) / 4) * 16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_float4(uq[4 * k], uq[4 * k + 1], uq[4 * k + 2], uq[4 * k + 3]);
+            }
+            if (lane == 31) {
+              float4* dst = reinterpret_cast<float4*>(a.cc + ((size_t)bg * a.ncu * 16 + entry0 / 32) * 16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = make_float4(e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
+            }
+          }
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_full);
+    // sums per head over the unit
+    const float ws = warp_sum16(lrow, lane);
+    if ((lane & 1) == 0) red_l[warp * NP + head_of_lane(lane)] = ws;
+    wg_sync();
+    // unit partial: max, sum, unnormalised O^T (lane = value dim)
+    const int slot_id = (MODE == 0) ? x : (a.ncu + a.nwu + x);
+    const size_t pbase = (size_t)bg * a.NS + slot_id;
+    if (ok && r < NP) {
+      a.pm[pbase * 16 + r] = mrow[r];
+      a.pl[pbase * 16 + r] = red_l[r] + red_l[NP + r] + red_l[2 * NP + r] + red_l[3 * NP + r];
+    }
+    if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 423)) {
+      tc_fence_after();
+      uint32_t rr[16];
+      tmem_ld16(tmem_o + lane_base, rr);
+      tmem_ld_wait(rr);
+      if (r < DV) {
+        float* dst = a.po + pbase * 16 * DV + r;
+#pragma unroll
+        for (int h = 0; h < NP; ++h) dst[(size_t)h * DV] = __uint_as_float(rr[h]);
+      }
+    }
   }
-
-  // ---------------------------------------------------------------- merge the 4 warps
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
   if (*abort_flag) return;
-  float* mw = reinterpret_cast<float*>(smem);   // [4][16]
-  float* lw = mw + 64;                          // [4][16]
-  float* fw = lw + 64;                          // [4][16]
-  float* ow = fw + 64;                          // [4][16][DV]
-  if (warp < 4) {
-    if (tq == 0) {
-      mw[warp * 16 + gq] = m0;
-      mw[warp * 16 + gq + 8] = m1;
-      lw[warp * 16 + gq] = l0;
-      lw[warp * 16 + gq + 8] = l1;
-    }
-#pragma unroll
-    for (int k = 0; k < DV / 8; ++k) {
-      float* r = ow + (size_t)(warp * 16 + gq) * DV + 8 * k + 2 * tq;
-      r[0] = o[k][0];
-      r[1] = o[k][1];
-      r[8 * DV] = o[k][2];
-      r[8 * DV + 1] = o[k][3];
-    }
-  }
-  __syncthreads();
-  const int slot_id = (MODE == 0) ? x : (a.splits + 1 + x);
-  const size_t pbase = (size_t)bg * a.NS + slot_id;
-  if (threadIdx.x < 16) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * 16 + h]);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float f = fast_exp2(mw[w * 16 + h] - Mu);
-      fw[w * 16 + h] = f;
-      L += lw[w * 16 + h] * f;
-    }
-    a.pm[pbase * 16 + h] = M;
-    a.pl[pbase * 16 + h] = L;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < 16 * DV; e += kThreads) {
-    const int h = e / DV;
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) acc += fw[w * 16 + h] * ow[(size_t)w * 16 * DV + e];
-    a.po[pbase * 16 * DV + e] = acc;
-  }
 
   // ---------------------------------------------------------------- last CTA of the group
   __threadfence();
@@ -642,25 +692,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ------------------------------------------------------------------ host side
-struct DecWs {
-  size_t cnt, pm, pl, po, u, cc, mref, stats, idx, end;
-};
-
 struct DecShape {
-  int Nc, nq, ntc, splits, sel_splits, NS, BG;
+  int Nc, ncu, nwu, nsu, NS, BG, win0, win_len;
 };
 
 DecShape dec_shape(const nsa_cfg& c) {
   DecShape s;
   s.Nc = c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
-  s.nq = (s.Nc + 15) / 16;
-  s.ntc = (s.Nc + 63) / 64;
-  s.splits = (s.ntc + kTilesPerSplit - 1) / kTilesPerSplit;
-  s.sel_splits = (c.n + kBlocksPerSelCta - 1) / kBlocksPerSelCta;
-  s.NS = s.splits + 1 + s.sel_splits;
+  s.ncu = (s.Nc + kUnitKeys - 1) / kUnitKeys;
+  s.win_len = c.w < c.T ? c.w : c.T;
+  s.win0 = c.T - s.win_len;
+  s.nwu = (s.win_len + kUnitKeys - 1) / kUnitKeys;
+  s.nsu = (c.n + 2 * kPairs - 1) / (2 * kPairs);
+  s.NS = s.ncu + s.nwu + s.nsu;
   s.BG = c.B * c.G;
   return s;
 }
+
+struct DecWs {
+  size_t cnt, pm, pl, po, u, cc, stats, idx, end;
+};
 
 DecWs dec_ws(const nsa_cfg& c) {
   const DecShape s = dec_shape(c);
@@ -671,38 +722,40 @@ DecWs dec_ws(const nsa_cfg& c) {
   w.pl = align_up(w.pm + sizeof(float) * BG * s.NS * 16, 256);
   w.po = align_up(w.pl + sizeof(float) * BG * s.NS * 16, 256);
   w.u = align_up(w.po + sizeof(float) * BG * s.NS * 16 * c.dv, 256);
-  w.cc = align_up(w.u + sizeof(float) * BG * 16 * 4 * (size_t)s.nq, 256);
-  w.mref = align_up(w.cc + sizeof(float) * BG * 16 * (size_t)(s.nq + 1), 256);
-  w.stats = align_up(w.mref + sizeof(float) * BG * (size_t)s.nq * 16, 256);
+  w.cc = align_up(w.u + sizeof(float) * BG * (size_t)s.ncu * 128 * 16, 256);
+  w.stats = align_up(w.cc + sizeof(float) * BG * (size_t)s.ncu * 16 * 16, 256);
   w.idx = align_up(w.stats + sizeof(float) * BG * 32, 256);
   w.end = align_up(w.idx + sizeof(int32_t) * BG * c.n, 256);
   return w;
 }
 
-struct DecSmem {
-  uint32_t off_bars, total;
+struct DecLayout {
+  uint32_t off_kring, off_vring, off_pt, off_red, off_bar, total;
 };
 
-DecSmem dec_smem(const nsa_cfg& c) {
+DecLayout dec_layout(const nsa_cfg& c) {
   const DecShape s = dec_shape(c);
-  const size_t ring = (size_t)kStages * (c.dk / 64 + c.dv / 64) * kBox;
-  const size_t merge = sizeof(float) * (3 * 64 + 4 * 16 * (size_t)c.dv);
+  DecLayout L;
+  L.off_kring = (uint32_t)align_up((size_t)(c.dk / 64) * kQBuf, 1024);
+  L.off_vring = L.off_kring + kRingK * kSlotK;
+  L.off_pt = L.off_vring + kRingV * kSlotV;
+  L.off_red = L.off_pt + kPBuf;
+  const size_t body = L.off_red + 2 * 4 * NP * sizeof(float);
+  // the last-CTA steps reuse the start of shared memory
   const size_t jt1 = (size_t)(c.T - 1) / 64 + 1;
-  const size_t select = sizeof(float) * (32 + 256 + 32 * (size_t)s.splits + 16 * (size_t)s.nq + jt1);
+  const size_t select = sizeof(float) * (32 + 256 + 48 * (size_t)s.ncu + jt1);
   const size_t combine = sizeof(float) * (48 * (size_t)s.NS + 48);
-  size_t body = ring;
-  if (merge > body) body = merge;
-  if (select > body) body = select;
-  if (combine > body) body = combine;
-  DecSmem m;
-  m.off_bars = (uint32_t)align_up(body, 256);
-  m.total = m.off_bars + (uint32_t)align_up(sizeof(DecBars), 256) + 1024;
-  return m;
+  size_t end = body;
+  if (select > end) end = select;
+  if (combine > end) end = combine;
+  L.off_bar = (uint32_t)align_up(end, 256);
+  L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;
+  return L;
 }
 
 template <int DK, int DV, int MODE>
-int launch_one(const DecArgs& a, dim3 grid, const CUtensorMap* maps, uint32_t off_bars, uint32_t smem,
-               cudaStream_t s, const char* name) {
+int launch_one(const DecArgs& a, dim3 grid, const CUtensorMap* maps, uint32_t smem, cudaStream_t s,
+               const char* name) {
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(dec_kernel<DK, DV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -711,28 +764,27 @@ int launch_one(const DecArgs& a, dim3 grid, const CUtensorMap* maps, uint32_t of
     attr = true;
   }
   prof::begin(name, s);
-  dec_kernel<DK, DV, MODE><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], a, off_bars);
+  dec_kernel<DK, DV, MODE><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
 template <int DK, int DV>
-int launch_dims(const DecArgs& a, const DecShape& sh, const CUtensorMap* maps_cmp, const CUtensorMap* maps_sel,
-                const DecSmem& m, cudaStream_t s) {
-  int rc = launch_one<DK, DV, 0>(a, dim3(sh.splits + 1, sh.BG), maps_cmp, m.off_bars, m.total, s, "dec_cmp_win");
+int launch_dims(const DecArgs& a, const DecShape& sh, const CUtensorMap* maps, uint32_t smem, cudaStream_t s) {
+  int rc = launch_one<DK, DV, 0>(a, dim3(sh.ncu + sh.nwu, sh.BG), maps, smem, s, "dec_cmp_win");
   if (rc != NSA_OK) return rc;
-  return launch_one<DK, DV, 1>(a, dim3(sh.sel_splits, sh.BG), maps_sel, m.off_bars, m.total, s, "dec_sel");
+  return launch_one<DK, DV, 1>(a, dim3(sh.nsu, sh.BG), maps, smem, s, "dec_sel");
 }
 
 }  // namespace
 
 int decode_supported(const nsa_cfg& c) {
   const int hpg = c.H / c.G;
-  if (hpg > 16) return NSA_ERR_UNSUPPORTED;
+  if (hpg > NP) return NSA_ERR_UNSUPPORTED;
   if (c.dk != 64 && c.dk != 128 && c.dk != 192 && c.dk != 256) return NSA_ERR_UNSUPPORTED;
   if (c.dv != 64 && c.dv != 128) return NSA_ERR_UNSUPPORTED;
   if ((size_t)c.B * c.G > 65535) return NSA_ERR_UNSUPPORTED;
-  if (dec_smem(c).total > smem_max()) return NSA_ERR_UNSUPPORTED;
+  if (dec_layout(c).total > smem_max()) return NSA_ERR_UNSUPPORTED;
   return NSA_OK;
 }
 
@@ -744,10 +796,10 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
                   const void* vc, const void* gates, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s) {
   const DecShape sh = dec_shape(c);
   const DecWs w = dec_ws(c);
-  const DecSmem m = dec_smem(c);
+  const DecLayout L = dec_layout(c);
   const uint64_t e = 2;
   const uint64_t BG = (uint64_t)sh.BG;
-  CUtensorMap maps_cmp[4], maps_sel[4];
+  CUtensorMap maps[5];
   const int Ncm = sh.Nc > 0 ? sh.Nc : 1;
   auto map3 = [&](CUtensorMap* mp, const void* base, int d, uint64_t rows) -> bool {
     const uint64_t dims[3] = {(uint64_t)d, rows, BG};
@@ -755,14 +807,16 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
     const uint32_t box[3] = {64, 64, 1};
     return make_tmap_bf16(mp, base, 3, dims, str, box);
   };
-  if (!map3(&maps_cmp[0], sh.Nc > 0 ? kc : kcache, c.dk, (uint64_t)Ncm)) return NSA_ERR_CUDA;
-  if (!map3(&maps_cmp[1], sh.Nc > 0 ? vc : vcache, c.dv, (uint64_t)Ncm)) return NSA_ERR_CUDA;
-  if (!map3(&maps_cmp[2], kcache, c.dk, (uint64_t)c.T)) return NSA_ERR_CUDA;
-  if (!map3(&maps_cmp[3], vcache, c.dv, (uint64_t)c.T)) return NSA_ERR_CUDA;
-  maps_sel[0] = maps_cmp[2];
-  maps_sel[1] = maps_cmp[3];
-  maps_sel[2] = maps_cmp[2];
-  maps_sel[3] = maps_cmp[3];
+  {  // q [B,H,dk]: box (64 columns, hpg heads, 1)
+    const uint64_t dims[3] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)c.B};
+    const uint64_t str[2] = {(uint64_t)c.dk * e, (uint64_t)c.H * c.dk * e};
+    const uint32_t box[3] = {64, (uint32_t)(c.H / c.G), 1};
+    if (!make_tmap_bf16(&maps[0], q, 3, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  if (!map3(&maps[1], sh.Nc > 0 ? kc : kcache, c.dk, (uint64_t)Ncm)) return NSA_ERR_CUDA;
+  if (!map3(&maps[2], sh.Nc > 0 ? vc : vcache, c.dv, (uint64_t)Ncm)) return NSA_ERR_CUDA;
+  if (!map3(&maps[3], kcache, c.dk, (uint64_t)c.T)) return NSA_ERR_CUDA;
+  if (!map3(&maps[4], vcache, c.dv, (uint64_t)c.T)) return NSA_ERR_CUDA;
 
   DecArgs a;
   a.B = c.B;
@@ -774,16 +828,14 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
   a.n = c.n;
   a.w = c.w;
   a.Nc = sh.Nc;
-  a.nq = sh.nq;
-  a.ntc = sh.ntc;
-  a.splits = sh.splits;
-  a.tps = kTilesPerSplit;
-  a.sel_splits = sh.sel_splits;
-  a.bps = kBlocksPerSelCta;
+  a.ncu = sh.ncu;
+  a.nwu = sh.nwu;
+  a.nsu = sh.nsu;
   a.NS = sh.NS;
+  a.win0 = sh.win0;
+  a.win_len = sh.win_len;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
-  a.q = static_cast<const __nv_bfloat16*>(q);
   a.gates = static_cast<const __nv_bfloat16*>(gates);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.idx_out = idx_out;
@@ -792,14 +844,18 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
   a.po = reinterpret_cast<float*>(ws + w.po);
   a.u = reinterpret_cast<float*>(ws + w.u);
   a.cc = reinterpret_cast<float*>(ws + w.cc);
-  a.mref = reinterpret_cast<float*>(ws + w.mref);
   a.stats = reinterpret_cast<float*>(ws + w.stats);
   a.idx = reinterpret_cast<int32_t*>(ws + w.idx);
   a.cnt = reinterpret_cast<int*>(ws + w.cnt);
   a.st = reinterpret_cast<DeviceStatus*>(ws);
+  a.off_kring = L.off_kring;
+  a.off_vring = L.off_vring;
+  a.off_pt = L.off_pt;
+  a.off_red = L.off_red;
+  a.off_bar = L.off_bar;
 
 #define NSA_DEC_CASE(DK_, DV_) \
-  if (c.dk == DK_ && c.dv == DV_) return launch_dims<DK_, DV_>(a, sh, maps_cmp, maps_sel, m, s);
+  if (c.dk == DK_ && c.dv == DV_) return launch_dims<DK_, DV_>(a, sh, maps, L.total, s);
   NSA_DEC_CASE(64, 64)
   NSA_DEC_CASE(64, 128)
   NSA_DEC_CASE(128, 64)
