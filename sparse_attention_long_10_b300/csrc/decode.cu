@@ -168,21 +168,30 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   {
     const float* ub = a.u + (size_t)bg * ncu * 128 * 16;
     const float* cb = a.cc + (size_t)bg * ncu * 16 * 16;
-    for (int j = tid; j <= jt; j += kThreads) {
-      float4 v[4];
-      float s = 0.f;
-      if (4 * j < a.Nc) {   // block j holds compressed entries (its partials were written)
+    // four blocks per thread per round, all their loads issued before use
+    for (int j0 = tid; j0 <= jt; j0 += 4 * kThreads) {
+      float4 v[4][4], w[4][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = ldcg4(ub + (size_t)j * 16 + 4 * k);
-        s = dot16(fsm + (j >> 7) * 16, v);
-      }
-      const int ch = (j >> 3) - 1;
-      if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) {
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q * kThreads;
+        const int ch = (j >> 3) - 1;
+        const bool hu = j <= jt && 4 * j < a.Nc;   // block j holds compressed entries
+        const bool hc = j <= jt && (j & 7) == 0 && j >= 8 && 32 * ch < a.Nc;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = ldcg4(cb + (size_t)ch * 16 + 4 * k);
-        s += dot16(fsm + (ch >> 4) * 16, v);
+        for (int k = 0; k < 4; ++k) {
+          v[q][k] = hu ? ldcg4(ub + (size_t)j * 16 + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+          w[q][k] = hc ? ldcg4(cb + (size_t)ch * 16 + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-      Ssm[j] = s;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = j0 + q * kThreads;
+        if (j > jt) continue;
+        const int ch = (j >> 3) - 1;
+        float s = (4 * j < a.Nc) ? dot16(fsm + (j >> 7) * 16, v[q]) : 0.f;
+        if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) s += dot16(fsm + (ch >> 4) * 16, w[q]);
+        Ssm[j] = s;
+      }
     }
   }
   __syncthreads();
@@ -325,27 +334,20 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
   for (int e4 = tid; e4 < a.hpg * DV / 4; e4 += kThreads) {
     const int h = (4 * e4) / DV;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 4 <= NS; s += 4) {
-      float4 v[4];
+    // up to 16 partials per round, all loads issued before use
+    for (int s0 = 0; s0 < NS; s0 += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = ldcg4(po + ((size_t)(s + k) * 16) * DV + 4 * e4);
+      for (int k = 0; k < 16; ++k)
+        v[k] = s0 + k < NS ? ldcg4(po + ((size_t)(s0 + k) * 16) * DV + 4 * e4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float f = fac[(s + k) * 16 + h];
+      for (int k = 0; k < 16; ++k) {
+        const float f = s0 + k < NS ? fac[(s0 + k) * 16 + h] : 0.f;
         acc.x += f * v[k].x;
         acc.y += f * v[k].y;
         acc.z += f * v[k].z;
         acc.w += f * v[k].w;
       }
-    }
-    for (; s < NS; ++s) {
-      const float4 v = ldcg4(po + ((size_t)s * 16) * DV + 4 * e4);
-      const float f = fac[s * 16 + h];
-      acc.x += f * v.x;
-      acc.y += f * v.y;
-      acc.z += f * v.z;
-      acc.w += f * v.w;
     }
     uint2 pk;
     pk.x = pack_bf16x2(acc.x, acc.y);
