@@ -15,9 +15,12 @@
 //
 // Rows of the MMA are (query, head) pairs of ONE GQA group: 128/HPG queries x
 // HPG heads share every K/V tile (group-centric loading).  Warp roles:
-//   warps 0-3  softmax / scores / top-k (thread = one row = one TMEM lane)
-//   warp  4    TMA producer (Q once, then a ring of 16 KB K/V chunks)
-//   warp  5    tcgen05 MMA issuer (single thread)
+//   warps 0-3, 4-7  softmax / scores / top-k; thread = one row (TMEM lane),
+//                   warpgroup 0 takes key columns 0-63 of every S tile,
+//                   warpgroup 1 columns 64-127 (per-row max/sum are merged
+//                   between the two at the end of a statistics pass)
+//   warp  8         TMA producer (Q once, then a ring of 16 KB K/V chunks)
+//   warp  9         tcgen05 MMA issuer (single thread)
 // TMEM: S double buffer (2 x 128 columns) + O (dv columns).
 #include "common.cuh"
 #include "kernels.hpp"
@@ -30,7 +33,7 @@ namespace {
 
 constexpr int kRing = 6;
 constexpr int kSlot = 16384;   // 128 rows x 128 bytes
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
 
 struct CmpWinArgs {
@@ -40,7 +43,7 @@ struct CmpWinArgs {
   __nv_bfloat16* part;             // [B,T,H,dv]
   int32_t* idx;                    // [B,T,G,n]
   DeviceStatus* st;
-  uint32_t off_ring, off_p, off_scores, off_bar;
+  uint32_t off_ring, off_p, off_scores, off_red, off_bar;
 };
 
 struct Bars {
@@ -52,7 +55,7 @@ struct Bars {
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
-  uint64_t wg;          // softmax-warpgroup rendezvous (count 4)
+  uint64_t all8;        // rendezvous of the 8 softmax warps
   uint32_t tmem;
   int abort_flag;
 };
@@ -68,13 +71,13 @@ __device__ __forceinline__ int visible_cmp(int t, int Nc) {
   return nv < Nc ? nv : Nc;
 }
 
-// Butterfly reduce-scatter of 32 values over groups of HPG lanes (HPG <= 32):
-// afterwards lane holds 32/HPG group sums in v[0..], original indices base+k.
+// Butterfly reduce-scatter of 16 values over groups of HPG lanes (HPG <= 16):
+// afterwards lane holds 16/HPG group sums in v[0..], original indices base+k.
 template <int HPG>
-__device__ __forceinline__ int reduce_scatter32(float (&v)[33], int lane) {
+__device__ __forceinline__ int reduce_scatter16(float (&v)[16], int lane) {
   int base = 0;
 #pragma unroll
-  for (int m = HPG / 2, n = 16; m >= 1; m >>= 1, n >>= 1) {
+  for (int m = HPG / 2, n = 8; m >= 1; m >>= 1, n >>= 1) {
     const bool up = (lane & m) != 0;
 #pragma unroll
     for (int k = 0; k < n; ++k) {
@@ -94,21 +97,33 @@ __device__ __forceinline__ float allreduce_group(float x) {
   return x;
 }
 
-// Write one row's 128 bf16 probabilities into the 128B-swizzled K-major P tile.
-__device__ __forceinline__ void store_p_row(uint8_t* ps, int r, const float (&p)[kTile], float gate) {
+// Write 64 bf16 probabilities of one row (keys 64*half .. 64*half+63) into the
+// 128B-swizzled K-major P tile.
+__device__ __forceinline__ void store_p_half(uint8_t* ps, int r, int half, const float (&p)[64], float gate) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const int i = q * 64 + cc * 8;
-      uint4 pk;
-      pk.x = pack_bf16x2(p[i + 0] * gate, p[i + 1] * gate);
-      pk.y = pack_bf16x2(p[i + 2] * gate, p[i + 3] * gate);
-      pk.z = pack_bf16x2(p[i + 4] * gate, p[i + 5] * gate);
-      pk.w = pack_bf16x2(p[i + 6] * gate, p[i + 7] * gate);
-      *reinterpret_cast<uint4*>(ps + q * kSlot + sw128_offset(r, cc)) = pk;
-    }
+  for (int cc = 0; cc < 8; ++cc) {
+    const int i = cc * 8;
+    uint4 pk;
+    pk.x = pack_bf16x2(p[i + 0] * gate, p[i + 1] * gate);
+    pk.y = pack_bf16x2(p[i + 2] * gate, p[i + 3] * gate);
+    pk.z = pack_bf16x2(p[i + 4] * gate, p[i + 5] * gate);
+    pk.w = pack_bf16x2(p[i + 6] * gate, p[i + 7] * gate);
+    *reinterpret_cast<uint4*>(ps + half * kSlot + sw128_offset(r, cc)) = pk;
   }
+}
+
+// 64 consecutive fp32 columns of one TMEM lane (four loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t rs[4][16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld16(taddr + c * 16, rs[c]);
+  tmem_ld_wait(rs[0]);
+#pragma unroll
+  for (int c = 1; c < 4; ++c) tmem_reg_fence(rs[c]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rs[c][i]);
 }
 
 template <int HPG>
@@ -149,12 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 4);
+      mbar_init(&bars->s_free[s], 8);
     }
-    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_full, 8);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->wg, 4);
+    mbar_init(&bars->all8, 8);
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
   }
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (*abort_flag) {
     // an earlier CTA failed: do nothing
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // =============================================================== producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
@@ -221,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_plain(&bars->ring_full[x % kRing], (uint32_t)((x / kRing) & 1), kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // =============================================================== MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false, false);
@@ -312,9 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&bars->o_full);
       if (!ok || *abort_flag) mbar_wait_plain(&bars->o_full, 0, kWaitLimitNs);
     }
-  } else {
-    // =============================================================== softmax warpgroup
-    const int r = threadIdx.x;               // row = TMEM lane
+  } else if (warp < 8) {
+    // =============================================================== softmax warpgroups
+    const int wg = warp >> 2;                // key columns 64*wg .. 64*wg+63 of every tile
+    const int lw = warp & 3;
+    const int r = lw * 32 + lane;            // row = TMEM lane
     const int qi = r / HPG;
     const int h = r % HPG;
     const int t = t0 + qi;
@@ -327,112 +344,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       g_c = __bfloat162float(gp[0]);
       g_w = __bfloat162float(gp[2]);
     }
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
+    const int c0 = 64 * wg;                  // first column of this warpgroup
+    float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2 wg][2 m/l][128 rows]
     bool ok = true;
     int u = 0, pv = 0;
-    uint32_t wg_phase = 0;
+    uint32_t all_phase = 0;
 
-    auto wg_sync = [&]() {
+    auto sync8 = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->wg);
-      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 221)) ok = false;
-      ++wg_phase;
+      if (lane == 0) mbar_arrive(&bars->all8);
+      if (!mbar_wait(&bars->all8, all_phase & 1, abort_flag, a.st, 221)) ok = false;
+      ++all_phase;
     };
-    // loads the next S tile (128 fp32 per row) and releases its TMEM buffer
-    auto consume_s = [&](float (&x)[kTile]) -> bool {
+    // loads this warpgroup's 64 columns of the next S tile and releases it
+    auto consume_s = [&](float (&x)[64]) -> bool {
       const int sb = u & 1;
       const uint32_t use = (uint32_t)(u >> 1);
       ++u;
       if (!mbar_wait(&bars->s_full[sb], use & 1, abort_flag, a.st, 222)) return false;
       tc_fence_after();
-      uint32_t rs[kTile / 16][16];
-#pragma unroll
-      for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem_s + lane_base + sb * kTile + c * 16, rs[c]);
-      tmem_ld_wait(rs[0]);
-#pragma unroll
-      for (int c = 1; c < kTile / 16; ++c) tmem_reg_fence(rs[c]);
-#pragma unroll
-      for (int c = 0; c < kTile / 16; ++c)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rs[c][i]);
+      tmem_ld64(tmem_s + lane_base + sb * kTile + c0, x);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free[sb]);
       return true;
     };
-    auto put_p = [&](const float (&p)[kTile], float gate) -> bool {
+    auto put_p = [&](const float (&p)[64], float gate) -> bool {
       if (!mbar_wait(&bars->p_free, (uint32_t)((pv & 1) ^ 1), abort_flag, a.st, 223)) return false;
       ++pv;
       tc_fence_after();
-      store_p_row(ps, r, p, gate);
+      store_p_half(ps, r, wg, p, gate);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full);
       return true;
     };
-
-    // zero the block-score rows
-    for (int i = r; i < QT * a.nbs; i += 128) scores[i] = 0.f;
-    wg_sync();
-
-    float x[kTile];
-    // ---------------- phase 1: compressed max / sum
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < ntc && ok; ++j) {
-      if (!consume_s(x)) { ok = false; break; }
+    // online max / sum over this warpgroup's columns
+    auto stats_add = [&](float (&x)[64], float& m, float& l) {
       float mt = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
-        x[i] = (j * kTile + i < n_t) ? x[i] * a.sc2 : -INFINITY;
-        mt = fmaxf(mt, x[i]);
-      }
+      for (int i = 0; i < 64; ++i) mt = fmaxf(mt, x[i]);
       const float mn = fmaxf(m, mt);
-      if (mn == -INFINITY) continue;
-      float s = 0.f;
+      if (mn == -INFINITY) return;
+      float sm = 0.f;
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) s += fast_exp2(x[i] - mn);
-      l = l * fast_exp2(m - mn) + s;
+      for (int i = 0; i < 64; ++i) sm += fast_exp2(x[i] - mn);
+      l = l * fast_exp2(m - mn) + sm;
       m = mn;
-    }
-    float inv_l = l > 0.f ? 1.f / l : 0.f;
-    // ---------------- phase 2: exact p, O_cmp, block scores
-    float* srow = scores + (size_t)qi * a.nbs;
-    const bool lead = (lane % (HPG < 32 ? HPG : 32)) == 0;
+    };
+    // merge with the other warpgroup: afterwards m = row max (0 if empty),
+    // il = 1 / row sum (0 if empty)
+    auto merge_stats = [&](float& m, float l, float& il) {
+      red[(wg * 2 + 0) * 128 + r] = m;
+      red[(wg * 2 + 1) * 128 + r] = l;
+      sync8();
+      const float mo = red[((1 - wg) * 2 + 0) * 128 + r];
+      const float lo = red[((1 - wg) * 2 + 1) * 128 + r];
+      const float M = fmaxf(m, mo);
+      float L = 0.f;
+      if (M != -INFINITY) L = l * fast_exp2(m - M) + lo * fast_exp2(mo - M);
+      m = (M == -INFINITY) ? 0.f : M;
+      il = L > 0.f ? 1.f / L : 0.f;
+      sync8();   // both warpgroups have read before the area is reused
+    };
+
+    // zero the block-score rows
+    for (int i = wg * 128 + r; i < QT * a.nbs; i += 256) scores[i] = 0.f;
+    sync8();
+
+    float x[64];
+    // ---------------- phase 1: compressed max / sum
+    float m = -INFINITY, l = 0.f, inv_l = 0.f;
     for (int j = 0; j < ntc && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
 #pragma unroll
-      for (int i = 0; i < kTile; ++i)
-        x[i] = (j * kTile + i < n_t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
-      // block importance: selection block 32j+u collects compressed blocks
-      // 4u-1 (one chunk), 4u..4u+2 (two chunks each), 4u+3 (one chunk)
-      float vsum[33];
+      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? x[i] * a.sc2 : -INFINITY;
+      stats_add(x, m, l);
+    }
+    merge_stats(m, l, inv_l);
+    // ---------------- phase 2: exact p, O_cmp, block scores
+    float* srow = scores + (size_t)qi * a.nbs;
+    const bool lead = (lane % HPG) == 0;
+    for (int j = 0; j < ntc && ok; ++j) {
+      if (!consume_s(x)) { ok = false; break; }
 #pragma unroll
-      for (int uu = 0; uu < 32; ++uu)
+      for (int i = 0; i < 64; ++i)
+        x[i] = (j * kTile + c0 + i < n_t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
+      // block importance: selection block 32j+16wg+uu collects compressed
+      // blocks 4u-1 (one chunk), 4u..4u+2 (two chunks each), 4u+3 (one chunk);
+      // entry 4u-1 of the first block is added by whoever holds it (the
+      // previous column half), as the carry below
+      float vsum[16];
+#pragma unroll
+      for (int uu = 0; uu < 16; ++uu)
         vsum[uu] = (uu > 0 ? x[4 * uu - 1] : 0.f) + 2.f * (x[4 * uu] + x[4 * uu + 1] + x[4 * uu + 2]) +
                    x[4 * uu + 3];
-      vsum[32] = x[kTile - 1];
-      if (HPG <= 32) {
-        const int base = reduce_scatter32<(HPG <= 32 ? HPG : 32)>(vsum, lane);
-        const float v32 = allreduce_group<(HPG <= 32 ? HPG : 32)>(vsum[32]);
-        if (row_ok) {
+      const float carry = allreduce_group<HPG>(x[63]);
+      const int base = reduce_scatter16<HPG>(vsum, lane);
+      if (row_ok) {
+        // every block receives at most two additions (its own columns and the
+        // carry of the columns before it), so the sums are order-independent
 #pragma unroll
-          for (int k = 0; k < 32 / (HPG <= 32 ? HPG : 32); ++k) srow[32 * j + base + k] += vsum[k];
-          if (lead) srow[32 * j + 32] += v32;
-        }
-      } else {
-        const int base = reduce_scatter32<32>(vsum, lane);
-        const float v32 = allreduce_group<32>(vsum[32]);
-        if (row_ok) {
-          atomicAdd(&srow[32 * j + base], vsum[0]);
-          if (lane == 0) atomicAdd(&srow[32 * j + 32], v32);
-        }
+        for (int k = 0; k < 16 / HPG; ++k) atomicAdd(&srow[32 * j + 16 * wg + base + k], vsum[k]);
+        if (lead) atomicAdd(&srow[32 * j + 16 * wg + 16], carry);
       }
       if (!put_p(x, g_c)) { ok = false; break; }
     }
     // ---------------- top-n selection (one warp per query)
-    wg_sync();
+    sync8();
     if (ok) {
-      for (int qq = warp; qq < QT; qq += 4) {
+      for (int qq = warp; qq < QT; qq += 8) {
         const int tq = t0 + qq;
         if (tq >= a.T) continue;
         const int jt = tq / 64;
@@ -446,8 +468,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float cv[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int j = 1 + lane + 32 * k;
-          cv[k] = (j <= jt - 2) ? sq[j] : -INFINITY;
+          const int jj = 1 + lane + 32 * k;
+          cv[k] = (jj <= jt - 2) ? sq[jj] : -INFINITY;
         }
         int mine = -1;
         const int nfree = a.n - 3;
@@ -495,47 +517,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w_lo = t - a.w + 1;
     for (int j = 0; j < ntw && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
-      float mt = -INFINITY;
-      const int s0 = s_lo + j * kTile;
+      const int s0 = s_lo + j * kTile + c0;
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
+      for (int i = 0; i < 64; ++i) {
         const int s = s0 + i;
         x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] * a.sc2 : -INFINITY;
-        mt = fmaxf(mt, x[i]);
       }
-      const float mn = fmaxf(m, mt);
-      if (mn == -INFINITY) continue;
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < kTile; ++i) s += fast_exp2(x[i] - mn);
-      l = l * fast_exp2(m - mn) + s;
-      m = mn;
+      stats_add(x, m, l);
     }
-    inv_l = l > 0.f ? 1.f / l : 0.f;
+    merge_stats(m, l, inv_l);
     // ---------------- phase 4: exact window p, accumulate g_w * O_win
     for (int j = 0; j < ntw && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
-      const int s0 = s_lo + j * kTile;
+      const int s0 = s_lo + j * kTile + c0;
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
+      for (int i = 0; i < 64; ++i) {
         const int s = s0 + i;
         x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
       }
       if (!put_p(x, g_w)) { ok = false; break; }
     }
-    // ---------------- epilogue: O -> bf16 partial output
+    // ---------------- epilogue: O -> bf16 partial output (each warpgroup half the columns)
     if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 224)) {
       tc_fence_after();
       __nv_bfloat16* dst = a.part + (((size_t)b * a.T + t) * a.H + head) * a.dv;
-      for (int c0 = 0; c0 < a.dv; c0 += 16) {
+      const int half = a.dv / 2;
+      for (int cc = wg * half; cc < (wg + 1) * half; cc += 16) {
         uint32_t rr[16];
-        tmem_ld16(tmem_o + lane_base + c0, rr);
+        tmem_ld16(tmem_o + lane_base + cc, rr);
         tmem_ld_wait(rr);
         if (row_ok) {
           uint32_t pk[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(__uint_as_float(rr[2 * k]), __uint_as_float(rr[2 * k + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
           d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
@@ -549,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Layout {
-  uint32_t off_ring, off_p, off_scores, off_bar, total;
+  uint32_t off_ring, off_p, off_scores, off_red, off_bar, total;
 };
 
 Layout layout_for(int dk, int QT, int nbs) {
@@ -557,7 +572,8 @@ Layout layout_for(int dk, int QT, int nbs) {
   L.off_ring = (uint32_t)(dk / 64) * kSlot;
   L.off_p = L.off_ring + kRing * kSlot;
   L.off_scores = L.off_p + 2 * kSlot;
-  L.off_bar = (uint32_t)align_up(L.off_scores + (size_t)QT * nbs * sizeof(float), 1024);
+  L.off_red = (uint32_t)align_up(L.off_scores + (size_t)QT * nbs * sizeof(float), 256);
+  L.off_bar = (uint32_t)align_up(L.off_red + 2 * 2 * 128 * sizeof(float), 1024);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;  // + alignment slack
   return L;
 }
@@ -655,6 +671,7 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
   a.off_ring = L.off_ring;
   a.off_p = L.off_p;
   a.off_scores = L.off_scores;
+  a.off_red = L.off_red;
   a.off_bar = L.off_bar;
   switch (hpg) {
     case 1: return launch_hpg<1>(a, c.B, maps, L.total, s);
@@ -662,9 +679,6 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
     case 4: return launch_hpg<4>(a, c.B, maps, L.total, s);
     case 8: return launch_hpg<8>(a, c.B, maps, L.total, s);
     case 16: return launch_hpg<16>(a, c.B, maps, L.total, s);
-    case 32: return launch_hpg<32>(a, c.B, maps, L.total, s);
-    case 64: return launch_hpg<64>(a, c.B, maps, L.total, s);
-    case 128: return launch_hpg<128>(a, c.B, maps, L.total, s);
     default: return NSA_ERR_UNSUPPORTED;
   }
 }
