@@ -380,21 +380,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->p_full);
       return true;
     };
-    // online max / sum over this warpgroup's columns
+    // online max / sum over this warpgroup's columns; x holds raw scores
+    // (-inf where masked), m is kept in log2 units (scores * scale * log2 e)
     auto stats_add = [&](float (&x)[64], float& m, float& l) {
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 64; ++i) mt = fmaxf(mt, x[i]);
-      const float mn = fmaxf(m, mt);
+      const float mn = fmaxf(m, mt * a.sc2);
       if (mn == -INFINITY) return;
       float sm = 0.f;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) sm += fast_exp2(x[i] - mn);
+      for (int i = 0; i < 64; ++i) sm += fast_exp2(fmaf(x[i], a.sc2, -mn));
       l = l * fast_exp2(m - mn) + sm;
       m = mn;
     };
-    // merge with the other warpgroup: afterwards m = row max (0 if empty),
-    // il = 1 / row sum (0 if empty)
+    // merge with the other warpgroup: afterwards m = max + log2(sum) of the
+    // row (p = exp2(s*scale - m) is then normalised), +inf if the row is empty
     auto merge_stats = [&](float& m, float l, float& il) {
       red[(wg * 2 + 0) * 128 + r] = m;
       red[(wg * 2 + 1) * 128 + r] = l;
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float M = fmaxf(m, mo);
       float L = 0.f;
       if (M != -INFINITY) L = l * fast_exp2(m - M) + lo * fast_exp2(mo - M);
-      m = (M == -INFINITY) ? 0.f : M;
+      m = (L > 0.f) ? M + __log2f(L) : INFINITY;
       il = L > 0.f ? 1.f / L : 0.f;
       sync8();   // both warpgroups have read before the area is reused
     };
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntc && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? x[i] * a.sc2 : -INFINITY;
+      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? x[i] : -INFINITY;
       stats_add(x, m, l);
     }
     merge_stats(m, l, inv_l);
@@ -429,8 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntc && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        x[i] = (j * kTile + c0 + i < n_t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
+      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? fast_exp2(fmaf(x[i], a.sc2, -m)) : 0.f;
       // block importance: selection block 32j+16wg+uu collects compressed
       // blocks 4u-1 (one chunk), 4u..4u+2 (two chunks each), 4u+3 (one chunk);
       // entry 4u-1 of the first block is added by whoever holds it (the
@@ -521,11 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const int s = s0 + i;
-        x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] * a.sc2 : -INFINITY;
+        x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] : -INFINITY;
       }
       stats_add(x, m, l);
     }
     merge_stats(m, l, inv_l);
+    // the window gate goes into the exponent: P = g_w * p
+    const float mw = m - __log2f(g_w);
     // ---------------- phase 4: exact window p, accumulate g_w * O_win
     for (int j = 0; j < ntw && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
@@ -533,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const int s = s0 + i;
-        x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(x[i] * a.sc2 - m) * inv_l : 0.f;
+        x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(fmaf(x[i], a.sc2, -mw)) : 0.f;
       }
-      if (!put_p(x, g_w)) { ok = false; break; }
+      if (!put_p(x, 1.f)) { ok = false; break; }
     }
     // ---------------- epilogue: O -> bf16 partial output (each warpgroup half the columns)
     if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 224)) {
