@@ -9,7 +9,7 @@
 // blocks and the w-token window once, for all hpg <= 16 query heads of the
 // group at the same time (group-centric loading).
 //
-// Work is cut into units of up to 4 pairs of 64-row key/value blocks (512
+// Work is cut into units of up to 2 pairs of 64-row key/value blocks (256
 // keys) of one group; one CTA takes one unit, two CTAs share an SM:
 //     S^T[key, head] = K_pair[key, :] . q[head, :]         (tcgen05, M=128, N=16)
 //     exact softmax over the unit's keys (max pass, then exp pass over TMEM)
@@ -37,8 +37,10 @@ namespace {
 
 constexpr int kThreads = 192;        // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
 constexpr int NP = 16;               // MMA N: heads of the group, padded to 16
-constexpr int kPairs = 4;            // block pairs per unit (512 keys)
+constexpr int kPairs = 2;            // block pairs per unit (256 keys)
 constexpr int kUnitKeys = 128 * kPairs;
+constexpr int kUnitBlocks = kUnitKeys / 4;   // selection blocks fed by one compressed unit
+constexpr int kUnitChunks = kUnitKeys / 32;  // 32-entry chunks of one compressed unit
 constexpr int kRingK = 3;            // 16 KB: one 64-column chunk of a pair
 constexpr int kRingV = 1;            // 32 KB: both 64-column chunks of a value pair
 constexpr int kSlotK = 16384;
@@ -57,8 +59,8 @@ struct DecArgs {
   float* pm;                         // [BG][NS][16] unit max (log2 units, -inf if empty)
   float* pl;                         // [BG][NS][16] unit sum
   float* po;                         // [BG][NS][16][dv] unit O (unnormalised)
-  float* u;                          // [BG][ncu*128][16] block partials within a 32-entry chunk
-  float* cc;                         // [BG][ncu*16][16] carry of each chunk's last entry
+  float* u;                          // [BG][ncu*kUnitBlocks][16] block partials within a 32-entry chunk
+  float* cc;                         // [BG][ncu*kUnitChunks][16] carry of each chunk's last entry
   float* stats;                      // [BG][32] compressed-branch max and 1/sum per head
   int32_t* idx;                      // [BG][n]
   int* cnt;                          // [2][BG]
@@ -166,8 +168,8 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   // block importance S[j], j <= jt: unit j/128; blocks 8k+8 also take the
   // carry of chunk k (entry 32k+31), which belongs to unit k/16
   {
-    const float* ub = a.u + (size_t)bg * ncu * 128 * 16;
-    const float* cb = a.cc + (size_t)bg * ncu * 16 * 16;
+    const float* ub = a.u + (size_t)bg * ncu * kUnitBlocks * 16;
+    const float* cb = a.cc + (size_t)bg * ncu * kUnitChunks * 16;
     // four blocks per thread per round, all their loads issued before use
     for (int j0 = tid; j0 <= jt; j0 += 4 * kThreads) {
       float4 v[4][4], w[4][4];
@@ -188,8 +190,8 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
         const int j = j0 + q * kThreads;
         if (j > jt) continue;
         const int ch = (j >> 3) - 1;
-        float s = (4 * j < a.Nc) ? dot16(fsm + (j >> 7) * 16, v[q]) : 0.f;
-        if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) s += dot16(fsm + (ch >> 4) * 16, w[q]);
+        float s = (4 * j < a.Nc) ? dot16(fsm + (j / kUnitBlocks) * 16, v[q]) : 0.f;
+        if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) s += dot16(fsm + (ch / kUnitChunks) * 16, w[q]);
         Ssm[j] = s;
       }
     }
@@ -632,12 +634,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int entry0 = base + 128 * p + 32 * warp;   // first entry of this warp
             if ((lane & 3) == 0) {
               float4* dst =
-                  reinterpret_cast<float4*>(a.u + ((size_t)bg * a.ncu * 128 + (entry0 + lane) / 4) * 16);
+                  reinterpret_cast<float4*>(a.u + ((size_t)bg * a.ncu * kUnitBlocks + (entry0 + lane) / 4) * 16);
 #pragma unroll
               for (int k = 0; k < 4; ++k) dst[k] = make_float4(uq[4 * k], uq[4 * k + 1], uq[4 * k + 2], uq[4 * k + 3]);
             }
             if (lane == 31) {
-              float4* dst = reinterpret_cast<float4*>(a.cc + ((size_t)bg * a.ncu * 16 + entry0 / 32) * 16);
+              float4* dst = reinterpret_cast<float4*>(a.cc + ((size_t)bg * a.ncu * kUnitChunks + entry0 / 32) * 16);
 #pragma unroll
               for (int k = 0; k < 4; ++k) dst[k] = make_float4(e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
             }
@@ -724,8 +726,8 @@ DecWs dec_ws(const nsa_cfg& c) {
   w.pl = align_up(w.pm + sizeof(float) * BG * s.NS * 16, 256);
   w.po = align_up(w.pl + sizeof(float) * BG * s.NS * 16, 256);
   w.u = align_up(w.po + sizeof(float) * BG * s.NS * 16 * c.dv, 256);
-  w.cc = align_up(w.u + sizeof(float) * BG * (size_t)s.ncu * 128 * 16, 256);
-  w.stats = align_up(w.cc + sizeof(float) * BG * (size_t)s.ncu * 16 * 16, 256);
+  w.cc = align_up(w.u + sizeof(float) * BG * (size_t)s.ncu * kUnitBlocks * 16, 256);
+  w.stats = align_up(w.cc + sizeof(float) * BG * (size_t)s.ncu * kUnitChunks * 16, 256);
   w.idx = align_up(w.stats + sizeof(float) * BG * 32, 256);
   w.end = align_up(w.idx + sizeof(int32_t) * BG * c.n, 256);
   return w;
