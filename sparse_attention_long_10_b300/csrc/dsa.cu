@@ -35,7 +35,7 @@ namespace {
 constexpr int kIdxThreads = 160;    // 4 compute warps + 1 TMA producer warp
 constexpr int kIdxTile = 128;       // keys per indexer tile
 constexpr int kIdxStages = 4;
-constexpr int kIdxPart = 4096;      // positions per indexer CTA
+constexpr int kIdxPartMax = 4096;   // most positions per indexer CTA
 constexpr int kBins = 4096;         // first radix level: top 12 bits
 constexpr int kSelThreads = 256;
 constexpr int kSelPart = 2048;      // positions per threshold / compaction CTA
@@ -48,6 +48,7 @@ constexpr int kAttnStages = 2;
 struct DsaArgs {
   int B, T, HI, dI, H, dk, dv, kk;  // kk = min(topk, T)
   int nparts;                       // threshold / compaction parts per row
+  int idx_part;                     // positions per indexer CTA (a multiple of kIdxTile)
   int attn_ctas;                    // attention CTAs per row
   int all;                          // kk == T: every position is kept
   float sc2;                        // softmax scale * log2(e)
@@ -108,8 +109,8 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   IdxBars* bars = reinterpret_cast<IdxBars*>(hs + kBins);
   volatile int* abort_flag = &bars->abort_flag;
   const int part = blockIdx.x, b = blockIdx.y;
-  const int s0 = part * kIdxPart;
-  const int npos = min(kIdxPart, a.T - s0);
+  const int s0 = part * a.idx_part;
+  const int npos = min(a.idx_part, a.T - s0);
   const int ntiles = (npos + kIdxTile - 1) / kIdxTile;
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -305,8 +306,8 @@ __device__ void block_cut(Get get, int nbins, uint32_t need, bool from_top, uint
 // elem(i, key, pos) that all share the top-12-bit bin B1: the need-th best
 // pair under (key descending, position ascending).  hist: 4096 words.
 template <class Elem>
-__device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need, uint32_t* hist, uint32_t* scan,
-                              uint32_t& Ks, uint32_t& Is) {
+__device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need, uint32_t max_pos, uint32_t* hist,
+                              uint32_t* scan, uint32_t& Ks, uint32_t& Is) {
   const int t = threadIdx.x;
   uint32_t prefix = B1 << 20, mask = 0xFFF00000u;
   // key bits 19..8 (4096 bins), then 7..0 (256 bins), from the top
@@ -330,9 +331,19 @@ __device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need,
     need -= before;
   }
   Ks = prefix;
-  // among the elements equal to K*, the need-th smallest position (8-bit digits)
+  // every element equal to K* is kept: no position cut needed
+  const uint32_t n_eq = hist[Ks & 255u];
+  __syncthreads();
+  if (n_eq == need) {
+    Is = 0xffffffffu;
+    return;
+  }
+  // among the elements equal to K*, the need-th smallest position (8-bit
+  // digits, from the highest digit a position below max_pos can have)
+  int top = 0;
+  while (top < 24 && (max_pos >> (top + 8)) != 0) top += 8;
   uint32_t pprefix = 0, pmask = 0;
-  for (int sh = 24; sh >= 0; sh -= 8) {
+  for (int sh = top; sh >= 0; sh -= 8) {
     for (int i = t; i < 256; i += 256) hist[i] = 0;
     __syncthreads();
     for (uint32_t i = t; i < n; i += 256) {
@@ -430,12 +441,12 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
       cp[i] = __ldcg(a.cand + ((size_t)b * kCandCap + i) * 2 + 1);
     }
     __syncthreads();
-    radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = ck[i]; pos = cp[i]; }, c1, B1, need1, h2,
-                  scan, Ks, Is);
+    radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = ck[i]; pos = cp[i]; }, c1, B1, need1,
+                  (uint32_t)(a.T - 1), h2, scan, Ks, Is);
   } else {
     // more boundary candidates than the buffer holds: resolve over the whole row
     radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = __ldcg(keys + i); pos = i; },
-                  (uint32_t)a.T, B1, need1, h2, scan, Ks, Is);
+                  (uint32_t)a.T, B1, need1, (uint32_t)(a.T - 1), h2, scan, Ks, Is);
   }
   // kept positions per part: above the boundary bin + kept boundary candidates
   for (int p = t; p < a.nparts; p += kSelThreads) pc[p] = __ldcg(a.gtcnt + (size_t)b * a.nparts + p);
@@ -842,7 +853,7 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
     attr = true;
   }
   prof::begin("dsa_index", s);
-  dsa_index_kernel<DI><<<dim3((a.T + kIdxPart - 1) / kIdxPart, a.B), kIdxThreads, smem, s>>>(map, a);
+  dsa_index_kernel<DI><<<dim3((a.T + a.idx_part - 1) / a.idx_part, a.B), kIdxThreads, smem, s>>>(map, a);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
@@ -899,6 +910,16 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.dv = c.dv;
   a.kk = sh.kk;
   a.nparts = sh.nparts;
+  {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                   cudaSuccess)
+      sms = 148;
+    const int per_row = (2 * sms + c.B - 1) / c.B;          // two indexer CTAs per SM
+    int part = (c.T + per_row - 1) / per_row;
+    part = (part + kIdxTile - 1) / kIdxTile * kIdxTile;
+    a.idx_part = part < kIdxTile ? kIdxTile : (part > kIdxPartMax ? kIdxPartMax : part);
+  }
   a.attn_ctas = sh.attn_ctas;
   a.all = sh.all;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
