@@ -20,7 +20,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 from oracle import nsa as O
-from workloads import NSAParams, PREFILL_CONFIGS, make_prefill
+from workloads import NSAParams, PREFILL_CONFIGS, PrefillWorkload, make_prefill
 
 MAX_ABS, MEAN_ABS, NEAR_TIE = 2e-2, 2e-3, 1e-5
 
@@ -139,3 +139,40 @@ def test_prefill_8k_sampled_rows(key, nrows):
     ref = O.nsa_prefill_reference(inp, rows=rows)
     out, idx, _, _ = run_prefill(inp, ref["kc"], ref["vc"])
     check_rows(inp, ref, out, idx, rows, label=key)
+
+
+@pytest.mark.parametrize("n,w", [(8, 256), (7, 100), (16, 1024)])
+def test_prefill_batch2_other_branch_parameters(n, w):
+    # two sequences, 8 heads in 2 groups, and selection / window sizes other
+    # than the pages' n=16, w=512 (an odd n leaves the last block pair half empty)
+    wl = PrefillWorkload("nsa_prefill_B2", 2, 1500, 8, 2, 64, 64, 9)
+    params = NSAParams(n=n, w=w)
+    inp = make_prefill(wl)
+    refs = [O.nsa_prefill_reference(inp, b=b, params=params) for b in range(wl.B)]
+    kc = np.stack([r["kc"] for r in refs])
+    vc = np.stack([r["vc"] for r in refs])
+    out, idx, _, _ = run_prefill(inp, kc, vc, params=params)
+    for b in range(wl.B):
+        check_rows(inp, refs[b], out, idx, list(range(wl.T)), b=b, params=params, label=f"B2 seq {b} n={n} w={w}")
+
+
+def test_prefill_64k_full_size_sampled_rows():
+    """The 65,536-token prefill in the launch configuration the benchmark
+    times (the GPU compresses too); the oracle checks sampled rows one by one
+    with its own compression, and every sampled row's kept set is checked to
+    be causal, sorted and to hold the forced blocks."""
+    wl = PREFILL_CONFIGS["prefill_64k"]
+    inp = make_prefill(wl)
+    out, idx, _, _ = run_prefill(inp)
+    T = wl.T
+    rng = np.random.default_rng(12)
+    rows = sorted(set([0, 31, 32, 1023, 1024, 4095, 32767, T - 64, T - 2, T - 1] + rng.integers(0, T, 40).tolist()))
+    ref = O.nsa_prefill_reference(inp, rows=rows)
+    check_rows(inp, ref, out, idx, rows, label="prefill 64k", near_tie=1e-3)
+    gi = idx[0, torch.as_tensor(rows)].cpu().numpy()
+    for r, t in enumerate(rows):
+        jt = t // 64
+        for g in range(wl.G):
+            kept = [int(j) for j in gi[r, g] if j >= 0]
+            assert kept == sorted(set(kept)) and len(kept) == min(16, jt + 1)
+            assert {0, jt} <= set(kept) and (jt < 1 or jt - 1 in kept) and max(kept) <= jt
