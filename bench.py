@@ -142,6 +142,36 @@ def max_over_ranks(x: float, ws: int) -> float:
     return float(t.item())
 
 
+# DRAM bytes (read + write) per launch or step from the ncu captures summarised
+# under profiles/.  A figure is reported only while the kernel sources it was
+# taken from are unchanged (sha256 prefix of the listed files); otherwise the
+# bench line says null.
+_CSRC = "sparse_attention_long_10_b300/csrc/"
+NCU_TRAFFIC = {
+    # profiles/prefill_T8192_cmp_win_sel.md: 331.0 MB per T=8192 launch, x8 for
+    # T=65536 (every stream of the kernel grows linearly in T)
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "8e95e29f6cf25549",
+                "bytes": 8 * 331.0e6, "how": "T=8192 capture scaled by 8 to T=65536"},
+    # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "d5cbd0ff85a2afaa",
+               "bytes": (189.2 + 10.2 + 52.0 + 0.4) * 1e6, "how": "full-size capture, both kernels"},
+    # profiles/dsa_B8_T131072_kernels.md: the five kernels of one step
+    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "d8c2d043ad94ac93",
+            "bytes": (134.4 + 4.7 + 4.3 + 4.2 + 35.9 + 0.1 + 8.4) * 1e6, "how": "full-size capture, five kernels"},
+}
+
+
+def ncu_traffic(key: str):
+    import hashlib
+    ent = NCU_TRAFFIC[key]
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in ent["files"]:
+        with open(os.path.join(root, _CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return ent["bytes"] if h.hexdigest()[:16] == ent["sha"] else None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -298,7 +328,8 @@ def run_ours(args, ws, rank):
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_sus"],
                      "peak_kind": f"bf16 dense sustained ({pk['src']})",
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "avg_launch_ms": dom_avg_ms,
-                     "traffic": None},
+                     "traffic": ncu_traffic("cmp_win") if dom_name == "cmp_win" else None,
+                     "traffic_how": NCU_TRAFFIC["cmp_win"]["how"] if dom_name == "cmp_win" else None},
         "kernels": {k: {"launches_per_step": c / args.steps, "ms_per_step": t / args.steps,
                         "share": t / sum(x[1] for x in prof.values())} for k, (c, t) in prof.items()},
         "gpu_launches": int(launches),
@@ -416,8 +447,9 @@ def run_decode_leg(args, ws):
         "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
                      "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})",
-                     "frac_of_8TBs": gbs / 8000.0, "traffic": None,
-                     "note": "whole step (memset + 2 kernels, CUDA graph replay), L2 flushed before each step"},
+                     "frac_of_8TBs": gbs / 8000.0, "traffic": ncu_traffic("decode"),
+                     "note": "whole step (memset + 2 kernels, CUDA graph replay), L2 flushed before each step; "
+                             "traffic: " + NCU_TRAFFIC["decode"]["how"]},
         "kernels": kern,
         "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
         "e2e": {"value": ms_e2e * 1e3, "unit": "us", "h2d_bytes_per_step": int(h2d),
@@ -498,8 +530,9 @@ def run_dsa_leg(args, ws):
         "value": ms * 1e3, "unit": "us", "higher_is_better": False,
         "workload": wl.name, "steps": args.steps, "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})", "traffic": None,
-                     "note": "whole step (memset + 4 kernels, CUDA graph replay), L2 flushed before each step"},
+                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})", "traffic": ncu_traffic("dsa"),
+                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step; "
+                             "traffic: " + NCU_TRAFFIC["dsa"]["how"]},
         "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
                     for k, (c, t) in prof.items()},
         "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
