@@ -26,6 +26,8 @@
 //   dec_kernel<MODE 1>  grid (selected units, B*G)
 //       the kept blocks; the last CTA of a group merges every unit and writes
 //       out = g_cmp*O_cmp + g_slc*O_slc + g_win*O_win (bf16).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -65,6 +67,7 @@ struct DecArgs {
   int32_t* idx;                      // [BG][n]
   int* cnt;                          // [2][BG]
   DeviceStatus* st;
+  int sel_cap, part_cap;             // last-CTA staging capacity: blocks, 16 x dv partials
   uint32_t off_kring, off_vring, off_pt, off_red, off_bar;
 };
 
@@ -119,44 +122,130 @@ __device__ __forceinline__ float dot16(const float* f, const float4* v) {
          f[15] * d.w;
 }
 
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t x) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+}
+// Copies n16 16-byte pieces global -> shared, spread over the CTA.
+__device__ __forceinline__ void stage(void* dst, const void* src, int n16) {
+  for (int i = threadIdx.x; i < n16; i += kThreads)
+    cp_async16(static_cast<uint8_t*>(dst) + 16 * (size_t)i, static_cast<const uint8_t*>(src) + 16 * (size_t)i);
+}
+// (max, sum) of the 16 heads of partial slots [s0, s1) of group bg into sp[r][32]
+__device__ __forceinline__ void stage_stats(const DecArgs& a, int bg, int s0, int s1, float* sp) {
+  for (int e = threadIdx.x; e < (s1 - s0) * 8; e += kThreads) {
+    const int r = e >> 3, q = e & 7;   // q < 4: max, q >= 4: sum
+    const float* src = (q < 4 ? a.pm : a.pl) + ((size_t)bg * a.NS + s0 + r) * 16 + 4 * (q & 3);
+    cp_async16(sp + r * 32 + (q < 4 ? 0 : 16) + 4 * (q & 3), src);
+  }
+}
+
+// Per-lane sorted list of the 8 best (score, block) candidates: higher score
+// first, equal scores in arrival order (lower block first).
+struct Top8 {
+  float v[8];
+  int j[8];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = -1.f;
+      j[k] = 0x7fffffff;
+    }
+  }
+  __device__ __forceinline__ void insert(float cv, int cj) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool sw = cv > v[k];
+      const float t = v[k];
+      const int u = j[k];
+      v[k] = sw ? cv : t;
+      j[k] = sw ? cj : u;
+      cv = sw ? t : cv;
+      cj = sw ? u : cj;
+    }
+  }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int k = 0; k < 7; ++k) {
+      v[k] = v[k + 1];
+      j[k] = j[k + 1];
+    }
+    v[7] = -1.f;
+    j[7] = 0x7fffffff;
+  }
+};
+
+// Shared-memory plan of the selection step (floats).
+struct SelStage {
+  int sp, fsm, car, cc, S, ub, misc, total;
+};
+__host__ __device__ inline SelStage sel_stage(int ncu, int jt, int cap) {
+  SelStage L;
+  L.sp = 0;                                  // [ncu][32] unit max, sum
+  L.fsm = 32 * ncu;                          // [ncu][16] factors exp2(m_unit - M) / L
+  L.car = L.fsm + 16 * ncu;                  // [ncu*kUnitChunks] carry term of each chunk
+  L.cc = (L.car + kUnitChunks * ncu + 3) & ~3;   // [ncu*kUnitChunks][16] last entry of each chunk
+  L.S = L.cc + 16 * kUnitChunks * ncu;       // [jt+1] block importance
+  L.ub = (L.S + jt + 1 + 3) & ~3;            // [cap][16] block partials
+  L.misc = L.ub + 16 * cap;                  // Mh[16], iL[16], wv[128], wj[128]
+  L.total = L.misc + 32 + 256;
+  return L;
+}
+
 // Selection step, run by the last compressed/window CTA of a group: exact
 // softmax statistics of the compressed branch (kept in ``stats`` for the
 // final combine), block importance S[j] for every causal block, top-n.
+// Its inputs are staged into shared memory with asynchronous copies, so
+// they cost one round trip through L2 for caches up to sel_cap*64 tokens.
 __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int warp = warp_id(), lane = lane_id();
-  const int ncu = a.ncu;
-  float* Mh = reinterpret_cast<float*>(smem);      // 16
-  float* iL = Mh + 16;                              // 16
-  float* wv = iL + 16;                              // [4][32] winner scores
-  int* wj = reinterpret_cast<int*>(wv + 128);       // [4][32] winner blocks
-  float* sp = reinterpret_cast<float*>(wj + 128);   // [ncu][2][16] unit max, sum
-  float* fsm = sp + 32 * ncu;                       // [ncu][16] factors exp(m_unit - M) / L
-  float* Ssm = fsm + 16 * ncu;                      // [jt+1]
-  for (int e = tid; e < ncu * 16; e += kThreads) {
-    const size_t o = ((size_t)bg * a.NS + e / 16) * 16 + (e & 15);
-    sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
-    sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
+  const int ncu = a.ncu, n = a.n;
+  const int jt = (a.T - 1) / 64;
+  const bool trivial = jt + 1 <= n;
+  const SelStage L = sel_stage(ncu, jt, a.sel_cap);
+  float* st = reinterpret_cast<float*>(smem);
+  float* sp = st + L.sp;
+  float* fsm = st + L.fsm;
+  float* car = st + L.car;
+  float* ccs = st + L.cc;
+  float* Ssm = st + L.S;
+  float* ubuf = st + L.ub;
+  float* Mh = st + L.misc;
+  float* iL = Mh + 16;
+  float* wv = iL + 16;
+  int* wj = reinterpret_cast<int*>(wv + 128);
+  const int nblk = min(jt + 1, (a.Nc + 3) / 4);   // blocks holding compressed entries
+  const float* ub = a.u + (size_t)bg * ncu * kUnitBlocks * 16;
+  stage_stats(a, bg, 0, ncu, sp);
+  if (!trivial) {
+    stage(ccs, a.cc + (size_t)bg * ncu * kUnitChunks * 16, ncu * kUnitChunks * 4);
+    stage(ubuf, ub, min(nblk, a.sel_cap) * 4);
   }
+  cp_async_wait_all();
   __syncthreads();
   if (tid < 16) {
     float M = -INFINITY;
     for (int s = 0; s < ncu; ++s) M = fmaxf(M, sp[s * 32 + tid]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f;
-    for (int s = 0; s < ncu; ++s) L += sp[s * 32 + 16 + tid] * fast_exp2(sp[s * 32 + tid] - Mu);
-    const float il = (L > 0.f && tid < a.hpg) ? 1.f / L : 0.f;
+    float Ls = 0.f;
+    for (int s = 0; s < ncu; ++s) Ls += sp[s * 32 + 16 + tid] * fast_exp2(sp[s * 32 + tid] - Mu);
+    const float il = (Ls > 0.f && tid < a.hpg) ? 1.f / Ls : 0.f;
     Mh[tid] = Mu;
     iL[tid] = il;
     a.stats[(size_t)bg * 32 + tid] = Mu;
     a.stats[(size_t)bg * 32 + 16 + tid] = il;
-    for (int s = 0; s < ncu; ++s) fsm[s * 16 + tid] = fast_exp2(sp[s * 32 + tid] - Mu) * il;
   }
-  const int jt = (a.T - 1) / 64;
-  const int n = a.n;
   int32_t* idx = a.idx + (size_t)bg * n;
   int32_t* idx_out = a.idx_out != nullptr ? a.idx_out + (size_t)bg * n : nullptr;
-  if (jt + 1 <= n) {
+  if (trivial) {
     if (tid < n) {
       const int v = tid <= jt ? tid : -1;
       idx[tid] = v;
@@ -165,113 +254,80 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
     return;
   }
   __syncthreads();
-  // block importance S[j], j <= jt: unit j/128; blocks 8k+8 also take the
-  // carry of chunk k (entry 32k+31), which belongs to unit k/16
-  {
-    const float* ub = a.u + (size_t)bg * ncu * kUnitBlocks * 16;
-    const float* cb = a.cc + (size_t)bg * ncu * kUnitChunks * 16;
-    // four blocks per thread per round, all their loads issued before use
-    for (int j0 = tid; j0 <= jt; j0 += 4 * kThreads) {
-      float4 v[4][4], w[4][4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + q * kThreads;
-        const int ch = (j >> 3) - 1;
-        const bool hu = j <= jt && 4 * j < a.Nc;   // block j holds compressed entries
-        const bool hc = j <= jt && (j & 7) == 0 && j >= 8 && 32 * ch < a.Nc;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[q][k] = hu ? ldcg4(ub + (size_t)j * 16 + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
-          w[q][k] = hc ? ldcg4(cb + (size_t)ch * 16 + 4 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + q * kThreads;
-        if (j > jt) continue;
-        const int ch = (j >> 3) - 1;
-        float s = (4 * j < a.Nc) ? dot16(fsm + (j / kUnitBlocks) * 16, v[q]) : 0.f;
-        if ((j & 7) == 0 && j >= 8 && 32 * ch < a.Nc) s += dot16(fsm + (ch / kUnitChunks) * 16, w[q]);
-        Ssm[j] = s;
-      }
+  for (int e = tid; e < ncu * 16; e += kThreads) fsm[e] = fast_exp2(sp[(e >> 4) * 32 + (e & 15)] - Mh[e & 15]) * iL[e & 15];
+  __syncthreads();
+  // block importance: block j takes the partial of its four entries (unit
+  // j/kUnitBlocks); blocks 8k+8 also take the carry of chunk k (entry 32k+31)
+  for (int k = tid; k < ncu * kUnitChunks; k += kThreads)
+    car[k] = (32 * k < a.Nc) ? dot16(fsm + (k / kUnitChunks) * 16, reinterpret_cast<const float4*>(ccs + 16 * k))
+                             : 0.f;
+  for (int c0 = 0; c0 <= jt; c0 += a.sel_cap) {
+    if (c0 > 0) {
+      __syncthreads();   // the previous chunk is consumed
+      if (c0 < nblk) stage(ubuf, ub + (size_t)c0 * 16, min(nblk - c0, a.sel_cap) * 4);
+      cp_async_wait_all();
+      __syncthreads();
     }
+    const int c1 = min(jt + 1, c0 + a.sel_cap);
+#pragma unroll 4
+    for (int j = c0 + tid; j < c1; j += kThreads)
+      Ssm[j] = (j < nblk) ? dot16(fsm + (j / kUnitBlocks) * 16, reinterpret_cast<const float4*>(ubuf + 16 * (j - c0)))
+                          : 0.f;
   }
+  __syncthreads();
+  for (int k = tid; 8 * k + 8 <= jt; k += kThreads)
+    if (32 * k < a.Nc) Ssm[8 * k + 8] += car[k];
   __syncthreads();
   // top-(n-3) among the free blocks 1 .. jt-2: each of 4 warps finds the best
   // of its quarter of the range, warp 0 merges.  Order: higher score, then
-  // lower block index.  Scores are >= 0; -2 marks a taken block.
+  // lower block index.  Scores are >= 0; -2 marks a taken block.  Each lane
+  // keeps its 8 best candidates sorted; a round's winner is a warp max
+  // reduction, ties to the lowest index, and only its owner lane pops.
   const int kfree = n - 3;
   const int ncand = jt - 2;
   if (warp < 4) {
     const int per = (ncand + 3) / 4;
     const int lo = 1 + warp * per;
     const int hi = min(1 + ncand, lo + per);
-    for (int rnd = 0; rnd < kfree; ++rnd) {
-      float best = -1.f;
-      int bj = 0x7fffffff;
+    Top8 t;
+    auto fill = [&]() {
+      t.clear();
       for (int j = lo + lane; j < hi; j += 32) {
         const float v = Ssm[j];
-        if (v > best) {
-          best = v;
-          bj = j;
-        }
+        if (v > t.v[7]) t.insert(v, j);
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-        if (ov > best || (ov == best && oj < bj)) {
-          best = ov;
-          bj = oj;
-        }
-      }
+    };
+    fill();
+    for (int rnd = 0; rnd < kfree; ++rnd) {
+      const float gv = warp_max_f32(t.v[0]);
+      const int gj = (int)warp_min_u32(t.v[0] == gv ? (uint32_t)t.j[0] : 0x7fffffffu);
       if (lane == 0) {
-        wv[warp * 32 + rnd] = best;
-        wj[warp * 32 + rnd] = bj;
-        if (bj != 0x7fffffff) Ssm[bj] = -2.f;
+        wv[warp * 32 + rnd] = gv;
+        wj[warp * 32 + rnd] = gj;
       }
-      __syncwarp();
+      if (gj != 0x7fffffff && t.j[0] == gj) {   // owner lane: candidates j = lo + lane (mod 32)
+        Ssm[gj] = -2.f;
+        t.pop();
+        if (t.v[0] < 0.f) fill();   // this lane gave all 8: refill from the untaken rest
+      }
     }
   }
   __syncthreads();
   if (warp == 0) {
     // lane holds candidates c = lane + 32k of the 4*kfree winners
-    float cv[4];
-    int cj[4];
+    Top8 t;
+    t.clear();
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int c = lane + 32 * k;
-      if (c < 4 * kfree) {
-        cv[k] = wv[(c / kfree) * 32 + c % kfree];
-        cj[k] = wj[(c / kfree) * 32 + c % kfree];
-      } else {
-        cv[k] = -1.f;
-        cj[k] = 0x7fffffff;
-      }
+      if (c < 4 * kfree) t.insert(wv[(c / kfree) * 32 + c % kfree], wj[(c / kfree) * 32 + c % kfree]);
     }
     int mine = -1;
     for (int rnd = 0; rnd < kfree; ++rnd) {
-      float best = -1.f;
-      int bj = 0x7fffffff;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (cv[k] > best || (cv[k] == best && cj[k] < bj)) {
-          best = cv[k];
-          bj = cj[k];
-        }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-        if (ov > best || (ov == best && oj < bj)) {
-          best = ov;
-          bj = oj;
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (cj[k] == bj) cv[k] = -2.f;
-      if (lane == rnd) mine = bj;
+      const float gv = warp_max_f32(t.v[0]);
+      const int gj = (int)warp_min_u32(t.v[0] == gv ? (uint32_t)t.j[0] : 0x7fffffffu);
+      if (t.j[0] == gj) t.pop();
+      if (lane == rnd) mine = gj;
     }
     if (lane == kfree) mine = 0;
     if (lane == kfree + 1) mine = jt - 1;
@@ -290,20 +346,25 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
 
 // Final combine, run by the last selection CTA of a group:
 //   out = g_cmp * O_cmp + g_slc * O_slc + g_win * O_win
-// with each branch's unit partials weighted by exp(m_unit - M) / L.
+// with each branch's unit partials weighted by exp(m_unit - M) / L.  The
+// statistics, the gates and part_cap partials at a time are staged into
+// shared memory with asynchronous copies.
 template <int DV>
 __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int b = bg / a.G, g = bg % a.G;
   const int NS = a.NS;
+  constexpr int kE4 = (16 * DV / 4 + kThreads - 1) / kThreads;   // float4 elements per thread
   float* sp = reinterpret_cast<float*>(smem);    // [NS][2][16] unit max, sum
   float* fac = sp + 32 * NS;                     // [NS][16] weight of each partial
   float* gt = fac + 16 * NS;                     // [16][3]
-  for (int e = tid; e < NS * 16; e += kThreads) {
-    const size_t o = ((size_t)bg * NS + e / 16) * 16 + (e & 15);
-    sp[(e / 16) * 32 + (e & 15)] = ldcg_f(a.pm + o);
-    sp[(e / 16) * 32 + 16 + (e & 15)] = ldcg_f(a.pl + o);
-  }
+  float* cst = gt + 48;                          // [32] compressed statistics
+  float* pos = reinterpret_cast<float*>(smem) + ((48 * NS + 48 + 32 + 31) & ~31);   // [part_cap][16][DV]
+  const float* po = a.po + (size_t)bg * NS * 16 * DV;
+  stage_stats(a, bg, 0, NS, sp);
+  stage(cst, a.stats + (size_t)bg * 32, 8);
+  const int pb = a.part_cap;
+  for (int r = 0; r < pb && r < NS; ++r) stage(pos + (size_t)r * 16 * DV, po + (size_t)r * 16 * DV, 16 * DV / 4);
   if (tid < 16) {
     const bool hv = tid < a.hpg;
     const __nv_bfloat16* gp = a.gates + ((size_t)b * a.H + g * a.hpg + (hv ? tid : 0)) * 3;
@@ -311,12 +372,12 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
     gt[tid * 3 + 1] = hv ? __bfloat162float(gp[1]) : 0.f;
     gt[tid * 3 + 2] = hv ? __bfloat162float(gp[2]) : 0.f;
   }
+  cp_async_wait_all();
   __syncthreads();
   if (tid < 16) {
     const int h = tid;
     // compressed: statistics from the selection step, folded with g_cmp
-    const float Mc = ldcg_f(a.stats + (size_t)bg * 32 + h);
-    const float iLc = ldcg_f(a.stats + (size_t)bg * 32 + 16 + h);
+    const float Mc = cst[h], iLc = cst[16 + h];
     for (int s = 0; s < a.ncu; ++s) fac[s * 16 + h] = gt[h * 3 + 0] * fast_exp2(sp[s * 32 + h] - Mc) * iLc;
     // window and selected: merge their units here
     auto branch = [&](int s0, int s1, float gate) {
@@ -332,29 +393,43 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
     branch(a.ncu + a.nwu, NS, gt[h * 3 + 1]);
   }
   __syncthreads();
-  const float* po = a.po + (size_t)bg * NS * 16 * DV;
-  for (int e4 = tid; e4 < a.hpg * DV / 4; e4 += kThreads) {
-    const int h = (4 * e4) / DV;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // up to 16 partials per round, all loads issued before use
-    for (int s0 = 0; s0 < NS; s0 += 16) {
-      float4 v[16];
+  float4 acc[kE4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        v[k] = s0 + k < NS ? ldcg4(po + ((size_t)(s0 + k) * 16) * DV + 4 * e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < kE4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b0 = 0; b0 < NS; b0 += pb) {
+    const int nb = min(pb, NS - b0);
+    if (b0 > 0) {
+      __syncthreads();   // the previous batch is consumed
+      for (int r = 0; r < nb; ++r)
+        stage(pos + (size_t)r * 16 * DV, po + (size_t)(b0 + r) * 16 * DV, 16 * DV / 4);
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    for (int r = 0; r < nb; ++r) {
+      const float4* src = reinterpret_cast<const float4*>(pos + (size_t)r * 16 * DV);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float f = s0 + k < NS ? fac[(s0 + k) * 16 + h] : 0.f;
-        acc.x += f * v[k].x;
-        acc.y += f * v[k].y;
-        acc.z += f * v[k].z;
-        acc.w += f * v[k].w;
+      for (int k = 0; k < kE4; ++k) {
+        const int e4 = tid + kThreads * k;
+        if (e4 < a.hpg * DV / 4) {
+          const float f = fac[(b0 + r) * 16 + (4 * e4) / DV];
+          const float4 v = src[e4];
+          acc[k].x += f * v.x;
+          acc[k].y += f * v.y;
+          acc[k].z += f * v.z;
+          acc[k].w += f * v.w;
+        }
       }
     }
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x, acc.y);
-    pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)b * a.H + g * a.hpg) * DV + 4 * e4) = pk;
+  }
+#pragma unroll
+  for (int k = 0; k < kE4; ++k) {
+    const int e4 = tid + kThreads * k;
+    if (e4 < a.hpg * DV / 4) {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[k].x, acc[k].y);
+      pk.y = pack_bf16x2(acc[k].z, acc[k].w);
+      *reinterpret_cast<uint2*>(a.out + ((size_t)b * a.H + g * a.hpg) * DV + 4 * e4) = pk;
+    }
   }
 }
 
@@ -735,6 +810,7 @@ DecWs dec_ws(const nsa_cfg& c) {
 
 struct DecLayout {
   uint32_t off_kring, off_vring, off_pt, off_red, off_bar, total;
+  int sel_cap, part_cap;
 };
 
 DecLayout dec_layout(const nsa_cfg& c) {
@@ -745,14 +821,22 @@ DecLayout dec_layout(const nsa_cfg& c) {
   L.off_pt = L.off_vring + kRingV * kSlotV;
   L.off_red = L.off_pt + kPBuf;
   const size_t body = L.off_red + 2 * 4 * NP * sizeof(float);
-  // the last-CTA steps reuse the start of shared memory
-  const size_t jt1 = (size_t)(c.T - 1) / 64 + 1;
-  const size_t select = sizeof(float) * (32 + 256 + 48 * (size_t)s.ncu + jt1);
-  const size_t combine = sizeof(float) * (48 * (size_t)s.NS + 48);
-  size_t end = body;
-  if (select > end) end = select;
-  if (combine > end) end = combine;
+  // The last-CTA steps reuse the start of shared memory as staging: at least
+  // 1,024 blocks (or all) of selection inputs and 4 (or all) partials, more if
+  // the pipeline area is larger.
+  const int jt = (c.T - 1) / 64;
+  const int nblk = s.Nc > 0 ? std::min(jt + 1, (s.Nc + 3) / 4) : 1;
+  const long sel_fixed = sel_stage(s.ncu, jt, 0).total;
+  const long head = (48L * s.NS + 48 + 32 + 31) & ~31L;
+  const long need_sel = sel_fixed + 16L * std::min(((long)nblk + 3) & ~3L, 1024L);
+  const long need_comb = head + 16L * c.dv * std::min(s.NS, 4);
+  size_t end = std::max<size_t>(body, 4 * (size_t)std::max(need_sel, need_comb));
   L.off_bar = (uint32_t)align_up(end, 256);
+  const long avail_f = L.off_bar / 4;
+  long cap = (avail_f - sel_fixed) / 16;
+  cap = std::min<long>(cap, ((long)nblk + 3) & ~3L) & ~3L;
+  L.sel_cap = (int)std::max(cap, 4L);
+  L.part_cap = (int)std::max(1L, std::min<long>((avail_f - head) / (16L * c.dv), s.NS));
   L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;
   return L;
 }
@@ -857,6 +941,8 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
   a.off_pt = L.off_pt;
   a.off_red = L.off_red;
   a.off_bar = L.off_bar;
+  a.sel_cap = L.sel_cap;
+  a.part_cap = L.part_cap;
 
 #define NSA_DEC_CASE(DK_, DV_) \
   if (c.dk == DK_ && c.dv == DV_) return launch_dims<DK_, DV_>(a, sh, maps, L.total, s);
