@@ -458,20 +458,25 @@ def run_decode_leg(args, ws):
 
 
 # ---------------------------------------------------------------- DSA decode leg
-def run_dsa_leg(args, ws):
+def run_dsa_leg(args, ws, latent=False):
     """One DSA-style decode step: batch 8, 131,072-token context, indexer of 4
     heads x 64 dims, top-2048 positions, attention of 16 heads (dk=576,
-    dv=512) over the kept positions only."""
+    dv=512) over the kept positions only.  latent: the values are the first
+    512 columns of the 576-column key rows (latent KV), so only keys are
+    gathered."""
     import sparse_attention_long_10_b300 as nsa
     wl = dsa_config()
     inp = make_dsa(wl)
-    dev = {k: v.cuda() for k, v in inp.items()}
+    if latent:
+        inp["v"] = None
+    dev = {k: v.cuda() for k, v in inp.items() if v is not None}
     cfg = nsa.make_dsa_cfg(wl.B, wl.T, wl.HI, wl.dI, wl.H, wl.dk, wl.dv, wl.topk)
     out = torch.empty(wl.B, wl.H, wl.dv, dtype=torch.bfloat16, device="cuda")
     wsp = nsa.workspace(nsa.dsa_decode_workspace_size(cfg))
 
     def step():
-        nsa.dsa_decode_step(cfg, dev["qI"], dev["wI"], dev["kI"], dev["q"], dev["k"], dev["v"], out, None, wsp)
+        nsa.dsa_decode_step(cfg, dev["qI"], dev["wI"], dev["kI"], dev["q"], dev["k"], dev.get("v"), out, None,
+                            wsp)
 
     for _ in range(args.warmup):
         step()
@@ -522,17 +527,19 @@ def run_dsa_leg(args, ws):
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_times), ws)
     kk = min(wl.topk, wl.T)
-    nbytes = wl.B * wl.T * wl.dI * 2 + wl.B * kk * (wl.dk + wl.dv) * 2
+    nbytes = wl.B * wl.T * wl.dI * 2 + wl.B * kk * (wl.dk + (0 if latent else wl.dv)) * 2
     pk = peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {
-        "metric": "DSA decode step latency (8 rows x 131,072-token context, top-2048)",
+        "metric": ("DSA decode step latency, latent KV (values = first 512 key columns)" if latent else
+                   "DSA decode step latency") + " (8 rows x 131,072-token context, top-2048)",
         "value": ms * 1e3, "unit": "us", "higher_is_better": False,
-        "workload": wl.name, "steps": args.steps, "bytes_per_step": nbytes,
+        "workload": wl.name + ("_latent" if latent else ""), "steps": args.steps, "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})", "traffic": ncu_traffic("dsa"),
-                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step; "
-                             "traffic: " + NCU_TRAFFIC["dsa"]["how"]},
+                     "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})",
+                     "traffic": None if latent else ncu_traffic("dsa"),
+                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step"
+                             + ("" if latent else "; traffic: " + NCU_TRAFFIC["dsa"]["how"])},
         "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
                     for k, (c, t) in prof.items()},
         "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
@@ -549,7 +556,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and DSA decode legs")
-    ap.add_argument("--workload", default="prefill_64k", choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k"],
+    ap.add_argument("--workload", default="prefill_64k",
+                    choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k", "dsa_latent_128k"],
                     help="prefill workload (the headline is prefill_64k; smaller ones serve profiling) or "
                          "decode_64k / dsa_128k: one decode leg alone")
     args = ap.parse_args()
@@ -578,8 +586,11 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
-    if args.workload in ("decode_64k", "dsa_128k"):
-        res = (run_decode_leg if args.workload == "decode_64k" else run_dsa_leg)(args, ws)
+    if args.workload in ("decode_64k", "dsa_128k", "dsa_latent_128k"):
+        if args.workload == "decode_64k":
+            res = run_decode_leg(args, ws)
+        else:
+            res = run_dsa_leg(args, ws, latent=args.workload == "dsa_latent_128k")
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
@@ -589,6 +600,8 @@ def main():
         res["gpu_launches"] += res["decode"]["gpu_launches_per_step"] * args.steps
         res["dsa"] = run_dsa_leg(args, ws)
         res["gpu_launches"] += res["dsa"]["gpu_launches_per_step"] * args.steps
+        res["dsa_latent"] = run_dsa_leg(args, ws, latent=True)
+        res["gpu_launches"] += res["dsa_latent"]["gpu_launches_per_step"] * args.steps
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         blas, ncpu = cpu_cores()
         rate, info = oracle_prefill_rate(inp, rows_per_step=16, steps=2)

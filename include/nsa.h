@@ -202,6 +202,11 @@ size_t dsa_decode_workspace_size(const dsa_cfg* cfg);
  *   qI [B,HI,dI]   wI [B,HI]   kI [B,T,dI]   q [B,H,dk]   k [B,T,dk]
  *   v [B,T,dv]     out [B,H,dv]
  *   idx_out (nullable): [B, min(topk,T)] int32, ascending
+ * v may be NULL when dv <= dk: value row s is then the first dv columns of
+ * key row s -- the latent KV of multi-head latent attention, on which the
+ * page builds DSA (one cached latent per token, positional part in the last
+ * dk-dv columns) -- and only the key rows are fetched.  A NULL v with
+ * dv > dk returns NSA_ERR_INVALID_ARG.
  */
 int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI,
                     const void* q, const void* k, const void* v, void* out, int32_t* idx_out,

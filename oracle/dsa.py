@@ -77,15 +77,29 @@ def dsa_attention(q: np.ndarray, Ksel: np.ndarray, Vsel: np.ndarray, scale: floa
 
 
 def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
-                         batches: Optional[Iterable[int]] = None) -> Dict[str, np.ndarray]:
+                         batches: Optional[Iterable[int]] = None,
+                         latent_dv: Optional[int] = None) -> Dict[str, np.ndarray]:
     """One DSA decode step for the batch rows ``batches`` (default all).
 
     inp: bf16 tensors of ``workloads.make_dsa``.  Returns out [S,H,dv],
     idx [S,min(k,T)] (ascending), I [S,T] fp64 and I32 [S,T] fp32 scores.
+
+    With ``inp["v"] is None`` the values are latent: value row s is the first
+    ``latent_dv`` columns of key row s.  Same page, the paragraph that puts
+    DSA on multi-head latent attention: one compressed latent vector is cached
+    per token (its positional part kept as a separate stream), so keys and
+    values are read from the same cached row.
     """
-    qI, wI, kI, q, k, v = (inp[n] for n in ("qI", "wI", "kI", "q", "k", "v"))
+    qI, wI, kI, q, k = (inp[n] for n in ("qI", "wI", "kI", "q", "k"))
+    v = inp.get("v")
     B, T, dk = k.shape
-    H, dv = q.shape[1], v.shape[2]
+    H = q.shape[1]
+    if v is None:
+        if latent_dv is None or latent_dv > dk:
+            raise ValueError("latent values need latent_dv <= dk")
+        dv = latent_dv
+    else:
+        dv = v.shape[2]
     scale = 1.0 / math.sqrt(dk)
     batches = list(range(B)) if batches is None else list(batches)
     kk = min(topk, T)
@@ -97,7 +111,9 @@ def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
         I32 = I.astype(np.float32)
         sel = topk_positions(I32, topk)
         ti = torch.as_tensor(sel)
-        res["out"][si] = dsa_attention(to_f64(q[b]), to_f64(k[b, ti]), to_f64(v[b, ti]), scale)
+        Ksel = to_f64(k[b, ti])
+        Vsel = Ksel[:, :dv] if v is None else to_f64(v[b, ti])
+        res["out"][si] = dsa_attention(to_f64(q[b]), Ksel, Vsel, scale)
         res["idx"][si], res["I"][si], res["I32"][si] = sel, I, I32
     res["batches"] = np.array(batches)
     return res

@@ -232,7 +232,9 @@ int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const vo
                     void* stream) {
   int rc = validate_dsa(cfg);
   if (rc != NSA_OK) return rc;
-  if ((rc = check_ptrs({qI, wI, kI, q, k, v, out})) != NSA_OK) return rc;
+  if ((rc = check_ptrs({qI, wI, kI, q, k, out})) != NSA_OK) return rc;
+  // v == NULL: values are the first dv columns of the key rows (latent KV)
+  if (v == nullptr ? cfg->dv > cfg->dk : !aligned16(v)) return v == nullptr ? NSA_ERR_INVALID_ARG : NSA_ERR_MISALIGNED;
   if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
   if ((rc = check_ws(ws, ws_bytes, dsa_ws_bytes(*cfg))) != NSA_OK) return rc;
   if ((rc = check_device()) != NSA_OK) return rc;

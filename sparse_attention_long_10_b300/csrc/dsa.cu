@@ -56,7 +56,8 @@ struct DsaArgs {
   const __nv_bfloat16* wI;          // [B,HI]
   const __nv_bfloat16* q;           // [B,H,dk]
   const __nv_bfloat16* k;           // [B,T,dk]
-  const __nv_bfloat16* v;           // [B,T,dv]
+  const __nv_bfloat16* v;           // [B,T,dv]; unused when v_from_k
+  int v_from_k;                     // values are the first dv columns of k (latent KV)
   __nv_bfloat16* out;               // [B,H,dv]
   int32_t* idx_out;                 // nullable [B,kk]
   uint32_t* keys;                   // [B,T]
@@ -602,18 +603,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs
         uint8_t* vs = ks + kAttnTile * L.kst;
         const int nv = min(kAttnTile, nent - i * kAttnTile);
         const int e = i * kAttnTile + lane;
+        // with latent KV the value rows are the first DV columns of the key
+        // rows: only the keys are fetched
+        const uint32_t vbytes = a.v_from_k ? 0u : 2u * DV;
         if (lane >= nv) {   // absent rows read as zeros
           for (int c = 0; c < dk / 8; ++c) *reinterpret_cast<uint4*>(ks + lane * L.kst + 16 * c) = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(vs + lane * L.vst + 16 * c) = make_uint4(0, 0, 0, 0);
+          if (!a.v_from_k)
+            for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(vs + lane * L.vst + 16 * c) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&bars->full[slot], (uint32_t)nv * (uint32_t)(2 * dk + 2 * DV));
+        if (lane == 0) mbar_arrive_expect_tx(&bars->full[slot], (uint32_t)nv * (2u * dk + vbytes));
         __syncwarp();
         if (lane < nv) {
           const int pos = __ldg(sel + e);
           bulk_load(ks + lane * L.kst, a.k + ((size_t)b * a.T + pos) * dk, 2u * dk, &bars->full[slot]);
-          bulk_load(vs + lane * L.vst, a.v + ((size_t)b * a.T + pos) * DV, 2u * DV, &bars->full[slot]);
+          if (!a.v_from_k)
+            bulk_load(vs + lane * L.vst, a.v + ((size_t)b * a.T + pos) * DV, 2u * DV, &bars->full[slot]);
         }
       }
       if (lane == 0 && (!ok || *abort_flag))
@@ -630,7 +636,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs
         break;
       }
       const uint32_t k_a = smem_u32(smem + L.ks_off + slot * L.stage);
-      const uint32_t v_a = k_a + kAttnTile * L.kst;
+      const uint32_t v_a = a.v_from_k ? k_a : k_a + kAttnTile * L.kst;
+      const uint32_t vst = a.v_from_k ? L.kst : L.vst;
       const int nv = min(kAttnTile, nent - i * kAttnTile);
       // S[16 heads x 8 keys] for keys 8*warp .. 8*warp+7
       float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs
 #pragma unroll
         for (int np = 0; np < DV4 / 16; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(v_a + (uint32_t)(16 * kk2 + (lane & 7) + ((lane >> 3) & 1) * 8) * L.vst +
+          ldsm_x4_t(v_a + (uint32_t)(16 * kk2 + (lane & 7) + ((lane >> 3) & 1) * 8) * vst +
                         (uint32_t)(warp * DV4 + 16 * np + (lane >> 4) * 8) * 2,
                     b0, b1, b2, b3);
           mma_16816(o[2 * np], pa, b0, b1);
@@ -928,7 +935,8 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.wI = static_cast<const __nv_bfloat16*>(wI);
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.v_from_k = v == nullptr ? 1 : 0;
+  a.v = static_cast<const __nv_bfloat16*>(v != nullptr ? v : k);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.idx_out = idx_out;
   a.keys = reinterpret_cast<uint32_t*>(ws + w.keys);

@@ -104,3 +104,20 @@ def test_valid_call_without_device_reports_no_device(nsa):
     rc = nsa.lib.nsa_compress_kv(ctypes.byref(c), 0, FAKE, FAKE, FAKE, FAKE, FAKE,
                                  nsa.nsa_compress_workspace_size(c), None)
     assert rc == 7
+
+
+def test_dsa_latent_values_argument_checks(nsa):
+    """dsa_decode_step with v == NULL reads the values from the key rows; that
+    needs dv <= dk (else INVALID_ARG), and a given v must be 16-byte aligned."""
+    f = nsa.lib.dsa_decode_step
+    c = nsa.make_dsa_cfg(8, 131072, 4, 64, 16, 576, 512, 2048)
+    need = nsa.dsa_decode_workspace_size(c)
+    assert need > 0
+    bad = nsa.make_dsa_cfg(8, 131072, 4, 64, 16, 64, 128, 2048)   # dv > dk
+    assert f(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE,
+             nsa.dsa_decode_workspace_size(bad), None) == 1
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, None, FAKE, need, None) == 3
+    if not torch.cuda.is_available():
+        # valid arguments, latent or not: the no-device status
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 7
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None) == 7

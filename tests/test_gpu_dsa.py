@@ -28,19 +28,20 @@ def _nsa():
     return nsa
 
 
-def run_dsa(inp, topk):
+def run_dsa(inp, topk, latent_dv=None):
+    """inp["v"] None: latent values, the first latent_dv columns of k."""
     nsa = _nsa()
-    d = {k: t.cuda() for k, t in inp.items()}
+    d = {k: t.cuda() for k, t in inp.items() if t is not None}
     B, T, dI = inp["kI"].shape
     HI = inp["qI"].shape[1]
     H, dk = inp["q"].shape[1], inp["q"].shape[2]
-    dv = inp["v"].shape[2]
+    dv = inp["v"].shape[2] if inp.get("v") is not None else latent_dv
     cfg = nsa.make_dsa_cfg(B, T, HI, dI, H, dk, dv, topk)
     kk = min(topk, T)
     out = torch.full((B, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     idx = torch.full((B, kk), -7, dtype=torch.int32, device="cuda")
     ws = nsa.workspace(nsa.dsa_decode_workspace_size(cfg))
-    nsa.dsa_decode_step(cfg, d["qI"], d["wI"], d["kI"], d["q"], d["k"], d["v"], out, idx, ws)
+    nsa.dsa_decode_step(cfg, d["qI"], d["wI"], d["kI"], d["q"], d["k"], d.get("v"), out, idx, ws)
     torch.cuda.synchronize()
     assert nsa.nsa_device_status(ws) == 0
     return out, idx
@@ -67,8 +68,9 @@ def check_dsa(inp, ref, out, idx, topk, label="", exact_idx=False):
         assert ok, f"{label} b={b}: GPU set is not a valid top-{topk} (gap {gap:.3g})"
         near += 1
         ti = torch.as_tensor(row.astype(np.int64))
-        expect[si] = D.dsa_attention(O.to_f64(inp["q"][b]), O.to_f64(inp["k"][b, ti]),
-                                     O.to_f64(inp["v"][b, ti]), scale)
+        Ksel = O.to_f64(inp["k"][b, ti])
+        Vsel = Ksel[:, :expect.shape[2]] if inp.get("v") is None else O.to_f64(inp["v"][b, ti])
+        expect[si] = D.dsa_attention(O.to_f64(inp["q"][b]), Ksel, Vsel, scale)
     assert np.isfinite(got).all(), f"{label}: non-finite output"
     err = np.abs(got - expect)
     print(f"{label}: rows={len(batches)} max_abs={err.max():.3e} mean_abs={err.mean():.3e} near_ties={near}")
@@ -133,3 +135,24 @@ def test_dsa_twice_is_deterministic():
     o1, i1 = run_dsa(inp, 256)
     o2, i2 = run_dsa(inp, 256)
     assert torch.equal(i1, i2) and torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("T,topk", [(3000, 256), (3000, 2048), (700, 2048), (1, 5)])
+def test_dsa_latent_values_small(T, topk):
+    """Latent KV: values are the first dv columns of the key rows (v = NULL)."""
+    inp = make_dsa(SMALL, T=T)
+    inp["v"] = None
+    ref = D.dsa_decode_reference(inp, topk, latent_dv=SMALL.dv)
+    out, idx = run_dsa(inp, topk, latent_dv=SMALL.dv)
+    check_dsa(inp, ref, out, idx, topk, label=f"dsa latent T={T} k={topk}")
+
+
+def test_dsa_latent_values_full_size():
+    """Batch 8 x 131,072-token context, top-2048, dk=576 latent keys whose
+    first 512 columns are the values; the oracle checks every row."""
+    wl = dsa_config()
+    inp = make_dsa(wl)
+    inp["v"] = None
+    out, idx = run_dsa(inp, wl.topk, latent_dv=wl.dv)
+    ref = D.dsa_decode_reference(inp, wl.topk, latent_dv=wl.dv)
+    check_dsa(inp, ref, out, idx, wl.topk, label="dsa latent 8x128k")

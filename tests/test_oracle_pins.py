@@ -375,3 +375,27 @@ def test_dsa_full_when_k_covers_context():
         V = O.to_f64(inp["v"][b])
         ref = np.stack([_sdpa(q[h:h + 1], K, V)[0] for h in range(q.shape[0])])
         np.testing.assert_allclose(res["out"][b], ref, rtol=0, atol=1e-12)
+
+
+def test_dsa_latent_values_when_k_covers_context():
+    """Latent KV (values = first dv columns of the key rows): with top-k
+    covering the context the step is full softmax attention over K with
+    V = K[:, :dv]."""
+    wl = dsa_config()
+    inp = make_dsa(wl, B=2, T=300)
+    inp["v"] = None
+    res = D.dsa_decode_reference(inp, topk=512, latent_dv=wl.dv)
+    assert res["out"].shape == (2, wl.H, wl.dv)
+    for b in range(2):
+        q = O.to_f64(inp["q"][b])
+        K = O.to_f64(inp["k"][b])
+        ref = np.stack([_sdpa(q[h:h + 1], K, K[:, :wl.dv])[0] for h in range(q.shape[0])])
+        np.testing.assert_allclose(res["out"][b], ref, rtol=0, atol=1e-12)
+
+
+def test_dsa_latent_values_need_dv_within_dk():
+    wl = dsa_config()
+    inp = make_dsa(wl, B=1, T=64)
+    inp["v"] = None
+    with pytest.raises(ValueError):
+        D.dsa_decode_reference(inp, topk=8, latent_dv=wl.dk + 64)
