@@ -153,11 +153,14 @@ NCU_TRAFFIC = {
     "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "8e95e29f6cf25549",
                 "bytes": 8 * 331.0e6, "how": "T=8192 capture scaled by 8 to T=65536"},
     # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
-    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "d5cbd0ff85a2afaa",
-               "bytes": (189.2 + 10.2 + 52.0 + 0.4) * 1e6, "how": "full-size capture, both kernels"},
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "47f3075901eb5801",
+               "bytes": (189.24 + 10.74 + 52.01 + 0.38) * 1e6, "how": "full-size capture, both kernels"},
     # profiles/dsa_B8_T131072_kernels.md: the five kernels of one step
-    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "d8c2d043ad94ac93",
-            "bytes": (134.4 + 4.7 + 4.3 + 4.2 + 35.9 + 0.1 + 8.4) * 1e6, "how": "full-size capture, five kernels"},
+    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "ff0775d98b4492d6",
+            "bytes": (134.38 + 4.37 + 4.25 + 4.21 + 35.89 + 0.08 + 8.44) * 1e6, "how": "full-size capture, five kernels"},
+    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "ff0775d98b4492d6",
+                   "bytes": (134.38 + 4.44 + 4.25 + 4.21 + 19.12 + 8.43) * 1e6,
+                   "how": "full-size capture, five kernels"},
 }
 
 
@@ -537,9 +540,9 @@ def run_dsa_leg(args, ws, latent=False):
         "workload": wl.name + ("_latent" if latent else ""), "steps": args.steps, "bytes_per_step": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
                      "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})",
-                     "traffic": None if latent else ncu_traffic("dsa"),
-                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step"
-                             + ("" if latent else "; traffic: " + NCU_TRAFFIC["dsa"]["how"])},
+                     "traffic": ncu_traffic("dsa_latent" if latent else "dsa"),
+                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step; "
+                             "traffic: " + NCU_TRAFFIC["dsa_latent" if latent else "dsa"]["how"]},
         "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
                     for k, (c, t) in prof.items()},
         "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
