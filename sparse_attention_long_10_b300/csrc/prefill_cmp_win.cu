@@ -19,9 +19,12 @@
 //                   warpgroup 0 takes key columns 0-63 of every S tile,
 //                   warpgroup 1 columns 64-127 (per-row max/sum are merged
 //                   between the two at the end of a statistics pass)
-//   warp  8         TMA producer (Q once, then a ring of 16 KB K/V chunks)
-//   warp  9         tcgen05 MMA issuer (single thread)
-// TMEM: S double buffer (2 x 128 columns) + O (dv columns).
+//   warp  8         TMA producer: Q once, then the key chunks (16 KB ring)
+//   warp  9         QK^T issuer (single thread), ahead by the two S buffers
+//   warp 10         TMA producer: the value chunks (16 KB ring)
+//   warp 11         PV issuer (single thread), P read from tensor memory
+// TMEM: S double buffer (2 x 128 columns), O (dv <= 128 columns), P as bf16
+// pairs (64 columns, the A operand of PV).
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -31,9 +34,10 @@ namespace nsa {
 
 namespace {
 
-constexpr int kRing = 6;
+constexpr int kRingK = 5;      // key chunks in flight
+constexpr int kRingV = 3;      // value chunks in flight
 constexpr int kSlot = 16384;   // 128 rows x 128 bytes
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
 
 struct CmpWinArgs {
@@ -43,18 +47,21 @@ struct CmpWinArgs {
   __nv_bfloat16* part;             // [B,T,H,dv]
   int32_t* idx;                    // [B,T,G,n]
   DeviceStatus* st;
-  uint32_t off_ring, off_p, off_scores, off_red, off_bar;
+  uint32_t off_kring, off_vring, off_scores, off_red, off_bar;
 };
 
 struct Bars {
   uint64_t q_full;
-  uint64_t ring_full[kRing];
-  uint64_t ring_empty[kRing];
+  uint64_t k_full[kRingK];
+  uint64_t k_empty[kRingK];
+  uint64_t v_full[kRingV];
+  uint64_t v_empty[kRingV];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
+  uint64_t drain[2];
   uint64_t all8;        // rendezvous of the 8 softmax warps
   uint32_t tmem;
   int abort_flag;
@@ -97,21 +104,6 @@ __device__ __forceinline__ float allreduce_group(float x) {
   return x;
 }
 
-// Write 64 bf16 probabilities of one row (keys 64*half .. 64*half+63) into the
-// 128B-swizzled K-major P tile.
-__device__ __forceinline__ void store_p_half(uint8_t* ps, int r, int half, const float (&p)[64], float gate) {
-#pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    const int i = cc * 8;
-    uint4 pk;
-    pk.x = pack_bf16x2(p[i + 0] * gate, p[i + 1] * gate);
-    pk.y = pack_bf16x2(p[i + 2] * gate, p[i + 3] * gate);
-    pk.z = pack_bf16x2(p[i + 4] * gate, p[i + 5] * gate);
-    pk.w = pack_bf16x2(p[i + 6] * gate, p[i + 7] * gate);
-    *reinterpret_cast<uint4*>(ps + half * kSlot + sw128_offset(r, cc)) = pk;
-  }
-}
-
 // 64 consecutive fp32 columns of one TMEM lane (four loads, one wait).
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
   uint32_t rs[4][16];
@@ -134,8 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qs = smem;
-  uint8_t* ring = smem + a.off_ring;
-  uint8_t* ps = smem + a.off_p;
+  uint8_t* kring = smem + a.off_kring;
+  uint8_t* vring = smem + a.off_vring;
   float* scores = reinterpret_cast<float*>(smem + a.off_scores);
   Bars* bars = reinterpret_cast<Bars*>(smem + a.off_bar);
   volatile int* abort_flag = &bars->abort_flag;
@@ -158,9 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&bars->ring_full[s], 1);
-      mbar_init(&bars->ring_empty[s], 1);
+    for (int s = 0; s < kRingK; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < kRingV; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -169,6 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
     mbar_init(&bars->all8, 8);
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
@@ -182,150 +180,143 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
   const uint32_t tmem_s = tmem;          // S buffers at columns 0 and 128
-  const uint32_t tmem_o = tmem + 256;    // O at columns 256 .. 256+dv
+  const uint32_t tmem_o = tmem + 256;    // O at columns 256 .. 256+dv (dv <= 128)
+  const uint32_t tmem_p = tmem + 384;    // P (bf16 pairs): 64 columns, the A operand of PV
 
   if (*abort_flag) {
     // an earlier CTA failed: do nothing
-  } else if (warp == 8) {
-    // =============================================================== producer
+  } else if (warp == 8 || warp == 10) {
+    // =============================================================== producers
+    // warp 8: Q, then the key chunks of every QK^T tile in issue order;
+    // warp 10: the value chunks of every PV tile
     if (lane == 0) {
-      tma_prefetch_desc(&mapQ);
-      tma_prefetch_desc(&mapKc);
-      tma_prefetch_desc(&mapVc);
-      tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * kSlot));
-      for (int c = 0; c < kcs; ++c) tma_load_4d(qs + c * kSlot, &mapQ, &bars->q_full, c * 64, g * HPG, t0, b);
+      const bool keys = warp == 8;
+      if (keys) {
+        tma_prefetch_desc(&mapQ);
+        tma_prefetch_desc(&mapKc);
+        tma_prefetch_desc(&mapK);
+        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * kSlot));
+        for (int c = 0; c < kcs; ++c) tma_load_4d(qs + c * kSlot, &mapQ, &bars->q_full, c * 64, g * HPG, t0, b);
+      } else {
+        tma_prefetch_desc(&mapVc);
+        tma_prefetch_desc(&mapV);
+      }
+      const int nring = keys ? kRingK : kRingV;
+      uint8_t* rbase = keys ? kring : vring;
+      uint64_t* full = keys ? bars->k_full : bars->v_full;
+      uint64_t* empty = keys ? bars->k_empty : bars->v_empty;
       int v = 0;
       bool ok = true;
       auto push = [&](const CUtensorMap* map, int c0, int c1, int c2, int c3) {
         if (!ok) return;
-        const int slot = v % kRing;
-        const uint32_t round = (uint32_t)(v / kRing);
-        if (!mbar_wait(&bars->ring_empty[slot], (round & 1) ^ 1, abort_flag, a.st, 201)) {
+        const int slot = v % nring;
+        const uint32_t round = (uint32_t)(v / nring);
+        if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_flag, a.st, keys ? 201 : 202)) {
           ok = false;
           return;
         }
-        mbar_arrive_expect_tx(&bars->ring_full[slot], kSlot);
-        tma_load_4d(ring + slot * kSlot, map, &bars->ring_full[slot], c0, c1, c2, c3);
+        mbar_arrive_expect_tx(&full[slot], kSlot);
+        tma_load_4d(rbase + slot * kSlot, map, &full[slot], c0, c1, c2, c3);
         ++v;
       };
-      auto push_kc = [&](int j) { for (int c = 0; c < kcs; ++c) push(&mapKc, c * 64, j * kTile, g, b); };
-      auto push_vc = [&](int j) { for (int c = 0; c < vcs; ++c) push(&mapVc, c * 64, j * kTile, g, b); };
-      auto push_k = [&](int j) { for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b); };
-      auto push_v = [&](int j) { for (int c = 0; c < vcs; ++c) push(&mapV, c * 64, g, s_lo + j * kTile, b); };
-      // phase 1: compressed keys; phase 2: compressed keys + values
-      for (int j = 0; j < ntc; ++j) push_kc(j);
-      if (ntc > 0) {
-        push_kc(0);
-        for (int j = 0; j < ntc; ++j) {
-          if (j + 1 < ntc) push_kc(j + 1);
-          push_vc(j);
-        }
-      }
-      // phase 3: window keys; phase 4: window keys + values
-      for (int j = 0; j < ntw; ++j) push_k(j);
-      push_k(0);
-      for (int j = 0; j < ntw; ++j) {
-        if (j + 1 < ntw) push_k(j + 1);
-        push_v(j);
+      if (keys) {
+        // compressed keys twice (statistics pass, exact pass), then window keys twice
+        for (int pass = 0; pass < 2; ++pass)
+          for (int j = 0; j < ntc; ++j)
+            for (int c = 0; c < kcs; ++c) push(&mapKc, c * 64, j * kTile, g, b);
+        for (int pass = 0; pass < 2; ++pass)
+          for (int j = 0; j < ntw; ++j)
+            for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b);
+      } else {
+        for (int j = 0; j < ntc; ++j)
+          for (int c = 0; c < vcs; ++c) push(&mapVc, c * 64, j * kTile, g, b);
+        for (int j = 0; j < ntw; ++j)
+          for (int c = 0; c < vcs; ++c) push(&mapV, c * 64, g, s_lo + j * kTile, b);
       }
       if (!ok || *abort_flag) {
-        mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
-        for (int x = (v > kRing ? v - kRing : 0); x < v; ++x)
-          mbar_wait_plain(&bars->ring_full[x % kRing], (uint32_t)((x / kRing) & 1), kWaitLimitNs);
+        if (keys) mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
+        for (int x = (v > nring ? v - nring : 0); x < v; ++x)
+          mbar_wait_plain(&full[x % nring], (uint32_t)((x / nring) & 1), kWaitLimitNs);
       }
     }
-  } else if (warp == 9) {
-    // =============================================================== MMA issuer
+  } else if (warp == 9 || warp == 11) {
+    // =============================================================== MMA issuers
+    // warp 9: QK^T of every tile (statistics and exact passes), limited only
+    // by the two S buffers; warp 11: PV of every exact-pass tile, as soon as
+    // its P is in tensor memory
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 64, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 211);
-      int u = 0, v = 0, pv = 0;
-      bool first_pv = true;
-      const uint32_t qs_a = smem_u32(qs);
-      const uint32_t ring_a = smem_u32(ring);
-      const uint32_t ps_a = smem_u32(ps);
-      auto take_slot = [&](uint32_t& addr) -> bool {
-        const int slot = v % kRing;
-        const uint32_t round = (uint32_t)(v / kRing);
-        if (!mbar_wait(&bars->ring_full[slot], round & 1, abort_flag, a.st, 212)) return false;
-        tc_fence_after();
-        addr = ring_a + slot * kSlot;
-        return true;
-      };
-      auto release_slot = [&]() {
-        umma_commit(&bars->ring_empty[v % kRing]);
-        ++v;
-      };
-      auto issue_qk = [&]() {
-        if (!ok) return;
-        const int sb = u & 1;
-        const uint32_t use = (uint32_t)(u >> 1);
-        if (!mbar_wait(&bars->s_free[sb], (use & 1) ^ 1, abort_flag, a.st, 213)) {
-          ok = false;
-          return;
-        }
-        tc_fence_after();
-        for (int c = 0; c < kcs; ++c) {
-          uint32_t kaddr;
-          if (!take_slot(kaddr)) {
+      bool ok = true;
+      if (warp == 9) {
+        const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false, false);
+        const uint32_t qs_a = smem_u32(qs), k_a = smem_u32(kring);
+        ok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 211);
+        const int ntiles = 2 * ntc + 2 * ntw;
+        int kv = 0;
+        for (int u = 0; u < ntiles && ok; ++u) {
+          const int sb = u & 1;
+          const uint32_t use = (uint32_t)(u >> 1);
+          if (!mbar_wait(&bars->s_free[sb], (use & 1) ^ 1, abort_flag, a.st, 213)) {
             ok = false;
-            return;
+            break;
           }
+          tc_fence_after();
+          for (int c = 0; c < kcs; ++c) {
+            const int slot = kv % kRingK;
+            if (!mbar_wait(&bars->k_full[slot], (uint32_t)((kv / kRingK) & 1), abort_flag, a.st, 212)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sdesc_sw128(qs_a + c * kSlot + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kaddr + k * 32, 16, 1024);
-            umma_bf16(tmem_s + sb * kTile, ad, bd, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(qs_a + c * kSlot + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(k_a + slot * kSlot + k * 32, 16, 1024);
+              umma_bf16(tmem_s + sb * kTile, ad, bd, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(&bars->k_empty[slot]);
+            ++kv;
           }
-          release_slot();
+          if (ok) umma_commit(&bars->s_full[sb]);
         }
-        umma_commit(&bars->s_full[sb]);
-        ++u;
-      };
-      auto issue_pv = [&]() {
-        if (!ok) return;
-        if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214)) {
-          ok = false;
-          return;
+        if (!ok || *abort_flag) {
+          umma_commit(&bars->drain[0]);
+          mbar_wait_plain(&bars->drain[0], 0, kWaitLimitNs);
         }
-        tc_fence_after();
-        for (int c = 0; c < vcs; ++c) {
-          uint32_t vaddr;
-          if (!take_slot(vaddr)) {
+      } else {
+        const uint32_t idesc_pv = idesc_bf16_f32(128, 64, false, true);
+        const uint32_t v_a = smem_u32(vring);
+        const int npv = ntc + ntw;
+        int vv = 0;
+        for (int pv = 0; pv < npv && ok; ++pv) {
+          if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214)) {
             ok = false;
-            return;
+            break;
           }
+          tc_fence_after();
+          for (int c = 0; c < vcs; ++c) {
+            const int slot = vv % kRingV;
+            if (!mbar_wait(&bars->v_full[slot], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 215)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_sw128(ps_a + (k >> 2) * kSlot + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vaddr + k * 2048, kSlot, 1024);
-            umma_bf16(tmem_o + c * 64, ad, bd, idesc_pv, (first_pv && k == 0) ? 0u : 1u);
+            for (int k = 0; k < 8; ++k) {
+              // A = P from tensor memory (keys 16k .. 16k+15 = columns 8k .. 8k+7)
+              const uint64_t bd = sdesc_sw128(v_a + slot * kSlot + k * 2048, kSlot, 1024);
+              umma_bf16_ts(tmem_o + c * 64, tmem_p + 8 * k, bd, idesc_pv, (pv == 0 && k == 0) ? 0u : 1u);
+            }
+            umma_commit(&bars->v_empty[slot]);
+            ++vv;
           }
-          release_slot();
+          if (ok) umma_commit(&bars->p_free);
         }
-        first_pv = false;
-        umma_commit(&bars->p_free);
-        ++pv;
-      };
-      for (int j = 0; j < ntc; ++j) issue_qk();
-      if (ntc > 0) {
-        issue_qk();
-        for (int j = 0; j < ntc; ++j) {
-          if (j + 1 < ntc) issue_qk();
-          issue_pv();
+        if (ok) umma_commit(&bars->o_full);
+        if (!ok || *abort_flag) {
+          umma_commit(&bars->drain[1]);
+          mbar_wait_plain(&bars->drain[1], 0, kWaitLimitNs);
         }
       }
-      for (int j = 0; j < ntw; ++j) issue_qk();
-      issue_qk();
-      for (int j = 0; j < ntw; ++j) {
-        if (j + 1 < ntw) issue_qk();
-        issue_pv();
-      }
-      umma_commit(&bars->o_full);
-      if (!ok || *abort_flag) mbar_wait_plain(&bars->o_full, 0, kWaitLimitNs);
     }
   } else if (warp < 8) {
     // =============================================================== softmax warpgroups
@@ -374,8 +365,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars->p_free, (uint32_t)((pv & 1) ^ 1), abort_flag, a.st, 223)) return false;
       ++pv;
       tc_fence_after();
-      store_p_half(ps, r, wg, p, gate);
-      fence_proxy_async_smem();
+      // this row's 64 keys of the warpgroup's half, as bf16 pairs, into
+      // columns 32*wg .. 32*wg+31 of P in tensor memory
+      {
+        uint32_t pk[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[32 * hh + 2 * j] * gate, p[32 * hh + 2 * j + 1] * gate);
+          tmem_st16(tmem_p + lane_base + 32 * wg + 16 * hh, pk);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full);
       return true;
@@ -566,14 +568,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Layout {
-  uint32_t off_ring, off_p, off_scores, off_red, off_bar, total;
+  uint32_t off_kring, off_vring, off_scores, off_red, off_bar, total;
 };
 
 Layout layout_for(int dk, int QT, int nbs) {
   Layout L;
-  L.off_ring = (uint32_t)(dk / 64) * kSlot;
-  L.off_p = L.off_ring + kRing * kSlot;
-  L.off_scores = L.off_p + 2 * kSlot;
+  L.off_kring = (uint32_t)(dk / 64) * kSlot;
+  L.off_vring = L.off_kring + kRingK * kSlot;
+  L.off_scores = L.off_vring + kRingV * kSlot;
   L.off_red = (uint32_t)align_up(L.off_scores + (size_t)QT * nbs * sizeof(float), 256);
   L.off_bar = (uint32_t)align_up(L.off_red + 2 * 2 * 128 * sizeof(float), 1024);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;  // + alignment slack
@@ -670,8 +672,8 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
   a.part = static_cast<__nv_bfloat16*>(part);
   a.idx = idx;
   a.st = st;
-  a.off_ring = L.off_ring;
-  a.off_p = L.off_p;
+  a.off_kring = L.off_kring;
+  a.off_vring = L.off_vring;
   a.off_scores = L.off_scores;
   a.off_red = L.off_red;
   a.off_bar = L.off_bar;
