@@ -372,7 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(p[32 * hh + 2 * j] * gate, p[32 * hh + 2 * j + 1] * gate);
+          for (int j = 0; j < 16; ++j) {
+            const float2 gp = __fmul2_rn(make_float2(p[32 * hh + 2 * j], p[32 * hh + 2 * j + 1]), make_float2(gate, gate));
+            pk[j] = pack_bf16x2(gp.x, gp.y);
+          }
           tmem_st16(tmem_p + lane_base + 32 * wg + 16 * hh, pk);
         }
         tmem_st_wait();
@@ -384,17 +387,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // online max / sum over this warpgroup's columns; x holds raw scores
     // (-inf where masked), m is kept in log2 units (scores * scale * log2 e)
+    const float2 sc2x2 = make_float2(a.sc2, a.sc2);
     auto stats_add = [&](float (&x)[64], float& m, float& l) {
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 64; ++i) mt = fmaxf(mt, x[i]);
       const float mn = fmaxf(m, mt * a.sc2);
       if (mn == -INFINITY) return;
-      float sm = 0.f;
+      // pairs of columns through the packed f32x2 FMA / add
+      const float2 nm = make_float2(-mn, -mn);
+      float2 sm = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) sm += fast_exp2(fmaf(x[i], a.sc2, -mn));
-      l = l * fast_exp2(m - mn) + sm;
+      for (int i = 0; i < 64; i += 2) {
+        const float2 y = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2x2, nm);
+        sm = __fadd2_rn(sm, make_float2(fast_exp2(y.x), fast_exp2(y.y)));
+      }
+      l = l * fast_exp2(m - mn) + (sm.x + sm.y);
       m = mn;
+    };
+    // p = exp2(x * scale - mu) for 64 columns, pairs through the packed FMA
+    auto exp_cols = [&](float (&x)[64], float mu) {
+      const float2 nm = make_float2(-mu, -mu);
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        const float2 y = __ffma2_rn(make_float2(x[i], x[i + 1]), sc2x2, nm);
+        x[i] = fast_exp2(y.x);
+        x[i + 1] = fast_exp2(y.y);
+      }
     };
     // merge with the other warpgroup: afterwards m = max + log2(sum) of the
     // row (p = exp2(s*scale - m) is then normalised), +inf if the row is empty
@@ -421,8 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f, inv_l = 0.f;
     for (int j = 0; j < ntc && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
+      if (j * kTile + c0 + 64 > n_t) {   // only a row's last visible tile is masked
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? x[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? x[i] : -INFINITY;
+      }
       stats_add(x, m, l);
     }
     merge_stats(m, l, inv_l);
@@ -431,8 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool lead = (lane % HPG) == 0;
     for (int j = 0; j < ntc && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
+      if (j * kTile + c0 + 64 > n_t) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? fast_exp2(fmaf(x[i], a.sc2, -m)) : 0.f;
+        for (int i = 0; i < 64; ++i) x[i] = (j * kTile + c0 + i < n_t) ? fast_exp2(fmaf(x[i], a.sc2, -m)) : 0.f;
+      } else {
+        exp_cols(x, m);
+      }
       // block importance: selection block 32j+16wg+uu collects compressed
       // blocks 4u-1 (one chunk), 4u..4u+2 (two chunks each), 4u+3 (one chunk);
       // entry 4u-1 of the first block is added by whoever holds it (the
@@ -520,10 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntw && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
       const int s0 = s_lo + j * kTile + c0;
+      if (!(row_ok && s0 >= w_lo && s0 + 63 <= t)) {   // interior tiles need no mask
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int s = s0 + i;
-        x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] : -INFINITY;
+        for (int i = 0; i < 64; ++i) {
+          const int s = s0 + i;
+          x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] : -INFINITY;
+        }
       }
       stats_add(x, m, l);
     }
@@ -534,10 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntw && ok; ++j) {
       if (!consume_s(x)) { ok = false; break; }
       const int s0 = s_lo + j * kTile + c0;
+      if (row_ok && s0 >= w_lo && s0 + 63 <= t) {
+        exp_cols(x, mw);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int s = s0 + i;
-        x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(fmaf(x[i], a.sc2, -mw)) : 0.f;
+        for (int i = 0; i < 64; ++i) {
+          const int s = s0 + i;
+          x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(fmaf(x[i], a.sc2, -mw)) : 0.f;
+        }
       }
       if (!put_p(x, 1.f)) { ok = false; break; }
     }
