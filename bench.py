@@ -148,10 +148,11 @@ def max_over_ranks(x: float, ws: int) -> float:
 # bench line says null.
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
-    # profiles/prefill_T8192_cmp_win_sel.md: 331.0 MB per T=8192 launch, x8 for
-    # T=65536 (every stream of the kernel grows linearly in T)
-    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "8e95e29f6cf25549",
-                "bytes": 8 * 331.0e6, "how": "T=8192 capture scaled by 8 to T=65536"},
+    # profiles/prefill_T65536_traffic.md: one-pass DRAM capture of the full-size launches
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "a86d22aa1bbe30f5",
+                "bytes": (1858.05 + 1058.01) * 1e6, "how": "full-size capture (one pass)"},
+    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
+            "bytes": (3178.59 + 1075.17) * 1e6, "how": "full-size capture (one pass)"},
     # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
     "decode": {"files": ["decode.cu", "common.cuh"], "sha": "47f3075901eb5801",
                "bytes": (189.24 + 10.74 + 52.01 + 0.38) * 1e6, "how": "full-size capture, both kernels"},
@@ -331,8 +332,8 @@ def run_ours(args, ws, rank):
                      "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_sus"],
                      "peak_kind": f"bf16 dense sustained ({pk['src']})",
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "avg_launch_ms": dom_avg_ms,
-                     "traffic": ncu_traffic("cmp_win") if dom_name == "cmp_win" else None,
-                     "traffic_how": NCU_TRAFFIC["cmp_win"]["how"] if dom_name == "cmp_win" else None},
+                     "traffic": ncu_traffic(dom_name) if dom_name in NCU_TRAFFIC else None,
+                     "traffic_how": NCU_TRAFFIC[dom_name]["how"] if dom_name in NCU_TRAFFIC else None},
         "kernels": {k: {"launches_per_step": c / args.steps, "ms_per_step": t / args.steps,
                         "share": t / sum(x[1] for x in prof.values())} for k, (c, t) in prof.items()},
         "gpu_launches": int(launches),
