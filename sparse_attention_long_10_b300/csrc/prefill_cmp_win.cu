@@ -97,6 +97,17 @@ __device__ __forceinline__ int reduce_scatter16(float (&v)[16], int lane) {
   return base;
 }
 
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t x) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
+  return r;
+}
+
 template <int HPG>
 __device__ __forceinline__ float allreduce_group(float x) {
 #pragma unroll
@@ -491,40 +502,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const float* sq = scores + (size_t)qq * a.nbs;
-        // candidates 1 .. jt-2 (blocks 0, jt-1, jt are forced)
-        float cv[32];
+        // candidates 1 .. jt-2 (blocks 0, jt-1, jt are forced): each lane
+        // keeps its 8 best (higher score, then lower block) in a sorted list;
+        // a round's winner is a warp max reduction, ties to the lowest block,
+        // and only its owner lane pops (and refills after giving all 8)
+        float tv[8];
+        int tj[8];
+        auto fill = [&]() {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int jj = 1 + lane + 32 * k;
-          cv[k] = (jj <= jt - 2) ? sq[jj] : -INFINITY;
-        }
+          for (int k = 0; k < 8; ++k) {
+            tv[k] = -INFINITY;
+            tj[k] = 0x7fffffff;
+          }
+          for (int jj = 1 + lane; jj <= jt - 2; jj += 32) {
+            float cv = sq[jj];
+            if (!(cv > tv[7])) continue;
+            int cj = jj;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const bool sw = cv > tv[k];
+              const float t0v = tv[k];
+              const int t0j = tj[k];
+              tv[k] = sw ? cv : t0v;
+              tj[k] = sw ? cj : t0j;
+              cv = sw ? t0v : cv;
+              cj = sw ? t0j : cj;
+            }
+          }
+        };
+        fill();
         int mine = -1;
         const int nfree = a.n - 3;
         for (int rnd = 0; rnd < nfree; ++rnd) {
-          float best = -INFINITY;
-          int bk = 0;
+          const float gv = warp_max_f32(tv[0]);
+          const uint32_t gj = warp_min_u32(tv[0] == gv ? (uint32_t)tj[0] : 0x7fffffffu);
+          if (lane == rnd) mine = (gv == -INFINITY) ? 0x7fffffff : (int)gj;
+          if (gv != -INFINITY && (uint32_t)tj[0] == gj) {
+            // taken: mark it, pop the head
+            const_cast<float*>(sq)[gj] = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (cv[k] > best) {  // strict: lower k (lower index) wins ties
-              best = cv[k];
-              bk = k;
+            for (int k = 0; k < 7; ++k) {
+              tv[k] = tv[k + 1];
+              tj[k] = tj[k + 1];
             }
-          int bj = (best == -INFINITY) ? 0x7fffffff : 1 + lane + 32 * bk;
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-            if (ob > best || (ob == best && oj < bj)) {
-              best = ob;
-              bj = oj;
-            }
-          }
-          if (lane == rnd) mine = bj;
-          if (((bj - 1) & 31) == lane) {
-            const int kk = (bj - 1) >> 5;
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (k == kk) cv[k] = -INFINITY;
+            tv[7] = -INFINITY;
+            tj[7] = 0x7fffffff;
+            if (tv[0] == -INFINITY) fill();
           }
         }
         if (lane == nfree) mine = 0;
