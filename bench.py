@@ -149,18 +149,18 @@ def max_over_ranks(x: float, ws: int) -> float:
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
     # profiles/prefill_T65536_traffic.md: one-pass DRAM capture of the full-size launches
-    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "a86d22aa1bbe30f5",
-                "bytes": (1858.05 + 1058.01) * 1e6, "how": "full-size capture (one pass)"},
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "cc6821f8b5efc4bd",
+                "bytes": (1857.68 + 1058.13) * 1e6, "how": "full-size capture (one pass)"},
     "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
-            "bytes": (3178.59 + 1075.17) * 1e6, "how": "full-size capture (one pass)"},
+            "bytes": (3178.94 + 1075.05) * 1e6, "how": "full-size capture (one pass)"},
     # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
-    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "47f3075901eb5801",
-               "bytes": (189.24 + 10.74 + 52.01 + 0.38) * 1e6, "how": "full-size capture, both kernels"},
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "bfa28731f3c14d38",
+               "bytes": (189.27 + 9.80 + 52.01 + 0.02) * 1e6, "how": "full-size capture, both kernels"},
     # profiles/dsa_B8_T131072_kernels.md: the five kernels of one step
-    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "ff0775d98b4492d6",
-            "bytes": (134.38 + 4.37 + 4.25 + 4.21 + 35.89 + 0.08 + 8.44) * 1e6, "how": "full-size capture, five kernels"},
-    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "ff0775d98b4492d6",
-                   "bytes": (134.38 + 4.44 + 4.25 + 4.21 + 19.12 + 8.43) * 1e6,
+    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
+            "bytes": (134.39 + 4.03 + 4.25 + 4.21 + 35.90 + 8.44) * 1e6, "how": "full-size capture, five kernels"},
+    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
+                   "bytes": (134.38 + 4.10 + 4.25 + 4.21 + 19.12 + 8.44) * 1e6,
                    "how": "full-size capture, five kernels"},
 }
 
