@@ -154,7 +154,7 @@ NCU_TRAFFIC = {
     "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
             "bytes": (3178.94 + 1075.05) * 1e6, "how": "full-size capture (one pass)"},
     # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
-    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "bfa28731f3c14d38",
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "109c5bfaf71b561b",
                "bytes": (189.27 + 9.80 + 52.01 + 0.02) * 1e6, "how": "full-size capture, both kernels"},
     # profiles/dsa_B8_T131072_kernels.md: the five kernels of one step
     "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",

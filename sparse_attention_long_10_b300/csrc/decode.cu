@@ -435,9 +435,10 @@ __device__ void combine_step(const DecArgs& a, int bg, uint8_t* smem) {
 
 // One unit: up to kPairs pairs of 64-row blocks of one group against the
 // group's query heads.
-//   MODE 0: x < ncu     compressed entries [512x, 512x+512) (limit Nc)
-//           x >= ncu    window tokens win0 + 512(x-ncu) + [0, 512) (limit T)
-//   MODE 1: x           kept blocks idx[8x .. 8x+7] (token rows 64*blk)
+//   MODE 0: x < ncu     compressed entries [U x, U x + U) (limit Nc)
+//           x >= ncu    window tokens win0 + U (x-ncu) + [0, U) (limit T)
+//           (U = kUnitKeys = 256)
+//   MODE 1: x           kept blocks idx[4x .. 4x+3] (token rows 64*blk)
 template <int DK, int DV, int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
     dec_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mK0,
