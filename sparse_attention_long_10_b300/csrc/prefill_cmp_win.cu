@@ -36,6 +36,7 @@ namespace {
 
 constexpr int kRingK = 5;      // key chunks in flight
 constexpr int kRingV = 3;      // value chunks in flight
+static_assert(kRingV >= 2, "a tile's two value chunks must fit the ring");
 constexpr int kSlot = 16384;   // 128 rows x 128 bytes
 constexpr int kThreads = 384;
 constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
@@ -239,10 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < ntw; ++j)
             for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b);
       } else {
-        for (int j = 0; j < ntc; ++j)
-          for (int c = 0; c < vcs; ++c) push(&mapVc, c * 64, j * kTile, g, b);
-        for (int j = 0; j < ntw; ++j)
-          for (int c = 0; c < vcs; ++c) push(&mapV, c * 64, g, s_lo + j * kTile, b);
+        // with two value chunks a tile's PV is one N = 128 MMA per key step,
+        // whose B operand takes dv 0..63 from the lower of the tile's two
+        // slots: a tile that straddles the ring end (slots kRingV-1, 0) loads
+        // dv 64..127 first
+        for (int j = 0; j < ntc + ntw; ++j) {
+          const bool swap = vcs == 2 && v % kRingV == kRingV - 1;   // tile's first slot
+          for (int c = 0; c < vcs; ++c) {
+            const int cc = swap ? 1 - c : c;
+            if (j < ntc) push(&mapVc, cc * 64, j * kTile, g, b);
+            else push(&mapV, cc * 64, g, s_lo + (j - ntc) * kTile, b);
+          }
+        }
       }
       if (!ok || *abort_flag) {
         if (keys) mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
@@ -298,12 +307,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t v_a = smem_u32(vring);
         const int npv = ntc + ntw;
         int vv = 0;
+        const uint32_t idesc_pv2 = idesc_bf16_f32(128, 128, false, true);
         for (int pv = 0; pv < npv && ok; ++pv) {
           if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          if (vcs == 2) {
+            // both dv halves in one N = 128 MMA per key step: dv 0..63 sit in
+            // the lower of the tile's two slots, dv 64..127 LBO bytes above
+            const int s0 = vv % kRingV, s1 = (vv + 1) % kRingV;
+            if (!mbar_wait(&bars->v_full[s0], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 215) ||
+                !mbar_wait(&bars->v_full[s1], (uint32_t)(((vv + 1) / kRingV) & 1), abort_flag, a.st, 215)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int lo = s0 < s1 ? s0 : s1;
+            const uint32_t lbo = (uint32_t)((s0 < s1 ? s1 - s0 : s0 - s1) * kSlot);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint64_t bd = sdesc_sw128(v_a + lo * kSlot + k * 2048, lbo, 1024);
+              umma_bf16_ts(tmem_o, tmem_p + 8 * k, bd, idesc_pv2, (pv == 0 && k == 0) ? 0u : 1u);
+            }
+            umma_commit(&bars->v_empty[s0]);
+            umma_commit(&bars->v_empty[s1]);
+            vv += 2;
+            if (ok) umma_commit(&bars->p_free);
+            continue;
+          }
           for (int c = 0; c < vcs; ++c) {
             const int slot = vv % kRingV;
             if (!mbar_wait(&bars->v_full[slot], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 215)) {
