@@ -149,10 +149,10 @@ def max_over_ranks(x: float, ws: int) -> float:
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
     # profiles/prefill_T65536_traffic.md: one-pass DRAM capture of the full-size launches
-    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "cc6821f8b5efc4bd",
-                "bytes": (1857.68 + 1058.13) * 1e6, "how": "full-size capture (one pass)"},
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "e407d00cbc77e17d",
+                "bytes": (1857.36 + 1058.00) * 1e6, "how": "full-size capture (one pass)"},
     "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
-            "bytes": (3178.94 + 1075.05) * 1e6, "how": "full-size capture (one pass)"},
+            "bytes": (3176.90 + 1074.45) * 1e6, "how": "full-size capture (one pass)"},
     # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
     "decode": {"files": ["decode.cu", "common.cuh"], "sha": "109c5bfaf71b561b",
                "bytes": (189.27 + 9.80 + 52.01 + 0.02) * 1e6, "how": "full-size capture, both kernels"},
