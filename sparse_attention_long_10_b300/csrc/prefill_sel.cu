@@ -40,7 +40,7 @@ constexpr int kSlotK = 16384;
 constexpr int kSlotV = 32768;
 constexpr int kQBuf = 2048;      // one 64-column chunk of NP query rows
 constexpr int kPBuf = 32768;     // P^T of one item: 8 pairs x 2 chunks x 2 KB
-constexpr int kItemsPerCta = 32;
+constexpr int kItemsPerCta = 64;
 
 struct SelArgs {
   int T, H, G, dk, dv, n, hpg, QPC;
