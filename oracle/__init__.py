@@ -36,6 +36,10 @@ docstring.  Parity status per function:
                           pages print no worked example)
   dsa_decode ............ pinned (k >= T reduces to full softmax attention;
                           brute-force top-k; 131072/2048 = 64)
+  nsa_bwd (backward) .... pinned (central finite differences of the forward
+                          with the selection fixed; torch autograd of an
+                          independent torch forward; one-key and mean-pool
+                          closed forms)
 """
 from .nsa import *  # noqa: F401,F403
 from .dsa import *  # noqa: F401,F403

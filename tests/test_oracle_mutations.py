@@ -71,3 +71,48 @@ def test_window_off_by_one_is_caught(monkeypatch):
 def test_missing_relu_is_caught(monkeypatch):
     monkeypatch.setattr(D, "dsa_indexer_scores", lambda qI, wI, kI: (kI @ qI.T) @ wI)
     _fails(P.test_dsa_indexer_brute_force)
+
+
+# ---------------------------------------------------------------- backward oracle
+from oracle import nsa_bwd as BW  # noqa: E402
+import tests.test_oracle_backward as PB  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def bwd_case():
+    return PB.make_case()
+
+
+def test_dropped_softmax_correction_is_caught(monkeypatch, bwd_case):
+    real = BW.attend_bwd
+
+    def wrong(q, K, V, keys, scale, dO):    # dS = P dP: the "- dO . O" term dropped
+        if keys.size == 0:
+            return real(q, K, V, keys, scale, dO)
+        Kk, Vk = K[keys], V[keys]
+        s = (q @ Kk.T) * scale
+        P = np.exp(s - s.max(axis=-1, keepdims=True))
+        P /= P.sum(axis=-1, keepdims=True)
+        dS = P * (dO @ Vk.T)
+        return P @ Vk, scale * dS @ Kk, scale * dS.T @ q, P.T @ dO
+    monkeypatch.setattr(BW, "attend_bwd", wrong)
+    _fails(PB.check_finite_differences, bwd_case)
+
+
+def test_unscaled_key_gradient_is_caught(monkeypatch, bwd_case):
+    real = BW.attend_bwd
+
+    def wrong(q, K, V, keys, scale, dO):
+        O_, dq, dK, dV = real(q, K, V, keys, scale, dO)
+        return O_, dq, dK / scale, dV
+    monkeypatch.setattr(BW, "attend_bwd", wrong)
+    _fails(PB.check_finite_differences, bwd_case)
+
+
+def test_shifted_compression_scatter_is_caught(monkeypatch, bwd_case):
+    def wrong(X, PE, W, l, d, dXc):         # block i's gradient lands one token late
+        dX, dPE, dW = real(X, PE, W, l, d, dXc)
+        return np.roll(dX, 1, axis=0), dPE, dW
+    real = BW.compress_bwd
+    monkeypatch.setattr(BW, "compress_bwd", wrong)
+    _fails(PB.check_finite_differences, bwd_case)

@@ -29,7 +29,7 @@ import torch
 __all__ = [
     "NSAParams", "PrefillWorkload", "DecodeWorkload", "DSAWorkload",
     "prefill_config", "decode_config", "dsa_config",
-    "make_prefill", "make_decode", "make_dsa", "PREFILL_CONFIGS",
+    "make_prefill", "make_prefill_dout", "make_decode", "make_dsa", "PREFILL_CONFIGS",
 ]
 
 
@@ -140,6 +140,15 @@ def make_prefill(wl: PrefillWorkload, T: Optional[int] = None) -> Dict[str, torc
     pe_k, pe_v, w_k, w_v = _phi_params(gen, wl.params.l, wl.dk, wl.dv)
     gates = _gates(gen, (wl.B, T, wl.H, 3))
     return dict(q=q, k=k, v=v, pe_k=pe_k, pe_v=pe_v, w_k=w_k, w_v=w_v, gates=gates)
+
+
+def make_prefill_dout(wl: PrefillWorkload, T: Optional[int] = None) -> torch.Tensor:
+    """Upstream gradient dout [B,T,H,dv] of the prefill output for the
+    backward pass: bf16 N(0,1) from a generator of its own (seed + 1,000,003),
+    so the forward inputs of ``make_prefill`` are unchanged."""
+    T = wl.T if T is None else T
+    gen = torch.Generator("cpu").manual_seed(wl.seed + 1_000_003)
+    return _draw(gen, (wl.B, T, wl.H, wl.dv), 1.0)
 
 
 def make_decode(wl: DecodeWorkload, B: Optional[int] = None, T: Optional[int] = None
