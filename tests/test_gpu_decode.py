@@ -126,7 +126,7 @@ def test_decode_mid_heads_and_dims():
 
 def test_decode_end_to_end_compression():
     # the GPU compresses the caches; bf16 rounding flips of the cache move a
-    # block score by ~1e-4 relative, so near-ties are judged at 1e-3 here
+    # block score by ~1e-4 relative, so near-ties are taken at 1e-3 here
     inp = make_decode(MID)
     out, idx, _, _ = run_decode(inp)
     ref = O.nsa_decode_reference(inp)

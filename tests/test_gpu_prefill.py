@@ -120,7 +120,7 @@ def test_prefill_tiny_end_to_end_compression():
     # The GPU compresses too.  Its bf16 cache can differ from the oracle's by
     # one rounding step where the exact value sits on a rounding midpoint;
     # such a flip moves a block score by ~1e-4 relative, so near-ties are
-    # judged at 1e-3 here.
+    # taken at 1e-3 here.
     wl = PREFILL_CONFIGS["tiny_2k"]
     inp = make_prefill(wl)
     out, idx, _, _ = run_prefill(inp)
