@@ -120,8 +120,11 @@ def dist_setup():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")   # host-only runs of this bookkeeping
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return ws, rank, local
@@ -137,9 +140,16 @@ def max_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ms_max: float, ws: int) -> float:
+    """Replicas: every rank processes ``units_per_rank``; the job takes the
+    slowest rank's time."""
+    return ws * units_per_rank / (ms_max * 1e-3)
 
 
 # DRAM bytes (read + write) per launch or step from the ncu captures summarised
@@ -308,7 +318,7 @@ def run_ours(args, ws, rank):
     dom_flops = dict(cmp_win=flops["cmp"] + flops["win"], sel=flops["sel"],
                      compress_gemm=flops["phi"] / 2).get(dom_name, float("nan"))
     achieved = dom_flops / (dom_avg_ms * 1e-3) / 1e12
-    tok_s = ws * B * T / (ms * 1e-3)
+    tok_s = whole_job_rate(B * T, ms, ws)
     res = {
         "metric": "NSA 64k prefill tokens/s" if T == 65536 else f"NSA prefill tokens/s (T={T})",
         "value": tok_s,
@@ -337,7 +347,7 @@ def run_ours(args, ws, rank):
         "kernels": {k: {"launches_per_step": c / args.steps, "ms_per_step": t / args.steps,
                         "share": t / sum(x[1] for x in prof.values())} for k, (c, t) in prof.items()},
         "gpu_launches": int(launches),
-        "e2e": {"value": ws * B * T / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": whole_job_rate(B * T, ms_e2e, ws), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
         "clocks": clk.summary(),
     }
