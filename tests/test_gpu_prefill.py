@@ -98,13 +98,23 @@ def _gate_only(inp, which):
     return d
 
 
-@pytest.mark.parametrize("T", [2048, 1000, 1234, 97, 37])
+@pytest.mark.parametrize("T", [2048, 1000, 1234, 97, 37, 31, 20, 1])
 def test_prefill_tiny_all_rows(T):
     wl = PREFILL_CONFIGS["tiny_2k"]
     inp = make_prefill(wl, T=T)
     ref = O.nsa_prefill_reference(inp)
     out, idx, _, _ = run_prefill(inp, ref["kc"], ref["vc"])
     check_rows(inp, ref, out, idx, list(range(T)), label=f"tiny T={T}")
+
+
+def test_prefill_short_without_compressed_cache():
+    # T < l: no compression block exists (empty compressed branch) and the
+    # library is asked to build the (empty) cache itself
+    wl = PREFILL_CONFIGS["tiny_2k"]
+    inp = make_prefill(wl, T=20)
+    ref = O.nsa_prefill_reference(inp)
+    out, idx, _, _ = run_prefill(inp)
+    check_rows(inp, ref, out, idx, list(range(20)), label="tiny T=20, cache built by the library")
 
 
 @pytest.mark.parametrize("which,name", [(0, "cmp"), (1, "slc"), (2, "win")])
