@@ -36,6 +36,11 @@ docstring.  Parity status per function:
                           pages print no worked example)
   dsa_decode ............ pinned (k >= T reduces to full softmax attention;
                           brute-force top-k; 131072/2048 = 64)
+  dsa_prefill ........... pinned (topk >= t+1 reduces to textbook causal
+                          attention; last row = the decode step; brute-force
+                          loops and tuple sort for the kept sets)
+  decode_multi .......... pinned (m = 1 is the decode step bit for bit; rows
+                          equal the prefill rows of token-major copies)
   nsa_bwd (backward) .... pinned (central finite differences of the forward
                           with the selection fixed; torch autograd of an
                           independent torch forward; one-key and mean-pool

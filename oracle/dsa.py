@@ -27,7 +27,7 @@ import torch
 from .nsa import to_f64
 
 __all__ = ["dsa_indexer_scores", "topk_positions", "topk_alternatives",
-           "dsa_attention", "dsa_decode_reference"]
+           "dsa_attention", "dsa_decode_reference", "dsa_prefill_reference"]
 
 
 def dsa_indexer_scores(qI: np.ndarray, wI: np.ndarray, kI: np.ndarray) -> np.ndarray:
@@ -117,3 +117,34 @@ def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
         res["idx"][si], res["I"][si], res["I32"][si] = sel, I, I32
     res["batches"] = np.array(batches)
     return res
+
+
+def dsa_prefill_reference(inp: Dict[str, torch.Tensor], topk: int, b: int = 0,
+                          rows: Optional[Iterable[int]] = None) -> Dict[str, np.ndarray]:
+    """DSA over a whole sequence ``b``: every position t is a query.
+
+    Same page, "쉽게 이해하기": the selection is made independently for each
+    query position.  Readings taken for the prefill form:
+      * the indexer query qI and weights wI belong to the query token, so
+        inp holds them per position (``workloads.make_dsa_prefill``);
+      * query t scores, keeps and attends over its causal prefix s <= t
+        (t itself included), keeping min(topk, t + 1) positions.
+    Returns out [R,H,dv] and, per row, the kept positions (a list of arrays,
+    ascending) and the fp32 scores of the prefix.
+    """
+    qI, wI, kI, q, k, v = (inp[n] for n in ("qI", "wI", "kI", "q", "k", "v"))
+    _, T, H, dk = q.shape
+    dv = v.shape[2]
+    scale = 1.0 / math.sqrt(dk)
+    rows = list(range(T)) if rows is None else list(rows)
+    kI_b, K, V = to_f64(kI[b]), to_f64(k[b]), to_f64(v[b])
+    out = np.zeros((len(rows), H, dv))
+    idx, I32s = [], []
+    for r, t in enumerate(rows):
+        I = dsa_indexer_scores(to_f64(qI[b, t]), to_f64(wI[b, t]), kI_b[: t + 1])
+        I32 = I.astype(np.float32)
+        sel = topk_positions(I32, topk)
+        out[r] = dsa_attention(to_f64(q[b, t]), K[sel], V[sel], scale)
+        idx.append(sel)
+        I32s.append(I32)
+    return dict(out=out, idx=idx, I32=I32s, rows=np.array(rows))

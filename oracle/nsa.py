@@ -48,7 +48,7 @@ __all__ = [
     "compress", "cmp_attention", "overlap_matrix", "block_scores",
     "select_blocks", "selection_alternatives", "selected_keys", "sel_attention",
     "win_attention", "nsa_group_rows", "nsa_prefill_reference",
-    "nsa_decode_reference", "decode_tokens_read",
+    "nsa_decode_reference", "nsa_decode_multi_reference", "decode_tokens_read",
 ]
 
 
@@ -360,6 +360,42 @@ def nsa_decode_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[i
             res["idx"][si, g] = r["idx"][0]
             res["S"][si, g] = r["S"][0]
             res["S32"][si, g] = r["S32"][0]
+    res["seqs"] = np.array(seqs)
+    return res
+
+
+def nsa_decode_multi_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[int]] = None,
+                               params: NSAParams = NSAParams()) -> Dict[str, np.ndarray]:
+    """Decode of m query tokens per sequence at positions T-m .. T-1 (all in
+    the caches): rows T-m .. T-1 of the same definition, each with its own
+    selection (several draft tokens checked at once, or a short chunk).
+
+    inp: ``workloads.make_decode_multi`` (caches [B,G,T,d], q [B,m,H,dk],
+    gates [B,m,H,3]).  Returns out [S,m,H,dv] and idx [S,m,G,n].
+    """
+    kcache, vcache, q_t = inp["kcache"], inp["vcache"], inp["q"]
+    B, G, T, dk = kcache.shape
+    m, H = q_t.shape[1], q_t.shape[2]
+    dv = vcache.shape[3]
+    hpg = H // G
+    scale = 1.0 / math.sqrt(dk)
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    pe_k, pe_v = to_f64(inp["pe_k"]), to_f64(inp["pe_v"])
+    w_k, w_v = to_f64(inp["w_k"]), to_f64(inp["w_v"])
+    res = dict(out=np.zeros((len(seqs), m, H, dv)), idx=np.zeros((len(seqs), m, G, params.n), dtype=np.int32))
+    t_rows = np.arange(T - m, T)
+    for si, b in enumerate(seqs):
+        qb = to_f64(q_t[b])
+        gb = to_f64(inp["gates"][b])
+        for g in range(G):
+            K = to_f64(kcache[b, g])
+            V = to_f64(vcache[b, g])
+            Kc = compress(K, pe_k, w_k, params.l, params.d)
+            Vc = compress(V, pe_v, w_v, params.l, params.d)
+            hs = slice(g * hpg, (g + 1) * hpg)
+            r = nsa_group_rows(qb[:, hs], t_rows, K, V, Kc, Vc, gb[:, hs], params, scale)
+            res["out"][si, :, hs] = r["out"]
+            res["idx"][si, :, g] = r["idx"]
     res["seqs"] = np.array(seqs)
     return res
 

@@ -29,7 +29,8 @@ import torch
 __all__ = [
     "NSAParams", "PrefillWorkload", "DecodeWorkload", "DSAWorkload",
     "prefill_config", "decode_config", "dsa_config",
-    "make_prefill", "make_prefill_dout", "make_decode", "make_dsa", "PREFILL_CONFIGS",
+    "make_prefill", "make_prefill_dout", "make_decode", "make_decode_multi", "make_dsa",
+    "make_dsa_prefill", "PREFILL_CONFIGS",
 ]
 
 
@@ -172,6 +173,26 @@ def make_decode(wl: DecodeWorkload, B: Optional[int] = None, T: Optional[int] = 
                 gates=gates)
 
 
+def make_decode_multi(wl: DecodeWorkload, m: int, B: Optional[int] = None, T: Optional[int] = None
+                      ) -> Dict[str, torch.Tensor]:
+    """Decode inputs with ``m`` query tokens per sequence (positions T-m ..
+    T-1, all already in the caches), bf16 on the CPU.
+
+    Draw order as ``make_decode`` with q [B,m,H,dk] and gates [B,m,H,3]; for
+    m = 1 the values equal those of ``make_decode``.
+    """
+    B = wl.B if B is None else B
+    T = wl.T if T is None else T
+    gen = torch.Generator("cpu").manual_seed(wl.seed)
+    kcache = _draw(gen, (B, wl.G, T, wl.dk), 1.0)
+    vcache = _draw(gen, (B, wl.G, T, wl.dv), 1.0)
+    q = _draw(gen, (B, m, wl.H, wl.dk), 1.0)
+    pe_k, pe_v, w_k, w_v = _phi_params(gen, wl.params.l, wl.dk, wl.dv)
+    gates = _gates(gen, (B, m, wl.H, 3))
+    return dict(kcache=kcache, vcache=vcache, q=q, pe_k=pe_k, pe_v=pe_v, w_k=w_k, w_v=w_v,
+                gates=gates)
+
+
 def make_dsa(wl: DSAWorkload, B: Optional[int] = None, T: Optional[int] = None
              ) -> Dict[str, torch.Tensor]:
     """DSA decode inputs, all bf16 N(0,1) on the CPU.
@@ -186,6 +207,26 @@ def make_dsa(wl: DSAWorkload, B: Optional[int] = None, T: Optional[int] = None
     wI = _draw(gen, (B, wl.HI), 1.0)
     kI = _draw(gen, (B, T, wl.dI), 1.0)
     q = _draw(gen, (B, wl.H, wl.dk), 1.0)
+    k = _draw(gen, (B, T, wl.dk), 1.0)
+    v = _draw(gen, (B, T, wl.dv), 1.0)
+    return dict(qI=qI, wI=wI, kI=kI, q=q, k=k, v=v)
+
+
+def make_dsa_prefill(wl: DSAWorkload, B: Optional[int] = None, T: Optional[int] = None
+                     ) -> Dict[str, torch.Tensor]:
+    """DSA prefill inputs (every position is a query), all bf16 N(0,1) on the
+    CPU.
+
+    Draw order: qI [B,T,HI,dI], wI [B,T,HI], kI [B,T,dI], q [B,T,H,dk],
+    k [B,T,dk], v [B,T,dv].
+    """
+    B = wl.B if B is None else B
+    T = wl.T if T is None else T
+    gen = torch.Generator("cpu").manual_seed(wl.seed)
+    qI = _draw(gen, (B, T, wl.HI, wl.dI), 1.0)
+    wI = _draw(gen, (B, T, wl.HI), 1.0)
+    kI = _draw(gen, (B, T, wl.dI), 1.0)
+    q = _draw(gen, (B, T, wl.H, wl.dk), 1.0)
     k = _draw(gen, (B, T, wl.dk), 1.0)
     v = _draw(gen, (B, T, wl.dv), 1.0)
     return dict(qI=qI, wI=wI, kI=kI, q=q, k=k, v=v)
