@@ -121,3 +121,73 @@ def test_dsa_latent_values_argument_checks(nsa):
         # valid arguments, latent or not: the no-device status
         assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 7
         assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None) == 7
+
+
+def _prefill_args(nsa, c, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, gates=FAKE, kc=FAKE, vc=FAKE, out=FAKE, idx=None, ws=FAKE,
+             ws_bytes=nsa.nsa_prefill_workspace_size(c))
+    a.update(kw)
+    return nsa.lib.nsa_prefill_fwd(ctypes.byref(c), a["q"], a["k"], a["v"], a["gates"], a["kc"], a["vc"],
+                                   a["out"], a["idx"], a["ws"], a["ws_bytes"], None)
+
+
+def test_prefill_argument_checks(nsa):
+    c = nsa.make_cfg(1, 4096, 64, 4, 192, 128)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    need = nsa.nsa_prefill_workspace_size(c)
+    # the workspace holds the bf16 cmp+win partial and the kept-block lists
+    assert need >= 4096 * 64 * 128 * 2 + 4096 * 4 * 16 * 4
+    assert nsa.nsa_prefill_workspace_size(nsa.make_cfg(1, 8192, 64, 4, 192, 128)) > need
+    assert _prefill_args(nsa, c, q=None) == 1
+    assert _prefill_args(nsa, c, k=FAKE + 2) == 3
+    assert _prefill_args(nsa, c, idx=FAKE + 4) == 3
+    assert _prefill_args(nsa, c, kc=None) == 1                     # a cache exists at T = 4096
+    assert _prefill_args(nsa, c, ws=FAKE + 16) == 3
+    assert _prefill_args(nsa, c, ws_bytes=need - 1) == 4
+    c.w_k = None                                                   # phi needed to build the cache ...
+    assert _prefill_args(nsa, c) == 1
+    c.flags = nsa.NSA_FLAG_KC_GIVEN                                # ... but not when it is given
+    if not torch.cuda.is_available():
+        assert _prefill_args(nsa, c) == 7
+        short = nsa.make_cfg(1, 20, 64, 4, 192, 128)               # T < l: no cache, kc/vc may be NULL
+        short.pe_k = short.pe_v = short.w_k = short.w_v = FAKE
+        assert _prefill_args(nsa, short, kc=None, vc=None,
+                             ws_bytes=nsa.nsa_prefill_workspace_size(short)) == 7
+
+
+@pytest.mark.parametrize("shape", [
+    dict(H=64, G=2),       # 32 heads per group: the kernels take at most 16
+    dict(T=70000),         # longer than the prefill kernels' 65,536
+    dict(dv=192),          # prefill values are 64 or 128 wide
+    dict(n=17),            # at most 16 kept blocks in prefill
+])
+def test_prefill_rejects_unimplemented_shapes(nsa, shape):
+    base = dict(B=1, T=4096, H=64, G=4, dk=192, dv=128)
+    n = shape.pop("n", 16)
+    base.update(shape)
+    c = nsa.make_cfg(**base, n=n)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    assert _prefill_args(nsa, c, ws_bytes=1 << 40) == 2
+
+
+def test_decode_argument_checks(nsa):
+    c = nsa.make_cfg(16, 65536, 64, 4, 192, 128)
+    need = nsa.nsa_decode_workspace_size(c)
+    assert need > 0
+    f = nsa.lib.nsa_decode_step
+
+    def call(**kw):
+        a = dict(q=FAKE, kcache=FAKE, vcache=FAKE, kc=FAKE, vc=FAKE, gates=FAKE, out=FAKE, idx=None, ws=FAKE,
+                 ws_bytes=need)
+        a.update(kw)
+        return f(ctypes.byref(c), a["q"], a["kcache"], a["vcache"], a["kc"], a["vc"], a["gates"], a["out"],
+                 a["idx"], a["ws"], a["ws_bytes"], None)
+    assert call(kcache=None) == 1
+    assert call(gates=FAKE + 8) == 3
+    assert call(vc=None) == 1
+    assert call(ws_bytes=need - 1) == 4
+    if not torch.cuda.is_available():
+        assert call() == 7
+    wide = nsa.make_cfg(16, 65536, 64, 2, 192, 128)                # 32 heads per group
+    assert nsa.nsa_decode_workspace_size(wide) == 0
+    assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == 2
