@@ -133,11 +133,23 @@ int nsa_compress_kv(const nsa_cfg* cfg, int layout, const void* k, const void* v
  *   - Every call shares the one array: calls that can overlap on the GPU
  *     (different streams without ordering) race on it.  Each call clears the
  *     status word before it launches.
- *   - Arguments and outputs as nsa_compress_kv; a cfg whose biases do not fit
- *     the array returns NSA_ERR_WORKSPACE.
+ *   - Arguments, outputs and argument errors as nsa_compress_kv; a cfg whose
+ *     biases do not fit the array returns NSA_ERR_WORKSPACE (unreachable
+ *     while dk, dv <= 256 is a cfg rule).
+ *   - The status word is read back with nsa_compress_kv_noalloc_status().
  */
 int nsa_compress_kv_noalloc(const nsa_cfg* cfg, int layout, const void* k, const void* v,
                             void* kc, void* vc, void* stream);
+
+/*
+ * nsa_compress_kv_noalloc_status -- the status word of the fixed array that
+ * nsa_compress_kv_noalloc uses, on the current device: synchronises
+ * ``stream``, returns the code the kernels of the last no-alloc call
+ * recorded (NSA_OK if none, NSA_ERR_DEVICE_TIMEOUT if a bounded wait ran out
+ * and the outputs were left unwritten) and clears it.  Like the call itself
+ * it allocates nothing.  No counterpart on the pages.
+ */
+int nsa_compress_kv_noalloc_status(void* stream);
 
 /*
  * nsa_prefill_fwd -- NSA forward over whole sequences [P2 II; P3].

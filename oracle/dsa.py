@@ -26,7 +26,7 @@ import torch
 
 from .nsa import to_f64
 
-__all__ = ["dsa_indexer_scores", "topk_positions", "topk_alternatives",
+__all__ = ["dsa_indexer_scores", "topk_positions", "topk_alternatives", "topk_set_valid",
            "dsa_attention", "dsa_decode_reference", "dsa_prefill_reference"]
 
 
@@ -66,6 +66,25 @@ def topk_alternatives(I32: np.ndarray, k: int, rel_tol: float):
     above = np.nonzero(s > cut + tol)[0]
     band = np.nonzero(np.abs(s - cut) <= tol)[0]
     return (last_in - first_out) / scale, above, band, k - above.size
+
+
+def topk_set_valid(I32: np.ndarray, kept, k: int, rel_tol: float):
+    """Is ``kept`` (positions, any order) an acceptable top-k set of the row?
+
+    Acceptable means: exactly min(k, T) distinct in-range positions, every
+    position clearly above the cut kept, and the rest taken from the band of
+    positions whose fp32 score lies within ``rel_tol`` (relative) of the cut
+    (reading: near-ties may resolve either way).  Returns (ok, gap_rel).
+    """
+    T = I32.shape[0]
+    kept = np.asarray(list(kept), dtype=np.int64)
+    kset = set(kept.tolist())
+    if len(kset) != kept.size or kept.size != min(k, T) or (kept.size and (kept.min() < 0 or kept.max() >= T)):
+        return False, float("nan")
+    gap, above, band, need = topk_alternatives(I32, k, rel_tol)
+    a = set(above.tolist())
+    extra = kset - a
+    return bool(a <= kset and extra <= set(band.tolist()) and len(extra) == need), gap
 
 
 def dsa_attention(q: np.ndarray, Ksel: np.ndarray, Vsel: np.ndarray, scale: float) -> np.ndarray:

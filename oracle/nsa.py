@@ -46,7 +46,7 @@ from workloads import NSAParams
 __all__ = [
     "to_f64", "bf16_round", "num_compressed", "num_visible_compressed",
     "compress", "cmp_attention", "overlap_matrix", "block_scores",
-    "select_blocks", "selection_alternatives", "selected_keys", "sel_attention",
+    "select_blocks", "selection_alternatives", "selection_set_valid", "selected_keys", "sel_attention",
     "win_attention", "nsa_group_rows", "nsa_prefill_reference",
     "nsa_decode_reference", "nsa_decode_multi_reference", "decode_tokens_read",
 ]
@@ -202,6 +202,22 @@ def selection_alternatives(S32: np.ndarray, t: int, n: int, lsel: int, rel_tol: 
     above = set(cand[s > cut + tol].tolist())
     band = set(cand[np.abs(s - cut) <= tol].tolist())
     return gap, forced | above, band, kfree - len(above)
+
+
+def selection_set_valid(S32: np.ndarray, t: int, row, n: int, lsel: int, rel_tol: float):
+    """Is the index row ``row`` (n entries, ascending, -1 padded) an acceptable
+    selection for query t?  Acceptable means: the kept blocks ascending and
+    distinct in front, -1 after them, the forced and clearly-above-the-cut
+    blocks all kept, and the remaining picks taken from the near-tie band of
+    ``selection_alternatives``.  Returns (ok, gap_rel)."""
+    row = [int(j) for j in row]
+    kept = [j for j in row if j >= 0]
+    if row[: len(kept)] != sorted(set(kept)) or any(j != -1 for j in row[len(kept):]):
+        return False, float("nan")
+    gap, definite, band, need = selection_alternatives(S32, t, n, lsel, rel_tol)
+    ks = set(kept)
+    extra = ks - definite
+    return bool(definite <= ks and extra <= band and len(extra) == need), gap
 
 
 def selected_keys(blocks: Sequence[int], t: int, lsel: int) -> np.ndarray:

@@ -21,7 +21,8 @@ __all__ = [
     "NSA_LAYOUT_BTGD", "NSA_LAYOUT_BGTD", "NSA_FLAG_KC_GIVEN",
     "nsa_status_string", "nsa_version", "nsa_num_compressed",
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
-    "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc", "nsa_prefill_fwd", "nsa_decode_step",
+    "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
+    "nsa_compress_kv_noalloc_status", "nsa_prefill_fwd", "nsa_decode_step",
     "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
@@ -79,6 +80,7 @@ def _load() -> ctypes.CDLL:
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
         "nsa_compress_kv_noalloc": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+        "nsa_compress_kv_noalloc_status": (_c_int, [_c_vp]),
         "nsa_profile_enable": (_c_int, [_c_int]),
         "nsa_profile_read": (_c_int, [_c_int, ctypes.c_char_p, _c_size, ctypes.POINTER(_c_int),
                                       ctypes.POINTER(_c_float)]),
@@ -191,6 +193,11 @@ def nsa_compress_kv_noalloc(cfg: NsaCfg, layout: int, k, v, kc, vc, stream=None)
     allocation, for callers that cannot allocate device memory."""
     _check(_lib().nsa_compress_kv_noalloc(ctypes.byref(cfg), layout, _ptr(k), _ptr(v), _ptr(kc), _ptr(vc),
                                        _stream(stream)), "nsa_compress_kv_noalloc")
+
+
+def nsa_compress_kv_noalloc_status(stream=None) -> int:
+    """Status word of the no-alloc call's fixed array (synchronises, clears)."""
+    return _lib().nsa_compress_kv_noalloc_status(_stream(stream))
 
 
 def nsa_prefill_fwd(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, ws, stream=None):

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.hpp"
@@ -117,6 +118,43 @@ int run_compress(const nsa_cfg& c, int layout, const void* k, const void* v, voi
 }
 
 }  // namespace
+
+namespace nsa {
+
+int check_nsa_cfg(const nsa_cfg* cfg) { return validate_cfg(cfg); }
+int check_nsa_phi(const nsa_cfg* cfg) { return cfg == nullptr ? NSA_ERR_INVALID_ARG : validate_phi(cfg); }
+
+int ensure_smem_attr(const void* func, size_t bytes) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return NSA_ERR_NO_DEVICE;
+  struct Entry {
+    const void* func;
+    int dev;
+    size_t bytes;
+  };
+  constexpr int kMax = 256;
+  static Entry table[kMax];
+  static int used = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  int slot = -1;
+  for (int i = 0; i < used; ++i)
+    if (table[i].func == func && table[i].dev == dev) {
+      if (table[i].bytes >= bytes) return NSA_OK;
+      slot = i;
+      break;
+    }
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    return NSA_ERR_CUDA;
+  if (slot < 0) {
+    if (used == kMax) return NSA_OK;   // table full: the attribute is set, only not remembered
+    slot = used++;
+  }
+  table[slot] = Entry{func, dev, bytes};
+  return NSA_OK;
+}
+
+}  // namespace nsa
 
 extern "C" {
 

@@ -227,13 +227,7 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
   a.out = static_cast<__nv_bfloat16*>(out);
   a.st = st;
   const size_t smem = compress_smem_bytes(N);
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(compress_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()) !=
-        cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&compress_gemm_kernel), smem_max())) return rc;
   dim3 grid((Nc + kTileM - 1) / kTileM, c.G, c.B);
   prof::begin("compress_gemm", stream);
   compress_gemm_kernel<<<grid, 128, smem, stream>>>(mapA, mapB, a);

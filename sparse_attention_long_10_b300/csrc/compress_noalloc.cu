@@ -24,6 +24,7 @@ namespace {
 
 // Fixed maximum: status word + bias_k + bias_v for dk, dv <= 256.
 constexpr size_t kNoAllocScratchBytes = 256 + 1024 + 1024;
+static_assert(kNoAllocScratchBytes >= 256 + 256 * sizeof(float) * 2, "scratch covers dk, dv <= 256");
 
 static __device__ __align__(256) uint8_t g_compress_scratch[kNoAllocScratchBytes];
 
@@ -52,22 +53,26 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" int nsa_compress_kv_noalloc(const nsa_cfg* cfg, int layout, const void* k, const void* v, void* kc,
                                        void* vc, void* stream) {
-  // same argument rules as nsa_compress_kv (nsa_num_compressed validates cfg)
-  const int Nc = nsa_num_compressed(cfg);
-  if (Nc < 0) return cfg == nullptr ? NSA_ERR_INVALID_ARG : NSA_ERR_UNSUPPORTED;
+  // the same argument rules, in the same order, as nsa_compress_kv
+  int rc = nsa::check_nsa_cfg(cfg);
+  if (rc != NSA_OK) return rc;
   const nsa_cfg& c = *cfg;
   if (layout != NSA_LAYOUT_BTGD && layout != NSA_LAYOUT_BGTD) return NSA_ERR_INVALID_ARG;
-  for (const void* p : {c.pe_k, c.pe_v, c.w_k, c.w_v, k, v}) {
+  if ((rc = nsa::check_nsa_phi(cfg)) != NSA_OK) return rc;
+  for (const void* p : {k, v}) {
     if (p == nullptr) return NSA_ERR_INVALID_ARG;
     if (!aligned16(p)) return NSA_ERR_MISALIGNED;
   }
+  const int Nc = nsa_num_compressed(cfg);
   if (Nc > 0) {
     for (const void* p : {static_cast<const void*>(kc), static_cast<const void*>(vc)}) {
       if (p == nullptr) return NSA_ERR_INVALID_ARG;
       if (!aligned16(p)) return NSA_ERR_MISALIGNED;
     }
   }
-  // the fixed scratch must hold the status word and both bias vectors
+  // the fixed scratch must hold the status word and both bias vectors; the
+  // cfg rules (dk, dv <= 256) keep this true today, the check keeps it true
+  // if those rules are ever widened
   const size_t off_bk = 256;
   const size_t off_bv = nsa::align_up(off_bk + sizeof(float) * (size_t)c.dk, 256);
   const size_t need = nsa::align_up(off_bv + sizeof(float) * (size_t)c.dv, 256);
@@ -77,7 +82,7 @@ extern "C" int nsa_compress_kv_noalloc(const nsa_cfg* cfg, int layout, const voi
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess || major != 10)
     return NSA_ERR_NO_DEVICE;
   void* scratch = nullptr;
-  int rc = scratch_for_current_device(&scratch);
+  rc = scratch_for_current_device(&scratch);
   if (rc != NSA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: clear the status word
@@ -89,4 +94,17 @@ extern "C" int nsa_compress_kv_noalloc(const nsa_cfg* cfg, int layout, const voi
   if (rc != NSA_OK) return rc;
   return nsa::launch_compress_one(c, layout, v, c.dv, c.pe_v, c.w_v, vc, reinterpret_cast<float*>(base + off_bv), st,
                                   s);
+}
+
+extern "C" int nsa_compress_kv_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  int rc = scratch_for_current_device(&scratch);
+  if (rc != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  nsa::DeviceStatus h;
+  if (cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, sizeof(h), s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
+  return h.code;
 }

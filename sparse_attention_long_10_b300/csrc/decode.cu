@@ -845,13 +845,7 @@ DecLayout dec_layout(const nsa_cfg& c) {
 template <int DK, int DV, int MODE>
 int launch_one(const DecArgs& a, dim3 grid, const CUtensorMap* maps, uint32_t smem, cudaStream_t s,
                const char* name) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(dec_kernel<DK, DV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_max()) != cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dec_kernel<DK, DV, MODE>), smem_max())) return rc;
   prof::begin(name, s);
   dec_kernel<DK, DV, MODE><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
   prof::end(s);

@@ -852,13 +852,7 @@ size_t thresh_smem(const DsaShape& s) {
 template <int DI>
 int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
   constexpr size_t smem = (size_t)kIdxStages * (DI / 64) * kIdxTile * 128 + kBins * 4 + 256 + 1024;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(dsa_index_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_index_kernel<DI>), smem)) return rc;
   prof::begin("dsa_index", s);
   dsa_index_kernel<DI><<<dim3((a.T + a.idx_part - 1) / a.idx_part, a.B), kIdxThreads, smem, s>>>(map, a);
   prof::end(s);
@@ -868,13 +862,7 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
 template <int DV>
 int launch_attn(const DsaArgs& a, cudaStream_t s) {
   const AttnLayout L = attn_layout(a.dk, DV);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(dsa_attn_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()) !=
-        cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_attn_kernel<DV>), smem_max())) return rc;
   prof::begin("dsa_attn", s);
   dsa_attn_kernel<DV><<<dim3(a.attn_ctas, a.B), kAttnThreads, L.total, s>>>(a);
   prof::end(s);

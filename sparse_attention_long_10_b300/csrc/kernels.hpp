@@ -18,6 +18,16 @@ constexpr size_t smem_max() { return 232448; }  // 227 KB
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Raises ``func``'s dynamic shared-memory limit to at least ``bytes`` on the
+// current device.  A function attribute belongs to one device context, so the
+// setting is remembered per (function, device); thread-safe.  Returns a status.
+int ensure_smem_attr(const void* func, size_t bytes);
+
+// The argument rules every NSA entry point applies to ``cfg`` and to its phi
+// parameters (api.cu); each returns NSA_OK or the status the call returns.
+int check_nsa_cfg(const nsa_cfg* cfg);
+int check_nsa_phi(const nsa_cfg* cfg);
+
 // ---- compression (compress.cu)
 size_t compress_smem_bytes(int N);
 // One of K or V: X in ``layout``, dX = head dim = output dim.

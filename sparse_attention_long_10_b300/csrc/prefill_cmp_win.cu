@@ -678,13 +678,7 @@ int scores_stride(int T, int Nc) {
 
 template <int HPG>
 int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(cmp_win_kernel<HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()) !=
-        cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&cmp_win_kernel<HPG>), smem_max())) return rc;
   dim3 grid((a0.T + a0.QT - 1) / a0.QT, a0.G, B);
   prof::begin("cmp_win", s);
   cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);

@@ -583,12 +583,7 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.off_pt = L.off_pt;
   a.off_red = L.off_red;
   a.off_bar = L.off_bar;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(sel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()) != cudaSuccess)
-      return NSA_ERR_CUDA;
-    attr = true;
-  }
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel), smem_max())) return rc;
   dim3 grid((c.T + a.QPC - 1) / a.QPC, c.G, c.B);
   prof::begin("sel", s);
   sel_kernel<<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);

@@ -31,3 +31,29 @@ def bf16_compare(got: torch.Tensor, exact: np.ndarray, absmag: np.ndarray, acc_r
     assert not bad.any(), f"{int(bad.sum())} elements outside the bound"
     assert np.isfinite(g).all()
     return nd
+
+
+def compress_exact(inp, B, G, layout_btgd, kname, pename, wname, seqs=None):
+    """Oracle's exact (pre-rounding) compressed values [S,G,Nc,d] of the
+    sequences ``seqs`` (default all B) and, for the tolerance of
+    ``bf16_compare``, the sum of the absolute values of each dot product's
+    terms."""
+    pe, w = O.to_f64(inp[pename]), O.to_f64(inp[wname])
+    seqs = list(range(B)) if seqs is None else list(seqs)
+    out, mag = [], []
+    for b in seqs:
+        for g in range(G):
+            X = O.to_f64(inp[kname][b, :, g] if layout_btgd else inp[kname][b, g])
+            out.append(O.compress(X, pe, w, 32, 16, round_bf16=False))
+            Nc = out[-1].shape[0]
+            flat = np.abs(np.stack([(X[16 * i: 16 * i + 32] + pe).reshape(-1) for i in range(Nc)])) \
+                if Nc else np.zeros((0, w.shape[0]))
+            mag.append(flat @ np.abs(w))
+    sh = out[0].shape
+    return np.stack(out).reshape(len(seqs), G, *sh), np.stack(mag).reshape(len(seqs), G, *sh)
+
+
+def cache_f64(t: torch.Tensor) -> np.ndarray:
+    """A bf16 device cache as fp64 numpy (exact): what the oracle is handed
+    when it scores the GPU's own compressed cache."""
+    return t.detach().float().cpu().numpy().astype(np.float64)

@@ -191,3 +191,36 @@ def test_decode_argument_checks(nsa):
     wide = nsa.make_cfg(16, 65536, 64, 2, 192, 128)                # 32 heads per group
     assert nsa.nsa_decode_workspace_size(wide) == 0
     assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == 2
+
+
+@pytest.mark.parametrize("mutate", [
+    dict(H=64, G=3), dict(B=0), dict(dk=100), dict(l=64), dict(H=48, G=1), dict(n=2), dict(T=0),
+    dict(dv=320),
+])
+def test_noalloc_rejects_bad_cfg_like_the_workspace_call(nsa, mutate):
+    """The allocation-free compression applies the same argument rules as
+    nsa_compress_kv and returns the same codes."""
+    base = dict(B=1, T=4096, H=64, G=4, dk=192, dv=128)
+    base.update(mutate)
+    c = nsa.make_cfg(**base)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    rc_ws = nsa.lib.nsa_compress_kv(ctypes.byref(c), 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    rc_na = nsa.lib.nsa_compress_kv_noalloc(ctypes.byref(c), 0, FAKE, FAKE, FAKE, FAKE, None)
+    assert rc_ws != 0 and rc_na == rc_ws
+
+
+def test_noalloc_argument_checks_match(nsa):
+    c = nsa.make_cfg(1, 4096, 64, 4, 192, 128)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    f_ws = lambda *p: nsa.lib.nsa_compress_kv(ctypes.byref(c), *p, FAKE, 1 << 30, None)
+    f_na = lambda *p: nsa.lib.nsa_compress_kv_noalloc(ctypes.byref(c), *p, None)
+    for args in [(7, FAKE, FAKE, FAKE, FAKE), (0, None, FAKE, FAKE, FAKE), (0, FAKE + 2, FAKE, FAKE, FAKE),
+                 (0, FAKE, FAKE, None, FAKE), (0, FAKE, FAKE, FAKE, FAKE + 8)]:
+        assert f_na(*args) == f_ws(*args) != 0
+    assert nsa.lib.nsa_compress_kv_noalloc(None, 0, FAKE, FAKE, FAKE, FAKE, None) == 1
+    c.pe_v = FAKE + 4
+    assert f_na(0, FAKE, FAKE, FAKE, FAKE) == f_ws(0, FAKE, FAKE, FAKE, FAKE) == 3
+    if not torch.cuda.is_available():
+        c.pe_v = FAKE
+        assert f_na(0, FAKE, FAKE, FAKE, FAKE) == 7
+        assert nsa.lib.nsa_compress_kv_noalloc_status(None) == 7

@@ -7,7 +7,7 @@ pytestmark = pytest.mark.gpu
 
 from oracle import nsa as O
 from workloads import PREFILL_CONFIGS, decode_config, make_prefill, make_decode
-from tests.gpu_util import bf16_compare
+from tests.gpu_util import bf16_compare, compress_exact
 
 
 def _nsa():
@@ -32,20 +32,7 @@ def _run(inp, B, T, H, G, dk, dv, layout):
 
 
 def _exact(inp, B, G, layout_btgd, kname, pename, wname):
-    """Oracle's exact compressed values and, for the tolerance, the sum of the
-    absolute values of each dot product's terms (same blocks, |.| inputs)."""
-    pe, w = O.to_f64(inp[pename]), O.to_f64(inp[wname])
-    out, mag = [], []
-    for b in range(B):
-        for g in range(G):
-            X = O.to_f64(inp[kname][b, :, g] if layout_btgd else inp[kname][b, g])
-            out.append(O.compress(X, pe, w, 32, 16, round_bf16=False))
-            Nc = out[-1].shape[0]
-            flat = np.abs(np.stack([(X[16 * i: 16 * i + 32] + pe).reshape(-1) for i in range(Nc)])) \
-                if Nc else np.zeros((0, w.shape[0]))
-            mag.append(flat @ np.abs(w))
-    sh = out[0].shape
-    return np.stack(out).reshape(B, G, *sh), np.stack(mag).reshape(B, G, *sh)
+    return compress_exact(inp, B, G, layout_btgd, kname, pename, wname)
 
 
 @pytest.mark.parametrize("key,T", [("tiny_2k", None), ("tiny_2k", 1000), ("tiny_2k", 47),

@@ -61,10 +61,7 @@ def check_dsa(inp, ref, out, idx, topk, label="", exact_idx=False):
         if np.array_equal(row, ref["idx"][si]):
             continue
         assert not exact_idx, f"{label} b={b}: kept set differs from the oracle's"
-        gap, above, band, need = D.topk_alternatives(ref["I32"][si], topk, NEAR_TIE)
-        kept = set(row.tolist())
-        ok = set(above.tolist()) <= kept and (kept - set(above.tolist())) <= set(band.tolist()) \
-            and len(kept - set(above.tolist())) == need
+        ok, gap = D.topk_set_valid(ref["I32"][si], row, topk, NEAR_TIE)
         assert ok, f"{label} b={b}: GPU set is not a valid top-{topk} (gap {gap:.3g})"
         near += 1
         ti = torch.as_tensor(row.astype(np.int64))

@@ -116,3 +116,32 @@ def test_shifted_compression_scatter_is_caught(monkeypatch, bwd_case):
     real = BW.compress_bwd
     monkeypatch.setattr(BW, "compress_bwd", wrong)
     _fails(PB.check_finite_differences, bwd_case)
+
+
+def test_widened_topk_band_is_caught(monkeypatch):
+    # a band 1000x too wide would let a wrong DSA top-k set pass the GPU check
+    real = D.topk_alternatives
+    monkeypatch.setattr(D, "topk_alternatives", lambda I32, k, rel_tol: real(I32, k, 1e3 * rel_tol))
+    _fails(P.test_topk_alternatives_cases)
+
+
+def test_topk_band_ignoring_need_is_caught(monkeypatch):
+    # accepting any number of picks from the band admits sets of the wrong size
+    real = D.topk_alternatives
+
+    def loose(I32, k, rel_tol):
+        gap, above, band, need = real(I32, k, rel_tol)
+        return gap, above, np.union1d(band, np.arange(I32.shape[0])), need
+    monkeypatch.setattr(D, "topk_alternatives", loose)
+    _fails(P.test_topk_set_valid_rejects_planted_invalid_sets)
+
+
+def test_selection_band_dropping_forced_blocks_is_caught(monkeypatch):
+    real = O.selection_alternatives
+
+    def no_forced(S32, t, n, lsel, rel_tol):
+        gap, definite, band, need = real(S32, t, n, lsel, rel_tol)
+        jt = t // lsel
+        return gap, definite - {0, jt - 1}, band | {0, jt - 1, 3}, need
+    monkeypatch.setattr(O, "selection_alternatives", no_forced)
+    _fails(P.test_selection_set_valid_rejects_planted_invalid_rows)

@@ -365,6 +365,105 @@ def test_dsa_topk_brute_force(seed):
     assert D.topk_positions(I, T + 5).tolist() == list(range(T))
 
 
+# ----------------------------------------------------------------- acceptance of differing top-k sets
+def _brute_acceptable(scores, k):
+    """Every k-subset that a ranking consistent with the scores can produce:
+    no dropped position scores strictly above a kept one (exact ties free)."""
+    import itertools
+    T = len(scores)
+    out = set()
+    for X in itertools.combinations(range(T), k):
+        xs = set(X)
+        lo = min(float(scores[x]) for x in X)
+        hi = max((float(scores[y]) for y in range(T) if y not in xs), default=-np.inf)
+        if lo >= hi:
+            out.add(X)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_set_valid_brute_force(seed):
+    # integer-valued scores (exact ties) far apart relative to the tolerance:
+    # the sets the predicate accepts are exactly the tie-permuted top-k sets
+    import itertools
+    rng = np.random.default_rng(100 + seed)
+    T, k = 9, 4
+    I = (rng.integers(0, 4, size=T) * 10 + 50).astype(np.float32)
+    acc = {X for X in itertools.combinations(range(T), k) if D.topk_set_valid(I, X, k, 1e-5)[0]}
+    assert acc == _brute_acceptable(I, k)
+    assert tuple(D.topk_positions(I, k).tolist()) in acc
+
+
+def test_topk_alternatives_cases():
+    # an exact tie at the cut: both tied positions in the band, one of them needed
+    I = np.array([9, 5, 7, 5, 1, 0], dtype=np.float32)
+    gap, above, band, need = D.topk_alternatives(I, 3, 1e-5)
+    assert gap == 0 and set(above.tolist()) == {0, 2} and set(band.tolist()) == {1, 3} and need == 1
+    assert D.topk_positions(I, 3).tolist() == [0, 1, 2]          # the tie goes to the lower position
+    assert D.topk_set_valid(I, [0, 2, 3], 3, 1e-5)[0]            # the other side of the tie is acceptable
+    # a clear gap: empty band, nothing needed
+    gap, above, band, need = D.topk_alternatives(I, 2, 1e-5)
+    assert gap > 0.1 and set(above.tolist()) == {0, 2} and band.size == 0 and need == 0
+    # k >= T keeps everything
+    gap, above, band, need = D.topk_alternatives(I, 6, 1e-5)
+    assert gap == float("inf") and above.tolist() == list(range(6)) and need == 0
+    assert D.topk_set_valid(I, range(6), 9, 1e-5)[0]
+    # a near-tie inside the tolerance is a band, one outside is not
+    J = np.array([3.0, 2.0, 2.0 * (1 + 4e-6), 1.0], dtype=np.float32)
+    assert set(D.topk_alternatives(J, 2, 1e-5)[2].tolist()) == {1, 2}
+    assert D.topk_alternatives(J, 2, 1e-7)[2].size == 0
+
+
+def test_topk_set_valid_rejects_planted_invalid_sets():
+    I = np.array([9, 5, 7, 5, 1, 0], dtype=np.float32)
+    ok = lambda X, k=3: D.topk_set_valid(I, X, k, 1e-5)[0]
+    assert ok([0, 1, 2]) and ok([2, 0, 3])
+    assert not ok([0, 1, 3])              # drops position 2, clearly above the cut
+    assert not ok([0, 2, 4])              # takes position 4, below the band
+    assert not ok([0, 2])                 # too few
+    assert not ok([0, 2, 1, 3])           # too many
+    assert not ok([0, 2, 2])              # a duplicate
+    assert not ok([0, 2, 6])              # out of range
+    assert not ok([0, 1, 2], k=4)         # k=4 needs 4 positions
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_selection_set_valid_brute_force(seed):
+    # NSA rows: forced blocks {0, j_t-1, j_t}; integer scores with exact ties
+    import itertools
+    rng = np.random.default_rng(200 + seed)
+    n, lsel = 6, 64
+    jt = 9
+    t = jt * lsel + 5
+    S = (rng.integers(0, 3, size=jt + 1) * 4 + 1).astype(np.float32)
+    forced = {0, jt - 1, jt}
+    free = [j for j in range(jt + 1) if j not in forced]
+    brute = {tuple(sorted(forced | {free[i] for i in X})) for X in _brute_acceptable(S[free], n - 3)}
+    acc = set()
+    for X in itertools.combinations(free, n - 3):
+        row = sorted(forced | set(X))
+        if O.selection_set_valid(S, t, row, n, lsel, 1e-5)[0]:
+            acc.add(tuple(row))
+    assert acc == brute
+    assert tuple(O.select_blocks(S, t, n, lsel).tolist()) in acc
+
+
+def test_selection_set_valid_rejects_planted_invalid_rows():
+    S = np.array([5, 0.5000001, 0.5, 0.3, 0.2, 0.1, 9, 9], dtype=np.float32)
+    t, n, lsel = 7 * 64, 4, 64
+    ok = lambda row: O.selection_set_valid(S, t, row, n, lsel, 1e-5)[0]
+    assert ok([0, 1, 6, 7]) and ok([0, 2, 6, 7])      # the near-tie resolves either way
+    assert not ok([0, 3, 6, 7])                        # below the band
+    assert not ok([1, 2, 6, 7])                        # drops forced block 0
+    assert not ok([0, 1, 5, 7])                        # drops forced block j_t - 1
+    assert not ok([0, 6, 1, 7])                        # not ascending
+    assert not ok([0, 1, 1, 7])                        # duplicate
+    # a short row (j_t + 1 <= n) keeps every block and pads with -1
+    assert O.selection_set_valid(S, 2 * 64, [0, 1, 2, -1], n, lsel, 1e-5)[0]
+    assert not O.selection_set_valid(S, 2 * 64, [0, 1, -1, 2], n, lsel, 1e-5)[0]
+    assert not O.selection_set_valid(S, 2 * 64, [0, 2, -1, -1], n, lsel, 1e-5)[0]
+
+
 def test_dsa_full_when_k_covers_context():
     wl = dsa_config()
     inp = make_dsa(wl, B=2, T=300)

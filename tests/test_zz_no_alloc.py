@@ -31,12 +31,14 @@ def _pair(inp, B, T, H, G, dk, dv, layout, kk, vk):
     ws = nsa.workspace(nsa.nsa_compress_workspace_size(cfg))
     nsa.nsa_compress_kv(cfg, layout, k, v, kc_ref, vc_ref, ws)
     outs = []
+    assert nsa.nsa_device_status(ws) == 0
     for _ in range(2):                      # two calls in a row share the static scratch
         kc, vc = buffers()
         nsa.nsa_compress_kv_noalloc(cfg, layout, k, v, kc, vc)
+        # the no-alloc call's own status word, in the fixed array
+        assert nsa.nsa_compress_kv_noalloc_status() == 0
         outs.append((kc, vc))
     torch.cuda.synchronize()
-    assert nsa.nsa_device_status(ws) == 0
     return (kc_ref, vc_ref), outs
 
 
