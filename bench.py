@@ -152,21 +152,20 @@ def whole_job_rate(units_per_rank: float, ms_max: float, ws: int) -> float:
     return ws * units_per_rank / (ms_max * 1e-3)
 
 
-# DRAM bytes (read + write) per launch or step from the ncu captures summarised
-# under profiles/.  A figure is reported only while the kernel sources it was
-# taken from are unchanged (sha256 prefix of the listed files); otherwise the
-# bench line says null.
+# DRAM bytes (read + write) per launch or step, from one-pass ncu captures of
+# the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  A figure
+# is reported only while the kernel sources it was taken from are unchanged
+# (sha256 prefix of the listed files); otherwise the bench line says null.
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
-    # profiles/prefill_T65536_traffic.md: one-pass DRAM capture of the full-size launches
     "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "e407d00cbc77e17d",
                 "bytes": (1857.36 + 1058.00) * 1e6, "how": "full-size capture (one pass)"},
     "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
             "bytes": (3176.90 + 1074.45) * 1e6, "how": "full-size capture (one pass)"},
-    # profiles/decode_B16_T65536_dec_kernels.md: both kernels of one step
+    # both kernels of one decode step
     "decode": {"files": ["decode.cu", "common.cuh"], "sha": "109c5bfaf71b561b",
                "bytes": (189.27 + 9.80 + 52.01 + 0.02) * 1e6, "how": "full-size capture, both kernels"},
-    # profiles/dsa_B8_T131072_kernels.md: the five kernels of one step
+    # the five kernels of one DSA step
     "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
             "bytes": (134.39 + 4.03 + 4.25 + 4.21 + 35.90 + 8.44) * 1e6, "how": "full-size capture, five kernels"},
     "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
@@ -312,6 +311,7 @@ def run_ours(args, ws, rank):
 
     flops, _ = prefill_counts(T, H, G, dk, dv, B)
     pk = peaks()
+    dense = run_dense_arm(nsa, cfg, dev, B, T, H, G, dk, dv, ms, stream, args)
     dom = max(prof.items(), key=lambda kv: kv[1][1])
     dom_name, (dom_n, dom_ms) = dom
     dom_avg_ms = dom_ms / dom_n
@@ -347,11 +347,41 @@ def run_ours(args, ws, rank):
         "kernels": {k: {"launches_per_step": c / args.steps, "ms_per_step": t / args.steps,
                         "share": t / sum(x[1] for x in prof.values())} for k, (c, t) in prof.items()},
         "gpu_launches": int(launches),
+        "dense": dense,
         "e2e": {"value": whole_job_rate(B * T, ms_e2e, ws), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
         "clocks": clk.summary(),
     }
     return res, inp
+
+
+def run_dense_arm(nsa, cfg, dev, B, T, H, G, dk, dv, nsa_ms, stream, args):
+    """Exact causal full attention on the same q/k/v (nsa_full_attn_fwd): the
+    dense comparison the pages quote NSA's 9.0x forward speed-up against."""
+    out = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device="cuda")
+    wsp = nsa.workspace(nsa.nsa_full_attn_workspace_size(cfg))
+
+    def step():
+        nsa.nsa_full_attn_fwd(cfg, dev["q"], dev["k"], dev["v"], out, wsp, stream)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("dense arm: device status set")
+    ms = e0.elapsed_time(e1) / n
+    fl = 2.0 * (dk + dv) * H * B * T * (T + 1) / 2
+    return {"what": "exact causal full attention on the same inputs (nsa_full_attn_fwd: one-pass online "
+                    "softmax, tcgen05, 8 queries x 16 heads per 128-row tile)",
+            "ms_per_step": ms, "steps": n, "useful_tflop_per_step": fl / 1e12,
+            "useful_tflops": fl / (ms * 1e-3) / 1e12,
+            "nsa_speedup": ms / nsa_ms, "pages_forward_speedup_64k_context": 9.0}
 
 
 # ---------------------------------------------------------------- decode leg

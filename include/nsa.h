@@ -174,20 +174,43 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
- * nsa_decode_step -- one new token per sequence [P2 II, III.3]: row t = T-1
+ * nsa_decode_step -- one new token per sequence [P2 II, III.3]: row t = len-1
  * of the prefill definition, read from the caches (the cache already holds
- * the new token).  Per KV head it reads the Nc compressed entries, the n
- * selected blocks and the w-token window.
+ * the new token).  Per KV head it reads the visible compressed entries, the
+ * n selected blocks and the w-token window of its own sequence.
  *   q      : [B,H,dk]        gates : [B,H,3]
- *   kcache : [B,G,T,dk]      vcache : [B,G,T,dv]   (head-major)
- *   kc, vc : [B,G,Nc,dk] / [B,G,Nc,dv] compressed caches (nsa_compress_kv
- *            with NSA_LAYOUT_BGTD)
+ *   kcache : [B,G,T,dk]      vcache : [B,G,T,dv]   (head-major; T = capacity)
+ *   kc, vc : [B,G,Nc,dk] / [B,G,Nc,dv] compressed caches at capacity T
+ *            (nsa_compress_kv with NSA_LAYOUT_BGTD; entry i only depends on
+ *            tokens 16i .. 16i+31, so a shorter sequence uses a prefix)
+ *   seq_lens (nullable): device int32 [B], sequence b's length len_b in
+ *            [1, T]; NULL means every sequence has length T.  The values are
+ *            read on the device: a length outside [1, T] is recorded as
+ *            NSA_ERR_INVALID_ARG in the workspace status word
+ *            (nsa_device_status) and that sequence is read as empty (its
+ *            out is zero, its idx_out all -1); the others are unaffected.
  *   out    : [B,H,dv]
  *   idx_out (nullable): [B,G,n] int32
  */
 int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const void* vcache,
-                    const void* kc, const void* vc, const void* gates, void* out,
-                    int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+                    const void* kc, const void* vc, const int32_t* seq_lens, const void* gates,
+                    void* out, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * nsa_full_attn_fwd -- exact causal full attention, the dense comparison the
+ * pages measure NSA against (9.0x forward at 64k, [P2] section III.3):
+ *   out[b,t,h,:] = softmax_{s <= t}(q[b,t,h,:] . k[b,s,g,:] * scale) @ v[b,:,g,:]
+ * with g = floor(h / (H/G)) and scale from cfg.  It runs the window path of
+ * the prefill kernel with a window covering the whole prefix, no compressed
+ * branch and gate 1.  Only B, T, H, G, dk, dv and scale of cfg are used (the
+ * rest must still pass the cfg rules); phi and gates are not read.
+ *   q [B,T,H,dk]   k [B,T,G,dk]   v [B,T,G,dv]   out [B,T,H,dv]
+ *   ws: nsa_full_attn_workspace_size(cfg) bytes (the status word).
+ * Supported: H/G <= 16, dv 64 or 128.
+ */
+size_t nsa_full_attn_workspace_size(const nsa_cfg* cfg);
+int nsa_full_attn_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, void* out,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- DSA */
 typedef struct dsa_cfg {

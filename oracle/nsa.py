@@ -332,15 +332,19 @@ def nsa_prefill_reference(inp: Dict[str, torch.Tensor], rows: Optional[Iterable[
 
 def nsa_decode_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[int]] = None,
                          params: NSAParams = NSAParams(),
-                         kc: Optional[np.ndarray] = None, vc: Optional[np.ndarray] = None
-                         ) -> Dict[str, np.ndarray]:
+                         kc: Optional[np.ndarray] = None, vc: Optional[np.ndarray] = None,
+                         seq_lens: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """Single-token decode for the sequences ``seqs`` (default all).
 
     inp: the bf16 tensors of ``workloads.make_decode`` (caches [B,G,T,d],
-    q [B,H,dk], gates [B,H,3]).  The query is at position t = T-1 (the cache
-    already holds the new token).  kc/vc: optional compressed caches
-    [B,G,Nc,d] (fp64); computed here when absent.  Returns out [S,H,dv],
-    idx [S,G,n], S32 [S,G,nb], kc/vc [S,G,Nc,d].
+    q [B,H,dk], gates [B,H,3]).  Sequence b holds len_b = seq_lens[b] tokens
+    (default T, the cache capacity); its query is at position t = len_b - 1
+    (the cache already holds the new token) and only cache rows < len_b exist
+    for it.  kc/vc: optional compressed caches [B,G,Nc,d] (fp64) at capacity;
+    a sequence uses the entries that lie inside its own tokens (entry i only
+    depends on tokens 16i .. 16i+31).  Computed here when absent.  Returns
+    out [S,H,dv], idx [S,G,n], S32 [S,G,nb], kc/vc [S,G,Nc,d] (nb, Nc at
+    capacity; a shorter sequence's rows are zero past its own).
     """
     kcache, vcache, q_t = inp["kcache"], inp["vcache"], inp["q"]
     B, G, T, dk = kcache.shape
@@ -349,6 +353,7 @@ def nsa_decode_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[i
     hpg = H // G
     scale = 1.0 / math.sqrt(dk)
     seqs = list(range(B)) if seqs is None else list(seqs)
+    lens = [T] * B if seq_lens is None else [int(x) for x in seq_lens]
     pe_k, pe_v = to_f64(inp["pe_k"]), to_f64(inp["pe_v"])
     w_k, w_v = to_f64(inp["w_k"]), to_f64(inp["w_v"])
     nb = -(-T // params.lsel)
@@ -359,24 +364,29 @@ def nsa_decode_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[i
                idx=np.zeros((S_, G, params.n), dtype=np.int32),
                S=np.zeros((S_, G, nb)), S32=np.zeros((S_, G, nb), dtype=np.float32),
                kc=np.zeros((S_, G, Nc, dk)), vc=np.zeros((S_, G, Nc, dv)))
-    t_rows = np.array([T - 1])
     for si, b in enumerate(seqs):
+        Tb = lens[b]
+        assert 1 <= Tb <= T, "a sequence holds between 1 and T tokens"
+        Ncb = num_compressed(Tb, params.l, params.d)
+        nbb = -(-Tb // params.lsel)
+        t_rows = np.array([Tb - 1])
         qb = to_f64(q_t[b])
         gb = to_f64(inp["gates"][b])
         for g in range(G):
-            K = to_f64(kcache[b, g])
-            V = to_f64(vcache[b, g])
-            Kc = compress(K, pe_k, w_k, params.l, params.d) if kc is None else kc[b, g]
-            Vc = compress(V, pe_v, w_v, params.l, params.d) if vc is None else vc[b, g]
-            res["kc"][si, g], res["vc"][si, g] = Kc, Vc
+            K = to_f64(kcache[b, g, :Tb])
+            V = to_f64(vcache[b, g, :Tb])
+            Kc = compress(K, pe_k, w_k, params.l, params.d) if kc is None else kc[b, g, :Ncb]
+            Vc = compress(V, pe_v, w_v, params.l, params.d) if vc is None else vc[b, g, :Ncb]
+            res["kc"][si, g, :Ncb], res["vc"][si, g, :Ncb] = Kc, Vc
             hs = slice(g * hpg, (g + 1) * hpg)
             r = nsa_group_rows(qb[None, hs], t_rows, K, V, Kc, Vc, gb[None, hs], params, scale)
             for key in ("out", "o_cmp", "o_slc", "o_win"):
                 res[key][si, hs] = r[key][0]
             res["idx"][si, g] = r["idx"][0]
-            res["S"][si, g] = r["S"][0]
-            res["S32"][si, g] = r["S32"][0]
+            res["S"][si, g, :nbb] = r["S"][0]
+            res["S32"][si, g, :nbb] = r["S32"][0]
     res["seqs"] = np.array(seqs)
+    res["lens"] = np.array([lens[b] for b in seqs])
     return res
 
 

@@ -22,7 +22,7 @@ __all__ = [
     "nsa_status_string", "nsa_version", "nsa_num_compressed",
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
-    "nsa_compress_kv_noalloc_status", "nsa_prefill_fwd", "nsa_decode_step",
+    "nsa_compress_kv_noalloc_status", "nsa_full_attn_workspace_size", "nsa_full_attn_fwd", "nsa_prefill_fwd", "nsa_decode_step",
     "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
@@ -74,11 +74,13 @@ def _load() -> ctypes.CDLL:
                                      _c_vp]),
         "nsa_prefill_fwd": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                      _c_vp, _c_vp, _c_size, _c_vp]),
-        "nsa_decode_step": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+        "nsa_decode_step": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "dsa_decode_step": (_c_int, [P(DsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
+        "nsa_full_attn_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_full_attn_fwd": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_compress_kv_noalloc": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
         "nsa_compress_kv_noalloc_status": (_c_int, [_c_vp]),
         "nsa_profile_enable": (_c_int, [_c_int]),
@@ -207,9 +209,21 @@ def nsa_prefill_fwd(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, ws, strea
            "nsa_prefill_fwd")
 
 
-def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None):
+def nsa_full_attn_workspace_size(cfg: NsaCfg) -> int:
+    return _lib().nsa_full_attn_workspace_size(ctypes.byref(cfg))
+
+
+def nsa_full_attn_fwd(cfg: NsaCfg, q, k, v, out, ws, stream=None):
+    """Exact causal full attention (the dense comparison)."""
+    _check(_lib().nsa_full_attn_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(ws),
+                                 ws.numel() if ws is not None else 0, _stream(stream)), "nsa_full_attn_fwd")
+
+
+def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None,
+                    seq_lens=None):
+    """seq_lens: optional int32 device tensor [B] of sequence lengths (None: all cfg.T)."""
     _check(_lib().nsa_decode_step(ctypes.byref(cfg), _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kc),
-                               _ptr(vc), _ptr(gates), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               _ptr(vc), _ptr(seq_lens), _ptr(gates), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_decode_step")
 

@@ -101,6 +101,14 @@ int prefill_supported(const nsa_cfg& c) {
   return NSA_OK;
 }
 
+// shapes the dense comparison implements (beyond validate_cfg)
+int full_attn_supported(const nsa_cfg& c) {
+  const int hpg = c.H / c.G;
+  if (hpg > 16 || (c.dv != 64 && c.dv != 128)) return NSA_ERR_UNSUPPORTED;
+  if (cmp_win_smem_bytes(c, true) > smem_max()) return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
 int check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (ws == nullptr) return NSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return NSA_ERR_MISALIGNED;
@@ -172,7 +180,7 @@ const char* nsa_status_string(int status) {
   }
 }
 
-int nsa_version(void) { return 100; }
+int nsa_version(void) { return 200; }
 
 int nsa_num_compressed(const nsa_cfg* cfg) {
   if (validate_cfg(cfg) != NSA_OK) return -1;
@@ -231,14 +239,34 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
   return launch_sel(c, q, k, v, gates, idx, part, out, st, s);
 }
 
+size_t nsa_full_attn_workspace_size(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK || full_attn_supported(*cfg) != NSA_OK) return 0;
+  return kHeader;
+}
+
+int nsa_full_attn_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, void* out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  const nsa_cfg& c = *cfg;
+  if ((rc = full_attn_supported(c)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, k, v, out})) != NSA_OK) return rc;
+  if ((rc = check_ws(ws, ws_bytes, kHeader)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  return launch_cmp_win(c, q, k, v, nullptr, nullptr, nullptr, out, nullptr, reinterpret_cast<DeviceStatus*>(ws), s,
+                        true);
+}
+
 size_t nsa_decode_workspace_size(const nsa_cfg* cfg) {
   if (validate_cfg(cfg) != NSA_OK || decode_supported(*cfg) != NSA_OK) return 0;
   return decode_ws_bytes(*cfg);
 }
 
 int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const void* vcache, const void* kc,
-                    const void* vc, const void* gates, void* out, int32_t* idx_out, void* ws, size_t ws_bytes,
-                    void* stream) {
+                    const void* vc, const int32_t* seq_lens, const void* gates, void* out, int32_t* idx_out,
+                    void* ws, size_t ws_bytes, void* stream) {
   int rc = validate_cfg(cfg);
   if (rc != NSA_OK) return rc;
   const nsa_cfg& c = *cfg;
@@ -246,11 +274,12 @@ int nsa_decode_step(const nsa_cfg* cfg, const void* q, const void* kcache, const
   if ((rc = check_ptrs({q, kcache, vcache, gates, out})) != NSA_OK) return rc;
   if (num_compressed(c) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
   if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  if (seq_lens != nullptr && (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0) return NSA_ERR_MISALIGNED;
   if ((rc = check_ws(ws, ws_bytes, decode_ws_bytes(c))) != NSA_OK) return rc;
   if ((rc = check_device()) != NSA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, decode_zero_bytes(c), s) != cudaSuccess) return NSA_ERR_CUDA;
-  return launch_decode(c, q, kcache, vcache, kc, vc, gates, out, idx_out, static_cast<uint8_t*>(ws), s);
+  return launch_decode(c, q, kcache, vcache, kc, vc, seq_lens, gates, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
 int validate_dsa(const dsa_cfg* c) {

@@ -35,24 +35,52 @@ struct CompressArgs {
   DeviceStatus* st;
 };
 
-// bias[n] = sum_r pe_flat[r] * W[r, n], r < rows = l*dX  (fp32)
-__global__ void phi_bias_kernel(const __nv_bfloat16* __restrict__ pe, const __nv_bfloat16* __restrict__ w,
-                                int rows, int N, float* __restrict__ bias) {
-  __shared__ float red[8][33];
+// bias[n] = sum_r pe_flat[r] * W[r, n], r < rows = l*dX  (fp32).
+// A cluster of kBiasSplit CTAs shares 32 columns: CTA c sums its slice of the
+// rows, and CTA 0 adds the slices' partials from the other CTAs' shared
+// memory (distributed shared memory) in a fixed order, so the result does not
+// depend on scheduling.
+constexpr int kBiasSplit = 8;
+constexpr int kBiasRowsY = 16;
+
+__global__ void __cluster_dims__(1, kBiasSplit, 1) __launch_bounds__(32 * kBiasRowsY)
+    phi_bias_kernel(const __nv_bfloat16* __restrict__ pe, const __nv_bfloat16* __restrict__ w, int rows, int N,
+                    float* __restrict__ bias) {
+  __shared__ float red[kBiasRowsY][33];
+  __shared__ float part[32];
   const int n = blockIdx.x * 32 + threadIdx.x;
+  const int per = (rows + kBiasSplit - 1) / kBiasSplit;
+  const int r0 = blockIdx.y * per, r1 = min(rows, r0 + per);
   float acc = 0.f;
   if (n < N) {
-    for (int r = threadIdx.y; r < rows; r += 8)
+#pragma unroll 4
+    for (int r = r0 + threadIdx.y; r < r1; r += kBiasRowsY)
       acc = fmaf(__bfloat162float(pe[r]), __bfloat162float(w[(size_t)r * N + n]), acc);
   }
   red[threadIdx.y][threadIdx.x] = acc;
   __syncthreads();
-  if (threadIdx.y == 0 && n < N) {
-    float s = 0.f;
+  if (threadIdx.y == 0) {
+    float sum = 0.f;
 #pragma unroll
-    for (int y = 0; y < 8; ++y) s += red[y][threadIdx.x];
-    bias[n] = s;
+    for (int y = 0; y < kBiasRowsY; ++y) sum += red[y][threadIdx.x];
+    part[threadIdx.x] = sum;
   }
+  // every CTA's partial is in its shared memory before CTA 0 reads them
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (blockIdx.y == 0 && threadIdx.y == 0) {
+    float sum = 0.f;
+    const uint32_t local = smem_u32(&part[threadIdx.x]);
+    for (int c = 0; c < kBiasSplit; ++c) {
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(c));
+      float v;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+      sum += v;
+    }
+    if (n < N) bias[n] = sum;
+  }
+  // no CTA leaves while CTA 0 may still read its shared memory
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -190,7 +218,7 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
   const int N = dX;
   // bias = flatten(PE) @ W
   {
-    dim3 grid((N + 31) / 32), block(32, 8);
+    dim3 grid((N + 31) / 32, kBiasSplit), block(32, kBiasRowsY);
     prof::begin("phi_bias", stream);
     phi_bias_kernel<<<grid, block, 0, stream>>>(static_cast<const __nv_bfloat16*>(pe),
                                                 static_cast<const __nv_bfloat16*>(W), c.l * dX, N, bias_ws);

@@ -51,10 +51,10 @@ constexpr int kQBuf = 2048;          // one 64-column chunk of NP query rows
 constexpr int kPBuf = kPairs * 2 * kQBuf;
 
 struct DecArgs {
-  int B, T, H, G, BG, hpg, n, w;
-  int Nc, ncu, nwu, nsu, NS;         // compressed / window / selected units per group, slots
-  int win0, win_len;                 // first window token, window length
+  int B, T, H, G, BG, hpg, n, w;     // T: cache capacity (row stride of the caches)
+  int Nc, ncu, nwu, nsu, NS;         // at capacity: compressed / window / selected units per group, slots
   float sc2;                         // softmax scale * log2(e)
+  const int32_t* lens;               // nullable [B]: tokens of each sequence (query at len-1)
   const __nv_bfloat16* gates;        // [B,H,3]
   __nv_bfloat16* out;                // [B,H,dv]
   int32_t* idx_out;                  // nullable [B,G,n]
@@ -82,6 +82,25 @@ struct Bars {
   int abort_flag;
   int last;
 };
+
+// This sequence's length, its compressed-entry count and window start.  A
+// length outside [1, T] is recorded as NSA_ERR_INVALID_ARG and the sequence
+// is treated as empty (nothing of it is read; its output is zero).
+struct SeqGeom {
+  int len, Nc, win0;
+};
+__device__ __forceinline__ SeqGeom seq_geom(const DecArgs& a, int b, DeviceStatus* st) {
+  int len = a.lens != nullptr ? __ldg(a.lens + b) : a.T;
+  if (len < 1 || len > a.T) {
+    record_error(st, NSA_ERR_INVALID_ARG, 400);
+    len = 0;
+  }
+  SeqGeom s;
+  s.len = len;
+  s.Nc = len < 32 ? 0 : min((len - 32) / 16 + 1, a.Nc);
+  s.win0 = len - min(a.w, len);
+  return s;
+}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -208,7 +227,9 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   const int tid = threadIdx.x;
   const int warp = warp_id(), lane = lane_id();
   const int ncu = a.ncu, n = a.n;
-  const int jt = (a.T - 1) / 64;
+  const SeqGeom sg = seq_geom(a, bg / a.G, nullptr);
+  const int Nc = sg.Nc;
+  const int jt = sg.len > 0 ? (sg.len - 1) / 64 : -1;   // -1: empty sequence, nothing kept
   const bool trivial = jt + 1 <= n;
   const SelStage L = sel_stage(ncu, jt, a.sel_cap);
   float* st = reinterpret_cast<float*>(smem);
@@ -222,7 +243,7 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   float* iL = Mh + 16;
   float* wv = iL + 16;
   int* wj = reinterpret_cast<int*>(wv + 128);
-  const int nblk = min(jt + 1, (a.Nc + 3) / 4);   // blocks holding compressed entries
+  const int nblk = min(jt + 1, (Nc + 3) / 4);     // blocks holding compressed entries
   const float* ub = a.u + (size_t)bg * ncu * kUnitBlocks * 16;
   stage_stats(a, bg, 0, ncu, sp);
   if (!trivial) {
@@ -259,7 +280,7 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   // block importance: block j takes the partial of its four entries (unit
   // j/kUnitBlocks); blocks 8k+8 also take the carry of chunk k (entry 32k+31)
   for (int k = tid; k < ncu * kUnitChunks; k += kThreads)
-    car[k] = (32 * k < a.Nc) ? dot16(fsm + (k / kUnitChunks) * 16, reinterpret_cast<const float4*>(ccs + 16 * k))
+    car[k] = (32 * k < Nc) ? dot16(fsm + (k / kUnitChunks) * 16, reinterpret_cast<const float4*>(ccs + 16 * k))
                              : 0.f;
   for (int c0 = 0; c0 <= jt; c0 += a.sel_cap) {
     if (c0 > 0) {
@@ -276,7 +297,7 @@ __device__ void select_step(const DecArgs& a, int bg, uint8_t* smem) {
   }
   __syncthreads();
   for (int k = tid; 8 * k + 8 <= jt; k += kThreads)
-    if (32 * k < a.Nc) Ssm[8 * k + 8] += car[k];
+    if (32 * k < Nc) Ssm[8 * k + 8] += car[k];
   __syncthreads();
   // top-(n-3) among the free blocks 1 .. jt-2: each of 4 warps finds the best
   // of its quarter of the range, warp 0 merges.  Order: higher score, then
@@ -459,22 +480,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = warp_id(), lane = lane_id();
 
   // ------------------------------------------------------------ unit geometry
+  // (the grid is sized for the cache capacity; a shorter sequence leaves some
+  // units empty: npairs = 0)
+  const SeqGeom sg = seq_geom(a, b, threadIdx.x == 0 && x == 0 ? a.st : nullptr);
   const bool cmp_unit = MODE == 0 && x < a.ncu;
-  int base = 0, limit = a.T, npairs = kPairs, sel0 = 0;
+  int base = 0, limit = sg.len, npairs = kPairs, sel0 = 0;
   if (MODE == 0) {
     if (cmp_unit) {
       base = kUnitKeys * x;
-      limit = a.Nc;
-      npairs = min(kPairs, (a.Nc - base + 127) / 128);
+      limit = sg.Nc;
+      npairs = min(kPairs, (sg.Nc - base + 127) / 128);
     } else {
-      base = a.win0 + kUnitKeys * (x - a.ncu);
-      limit = a.T;
-      npairs = min(kPairs, (a.T - base + 127) / 128);
+      base = sg.win0 + kUnitKeys * (x - a.ncu);
+      limit = sg.len;
+      npairs = min(kPairs, (sg.len - base + 127) / 128);
     }
   } else {
     sel0 = 2 * kPairs * x;
-    npairs = min(kPairs, (a.n - sel0 + 1) / 2);
+    npairs = sg.len > 0 ? min(kPairs, (a.n - sel0 + 1) / 2) : 0;
   }
+  npairs = max(npairs, 0);
   const CUtensorMap* mapK = cmp_unit ? &mK0 : &mK1;
   const CUtensorMap* mapV = cmp_unit ? &mV0 : &mV1;
   // first map row of block 2p+hb of this unit; -1 if absent (reads zeros)
@@ -742,6 +767,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t rr[16];
       tmem_ld16(tmem_o + lane_base, rr);
       tmem_ld_wait(rr);
+      if (npairs == 0) {   // no MMA wrote O: the unit's partial is zero
+#pragma unroll
+        for (int h = 0; h < NP; ++h) rr[h] = 0u;
+      }
       if (r < DV) {
         float* dst = a.po + pbase * 16 * DV + r;
 #pragma unroll
@@ -876,7 +905,8 @@ size_t decode_ws_bytes(const nsa_cfg& c) { return dec_ws(c).end; }
 size_t decode_zero_bytes(const nsa_cfg& c) { return dec_ws(c).pm; }
 
 int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const void* vcache, const void* kc,
-                  const void* vc, const void* gates, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s) {
+                  const void* vc, const int32_t* lens, const void* gates, void* out, int32_t* idx_out, uint8_t* ws,
+                  cudaStream_t s) {
   const DecShape sh = dec_shape(c);
   const DecWs w = dec_ws(c);
   const DecLayout L = dec_layout(c);
@@ -915,8 +945,7 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
   a.nwu = sh.nwu;
   a.nsu = sh.nsu;
   a.NS = sh.NS;
-  a.win0 = sh.win0;
-  a.win_len = sh.win_len;
+  a.lens = lens;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
   a.gates = static_cast<const __nv_bfloat16*>(gates);

@@ -35,12 +35,15 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
                         void* out, float* bias_ws, DeviceStatus* st, cudaStream_t stream);
 
 // ---- prefill (prefill_cmp_win.cu, prefill_sel.cu)
-size_t cmp_win_smem_bytes(const nsa_cfg& c);
+size_t cmp_win_smem_bytes(const nsa_cfg& c, bool dense = false);
 size_t sel_smem_bytes(const nsa_cfg& c);
 // compressed attention + block scores + top-n + window; writes
-// part = g_cmp*O_cmp + g_win*O_win (bf16 [B,T,H,dv]) and idx [B,T,G,n]
+// part = g_cmp*O_cmp + g_win*O_win (bf16 [B,T,H,dv]) and idx [B,T,G,n].
+// dense: exact causal full attention of q over k/v written to ``part``
+// (no compressed branch, no selection, gates unused).
 int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
-                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s);
+                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s,
+                   bool dense = false);
 // selected attention; out = part + g_slc*O_slc
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
                const void* part, void* out, DeviceStatus* st, cudaStream_t s);
@@ -51,8 +54,10 @@ size_t decode_ws_bytes(const nsa_cfg& c);
 // bytes at the start of the decode workspace (status word + counters) that
 // must be zero when the step starts
 size_t decode_zero_bytes(const nsa_cfg& c);
+// lens: nullable device array [B] of sequence lengths (each in [1, c.T])
 int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const void* vcache, const void* kc,
-                  const void* vc, const void* gates, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
+                  const void* vc, const int32_t* lens, const void* gates, void* out, int32_t* idx_out, uint8_t* ws,
+                  cudaStream_t s);
 
 // ---- DSA decode (dsa.cu)
 int dsa_supported(const dsa_cfg& c);

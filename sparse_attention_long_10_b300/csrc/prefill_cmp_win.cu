@@ -1,4 +1,10 @@
 // prefill_cmp_win.cu -- NSA prefill, per (sequence, KV group, tile of queries):
+//   0. sliding-window attention over (t-w, t] [P2 II.3; P3], one pass with an
+//      online softmax: both softmax warpgroups share each row's reference max
+//      (exchanged once per key tile) and rescale their half of O, while O is
+//      idle, when the max grows by more than 2^8; at the end O is scaled by
+//      g_win / sum.  The window runs first so that these rescales never touch
+//      the compressed branch's part of O;
 //   1. compressed attention [P2 II.1; P3 token compression], two passes over
 //      the compressed keys: pass 1 finds each row's softmax max and sum, pass 2
 //      recomputes the scores, forms the exactly normalised probabilities p,
@@ -6,9 +12,10 @@
 //          S[t,j] = sum_{h in group} sum_i w(i,j) p[t,h,i]
 //      (w = d-token chunks shared by compressed block i and selection block j);
 //   2. top-n block selection [P2 II: n blocks incl. block 0 and the 2 local
-//      blocks; P3 token selection], ties to the lower block index;
-//   3. sliding-window attention over (t-w, t] [P2 II.3; P3], again two
-//      passes so the probabilities are exactly normalised.
+//      blocks; P3 token selection], ties to the lower block index.
+// Dense mode (``dense``): step 0 alone with w >= T and gate 1, i.e. exact
+// causal full attention -- the comparison the pages quote NSA's speed-ups
+// against [P2 III.3] -- written straight to the output.
 // The gates are folded into the probabilities (P' = g * p), so one TMEM
 // accumulator holds g_cmp*O_cmp + g_win*O_win; that partial sum is written in
 // bf16 and the selected-attention kernel adds g_slc*O_slc to it.
@@ -42,7 +49,7 @@ constexpr int kThreads = 384;
 constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
 
 struct CmpWinArgs {
-  int T, H, G, dk, dv, n, w, Nc, QT, nbs;
+  int T, H, G, dk, dv, n, w, Nc, QT, nbs, dense;
   float sc2;                       // softmax scale * log2(e)
   const __nv_bfloat16* gates;      // [B,T,H,3]
   __nv_bfloat16* part;             // [B,T,H,dv]
@@ -145,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
 
   const int QT = a.QT;
-  const int t0 = blockIdx.x * QT;
+  // the last query tiles see the most keys: launch them first
+  const int t0 = (gridDim.x - 1 - blockIdx.x) * QT;
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = warp_id();
@@ -232,13 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++v;
       };
       if (keys) {
-        // compressed keys twice (statistics pass, exact pass), then window keys twice
+        // window keys once (online softmax), then compressed keys twice
+        // (statistics pass, exact pass)
+        for (int j = 0; j < ntw; ++j)
+          for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b);
         for (int pass = 0; pass < 2; ++pass)
           for (int j = 0; j < ntc; ++j)
             for (int c = 0; c < kcs; ++c) push(&mapKc, c * 64, j * kTile, g, b);
-        for (int pass = 0; pass < 2; ++pass)
-          for (int j = 0; j < ntw; ++j)
-            for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b);
       } else {
         // with two value chunks a tile's PV is one N = 128 MMA per key step,
         // whose B operand takes dv 0..63 from the lower of the tile's two
@@ -248,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool swap = vcs == 2 && v % kRingV == kRingV - 1;   // tile's first slot
           for (int c = 0; c < vcs; ++c) {
             const int cc = swap ? 1 - c : c;
-            if (j < ntc) push(&mapVc, cc * 64, j * kTile, g, b);
-            else push(&mapV, cc * 64, g, s_lo + (j - ntc) * kTile, b);
+            if (j < ntw) push(&mapV, cc * 64, g, s_lo + j * kTile, b);
+            else push(&mapVc, cc * 64, (j - ntw) * kTile, g, b);
           }
         }
       }
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idesc_qk = idesc_bf16_f32(128, kTile, false, false);
         const uint32_t qs_a = smem_u32(qs), k_a = smem_u32(kring);
         ok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 211);
-        const int ntiles = 2 * ntc + 2 * ntw;
+        const int ntiles = ntw + 2 * ntc;
         int kv = 0;
         for (int u = 0; u < ntiles && ok; ++u) {
           const int sb = u & 1;
@@ -373,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = t < a.T;
     const int head = g * HPG + h;
     const int n_t = row_ok ? visible_cmp(t, a.Nc) : 0;
-    float g_c = 0.f, g_w = 0.f;
-    if (row_ok) {
+    float g_c = 0.f, g_w = a.dense ? 1.f : 0.f;
+    if (row_ok && !a.dense) {
       const __nv_bfloat16* gp = a.gates + (((size_t)b * a.T + t) * a.H + head) * 3;
       g_c = __bfloat162float(gp[0]);
       g_w = __bfloat162float(gp[2]);
@@ -382,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
     const int c0 = 64 * wg;                  // first column of this warpgroup
     float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2 wg][2 m/l][128 rows]
+    float* xmax = red + 2 * 2 * 128;                            // [2 tiles][2 wg][128 rows]
     bool ok = true;
     int u = 0, pv = 0;
     uint32_t all_phase = 0;
@@ -405,10 +414,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->s_free[sb]);
       return true;
     };
-    auto put_p = [&](const float (&p)[64], float gate) -> bool {
+    const int half = a.dv / 2;               // O columns of this warpgroup: wg*half ..
+    // multiplies this row's half of O by f; O must be idle (no PV in flight)
+    auto scale_o = [&](float f) {
+      for (int cc = wg * half; cc < (wg + 1) * half; cc += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tmem_o + lane_base + cc, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const float2 y = __fmul2_rn(make_float2(__uint_as_float(rr[k]), __uint_as_float(rr[k + 1])), make_float2(f, f));
+          rr[k] = __float_as_uint(y.x);
+          rr[k + 1] = __float_as_uint(y.y);
+        }
+        tmem_st16(tmem_o + lane_base + cc, rr);
+      }
+    };
+    // waits until every PV issued so far has completed: O is then idle until
+    // this thread's next P arrives (the PV issuer waits for all 8 warps' P)
+    auto wait_o_idle = [&]() -> bool {
       if (!mbar_wait(&bars->p_free, (uint32_t)((pv & 1) ^ 1), abort_flag, a.st, 223)) return false;
-      ++pv;
       tc_fence_after();
+      return true;
+    };
+    // P (times ``gate``) of the next PV tile; when oscale != 1 this row's half
+    // of O is first multiplied by it (O is idle at that point)
+    auto put_p = [&](const float (&p)[64], float gate, float oscale) -> bool {
+      if (!wait_o_idle()) return false;
+      if (oscale != 1.f && pv > 0) scale_o(oscale);
+      ++pv;
       // this row's 64 keys of the warpgroup's half, as bf16 pairs, into
       // columns 32*wg .. 32*wg+31 of P in tensor memory
       {
@@ -476,10 +510,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // zero the block-score rows
-    for (int i = wg * 128 + r; i < QT * a.nbs; i += 256) scores[i] = 0.f;
-    sync8();
-
+    if (!a.dense) {
+      for (int i = wg * 128 + r; i < QT * a.nbs; i += 256) scores[i] = 0.f;
+      sync8();
+    }
     float x[64];
+    // ---------------- phase 0: window, online softmax
+    // mref: this row's reference max (log2 units, shared by both warpgroups),
+    // p = exp2(s*scale - mref); O and the sum follow mref when it moves up
+    {
+      const int w_lo = t - a.w + 1;
+      float mref = -INFINITY, lw = 0.f;
+      for (int j = 0; j < ntw && ok; ++j) {
+        if (!consume_s(x)) { ok = false; break; }
+        const int s0 = s_lo + j * kTile + c0;
+        if (!(row_ok && s0 >= w_lo && s0 + 63 <= t)) {   // interior tiles need no mask
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const int sx = s0 + i;
+            x[i] = (row_ok && sx >= w_lo && sx <= t) ? x[i] : -INFINITY;
+          }
+        }
+        float mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mt = fmaxf(mt, x[i]);
+        float* xm = xmax + (j & 1) * 256;
+        xm[wg * 128 + r] = mt;
+        sync8();
+        if (!ok) break;
+        const float mtile = fmaxf(mt, xm[(1 - wg) * 128 + r]) * a.sc2;
+        float fac = 1.f;
+        if (mtile > mref + 8.f) {     // also the first finite tile (mref = -inf)
+          fac = fast_exp2(mref - mtile);
+          lw *= fac;
+          mref = mtile;
+        }
+        if (mref == -INFINITY) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) x[i] = 0.f;
+        } else {
+          exp_cols(x, mref);
+        }
+        float2 sm = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) sm = __fadd2_rn(sm, make_float2(x[i], x[i + 1]));
+        lw += sm.x + sm.y;
+        if (!put_p(x, 1.f, fac)) { ok = false; break; }
+      }
+      // O <- O * g_win / sum, once every window PV has completed
+      red[wg * 128 + r] = lw;
+      sync8();
+      const float L = lw + red[(1 - wg) * 128 + r];
+      sync8();
+      if (ok && pv > 0) {
+        if (!wait_o_idle()) ok = false;
+        else {
+          scale_o(L > 0.f ? g_w / L : 0.f);
+          tmem_st_wait();
+          tc_fence_before();
+        }
+      }
+    }
     // ---------------- phase 1: compressed max / sum
     float m = -INFINITY, l = 0.f, inv_l = 0.f;
     for (int j = 0; j < ntc && ok; ++j) {
@@ -520,11 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16 / HPG; ++k) atomicAdd(&srow[32 * j + 16 * wg + base + k], vsum[k]);
         if (lead) atomicAdd(&srow[32 * j + 16 * wg + 16], carry);
       }
-      if (!put_p(x, g_c)) { ok = false; break; }
+      if (!put_p(x, g_c, 1.f)) { ok = false; break; }
     }
     // ---------------- top-n selection (one warp per query)
     sync8();
-    if (ok) {
+    if (ok && !a.dense) {
       for (int qq = warp; qq < QT; qq += 8) {
         const int tq = t0 + qq;
         if (tq >= a.T) continue;
@@ -594,45 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < a.n) out[rank] = mine;
       }
     }
-    // ---------------- phase 3: window max / sum
-    m = -INFINITY;
-    l = 0.f;
-    const int w_lo = t - a.w + 1;
-    for (int j = 0; j < ntw && ok; ++j) {
-      if (!consume_s(x)) { ok = false; break; }
-      const int s0 = s_lo + j * kTile + c0;
-      if (!(row_ok && s0 >= w_lo && s0 + 63 <= t)) {   // interior tiles need no mask
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int s = s0 + i;
-          x[i] = (row_ok && s >= w_lo && s <= t) ? x[i] : -INFINITY;
-        }
-      }
-      stats_add(x, m, l);
-    }
-    merge_stats(m, l, inv_l);
-    // the window gate goes into the exponent: P = g_w * p
-    const float mw = m - __log2f(g_w);
-    // ---------------- phase 4: exact window p, accumulate g_w * O_win
-    for (int j = 0; j < ntw && ok; ++j) {
-      if (!consume_s(x)) { ok = false; break; }
-      const int s0 = s_lo + j * kTile + c0;
-      if (row_ok && s0 >= w_lo && s0 + 63 <= t) {
-        exp_cols(x, mw);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int s = s0 + i;
-          x[i] = (row_ok && s >= w_lo && s <= t) ? fast_exp2(fmaf(x[i], a.sc2, -mw)) : 0.f;
-        }
-      }
-      if (!put_p(x, 1.f)) { ok = false; break; }
-    }
     // ---------------- epilogue: O -> bf16 partial output (each warpgroup half the columns)
     if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 224)) {
       tc_fence_after();
       __nv_bfloat16* dst = a.part + (((size_t)b * a.T + t) * a.H + head) * a.dv;
-      const int half = a.dv / 2;
       for (int cc = wg * half; cc < (wg + 1) * half; cc += 16) {
         uint32_t rr[16];
         tmem_ld16(tmem_o + lane_base + cc, rr);
@@ -664,7 +720,8 @@ Layout layout_for(int dk, int QT, int nbs) {
   L.off_vring = L.off_kring + kRingK * kSlot;
   L.off_scores = L.off_vring + kRingV * kSlot;
   L.off_red = (uint32_t)align_up(L.off_scores + (size_t)QT * nbs * sizeof(float), 256);
-  L.off_bar = (uint32_t)align_up(L.off_red + 2 * 2 * 128 * sizeof(float), 1024);
+  // red: [2 wg][2 m/l][128 rows] statistics, then [2 tiles][2 wg][128 rows] window tile maxima
+  L.off_bar = (uint32_t)align_up(L.off_red + 4 * 2 * 128 * sizeof(float), 1024);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(Bars), 256) + 1024;  // + alignment slack
   return L;
 }
@@ -680,7 +737,7 @@ template <int HPG>
 int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
   if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&cmp_win_kernel<HPG>), smem_max())) return rc;
   dim3 grid((a0.T + a0.QT - 1) / a0.QT, a0.G, B);
-  prof::begin("cmp_win", s);
+  prof::begin(a0.dense ? "full_attn" : "cmp_win", s);
   cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
@@ -688,19 +745,20 @@ int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem
 
 }  // namespace
 
-size_t cmp_win_smem_bytes(const nsa_cfg& c) {
+size_t cmp_win_smem_bytes(const nsa_cfg& c, bool dense) {
   const int hpg = c.H / c.G;
   const int QT = 128 / hpg;
   const int Nc = c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
-  return layout_for(c.dk, QT, scores_stride(c.T, Nc)).total;
+  return layout_for(c.dk, QT, dense ? 0 : scores_stride(c.T, Nc)).total;
 }
 
 int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
-                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s) {
+                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s, bool dense) {
   const int hpg = c.H / c.G;
   const int QT = 128 / hpg;
-  const int Nc = c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
-  const int nbs = scores_stride(c.T, Nc);
+  // dense: no compressed branch, a window covering the whole prefix
+  const int Nc = dense || c.T < c.l ? 0 : (c.T - c.l) / c.d + 1;
+  const int nbs = dense ? 0 : scores_stride(c.T, Nc);
   const Layout L = layout_for(c.dk, QT, nbs);
   if (L.total > smem_max()) return NSA_ERR_UNSUPPORTED;
   const uint64_t e = 2;
@@ -743,10 +801,11 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
   a.dk = c.dk;
   a.dv = c.dv;
   a.n = c.n;
-  a.w = c.w;
+  a.w = dense ? c.T : c.w;
   a.Nc = Nc;
   a.QT = QT;
   a.nbs = nbs;
+  a.dense = dense ? 1 : 0;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
   a.gates = static_cast<const __nv_bfloat16*>(gates);

@@ -180,17 +180,19 @@ def test_decode_argument_checks(nsa):
         a = dict(q=FAKE, kcache=FAKE, vcache=FAKE, kc=FAKE, vc=FAKE, gates=FAKE, out=FAKE, idx=None, ws=FAKE,
                  ws_bytes=need)
         a.update(kw)
-        return f(ctypes.byref(c), a["q"], a["kcache"], a["vcache"], a["kc"], a["vc"], a["gates"], a["out"],
-                 a["idx"], a["ws"], a["ws_bytes"], None)
+        return f(ctypes.byref(c), a["q"], a["kcache"], a["vcache"], a["kc"], a["vc"], a.get("lens"), a["gates"],
+                 a["out"], a["idx"], a["ws"], a["ws_bytes"], None)
     assert call(kcache=None) == 1
     assert call(gates=FAKE + 8) == 3
     assert call(vc=None) == 1
     assert call(ws_bytes=need - 1) == 4
+    assert call(lens=FAKE + 2) == 3                                 # int32 lengths, 4-byte aligned
     if not torch.cuda.is_available():
         assert call() == 7
+        assert call(lens=FAKE + 4) == 7                             # a device array of lengths
     wide = nsa.make_cfg(16, 65536, 64, 2, 192, 128)                # 32 heads per group
     assert nsa.nsa_decode_workspace_size(wide) == 0
-    assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None) == 2
+    assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, 1 << 40, None) == 2
 
 
 @pytest.mark.parametrize("mutate", [
@@ -224,3 +226,18 @@ def test_noalloc_argument_checks_match(nsa):
         c.pe_v = FAKE
         assert f_na(0, FAKE, FAKE, FAKE, FAKE) == 7
         assert nsa.lib.nsa_compress_kv_noalloc_status(None) == 7
+
+
+def test_full_attention_argument_checks(nsa):
+    c = nsa.make_cfg(1, 4096, 64, 4, 192, 128)
+    need = nsa.nsa_full_attn_workspace_size(c)
+    assert need == 256                                   # the status word only
+    f = nsa.lib.nsa_full_attn_fwd
+    assert f(ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, need, None) == 1
+    assert f(ctypes.byref(c), FAKE, FAKE + 2, FAKE, FAKE, FAKE, need, None) == 3
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, None) == 4
+    wide = nsa.make_cfg(1, 4096, 64, 2, 192, 128)        # 32 heads per group
+    assert nsa.nsa_full_attn_workspace_size(wide) == 0
+    assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 2
+    if not torch.cuda.is_available():
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 7

@@ -27,7 +27,7 @@ def _nsa():
     return nsa
 
 
-def run_decode(inp, kc=None, vc=None, params=NSAParams(), idx_fill=-7):
+def run_decode(inp, kc=None, vc=None, params=NSAParams(), idx_fill=-7, seq_lens=None, expect_status=0):
     """Decode through the C-ABI.  kc/vc: oracle compressed caches [B,G,Nc,d]
     (fp64 on the bf16 grid); when None the GPU compresses the caches itself
     with nsa_compress_kv (head-major layout)."""
@@ -50,9 +50,11 @@ def run_decode(inp, kc=None, vc=None, params=NSAParams(), idx_fill=-7):
     out = torch.full((B, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     idx = torch.full((B, G, params.n), idx_fill, dtype=torch.int32, device="cuda")
     ws = nsa.workspace(nsa.nsa_decode_workspace_size(cfg))
-    nsa.nsa_decode_step(cfg, d["q"], d["kcache"], d["vcache"], kc_t, vc_t, d["gates"], out, idx, ws)
+    lens = None if seq_lens is None else torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    nsa.nsa_decode_step(cfg, d["q"], d["kcache"], d["vcache"], kc_t, vc_t, d["gates"], out, idx, ws,
+                        seq_lens=lens)
     torch.cuda.synchronize()
-    assert nsa.nsa_device_status(ws) == 0
+    assert nsa.nsa_device_status(ws) == expect_status
     return out, idx, kc_t, vc_t
 
 
@@ -62,13 +64,14 @@ def check_decode(inp, ref, out, idx, params=NSAParams(), label="", near_tie=NEAR
     H = inp["q"].shape[1]
     hpg = H // G
     scale = 1.0 / math.sqrt(dk)
-    t = T - 1
     seqs = [int(s) for s in ref["seqs"]]
+    lens = [int(x) for x in ref["lens"]]
     got = out[torch.as_tensor(seqs)].float().cpu().numpy()       # [S,H,dv]
     gidx = idx[torch.as_tensor(seqs)].cpu().numpy()              # [S,G,n]
     expect = ref["out"].copy()
     near = 0
     for si, b in enumerate(seqs):
+        t = lens[si] - 1
         for g in range(G):
             if np.array_equal(gidx[si, g], ref["idx"][si, g]):
                 continue
@@ -78,8 +81,8 @@ def check_decode(inp, ref, out, idx, params=NSAParams(), label="", near_tie=NEAR
             near += 1
             hs = slice(g * hpg, (g + 1) * hpg)
             q = O.to_f64(inp["q"][b, hs])
-            K = O.to_f64(inp["kcache"][b, g])
-            V = O.to_f64(inp["vcache"][b, g])
+            K = O.to_f64(inp["kcache"][b, g, :t + 1])
+            V = O.to_f64(inp["vcache"][b, g, :t + 1])
             o_slc = O.sel_attention(q, t, K, V, gidx[si, g], params.lsel, scale)
             gt = O.to_f64(inp["gates"][b, hs])
             expect[si, hs] = (gt[:, 0:1] * ref["o_cmp"][si, hs] + gt[:, 1:2] * o_slc
@@ -131,6 +134,44 @@ def test_decode_end_to_end_compression():
     bf16_compare(vc, *compress_exact(inp, B, G, False, "vcache", "pe_v", "w_v"))
     ref = O.nsa_decode_reference(inp, kc=cache_f64(kc), vc=cache_f64(vc))
     check_decode(inp, ref, out, idx, label="decode end-to-end")
+
+
+RAGGED = DecodeWorkload("nsa_decode_ragged", 7, 5000, 32, 2, 192, 128, 8)
+
+
+def test_decode_ragged_batch_lengths():
+    """One batch whose sequences have different lengths (seq_lens): each
+    query sits at its own len-1 and reads only its own tokens."""
+    inp = make_decode(RAGGED)
+    lens = [1, 31, 64, 1087, 2048, 5000, 4999]
+    ref = O.nsa_decode_reference(inp, seq_lens=lens)
+    out, idx, _, _ = run_decode(inp, ref["kc"], ref["vc"], seq_lens=lens)
+    check_decode(inp, ref, out, idx, label="decode ragged")
+
+
+def test_decode_ragged_end_to_end_compression():
+    # the GPU compresses the caches at capacity; each sequence uses its prefix
+    inp = make_decode(RAGGED)
+    lens = [5000, 97, 4096, 4097, 600, 33, 1]
+    out, idx, kc, vc = run_decode(inp, seq_lens=lens)
+    ref = O.nsa_decode_reference(inp, kc=cache_f64(kc), vc=cache_f64(vc), seq_lens=lens)
+    check_decode(inp, ref, out, idx, label="decode ragged end-to-end")
+
+
+def test_decode_invalid_lengths_are_reported_and_skipped():
+    """Lengths outside [1, T] are read on the device: the step records
+    NSA_ERR_INVALID_ARG, reads nothing of those sequences (output zero, no
+    kept blocks) and computes the valid ones as usual."""
+    inp = make_decode(RAGGED)
+    T = RAGGED.T
+    lens = [0, 2048, -3, T + 1, 777, T, 1 << 30]
+    out, idx, kc, vc = run_decode(inp, seq_lens=lens, expect_status=1)   # 1 = NSA_ERR_INVALID_ARG
+    bad = torch.as_tensor([0, 2, 3, 6])
+    assert torch.all(out[bad].float() == 0) and torch.all(idx[bad] == -1)
+    good = [1, 4, 5]
+    ref = O.nsa_decode_reference(inp, seqs=good, kc=cache_f64(kc), vc=cache_f64(vc),
+                                 seq_lens=[L if 1 <= L <= T else T for L in lens])
+    check_decode(inp, ref, out, idx, label="decode with invalid lengths")
 
 
 def test_decode_twice_is_deterministic():

@@ -104,7 +104,7 @@ def check_all_rows_valid(idx, T, n=16, lsel=64):
     last = np.take_along_axis(gi, np.maximum(cnt - 1, 0)[..., None], -1)[..., 0]
     assert (last == jt).all(), "own block j_t kept"
     prev = np.take_along_axis(gi, np.maximum(cnt - 2, 0)[..., None], -1)[..., 0]
-    assert np.where(jt[..., 0] >= 1, prev == jt[..., 0] - 1, True).all(), "block j_t-1 kept"
+    assert np.where(jt >= 1, prev == jt - 1, True).all(), "block j_t-1 kept"
 
 
 def _gate_only(inp, which):

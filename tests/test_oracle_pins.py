@@ -338,6 +338,32 @@ def test_decode_equals_last_prefill_row():
 
 
 # ----------------------------------------------------------------- DSA
+def test_decode_with_lengths_equals_cropped_caches():
+    """A sequence of length L inside a larger cache is decoded exactly as the
+    same L tokens alone: nothing past L is read."""
+    from workloads import decode_config, make_decode
+    wl = decode_config()
+    inp = make_decode(wl, B=3, T=700)
+    lens = [700, 64, 333]
+    res = O.nsa_decode_reference(inp, seq_lens=lens)
+    for b, L in enumerate(lens):
+        one = {k: v for k, v in inp.items()}
+        for key in ("kcache", "vcache"):
+            big = inp[key][b:b + 1, :, :L].clone()
+            one[key] = big
+        for key in ("q", "gates"):
+            one[key] = inp[key][b:b + 1]
+        ref = O.nsa_decode_reference(one)
+        np.testing.assert_array_equal(res["out"][b], ref["out"][0])
+        np.testing.assert_array_equal(res["idx"][b], ref["idx"][0])
+    # poisoning the rows past each length changes nothing
+    for key in ("kcache", "vcache"):
+        for b, L in enumerate(lens):
+            inp[key][b, :, L:] = 1e4
+    res2 = O.nsa_decode_reference(inp, seq_lens=lens)
+    np.testing.assert_array_equal(res["out"], res2["out"])
+
+
 def test_dsa_indexer_brute_force():
     rng = np.random.default_rng(7)
     HI, dI, T = 3, 5, 40
