@@ -60,9 +60,15 @@ struct CmpWinArgs {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kRingK];
+  // a tile's chunks complete on ONE barrier (one arrival with its bytes per
+  // chunk), so the MMA issuers wait once per tile: key tile u on
+  // kt_full[u % kRingK], value tile u on vt_full[u % kRingV].  One barrier per
+  // ring slot: tile u's first slot was last used by tile u - ceil(R / chunks
+  // per tile) >= u - R, which the issuer waited for before freeing the slot,
+  // so a barrier is re-armed only after its previous phase was consumed.
+  uint64_t kt_full[kRingK];
   uint64_t k_empty[kRingK];
-  uint64_t v_full[kRingV];
+  uint64_t vt_full[kRingV];
   uint64_t v_empty[kRingV];
   uint64_t s_full[2];
   uint64_t s_free[2];
@@ -171,12 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kRingK; ++s) {
-      mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->kt_full[s], kcs);
     }
     for (int s = 0; s < kRingV; ++s) {
-      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->vt_full[s], vcs);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -222,31 +228,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mapV);
       }
       const int nring = keys ? kRingK : kRingV;
+      const int nc = keys ? kcs : vcs;         // chunks per tile
       uint8_t* rbase = keys ? kring : vring;
-      uint64_t* full = keys ? bars->k_full : bars->v_full;
+      uint64_t* tile_full = keys ? bars->kt_full : bars->vt_full;
       uint64_t* empty = keys ? bars->k_empty : bars->v_empty;
-      int v = 0;
+      int v = 0, ut = 0;                       // chunks and tiles pushed
       bool ok = true;
-      auto push = [&](const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+      // chunk c of tile ut, completing on the tile's barrier
+      auto push = [&](int c, const CUtensorMap* map, int c0, int c1, int c2, int c3) {
         if (!ok) return;
+        uint64_t* tf = &tile_full[ut % nring];
         const int slot = v % nring;
         const uint32_t round = (uint32_t)(v / nring);
         if (!mbar_wait(&empty[slot], (round & 1) ^ 1, abort_flag, a.st, keys ? 201 : 202)) {
+          // complete the tile's arrivals so its phase ends once the chunks
+          // already issued have landed (the drain below waits for it)
+          for (int x = c; x < nc; ++x) mbar_arrive(tf);
+          ++ut;
           ok = false;
           return;
         }
-        mbar_arrive_expect_tx(&full[slot], kSlot);
-        tma_load_4d(rbase + slot * kSlot, map, &full[slot], c0, c1, c2, c3);
+        mbar_arrive_expect_tx(tf, kSlot);
+        tma_load_4d(rbase + slot * kSlot, map, tf, c0, c1, c2, c3);
         ++v;
+        if (c == nc - 1) ++ut;
       };
       if (keys) {
         // window keys once (online softmax), then compressed keys twice
         // (statistics pass, exact pass)
         for (int j = 0; j < ntw; ++j)
-          for (int c = 0; c < kcs; ++c) push(&mapK, c * 64, g, s_lo + j * kTile, b);
+          for (int c = 0; c < kcs; ++c) push(c, &mapK, c * 64, g, s_lo + j * kTile, b);
         for (int pass = 0; pass < 2; ++pass)
           for (int j = 0; j < ntc; ++j)
-            for (int c = 0; c < kcs; ++c) push(&mapKc, c * 64, j * kTile, g, b);
+            for (int c = 0; c < kcs; ++c) push(c, &mapKc, c * 64, j * kTile, g, b);
       } else {
         // with two value chunks a tile's PV is one N = 128 MMA per key step,
         // whose B operand takes dv 0..63 from the lower of the tile's two
@@ -256,15 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool swap = vcs == 2 && v % kRingV == kRingV - 1;   // tile's first slot
           for (int c = 0; c < vcs; ++c) {
             const int cc = swap ? 1 - c : c;
-            if (j < ntw) push(&mapV, cc * 64, g, s_lo + j * kTile, b);
-            else push(&mapVc, cc * 64, (j - ntw) * kTile, g, b);
+            if (j < ntw) push(c, &mapV, cc * 64, g, s_lo + j * kTile, b);
+            else push(c, &mapVc, cc * 64, (j - ntw) * kTile, g, b);
           }
         }
       }
       if (!ok || *abort_flag) {
         if (keys) mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
-        for (int x = (v > nring ? v - nring : 0); x < v; ++x)
-          mbar_wait_plain(&full[x % nring], (uint32_t)((x / nring) & 1), kWaitLimitNs);
+        // only the last nring started tiles can still have copies in flight
+        for (int x = (ut > nring ? ut - nring : 0); x < ut; ++x)
+          mbar_wait_plain(&tile_full[x % nring], (uint32_t)((x / nring) & 1), kWaitLimitNs);
       }
     }
   } else if (warp == 9 || warp == 11) {
@@ -287,14 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (!mbar_wait(&bars->kt_full[u % kRingK], (uint32_t)((u / kRingK) & 1), abort_flag, a.st, 212)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           for (int c = 0; c < kcs; ++c) {
             const int slot = kv % kRingK;
-            if (!mbar_wait(&bars->k_full[slot], (uint32_t)((kv / kRingK) & 1), abort_flag, a.st, 212)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t ad = sdesc_sw128(qs_a + c * kSlot + k * 32, 16, 1024);
@@ -317,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int vv = 0;
         const uint32_t idesc_pv2 = idesc_bf16_f32(128, 128, false, true);
         for (int pv = 0; pv < npv && ok; ++pv) {
-          if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214)) {
+          if (!mbar_wait(&bars->p_full, (uint32_t)(pv & 1), abort_flag, a.st, 214) ||
+              !mbar_wait(&bars->vt_full[pv % kRingV], (uint32_t)((pv / kRingV) & 1), abort_flag, a.st, 215)) {
             ok = false;
             break;
           }
@@ -326,12 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // both dv halves in one N = 128 MMA per key step: dv 0..63 sit in
             // the lower of the tile's two slots, dv 64..127 LBO bytes above
             const int s0 = vv % kRingV, s1 = (vv + 1) % kRingV;
-            if (!mbar_wait(&bars->v_full[s0], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 215) ||
-                !mbar_wait(&bars->v_full[s1], (uint32_t)(((vv + 1) / kRingV) & 1), abort_flag, a.st, 215)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
             const int lo = s0 < s1 ? s0 : s1;
             const uint32_t lbo = (uint32_t)((s0 < s1 ? s1 - s0 : s0 - s1) * kSlot);
 #pragma unroll
@@ -347,11 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int c = 0; c < vcs; ++c) {
             const int slot = vv % kRingV;
-            if (!mbar_wait(&bars->v_full[slot], (uint32_t)((vv / kRingV) & 1), abort_flag, a.st, 215)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               // A = P from tensor memory (keys 16k .. 16k+15 = columns 8k .. 8k+7)
