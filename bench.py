@@ -501,6 +501,63 @@ def run_decode_leg(args, ws):
     }
 
 
+# ---------------------------------------------------------------- multi-token decode leg
+def run_decode_multi_leg(args, ws, m=4):
+    """m new tokens per sequence (positions T-m .. T-1) for the 16 sequences
+    with 65,536-token caches, in one nsa_decode_multi call: each token keeps
+    its own selection; the chunk shares the compressed and window tiles."""
+    import sparse_attention_long_10_b300 as nsa
+    from workloads import make_decode_multi
+    wl = decode_config()
+    B, T, H, G, dk, dv = wl.B, wl.T, wl.H, wl.G, wl.dk, wl.dv
+    inp = make_decode_multi(wl, m)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    cfg = nsa.make_cfg(B, T, H, G, dk, dv, phi=dev)
+    Nc = nsa.nsa_num_compressed(cfg)
+    kc = torch.empty(B, G, Nc, dk, dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty(B, G, Nc, dv, dtype=torch.bfloat16, device="cuda")
+    cws = nsa.workspace(nsa.nsa_compress_workspace_size(cfg))
+    nsa.nsa_compress_kv(cfg, nsa.NSA_LAYOUT_BGTD, dev["kcache"], dev["vcache"], kc, vc, cws)
+    out = torch.empty(B, m, H, dv, dtype=torch.bfloat16, device="cuda")
+    wsp = nsa.workspace(nsa.nsa_decode_multi_workspace_size(cfg, m))
+
+    def step():
+        nsa.nsa_decode_multi(cfg, m, dev["q"], dev["kcache"], dev["vcache"], kc, vc, dev["gates"], out, None, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("decode multi: device status set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(statistics.mean(time_graph_steps(graph, args.steps, flush)), ws)
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("decode multi: device status set in the timed region")
+    nsa.nsa_profile_enable(True)
+    for _ in range(args.steps):
+        flush.add_(1)
+        step()
+    torch.cuda.synchronize()
+    prof = nsa.nsa_profile_read()
+    nsa.nsa_profile_enable(False)
+    return {
+        "metric": f"NSA multi-token decode step latency (16 seqs x 65,536-token caches, {m} new tokens each)",
+        "value": ms * 1e3, "unit": "us", "higher_is_better": False, "workload": f"{wl.name}_m{m}",
+        "steps": args.steps, "tokens_per_step": B * m, "tokens_per_s": B * m / (ms * 1e-3),
+        "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
+                    for k, (c, t) in prof.items()},
+        "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
+        "note": "CUDA graph replay, L2 flushed before each step",
+    }
+
+
 # ---------------------------------------------------------------- DSA decode leg
 def run_dsa_leg(args, ws, latent=False):
     """One DSA-style decode step: batch 8, 131,072-token context, indexer of 4
@@ -642,6 +699,8 @@ def main():
     if not args.no_decode:
         res["decode"] = run_decode_leg(args, ws)
         res["gpu_launches"] += res["decode"]["gpu_launches_per_step"] * args.steps
+        res["decode_multi"] = run_decode_multi_leg(args, ws)
+        res["gpu_launches"] += res["decode_multi"]["gpu_launches_per_step"] * args.steps
         res["dsa"] = run_dsa_leg(args, ws)
         res["gpu_launches"] += res["dsa"]["gpu_launches_per_step"] * args.steps
         res["dsa_latent"] = run_dsa_leg(args, ws, latent=True)

@@ -212,6 +212,28 @@ size_t nsa_full_attn_workspace_size(const nsa_cfg* cfg);
 int nsa_full_attn_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, void* out,
                       void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * nsa_decode_multi -- m new tokens per sequence at once (a chunk of tokens,
+ * or draft tokens checked together): rows t = T-m .. T-1 of the prefill
+ * definition [P2 II; P3], each query with its own compressed attention,
+ * block scores, top-n selection and window, read from the caches that
+ * already hold the m tokens.  The 128-row tiles of the compressed and window
+ * branches cover 128/(H/G) of the m queries at once, so the chunk shares
+ * every compressed and window K/V tile it reads.
+ *   q      : [B,m,H,dk]      gates : [B,m,H,3]     out : [B,m,H,dv]
+ *   kcache : [B,G,T,dk]      vcache : [B,G,T,dv]   (head-major, T = length)
+ *   kc, vc : [B,G,Nc,dk] / [B,G,Nc,dv] compressed caches (nsa_compress_kv,
+ *            NSA_LAYOUT_BGTD); read only
+ *   idx_out (nullable): [B,m,G,n] int32
+ *   ws     : nsa_decode_multi_workspace_size(cfg, m) bytes
+ * 1 <= m <= T; shapes as nsa_prefill_fwd (H/G <= 16, n <= 16, dv 64 or 128,
+ * T <= 65536).
+ */
+size_t nsa_decode_multi_workspace_size(const nsa_cfg* cfg, int m);
+int nsa_decode_multi(const nsa_cfg* cfg, int m, const void* q, const void* kcache, const void* vcache,
+                     const void* kc, const void* vc, const void* gates, void* out, int32_t* idx_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- DSA */
 typedef struct dsa_cfg {
   int B;       /* batch rows (one query token each, at position T-1)  */
@@ -259,8 +281,11 @@ int nsa_profile_enable(int on);
 int nsa_profile_read(int max_kernels, char* names, size_t name_cap, int* launches, float* total_ms);
 
 /* ---------------------------------------------------------------- status word */
-/* Synchronises ``stream``, returns the status word the kernels of the last
-   call on ``ws`` recorded (NSA_OK if none) and clears it. */
+/* Synchronises ``stream``, returns the status the kernels of the last call on
+   ``ws`` recorded (NSA_OK if none) and clears it: a device-side failure (such
+   as NSA_ERR_DEVICE_TIMEOUT, after which the call's outputs are not valid)
+   first, else a bad argument that only the device could see (such as a
+   sequence length out of range, whose sequence was skipped). */
 int nsa_device_status(void* ws, void* stream);
 
 #ifdef __cplusplus

@@ -391,13 +391,17 @@ def nsa_decode_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[i
 
 
 def nsa_decode_multi_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iterable[int]] = None,
-                               params: NSAParams = NSAParams()) -> Dict[str, np.ndarray]:
+                               params: NSAParams = NSAParams(),
+                               kc: Optional[np.ndarray] = None, vc: Optional[np.ndarray] = None
+                               ) -> Dict[str, np.ndarray]:
     """Decode of m query tokens per sequence at positions T-m .. T-1 (all in
     the caches): rows T-m .. T-1 of the same definition, each with its own
     selection (several draft tokens checked at once, or a short chunk).
 
     inp: ``workloads.make_decode_multi`` (caches [B,G,T,d], q [B,m,H,dk],
-    gates [B,m,H,3]).  Returns out [S,m,H,dv] and idx [S,m,G,n].
+    gates [B,m,H,3]).  kc/vc: optional compressed caches [B,G,Nc,d] (fp64);
+    computed here when absent.  Returns out [S,m,H,dv], o_cmp/o_slc/o_win,
+    idx [S,m,G,n] and S32 [S,m,G,nb].
     """
     kcache, vcache, q_t = inp["kcache"], inp["vcache"], inp["q"]
     B, G, T, dk = kcache.shape
@@ -408,7 +412,11 @@ def nsa_decode_multi_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iter
     seqs = list(range(B)) if seqs is None else list(seqs)
     pe_k, pe_v = to_f64(inp["pe_k"]), to_f64(inp["pe_v"])
     w_k, w_v = to_f64(inp["w_k"]), to_f64(inp["w_v"])
-    res = dict(out=np.zeros((len(seqs), m, H, dv)), idx=np.zeros((len(seqs), m, G, params.n), dtype=np.int32))
+    nb = -(-T // params.lsel)
+    res = dict(out=np.zeros((len(seqs), m, H, dv)), o_cmp=np.zeros((len(seqs), m, H, dv)),
+               o_slc=np.zeros((len(seqs), m, H, dv)), o_win=np.zeros((len(seqs), m, H, dv)),
+               idx=np.zeros((len(seqs), m, G, params.n), dtype=np.int32),
+               S32=np.zeros((len(seqs), m, G, nb), dtype=np.float32))
     t_rows = np.arange(T - m, T)
     for si, b in enumerate(seqs):
         qb = to_f64(q_t[b])
@@ -416,12 +424,14 @@ def nsa_decode_multi_reference(inp: Dict[str, torch.Tensor], seqs: Optional[Iter
         for g in range(G):
             K = to_f64(kcache[b, g])
             V = to_f64(vcache[b, g])
-            Kc = compress(K, pe_k, w_k, params.l, params.d)
-            Vc = compress(V, pe_v, w_v, params.l, params.d)
+            Kc = compress(K, pe_k, w_k, params.l, params.d) if kc is None else kc[b, g]
+            Vc = compress(V, pe_v, w_v, params.l, params.d) if vc is None else vc[b, g]
             hs = slice(g * hpg, (g + 1) * hpg)
             r = nsa_group_rows(qb[:, hs], t_rows, K, V, Kc, Vc, gb[:, hs], params, scale)
-            res["out"][si, :, hs] = r["out"]
+            for key in ("out", "o_cmp", "o_slc", "o_win"):
+                res[key][si, :, hs] = r[key]
             res["idx"][si, :, g] = r["idx"]
+            res["S32"][si, :, g] = r["S32"]
     res["seqs"] = np.array(seqs)
     return res
 

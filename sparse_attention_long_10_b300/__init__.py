@@ -22,7 +22,8 @@ __all__ = [
     "nsa_status_string", "nsa_version", "nsa_num_compressed",
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
-    "nsa_compress_kv_noalloc_status", "nsa_full_attn_workspace_size", "nsa_full_attn_fwd", "nsa_prefill_fwd", "nsa_decode_step",
+    "nsa_compress_kv_noalloc_status", "nsa_full_attn_workspace_size", "nsa_full_attn_fwd",
+    "nsa_decode_multi_workspace_size", "nsa_decode_multi", "nsa_prefill_fwd", "nsa_decode_step",
     "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
@@ -80,6 +81,9 @@ def _load() -> ctypes.CDLL:
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
         "nsa_full_attn_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_decode_multi_workspace_size": (_c_size, [P(NsaCfg), _c_int]),
+        "nsa_decode_multi": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                      _c_vp, _c_size, _c_vp]),
         "nsa_full_attn_fwd": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_compress_kv_noalloc": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
         "nsa_compress_kv_noalloc_status": (_c_int, [_c_vp]),
@@ -217,6 +221,17 @@ def nsa_full_attn_fwd(cfg: NsaCfg, q, k, v, out, ws, stream=None):
     """Exact causal full attention (the dense comparison)."""
     _check(_lib().nsa_full_attn_fwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(ws),
                                  ws.numel() if ws is not None else 0, _stream(stream)), "nsa_full_attn_fwd")
+
+
+def nsa_decode_multi_workspace_size(cfg: NsaCfg, m: int) -> int:
+    return _lib().nsa_decode_multi_workspace_size(ctypes.byref(cfg), m)
+
+
+def nsa_decode_multi(cfg: NsaCfg, m: int, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None):
+    """m new tokens per sequence (rows T-m .. T-1) from head-major caches."""
+    _check(_lib().nsa_decode_multi(ctypes.byref(cfg), m, _ptr(q), _ptr(kcache), _ptr(vcache), _ptr(kc), _ptr(vc),
+                                _ptr(gates), _ptr(out), _ptr(idx_out), _ptr(ws),
+                                ws.numel() if ws is not None else 0, _stream(stream)), "nsa_decode_multi")
 
 
 def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out, ws, stream=None,

@@ -84,11 +84,23 @@ struct PrefillWs {
   CompressWs cw;
   size_t part, idx, end;
 };
+
+// multi-token decode: status word, then the partial and kept blocks of R rows
+struct MultiWs {
+  size_t part, idx, end;
+};
+MultiWs multi_ws(const nsa_cfg& c, int R) {
+  MultiWs w;
+  w.part = kHeader;
+  w.idx = align_up(w.part + sizeof(float) * (size_t)c.B * R * c.H * c.dv, 256);
+  w.end = align_up(w.idx + sizeof(int32_t) * (size_t)c.B * R * c.G * c.n, 256);
+  return w;
+}
 PrefillWs prefill_ws(const nsa_cfg& c) {
   PrefillWs w;
   w.cw = compress_ws(c);
   w.part = w.cw.end;
-  w.idx = align_up(w.part + sizeof(uint16_t) * (size_t)c.B * c.T * c.H * c.dv, 256);
+  w.idx = align_up(w.part + sizeof(float) * (size_t)c.B * c.T * c.H * c.dv, 256);
   w.end = align_up(w.idx + sizeof(int32_t) * (size_t)c.B * c.T * c.G * c.n, 256);
   return w;
 }
@@ -259,6 +271,39 @@ int nsa_full_attn_fwd(const nsa_cfg* cfg, const void* q, const void* k, const vo
                         true);
 }
 
+size_t nsa_decode_multi_workspace_size(const nsa_cfg* cfg, int m) {
+  if (validate_cfg(cfg) != NSA_OK || prefill_supported(*cfg) != NSA_OK || m < 1 || m > cfg->T) return 0;
+  return multi_ws(*cfg, m).end;
+}
+
+int nsa_decode_multi(const nsa_cfg* cfg, int m, const void* q, const void* kcache, const void* vcache,
+                     const void* kc, const void* vc, const void* gates, void* out, int32_t* idx_out, void* ws,
+                     size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  const nsa_cfg& c = *cfg;
+  if (m < 1 || m > c.T) return NSA_ERR_INVALID_ARG;
+  if ((rc = prefill_supported(c)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, kcache, vcache, gates, out})) != NSA_OK) return rc;
+  if (num_compressed(c) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  const MultiWs w = multi_ws(c, m);
+  if ((rc = check_ws(ws, ws_bytes, w.end)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(wsb);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  QueryRows rows;
+  rows.R = m;
+  rows.qoff = c.T - m;
+  rows.head_major = true;
+  void* part = wsb + w.part;
+  int32_t* idx = idx_out != nullptr ? idx_out : reinterpret_cast<int32_t*>(wsb + w.idx);
+  if ((rc = launch_cmp_win(c, q, kcache, vcache, kc, vc, gates, part, idx, st, s, false, rows)) != NSA_OK) return rc;
+  return launch_sel(c, q, kcache, vcache, gates, idx, part, out, st, s, rows);
+}
+
 size_t nsa_decode_workspace_size(const nsa_cfg* cfg) {
   if (validate_cfg(cfg) != NSA_OK || decode_supported(*cfg) != NSA_OK) return 0;
   return decode_ws_bytes(*cfg);
@@ -318,7 +363,7 @@ int nsa_device_status(void* ws, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, sizeof(h), s) != cudaSuccess) return NSA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
-  return h.code;
+  return h.code != NSA_OK ? h.code : h.arg_code;
 }
 
 }  // extern "C"

@@ -19,9 +19,11 @@ namespace nsa {
 // Status word (first bytes of every workspace).
 // ---------------------------------------------------------------------------
 struct DeviceStatus {
-  int code;        // first error recorded (NSA_OK if none)
+  int code;        // first error recorded (NSA_OK if none); later CTAs skip their work
   int where;       // site id of the first error
-  int pad[62];
+  int arg_code;    // first bad argument found on the device (e.g. a sequence
+  int arg_where;   // length): recorded only, the other work goes on
+  int pad[60];
 };
 static_assert(sizeof(DeviceStatus) == 256, "status header is 256 bytes");
 
@@ -36,6 +38,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ void record_error(DeviceStatus* st, int code, int where) {
   if (st != nullptr && atomicCAS(&st->code, 0, code) == 0) st->where = where;
+}
+
+// A bad argument read on the device (the host cannot see it): recorded for the
+// caller, without making the other CTAs skip their work.
+__device__ __forceinline__ void record_arg_error(DeviceStatus* st, int code, int where) {
+  if (st != nullptr && atomicCAS(&st->arg_code, 0, code) == 0) st->arg_where = where;
 }
 
 // True when an earlier CTA (of any kernel on this workspace) recorded an error:

@@ -106,5 +106,5 @@ extern "C" int nsa_compress_kv_noalloc_status(void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
   if (cudaMemsetAsync(scratch, 0, sizeof(h), s) != cudaSuccess) return NSA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return NSA_ERR_CUDA;
-  return h.code;
+  return h.code != NSA_OK ? h.code : h.arg_code;
 }

@@ -92,7 +92,7 @@ struct SeqGeom {
 __device__ __forceinline__ SeqGeom seq_geom(const DecArgs& a, int b, DeviceStatus* st) {
   int len = a.lens != nullptr ? __ldg(a.lens + b) : a.T;
   if (len < 1 || len > a.T) {
-    record_error(st, NSA_ERR_INVALID_ARG, 400);
+    record_arg_error(st, NSA_ERR_INVALID_ARG, 400);
     len = 0;
   }
   SeqGeom s;

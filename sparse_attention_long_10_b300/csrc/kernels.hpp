@@ -35,18 +35,29 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
                         void* out, float* bias_ws, DeviceStatus* st, cudaStream_t stream);
 
 // ---- prefill (prefill_cmp_win.cu, prefill_sel.cu)
+// Query rows of a prefill-kernel launch.  Default: one row per position
+// (R = T, qoff = 0, k/v token-major [B,T,G,d]).  A multi-token decode runs
+// R rows at positions qoff .. qoff+R-1 against head-major caches [B,G,T,d];
+// q, gates, out, the partial and idx are then addressed by row.
+struct QueryRows {
+  int R = 0;          // 0: T
+  int qoff = 0;
+  bool head_major = false;
+};
+
 size_t cmp_win_smem_bytes(const nsa_cfg& c, bool dense = false);
 size_t sel_smem_bytes(const nsa_cfg& c);
 // compressed attention + block scores + top-n + window; writes
-// part = g_cmp*O_cmp + g_win*O_win (bf16 [B,T,H,dv]) and idx [B,T,G,n].
+// part = g_cmp*O_cmp + g_win*O_win (fp32 [B,T,H,dv]) and idx [B,T,G,n].
 // dense: exact causal full attention of q over k/v written to ``part``
 // (no compressed branch, no selection, gates unused).
 int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
                    const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s,
-                   bool dense = false);
+                   bool dense = false, const QueryRows& rows = QueryRows());
 // selected attention; out = part + g_slc*O_slc
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
-               const void* part, void* out, DeviceStatus* st, cudaStream_t s);
+               const void* part, void* out, DeviceStatus* st, cudaStream_t s,
+               const QueryRows& rows = QueryRows());
 
 // ---- decode (decode.cu)
 int decode_supported(const nsa_cfg& c);

@@ -18,7 +18,8 @@
 // against [P2 III.3] -- written straight to the output.
 // The gates are folded into the probabilities (P' = g * p), so one TMEM
 // accumulator holds g_cmp*O_cmp + g_win*O_win; that partial sum is written in
-// bf16 and the selected-attention kernel adds g_slc*O_slc to it.
+// fp32 (an accumulation intermediate: the output is rounded to bf16 once) and
+// the selected-attention kernel adds g_slc*O_slc to it.
 //
 // Rows of the MMA are (query, head) pairs of ONE GQA group: 128/HPG queries x
 // HPG heads share every K/V tile (group-centric loading).  Warp roles:
@@ -50,9 +51,11 @@ constexpr int kTile = 128;     // keys (or compressed blocks) per S tile
 
 struct CmpWinArgs {
   int T, H, G, dk, dv, n, w, Nc, QT, nbs, dense;
+  int R, qoff;                     // query rows; row r sits at position qoff + r
+  int hm;                          // k/v head-major [B,G,T,d] (else [B,T,G,d])
   float sc2;                       // softmax scale * log2(e)
   const __nv_bfloat16* gates;      // [B,T,H,3]
-  __nv_bfloat16* part;             // [B,T,H,dv]
+  void* part;                      // [B,R,H,dv]: fp32 partial (NSA), bf16 output (dense)
   int32_t* idx;                    // [B,T,G,n]
   DeviceStatus* st;
   uint32_t off_kring, off_vring, off_scores, off_red, off_bar;
@@ -159,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int QT = a.QT;
   // the last query tiles see the most keys: launch them first
-  const int t0 = (gridDim.x - 1 - blockIdx.x) * QT;
+  const int t0 = (gridDim.x - 1 - blockIdx.x) * QT;   // first row of the tile
+  const int p0 = a.qoff + t0;                          // its position
   const int g = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = warp_id();
@@ -168,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int vcs = a.dv / 64;
 
   // per-CTA schedule (identical in every role)
-  const int t_last = min(t0 + QT - 1, a.T - 1);
+  const int t_last = a.qoff + min(t0 + QT - 1, a.R - 1);
   const int nmax = visible_cmp(t_last, a.Nc);
   const int ntc = (nmax + kTile - 1) / kTile;
-  const int s_lo = max(0, t0 - a.w + 1);
+  const int s_lo = max(0, p0 - a.w + 1);
   const int ntw = (t_last - s_lo) / kTile + 1;
 
   if (threadIdx.x == 0) {
@@ -257,7 +261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // window keys once (online softmax), then compressed keys twice
         // (statistics pass, exact pass)
         for (int j = 0; j < ntw; ++j)
-          for (int c = 0; c < kcs; ++c) push(c, &mapK, c * 64, g, s_lo + j * kTile, b);
+          for (int c = 0; c < kcs; ++c) {
+            if (a.hm) push(c, &mapK, c * 64, s_lo + j * kTile, g, b);
+            else push(c, &mapK, c * 64, g, s_lo + j * kTile, b);
+          }
         for (int pass = 0; pass < 2; ++pass)
           for (int j = 0; j < ntc; ++j)
             for (int c = 0; c < kcs; ++c) push(c, &mapKc, c * 64, j * kTile, g, b);
@@ -270,8 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool swap = vcs == 2 && v % kRingV == kRingV - 1;   // tile's first slot
           for (int c = 0; c < vcs; ++c) {
             const int cc = swap ? 1 - c : c;
-            if (j < ntw) push(c, &mapV, cc * 64, g, s_lo + j * kTile, b);
-            else push(c, &mapVc, cc * 64, (j - ntw) * kTile, g, b);
+            if (j >= ntw) push(c, &mapVc, cc * 64, (j - ntw) * kTile, g, b);
+            else if (a.hm) push(c, &mapV, cc * 64, s_lo + j * kTile, g, b);
+            else push(c, &mapV, cc * 64, g, s_lo + j * kTile, b);
           }
         }
       }
@@ -381,13 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = lw * 32 + lane;            // row = TMEM lane
     const int qi = r / HPG;
     const int h = r % HPG;
-    const int t = t0 + qi;
-    const bool row_ok = t < a.T;
+    const int row = t0 + qi;
+    const int t = p0 + qi;                   // position of the query
+    const bool row_ok = row < a.R;
     const int head = g * HPG + h;
     const int n_t = row_ok ? visible_cmp(t, a.Nc) : 0;
     float g_c = 0.f, g_w = a.dense ? 1.f : 0.f;
     if (row_ok && !a.dense) {
-      const __nv_bfloat16* gp = a.gates + (((size_t)b * a.T + t) * a.H + head) * 3;
+      const __nv_bfloat16* gp = a.gates + (((size_t)b * a.R + row) * a.H + head) * 3;
       g_c = __bfloat162float(gp[0]);
       g_w = __bfloat162float(gp[2]);
     }
@@ -621,10 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sync8();
     if (ok && !a.dense) {
       for (int qq = warp; qq < QT; qq += 8) {
-        const int tq = t0 + qq;
-        if (tq >= a.T) continue;
+        const int tq = p0 + qq;
+        if (t0 + qq >= a.R) continue;
         const int jt = tq / 64;
-        int32_t* out = a.idx + (((size_t)b * a.T + tq) * a.G + g) * a.n;
+        int32_t* out = a.idx + (((size_t)b * a.R + t0 + qq) * a.G + g) * a.n;
         if (jt + 1 <= a.n) {
           if (lane < a.n) out[lane] = lane <= jt ? lane : -1;
           continue;
@@ -689,21 +698,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < a.n) out[rank] = mine;
       }
     }
-    // ---------------- epilogue: O -> bf16 partial output (each warpgroup half the columns)
+    // ---------------- epilogue: O -> fp32 partial (NSA) or bf16 output
+    // (dense), each warpgroup half the columns
     if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 224)) {
       tc_fence_after();
-      __nv_bfloat16* dst = a.part + (((size_t)b * a.T + t) * a.H + head) * a.dv;
+      const size_t off = (((size_t)b * a.R + row) * a.H + head) * a.dv;
       for (int cc = wg * half; cc < (wg + 1) * half; cc += 16) {
         uint32_t rr[16];
         tmem_ld16(tmem_o + lane_base + cc, rr);
         tmem_ld_wait(rr);
-        if (row_ok) {
+        if (row_ok && a.dense) {
           uint32_t pk[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(__uint_as_float(rr[2 * k]), __uint_as_float(rr[2 * k + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.part) + off + cc);
           d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        } else if (row_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(a.part) + off + cc);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) d4[k] = make_uint4(rr[4 * k], rr[4 * k + 1], rr[4 * k + 2], rr[4 * k + 3]);
         }
       }
     }
@@ -740,7 +754,7 @@ int scores_stride(int T, int Nc) {
 template <int HPG>
 int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
   if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&cmp_win_kernel<HPG>), smem_max())) return rc;
-  dim3 grid((a0.T + a0.QT - 1) / a0.QT, a0.G, B);
+  dim3 grid((a0.R + a0.QT - 1) / a0.QT, a0.G, B);
   prof::begin(a0.dense ? "full_attn" : "cmp_win", s);
   cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
   prof::end(s);
@@ -757,7 +771,9 @@ size_t cmp_win_smem_bytes(const nsa_cfg& c, bool dense) {
 }
 
 int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
-                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s, bool dense) {
+                   const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s, bool dense,
+                   const QueryRows& rows) {
+  const int R = rows.R > 0 ? rows.R : c.T;
   const int hpg = c.H / c.G;
   const int QT = 128 / hpg;
   // dense: no compressed branch, a window covering the whole prefix
@@ -767,9 +783,9 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
   if (L.total > smem_max()) return NSA_ERR_UNSUPPORTED;
   const uint64_t e = 2;
   CUtensorMap maps[5];
-  {  // q [B,T,H,dk]: box (64, hpg heads, QT queries)
-    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dk * e, (uint64_t)c.H * c.dk * e, (uint64_t)c.T * c.H * c.dk * e};
+  {  // q [B,R,H,dk]: box (64, hpg heads, QT query rows)
+    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)R, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dk * e, (uint64_t)c.H * c.dk * e, (uint64_t)R * c.H * c.dk * e};
     const uint32_t box[4] = {64, (uint32_t)hpg, (uint32_t)QT, 1};
     if (!make_tmap_bf16(&maps[0], q, 4, dims, str, box)) return NSA_ERR_CUDA;
   }
@@ -786,18 +802,8 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
     const uint32_t box[4] = {64, 128, 1, 1};
     if (!make_tmap_bf16(&maps[2], Nc > 0 ? vc : v, 4, dims, str, box)) return NSA_ERR_CUDA;
   }
-  {  // k [B,T,G,dk]: box (64, 1 group, 128 tokens)
-    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dk * e, (uint64_t)c.G * c.dk * e, (uint64_t)c.T * c.G * c.dk * e};
-    const uint32_t box[4] = {64, 1, 128, 1};
-    if (!make_tmap_bf16(&maps[3], k, 4, dims, str, box)) return NSA_ERR_CUDA;
-  }
-  {  // v [B,T,G,dv]
-    const uint64_t dims[4] = {(uint64_t)c.dv, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dv * e, (uint64_t)c.G * c.dv * e, (uint64_t)c.T * c.G * c.dv * e};
-    const uint32_t box[4] = {64, 1, 128, 1};
-    if (!make_tmap_bf16(&maps[4], v, 4, dims, str, box)) return NSA_ERR_CUDA;
-  }
+  if (!make_kv_map(&maps[3], k, c.B, c.T, c.G, c.dk, 128, rows.head_major)) return NSA_ERR_CUDA;
+  if (!make_kv_map(&maps[4], v, c.B, c.T, c.G, c.dv, 128, rows.head_major)) return NSA_ERR_CUDA;
   CmpWinArgs a;
   a.T = c.T;
   a.H = c.H;
@@ -810,10 +816,13 @@ int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v
   a.QT = QT;
   a.nbs = nbs;
   a.dense = dense ? 1 : 0;
+  a.R = R;
+  a.qoff = rows.qoff;
+  a.hm = rows.head_major ? 1 : 0;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
   a.gates = static_cast<const __nv_bfloat16*>(gates);
-  a.part = static_cast<__nv_bfloat16*>(part);
+  a.part = part;
   a.idx = idx;
   a.st = st;
   a.off_kring = L.off_kring;

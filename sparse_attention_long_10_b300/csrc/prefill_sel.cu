@@ -12,8 +12,8 @@
 // All n*l' scores of the item sit in TMEM at once, so the softmax over the
 // kept keys is exact: one pass over TMEM finds each head's max, a second forms
 // p = exp(s - max) (unnormalised, bf16) and the sums.  The epilogue applies
-// g_slc / sum and adds the cmp+win partial sum from prefill_cmp_win.cu:
-//     out = part + g_slc * O_slc          (bf16)
+// g_slc / sum and adds the cmp+win partial sum (fp32) from prefill_cmp_win.cu:
+//     out = bf16(part + g_slc * O_slc)
 //
 // Warp roles (12 warps):
 //   warps 0-3, 4-7  two softmax + epilogue warpgroups, taking alternate items
@@ -44,10 +44,12 @@ constexpr int kItemsPerCta = 64;
 
 struct SelArgs {
   int T, H, G, dk, dv, n, hpg, QPC;
+  int R, qoff;                     // query rows; row r sits at position qoff + r
+  int hm;                          // k/v head-major [B,G,T,d] (else [B,T,G,d])
   float sc2;
   const int32_t* idx;              // [B,T,G,n]
   const __nv_bfloat16* gates;      // [B,T,H,3]
-  const __nv_bfloat16* part;       // [B,T,H,dv]
+  const float* part;               // [B,R,H,dv] fp32
   __nv_bfloat16* out;              // [B,T,H,dv]
   DeviceStatus* st;
   uint32_t off_kring, off_vring, off_pt, off_red, off_bar;
@@ -73,6 +75,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // token coordinate of block ``blk`` for a TMA load; an absent block reads
 // zeros from a negative coordinate
 __device__ __forceinline__ int block_token(int blk) { return blk >= 0 ? blk * 64 : -128; }
+
+// one 64-token box of K or V (see make_kv_map for the coordinate order)
+__device__ __forceinline__ void tma_kv(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int g, int tok,
+                                       int b, bool head_major) {
+  if (head_major) tma_load_4d(dst, map, bar, col, tok, g, b);
+  else tma_load_4d(dst, map, bar, col, g, tok, b);
+}
 
 // The n (<= 16) kept blocks of one item, -1 past n: issued as independent
 // loads (four 16-byte loads when n == 16) so they cost one memory round trip.
@@ -118,9 +127,16 @@ __device__ __forceinline__ int head_of_lane(int lane) {
   return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
+// kMulti: query rows at positions qoff + row against head-major caches (a
+// multi-token decode); otherwise one row per position of token-major inputs
+// (the prefill), with those values known at compile time.
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
     sel_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const SelArgs a) {
+  const int R = kMulti ? a.R : a.T;
+  const int qoff = kMulti ? a.qoff : 0;
+  constexpr bool hm = kMulti;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* qbuf = smem;                        // 2 items x kcs chunks x 2 KB
@@ -133,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int g = blockIdx.y;
   const int b = blockIdx.z;
-  const int t0 = blockIdx.x * a.QPC;
-  const int nitems = min(a.QPC, a.T - t0);
+  const int t0 = blockIdx.x * a.QPC;          // first row of the CTA
+  const int nitems = min(a.QPC, R - t0);
   const int warp = warp_id();
   const int lane = lane_id();
   const int kcs = a.dk / 64;
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto load_k = [&](int i) {
         int bks[16];
-        load_blocks(a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n, a.n, bks);
+        load_blocks(a.idx + (((size_t)b * R + t0 + i) * a.G + g) * a.n, a.n, bks);
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           if (p >= npairs || !ok) break;
@@ -223,15 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint8_t* dst = kring + slot * kSlotK;
             mbar_arrive_expect_tx(&bars->k_full[slot], kSlotK);
-            tma_load_4d(dst, &mapK, &bars->k_full[slot], c * 64, g, tk0, b);
-            tma_load_4d(dst + 8192, &mapK, &bars->k_full[slot], c * 64, g, tk1, b);
+            tma_kv(dst, &mapK, &bars->k_full[slot], c * 64, g, tk0, b, hm);
+            tma_kv(dst + 8192, &mapK, &bars->k_full[slot], c * 64, g, tk1, b, hm);
             ++kv;
           }
         }
       };
       auto load_v = [&](int i) {
         int bks[16];
-        load_blocks(a.idx + (((size_t)b * a.T + t0 + i) * a.G + g) * a.n, a.n, bks);
+        load_blocks(a.idx + (((size_t)b * R + t0 + i) * a.G + g) * a.n, a.n, bks);
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
           if (p >= npairs || !ok) break;
@@ -245,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* dst = vring + slot * kSlotV;
           mbar_arrive_expect_tx(&bars->v_full[slot], (uint32_t)(vcs * 16384));
           for (int c = 0; c < vcs; ++c) {
-            tma_load_4d(dst + c * 16384, &mapV, &bars->v_full[slot], c * 64, g, tk0, b);
-            tma_load_4d(dst + c * 16384 + 8192, &mapV, &bars->v_full[slot], c * 64, g, tk1, b);
+            tma_kv(dst + c * 16384, &mapV, &bars->v_full[slot], c * 64, g, tk0, b, hm);
+            tma_kv(dst + c * 16384 + 8192, &mapV, &bars->v_full[slot], c * 64, g, tk1, b, hm);
           }
           ++vv;
         }
@@ -375,14 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // coef[h] = g_slc[h] / sum[h]
     auto softmax = [&](int i) {
       if (!ok) return;
-      const int t = t0 + i;
+      const int row = t0 + i;
+      const int t = qoff + row;               // position of the query
       const int sb = i & 1;
       const uint32_t par = (uint32_t)((i >> 1) & 1);
       int bks[16];
-      load_blocks(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
+      load_blocks(a.idx + (((size_t)b * R + row) * a.G + g) * a.n, a.n, bks);
       float gsl[NP];
       {
-        const __nv_bfloat16* gp = a.gates + (((size_t)b * a.T + t) * a.H + g * a.hpg) * 3 + 1;
+        const __nv_bfloat16* gp = a.gates + (((size_t)b * R + row) * a.H + g * a.hpg) * 3 + 1;
 #pragma unroll
         for (int h = 0; h < NP; ++h) gsl[h] = h < a.hpg ? __bfloat162float(gp[3 * h]) : 0.f;
       }
@@ -466,15 +483,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto epilogue = [&](int i, const float (&cf)[NP]) {
       if (!ok) return;
-      const int t = t0 + i;
       const int ob = i & 3;
       const int d = r;
-      const size_t rowbase = ((size_t)b * a.T + t) * a.H + g * a.hpg;
+      const size_t rowbase = ((size_t)b * R + t0 + i) * a.H + g * a.hpg;
       // the cmp+win partial sum of this item, read before waiting for O
       float prt[NP];
 #pragma unroll
       for (int h = 0; h < NP; ++h)
-        prt[h] = (h < a.hpg && d < a.dv) ? __bfloat162float(a.part[(rowbase + h) * a.dv + d]) : 0.f;
+        prt[h] = (h < a.hpg && d < a.dv) ? a.part[(rowbase + h) * a.dv + d] : 0.f;
       if (!mbar_wait(&bars->o_full[ob], (uint32_t)((i >> 2) & 1), abort_flag, a.st, 324)) {
         ok = false;
         return;
@@ -537,31 +553,23 @@ Layout layout_for(int dk, int n) {
 size_t sel_smem_bytes(const nsa_cfg& c) { return layout_for(c.dk, c.n).total; }
 
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
-               const void* part, void* out, DeviceStatus* st, cudaStream_t s) {
+               const void* part, void* out, DeviceStatus* st, cudaStream_t s, const QueryRows& rows) {
+  const int R = rows.R > 0 ? rows.R : c.T;
   const int hpg = c.H / c.G;
   if (hpg > NP || c.n > 16 || (c.dv != 64 && c.dv != 128)) return NSA_ERR_UNSUPPORTED;
   const Layout L = layout_for(c.dk, c.n);
   if (L.total > smem_max()) return NSA_ERR_UNSUPPORTED;
   const uint64_t e = 2;
   CUtensorMap mq, mk, mv;
-  {  // q [B,T,H,dk]: box (64, hpg heads, 1 query)
-    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dk * e, (uint64_t)c.H * c.dk * e, (uint64_t)c.T * c.H * c.dk * e};
+  {  // q [B,R,H,dk]: box (64, hpg heads, 1 query row)
+    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.H, (uint64_t)R, (uint64_t)c.B};
+    const uint64_t str[3] = {c.dk * e, (uint64_t)c.H * c.dk * e, (uint64_t)R * c.H * c.dk * e};
     const uint32_t box[4] = {64, (uint32_t)hpg, 1, 1};
     if (!make_tmap_bf16(&mq, q, 4, dims, str, box)) return NSA_ERR_CUDA;
   }
-  {  // k [B,T,G,dk]: box (64, 1 group, 64 tokens = one selection block)
-    const uint64_t dims[4] = {(uint64_t)c.dk, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dk * e, (uint64_t)c.G * c.dk * e, (uint64_t)c.T * c.G * c.dk * e};
-    const uint32_t box[4] = {64, 1, 64, 1};
-    if (!make_tmap_bf16(&mk, k, 4, dims, str, box)) return NSA_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[4] = {(uint64_t)c.dv, (uint64_t)c.G, (uint64_t)c.T, (uint64_t)c.B};
-    const uint64_t str[3] = {c.dv * e, (uint64_t)c.G * c.dv * e, (uint64_t)c.T * c.G * c.dv * e};
-    const uint32_t box[4] = {64, 1, 64, 1};
-    if (!make_tmap_bf16(&mv, v, 4, dims, str, box)) return NSA_ERR_CUDA;
-  }
+  // k, v: boxes of 64 columns x 64 tokens (one selection block) of one head
+  if (!make_kv_map(&mk, k, c.B, c.T, c.G, c.dk, 64, rows.head_major)) return NSA_ERR_CUDA;
+  if (!make_kv_map(&mv, v, c.B, c.T, c.G, c.dv, 64, rows.head_major)) return NSA_ERR_CUDA;
   SelArgs a;
   a.T = c.T;
   a.H = c.H;
@@ -571,11 +579,14 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.n = c.n;
   a.hpg = hpg;
   a.QPC = kItemsPerCta;
+  a.R = R;
+  a.qoff = rows.qoff;
+  a.hm = rows.head_major ? 1 : 0;
   const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
   a.sc2 = scale * 1.4426950408889634f;
   a.idx = idx;
   a.gates = static_cast<const __nv_bfloat16*>(gates);
-  a.part = static_cast<const __nv_bfloat16*>(part);
+  a.part = static_cast<const float*>(part);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.st = st;
   a.off_kring = L.off_kring;
@@ -583,10 +594,17 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.off_pt = L.off_pt;
   a.off_red = L.off_red;
   a.off_bar = L.off_bar;
-  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel), smem_max())) return rc;
-  dim3 grid((c.T + a.QPC - 1) / a.QPC, c.G, c.B);
-  prof::begin("sel", s);
-  sel_kernel<<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+  dim3 grid((R + a.QPC - 1) / a.QPC, c.G, c.B);
+  if (rows.head_major) {
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<true>), smem_max())) return rc;
+    prof::begin("sel_multi", s);
+    sel_kernel<true><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+  } else {
+    if (rows.R > 0 && rows.R != c.T) return NSA_ERR_UNSUPPORTED;   // token-major rows are positions
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<false>), smem_max())) return rc;
+    prof::begin("sel", s);
+    sel_kernel<false><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+  }
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }

@@ -49,4 +49,23 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const u
   return r == CUDA_SUCCESS;
 }
 
+// K or V, token-major [B,T,G,d] or head-major [B,G,T,d], as a 4-D map with
+// 64-column x ``tokens``-token boxes of one head.  Coordinates are
+// (column, g, token, b) for token-major and (column, token, g, b) for
+// head-major (dimensions always in increasing stride order).
+inline bool make_kv_map(CUtensorMap* map, const void* base, int B, int T, int G, int d, int tokens,
+                        bool head_major) {
+  const uint64_t e = 2;
+  if (!head_major) {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)G, (uint64_t)T, (uint64_t)B};
+    const uint64_t str[3] = {d * e, (uint64_t)G * d * e, (uint64_t)T * G * d * e};
+    const uint32_t box[4] = {64, 1, (uint32_t)tokens, 1};
+    return make_tmap_bf16(map, base, 4, dims, str, box);
+  }
+  const uint64_t dims[4] = {(uint64_t)d, (uint64_t)T, (uint64_t)G, (uint64_t)B};
+  const uint64_t str[3] = {d * e, (uint64_t)T * d * e, (uint64_t)G * T * d * e};
+  const uint32_t box[4] = {64, (uint32_t)tokens, 1, 1};
+  return make_tmap_bf16(map, base, 4, dims, str, box);
+}
+
 }  // namespace nsa

@@ -135,8 +135,8 @@ def test_prefill_argument_checks(nsa):
     c = nsa.make_cfg(1, 4096, 64, 4, 192, 128)
     c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
     need = nsa.nsa_prefill_workspace_size(c)
-    # the workspace holds the bf16 cmp+win partial and the kept-block lists
-    assert need >= 4096 * 64 * 128 * 2 + 4096 * 4 * 16 * 4
+    # the workspace holds the fp32 cmp+win partial and the kept-block lists
+    assert need >= 4096 * 64 * 128 * 4 + 4096 * 4 * 16 * 4        # fp32 partial + kept blocks
     assert nsa.nsa_prefill_workspace_size(nsa.make_cfg(1, 8192, 64, 4, 192, 128)) > need
     assert _prefill_args(nsa, c, q=None) == 1
     assert _prefill_args(nsa, c, k=FAKE + 2) == 3
@@ -241,3 +241,27 @@ def test_full_attention_argument_checks(nsa):
     assert f(ctypes.byref(wide), FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 2
     if not torch.cuda.is_available():
         assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 7
+
+
+def test_decode_multi_argument_checks(nsa):
+    c = nsa.make_cfg(16, 65536, 64, 4, 192, 128)
+    need = nsa.nsa_decode_multi_workspace_size(c, 4)
+    assert need >= 256 + 16 * 4 * 64 * 128 * 4
+    assert nsa.nsa_decode_multi_workspace_size(c, 0) == 0
+    assert nsa.nsa_decode_multi_workspace_size(c, 65537) == 0
+    f = nsa.lib.nsa_decode_multi
+
+    def call(m=4, **kw):
+        a = dict(q=FAKE, kcache=FAKE, vcache=FAKE, kc=FAKE, vc=FAKE, gates=FAKE, out=FAKE, idx=None, ws=FAKE,
+                 ws_bytes=need)
+        a.update(kw)
+        return f(ctypes.byref(c), m, a["q"], a["kcache"], a["vcache"], a["kc"], a["vc"], a["gates"], a["out"],
+                 a["idx"], a["ws"], a["ws_bytes"], None)
+    assert call(m=0) == 1
+    assert call(m=65537) == 1
+    assert call(q=None) == 1
+    assert call(vc=None) == 1
+    assert call(out=FAKE + 2) == 3
+    assert call(ws_bytes=need - 1) == 4
+    if not torch.cuda.is_available():
+        assert call() == 7
