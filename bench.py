@@ -158,21 +158,20 @@ def whole_job_rate(units_per_rank: float, ms_max: float, ws: int) -> float:
 # (sha256 prefix of the listed files); otherwise the bench line says null.
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
-    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "e407d00cbc77e17d",
-                "bytes": (1857.36 + 1058.00) * 1e6, "how": "full-size capture (one pass)"},
-    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "aef9a954b7e55832",
-            "bytes": (3176.90 + 1074.45) * 1e6, "how": "full-size capture (one pass)"},
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "daee54b7ef57bd80",
+                "bytes": (1858.56 + 2115.71) * 1e6, "how": "full-size capture (one pass)"},
+    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "14a40cd57cf681c4",
+            "bytes": (4426.66 + 1073.95) * 1e6, "how": "full-size capture (one pass)"},
     # both kernels of one decode step
-    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "109c5bfaf71b561b",
-               "bytes": (189.27 + 9.80 + 52.01 + 0.02) * 1e6, "how": "full-size capture, both kernels"},
-    # the five kernels of one DSA step
-    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
-            "bytes": (134.39 + 4.03 + 4.25 + 4.21 + 35.90 + 8.44) * 1e6, "how": "full-size capture, five kernels"},
-    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "b28d22c4db17ecbb",
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "bb2bfdd8c4b6194f",
+               "bytes": (189.27 + 10.00 + 52.02 + 0.01) * 1e6, "how": "full-size capture, both kernels"},
+    # the five kernels of one DSA step (captured before per-row context lengths)
+    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "recapture-needed",
+            "bytes": (134.39 + 4.10 + 4.25 + 4.21 + 35.90 + 8.43) * 1e6, "how": "full-size capture, five kernels"},
+    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "recapture-needed",
                    "bytes": (134.38 + 4.10 + 4.25 + 4.21 + 19.12 + 8.44) * 1e6,
                    "how": "full-size capture, five kernels"},
 }
-
 
 def ncu_traffic(key: str):
     import hashlib

@@ -63,6 +63,14 @@ int nsa_version(void);
 /* Flags for nsa_cfg.flags */
 #define NSA_FLAG_KC_GIVEN 1u   /* nsa_prefill_fwd: kc/vc already hold the compressed
                                   cache; skip the compression step */
+#define NSA_FLAG_TEST_STALL 0x80000000u
+                               /* test hook of the failure path (no counterpart on the
+                                  pages): in the compression step the first CTA's producer
+                                  never signals one pipeline stage, so a bounded device
+                                  wait runs out after 0.5 s.  The call then records
+                                  NSA_ERR_DEVICE_TIMEOUT (nsa_device_status), its outputs
+                                  are not valid, and the next call on the same workspace
+                                  runs normally.  Never set in normal use. */
 
 typedef struct nsa_cfg {
   int B;        /* sequences                                            */
@@ -252,13 +260,19 @@ typedef struct dsa_cfg {
 size_t dsa_decode_workspace_size(const dsa_cfg* cfg);
 
 /*
- * dsa_decode_step -- indexed sparse decode [P4, "쉽게 이해하기"]:
- *   I[b,s]   = sum_h wI[b,h] * max(0, qI[b,h,:] . kI[b,s,:])    for s < T
- *   keep     = the min(topk,T) positions of largest fp32 I, ties to the lower s
+ * dsa_decode_step -- indexed sparse decode [P4, "쉽게 이해하기"]; row b's
+ * context holds T_b tokens and its query sits at T_b - 1:
+ *   I[b,s]   = sum_h wI[b,h] * max(0, qI[b,h,:] . kI[b,s,:])    for s < T_b
+ *   keep     = the min(topk,T_b) positions of largest fp32 I, ties to the lower s
  *   out[b,h] = softmax_{s in keep}(q[b,h,:] . k[b,s,:] * scale) @ v[b,keep,:]
  *   qI [B,HI,dI]   wI [B,HI]   kI [B,T,dI]   q [B,H,dk]   k [B,T,dk]
- *   v [B,T,dv]     out [B,H,dv]
- *   idx_out (nullable): [B, min(topk,T)] int32, ascending
+ *   v [B,T,dv]     out [B,H,dv]      (T = capacity)
+ *   seq_lens (nullable): device int32 [B], T_b in [1, T]; NULL means T for
+ *            every row.  Read on the device: a length outside [1, T] is
+ *            recorded as NSA_ERR_INVALID_ARG (nsa_device_status) and that row
+ *            is read as empty (out zero, idx_out row -1); the others are
+ *            unaffected.
+ *   idx_out (nullable): [B, min(topk,T)] int32, ascending, -1 past min(topk,T_b)
  * v may be NULL when dv <= dk: value row s is then the first dv columns of
  * key row s -- the latent KV of multi-head latent attention, on which the
  * page builds DSA (one cached latent per token, positional part in the last
@@ -266,8 +280,8 @@ size_t dsa_decode_workspace_size(const dsa_cfg* cfg);
  * dv > dk returns NSA_ERR_INVALID_ARG.
  */
 int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI,
-                    const void* q, const void* k, const void* v, void* out, int32_t* idx_out,
-                    void* ws, size_t ws_bytes, void* stream);
+                    const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                    void* out, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- profiling */
 /* No counterpart on the pages: measurement support.  When enabled, every

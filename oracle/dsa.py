@@ -97,11 +97,15 @@ def dsa_attention(q: np.ndarray, Ksel: np.ndarray, Vsel: np.ndarray, scale: floa
 
 def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
                          batches: Optional[Iterable[int]] = None,
-                         latent_dv: Optional[int] = None) -> Dict[str, np.ndarray]:
+                         latent_dv: Optional[int] = None,
+                         seq_lens: Optional[Iterable[int]] = None) -> Dict[str, np.ndarray]:
     """One DSA decode step for the batch rows ``batches`` (default all).
 
-    inp: bf16 tensors of ``workloads.make_dsa``.  Returns out [S,H,dv],
-    idx [S,min(k,T)] (ascending), I [S,T] fp64 and I32 [S,T] fp32 scores.
+    inp: bf16 tensors of ``workloads.make_dsa``.  Row b's context holds
+    T_b = seq_lens[b] tokens (default T): its query scores and keeps among
+    positions s < T_b only.  Returns out [S,H,dv], idx [S,min(k,T)]
+    (ascending, -1 past min(k,T_b)), I [S,T] fp64 and I32 [S,T] fp32 scores
+    (zero past T_b).
 
     With ``inp["v"] is None`` the values are latent: value row s is the first
     ``latent_dv`` columns of key row s.  Same page, the paragraph that puts
@@ -122,19 +126,24 @@ def dsa_decode_reference(inp: Dict[str, torch.Tensor], topk: int,
     scale = 1.0 / math.sqrt(dk)
     batches = list(range(B)) if batches is None else list(batches)
     kk = min(topk, T)
+    lens = [T] * B if seq_lens is None else [int(x) for x in seq_lens]
     res = dict(out=np.zeros((len(batches), H, dv)),
-               idx=np.zeros((len(batches), kk), dtype=np.int64),
+               idx=np.full((len(batches), kk), -1, dtype=np.int64),
                I=np.zeros((len(batches), T)), I32=np.zeros((len(batches), T), dtype=np.float32))
     for si, b in enumerate(batches):
-        I = dsa_indexer_scores(to_f64(qI[b]), to_f64(wI[b]), to_f64(kI[b]))
+        Tb = lens[b]
+        assert 1 <= Tb <= T, "a row's context holds between 1 and T tokens"
+        I = dsa_indexer_scores(to_f64(qI[b]), to_f64(wI[b]), to_f64(kI[b, :Tb]))
         I32 = I.astype(np.float32)
         sel = topk_positions(I32, topk)
         ti = torch.as_tensor(sel)
         Ksel = to_f64(k[b, ti])
         Vsel = Ksel[:, :dv] if v is None else to_f64(v[b, ti])
         res["out"][si] = dsa_attention(to_f64(q[b]), Ksel, Vsel, scale)
-        res["idx"][si], res["I"][si], res["I32"][si] = sel, I, I32
+        res["idx"][si, :sel.size] = sel
+        res["I"][si, :Tb], res["I32"][si, :Tb] = I, I32
     res["batches"] = np.array(batches)
+    res["lens"] = np.array([lens[b] for b in batches])
     return res
 
 

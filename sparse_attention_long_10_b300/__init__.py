@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "NsaError", "NsaCfg", "DsaCfg", "LIB_PATH", "lib", "make_cfg", "make_dsa_cfg",
-    "NSA_LAYOUT_BTGD", "NSA_LAYOUT_BGTD", "NSA_FLAG_KC_GIVEN",
+    "NSA_LAYOUT_BTGD", "NSA_LAYOUT_BGTD", "NSA_FLAG_KC_GIVEN", "NSA_FLAG_TEST_STALL",
     "nsa_status_string", "nsa_version", "nsa_num_compressed",
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
@@ -32,6 +32,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnsa.so")
 NSA_LAYOUT_BTGD = 0
 NSA_LAYOUT_BGTD = 1
 NSA_FLAG_KC_GIVEN = 1
+NSA_FLAG_TEST_STALL = 0x80000000
 
 _c_int, _c_float, _c_uint, _c_vp, _c_size = (ctypes.c_int, ctypes.c_float, ctypes.c_uint,
                                              ctypes.c_void_p, ctypes.c_size_t)
@@ -78,7 +79,7 @@ def _load() -> ctypes.CDLL:
         "nsa_decode_step": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                      _c_vp, _c_vp, _c_size, _c_vp]),
         "dsa_decode_step": (_c_int, [P(DsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
-                                     _c_vp, _c_vp, _c_size, _c_vp]),
+                                     _c_vp, _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
         "nsa_full_attn_workspace_size": (_c_size, [P(NsaCfg)]),
         "nsa_decode_multi_workspace_size": (_c_size, [P(NsaCfg), _c_int]),
@@ -243,9 +244,10 @@ def nsa_decode_step(cfg: NsaCfg, q, kcache, vcache, kc, vc, gates, out, idx_out,
            "nsa_decode_step")
 
 
-def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=None):
+def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=None, seq_lens=None):
+    """seq_lens: optional int32 device tensor [B] of context lengths (None: all cfg.T)."""
     _check(_lib().dsa_decode_step(ctypes.byref(cfg), _ptr(qI), _ptr(wI), _ptr(kI), _ptr(q), _ptr(k),
-                               _ptr(v), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               _ptr(v), _ptr(seq_lens), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "dsa_decode_step")
 

@@ -340,19 +340,20 @@ size_t dsa_decode_workspace_size(const dsa_cfg* cfg) {
 }
 
 int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI, const void* q,
-                    const void* k, const void* v, void* out, int32_t* idx_out, void* ws, size_t ws_bytes,
-                    void* stream) {
+                    const void* k, const void* v, const int32_t* seq_lens, void* out, int32_t* idx_out, void* ws,
+                    size_t ws_bytes, void* stream) {
   int rc = validate_dsa(cfg);
   if (rc != NSA_OK) return rc;
   if ((rc = check_ptrs({qI, wI, kI, q, k, out})) != NSA_OK) return rc;
   // v == NULL: values are the first dv columns of the key rows (latent KV)
   if (v == nullptr ? cfg->dv > cfg->dk : !aligned16(v)) return v == nullptr ? NSA_ERR_INVALID_ARG : NSA_ERR_MISALIGNED;
   if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  if (seq_lens != nullptr && (reinterpret_cast<uintptr_t>(seq_lens) & 3u) != 0) return NSA_ERR_MISALIGNED;
   if ((rc = check_ws(ws, ws_bytes, dsa_ws_bytes(*cfg))) != NSA_OK) return rc;
   if ((rc = check_device()) != NSA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, dsa_zero_bytes(*cfg), s) != cudaSuccess) return NSA_ERR_CUDA;
-  return launch_dsa(*cfg, qI, wI, kI, q, k, v, out, idx_out, static_cast<uint8_t*>(ws), s);
+  return launch_dsa(*cfg, qI, wI, kI, q, k, v, seq_lens, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
 int nsa_device_status(void* ws, void* stream) {

@@ -30,6 +30,7 @@ struct CompressArgs {
   int cpr;         // 64-column chunks per token row: dX / 64
   int layout;      // NSA_LAYOUT_*
   int G;
+  int stall;              // test hook: CTA (0,0,0) withholds stage 1 (NSA_FLAG_TEST_STALL)
   const float* bias;      // [N]
   __nv_bfloat16* out;     // [B, G, Nc, N]
   DeviceStatus* st;
@@ -137,6 +138,12 @@ __global__ void __launch_bounds__(128, 1)
       const int s = kb % kStages;
       const uint32_t ph = (kb / kStages) & 1;
       if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, a.st, 101)) break;
+      if (a.stall && kb == 1 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+        // test hook: this stage is never armed, so the MMA issuer's bounded
+        // wait for it runs out (and the drain below gives up on it)
+        ++issued;
+        continue;
+      }
       const int r = kb / a.cpr;            // token offset inside the block
       const int c = kb % a.cpr;            // 64-column chunk of the token row
       uint8_t* sa = smem + s * stage_bytes;
@@ -251,6 +258,7 @@ int launch_compress_one(const nsa_cfg& c, int layout, const void* X, int dX, con
   a.nkb = c.l * a.cpr;
   a.layout = layout;
   a.G = c.G;
+  a.stall = (c.flags & NSA_FLAG_TEST_STALL) != 0 ? 1 : 0;
   a.bias = bias_ws;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.st = st;

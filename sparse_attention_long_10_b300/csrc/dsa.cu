@@ -46,7 +46,9 @@ constexpr int kAttnTilesPerCta = 2;
 constexpr int kAttnStages = 2;
 
 struct DsaArgs {
-  int B, T, HI, dI, H, dk, dv, kk;  // kk = min(topk, T)
+  int B, T, HI, dI, H, dk, dv, kk;  // T: context capacity; kk = min(topk, T) (row stride of idx)
+  int topk;
+  const int32_t* lens;              // nullable [B]: context length of each row (query at len-1)
   int nparts;                       // threshold / compaction parts per row
   int idx_part;                     // positions per indexer CTA (a multiple of kIdxTile)
   int attn_ctas;                    // attention CTAs per row
@@ -88,6 +90,26 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// One row's context: its length, the positions it keeps, whether it keeps
+// them all.  A length outside [1, T] is recorded (NSA_ERR_INVALID_ARG, read
+// back by nsa_device_status) and the row is read as empty: no position is
+// kept, its output is zero, its idx_out row -1.
+struct RowGeom {
+  int T, kk, all;
+};
+__device__ __forceinline__ RowGeom row_geom(const DsaArgs& a, int b, DeviceStatus* st) {
+  int T = a.lens != nullptr ? __ldg(a.lens + b) : a.T;
+  if (T < 1 || T > a.T) {
+    record_arg_error(st, NSA_ERR_INVALID_ARG, 500);
+    T = 0;
+  }
+  RowGeom r;
+  r.T = T;
+  r.kk = min(a.topk, T);
+  r.all = r.kk == T;
+  return r;
+}
+
 __device__ __forceinline__ bool kept(uint32_t key, uint32_t pos, uint32_t Ks, uint32_t Is) {
   return key > Ks || (key == Ks && pos <= Is);
 }
@@ -110,9 +132,10 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   IdxBars* bars = reinterpret_cast<IdxBars*>(hs + kBins);
   volatile int* abort_flag = &bars->abort_flag;
   const int part = blockIdx.x, b = blockIdx.y;
+  const RowGeom rg = row_geom(a, b, part == 0 && threadIdx.x == 0 ? a.st : nullptr);
   const int s0 = part * a.idx_part;
-  const int npos = min(a.idx_part, a.T - s0);
-  const int ntiles = (npos + kIdxTile - 1) / kIdxTile;
+  const int npos = min(a.idx_part, rg.T - s0);
+  const int ntiles = npos > 0 ? (npos + kIdxTile - 1) / kIdxTile : 0;
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kIdxStages; ++s) {
@@ -185,7 +208,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
         for (int e = 0; e < 2; ++e) {
           const int pos = e ? pb : pa;
           const uint32_t key = e ? kb : ka;
-          const bool mine = tq == 0 && pos < a.T;
+          const bool mine = tq == 0 && pos < rg.T;
           if (mine) a.keys[(size_t)b * a.T + pos] = key;
           const uint32_t bin = mine ? (key >> 20) : 0xffffffffu;
           const unsigned same = __match_any_sync(0xffffffffu, bin);
@@ -206,7 +229,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   __shared__ int s_last;
   if (threadIdx.x == 0) s_last = (atomicAdd(&a.cnt[a.B + b], 1) == (int)gridDim.x - 1) ? 1 : 0;
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last || rg.all) return;   // a row that keeps every position needs no cut
   __threadfence();
   // suffix counts over the bins, 16 per thread for the first 256 threads' worth
   uint32_t* hg = hs;   // reuse: copy of the row's histogram
@@ -244,11 +267,11 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   if (t < 128) {
     for (int k = 0; k < warp; ++k) incl += wtot[k];
     const uint32_t excl = incl - sum;
-    if (excl < (uint32_t)a.kk && incl >= (uint32_t)a.kk) {
+    if (excl < (uint32_t)rg.kk && incl >= (uint32_t)rg.kk) {
       uint32_t cum = excl;
       for (int i = 0; i < 32; ++i) {
         const int bin = kBins - 32 * t - 1 - i;
-        if (cum + hg[bin] >= (uint32_t)a.kk) {
+        if (cum + hg[bin] >= (uint32_t)rg.kk) {
           a.cut1[(size_t)b * 2] = (uint32_t)bin;
           a.cut1[(size_t)b * 2 + 1] = cum;
           break;
@@ -373,10 +396,12 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
   __syncthreads();
   if (s_last) return;
   __syncthreads();
+  const RowGeom rg = row_geom(a, b, nullptr);
+  if (rg.all) return;   // every position kept (or an empty row): no threshold
   const uint32_t* hist = a.hist + (size_t)b * kBins;
   const uint32_t B1 = __ldcg(a.cut1 + (size_t)b * 2), above = __ldcg(a.cut1 + (size_t)b * 2 + 1);
   // this part's keys: count those above the boundary bin, collect the boundary bin
-  const int p0 = part * kSelPart, p1 = min(a.T, p0 + kSelPart);
+  const int p0 = part * kSelPart, p1 = min(rg.T, p0 + kSelPart);
   const uint32_t* keys = a.keys + (size_t)b * a.T;
   uint32_t gt = 0;
   constexpr int kChunks = kSelPart / kSelThreads;
@@ -433,7 +458,7 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
   uint32_t* h2 = cp + kCandCap;                        // [4096]
   uint32_t* pc = h2 + 4096;                            // [nparts]
   const uint32_t c1 = __ldcg(hist + B1);
-  const uint32_t need1 = (uint32_t)a.kk - above;
+  const uint32_t need1 = (uint32_t)rg.kk - above;
   uint32_t Ks, Is;
   const bool fast = c1 <= (uint32_t)kCandCap;
   if (fast) {
@@ -443,11 +468,11 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
     }
     __syncthreads();
     radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = ck[i]; pos = cp[i]; }, c1, B1, need1,
-                  (uint32_t)(a.T - 1), h2, scan, Ks, Is);
+                  (uint32_t)(rg.T - 1), h2, scan, Ks, Is);
   } else {
     // more boundary candidates than the buffer holds: resolve over the whole row
     radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = __ldcg(keys + i); pos = i; },
-                  (uint32_t)a.T, B1, need1, (uint32_t)(a.T - 1), h2, scan, Ks, Is);
+                  (uint32_t)rg.T, B1, need1, (uint32_t)(rg.T - 1), h2, scan, Ks, Is);
   }
   // kept positions per part: above the boundary bin + kept boundary candidates
   for (int p = t; p < a.nparts; p += kSelThreads) pc[p] = __ldcg(a.gtcnt + (size_t)b * a.nparts + p);
@@ -456,7 +481,7 @@ __global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a
     for (uint32_t i = t; i < c1; i += kSelThreads)
       if (kept(ck[i], cp[i], Ks, Is)) atomicAdd(&pc[cp[i] / kSelPart], 1u);
   } else {
-    for (uint32_t i = t; i < (uint32_t)a.T; i += kSelThreads) {
+    for (uint32_t i = t; i < (uint32_t)rg.T; i += kSelThreads) {
       const uint32_t key = __ldcg(keys + i);
       if ((key >> 20) == B1 && kept(key, i, Ks, Is)) atomicAdd(&pc[i / kSelPart], 1u);
     }
@@ -482,19 +507,26 @@ __global__ void __launch_bounds__(kSelThreads) dsa_compact_kernel(const DsaArgs 
   if (t == 0) s_abort = prior_error(a.st);
   __syncthreads();
   if (s_abort) return;
-  const int p0 = part * kSelPart, p1 = min(a.T, p0 + kSelPart);
-  uint32_t run = a.all ? (uint32_t)p0 : __ldcg(a.offs + (size_t)b * a.nparts + part);
-  const uint32_t Ks = a.all ? 0u : __ldcg(a.thr + (size_t)b * 2);
-  const uint32_t Is = a.all ? 0u : __ldcg(a.thr + (size_t)b * 2 + 1);
+  const RowGeom rg = row_geom(a, b, part == 0 && t == 0 ? a.st : nullptr);
+  const int p0 = part * kSelPart, p1 = min(rg.T, p0 + kSelPart);
+  uint32_t run = rg.all ? (uint32_t)p0 : __ldcg(a.offs + (size_t)b * a.nparts + part);
+  const uint32_t Ks = rg.all ? 0u : __ldcg(a.thr + (size_t)b * 2);
+  const uint32_t Is = rg.all ? 0u : __ldcg(a.thr + (size_t)b * 2 + 1);
   const uint32_t* keys = a.keys + (size_t)b * a.T;
   int32_t* dst = a.idx + (size_t)b * a.kk;
   int32_t* dst2 = a.idx_out != nullptr ? a.idx_out + (size_t)b * a.kk : nullptr;
+  // a row that keeps fewer than kk positions: its index row ends in -1
+  if (part == 0)
+    for (int e = rg.kk + t; e < a.kk; e += kSelThreads) {
+      dst[e] = -1;
+      if (dst2) dst2[e] = -1;
+    }
   constexpr int kChunks = kSelPart / kSelThreads;
   bool selv[kChunks];
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     const int pos = p0 + c * kSelThreads + t;
-    selv[c] = pos < p1 && (a.all || kept(__ldcg(keys + pos), (uint32_t)pos, Ks, Is));
+    selv[c] = pos < p1 && (rg.all || kept(__ldcg(keys + pos), (uint32_t)pos, Ks, Is));
   }
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
@@ -561,8 +593,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs
   const int x = blockIdx.x, b = blockIdx.y;
   const int warp = warp_id(), lane = lane_id();
   const int e0 = x * kAttnTile * kAttnTilesPerCta;
-  const int nent = min(kAttnTile * kAttnTilesPerCta, a.kk - e0);
-  const int ntiles = (nent + kAttnTile - 1) / kAttnTile;
+  const int nent = min(kAttnTile * kAttnTilesPerCta, row_geom(a, b, nullptr).kk - e0);
+  const int ntiles = nent > 0 ? (nent + kAttnTile - 1) / kAttnTile : 0;
   const int dk = a.dk;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
@@ -892,7 +924,7 @@ size_t dsa_ws_bytes(const dsa_cfg& c) { return dsa_ws(c).end; }
 size_t dsa_zero_bytes(const dsa_cfg& c) { return dsa_ws(c).zero_end; }
 
 int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
-               const void* v, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s) {
+               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s) {
   const DsaShape sh = dsa_shape(c);
   const DsaWs w = dsa_ws(c);
   DsaArgs a;
@@ -904,6 +936,8 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.dk = c.dk;
   a.dv = c.dv;
   a.kk = sh.kk;
+  a.topk = c.topk;
+  a.lens = lens;
   a.nparts = sh.nparts;
   {
     int dev = 0, sms = 148;
@@ -956,13 +990,8 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
     }
     if (rc != NSA_OK) return rc;
     // dynamic size actually needed (the kernel also has ~1 KB of static shared memory)
-    static size_t attr_bytes = 0;
-    if (thresh_smem(sh) > attr_bytes) {
-      if (cudaFuncSetAttribute(dsa_thresh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)thresh_smem(sh)) != cudaSuccess)
-        return NSA_ERR_CUDA;
-      attr_bytes = thresh_smem(sh);
-    }
+    if ((rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_thresh_kernel), thresh_smem(sh))) != NSA_OK)
+      return rc;
     prof::begin("dsa_thresh", s);
     dsa_thresh_kernel<<<dim3(sh.nparts, c.B), kSelThreads, thresh_smem(sh), s>>>(a);
     prof::end(s);

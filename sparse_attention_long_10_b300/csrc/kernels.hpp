@@ -74,7 +74,8 @@ int launch_decode(const nsa_cfg& c, const void* q, const void* kcache, const voi
 int dsa_supported(const dsa_cfg& c);
 size_t dsa_ws_bytes(const dsa_cfg& c);
 size_t dsa_zero_bytes(const dsa_cfg& c);
+// lens: nullable device array [B] of context lengths (each in [1, c.T])
 int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
-               const void* v, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
+               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
 
 }  // namespace nsa

@@ -146,7 +146,9 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     for (int i = 0; i < 16; ++i) x[c * 16 + i] = __uint_as_float(rs[c][i]);
 }
 
-template <int HPG>
+// kDense: exact causal full attention (window covering the prefix, gate 1,
+// no compressed branch, no selection), a separate instance of the kernel.
+template <int HPG, bool kDense>
 __global__ void __launch_bounds__(kThreads, 1)
     cmp_win_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapKc,
                    const __grid_constant__ CUtensorMap mapVc, const __grid_constant__ CUtensorMap mapK,
@@ -394,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = row < a.R;
     const int head = g * HPG + h;
     const int n_t = row_ok ? visible_cmp(t, a.Nc) : 0;
-    float g_c = 0.f, g_w = a.dense ? 1.f : 0.f;
-    if (row_ok && !a.dense) {
+    float g_c = 0.f, g_w = kDense ? 1.f : 0.f;
+    if (row_ok && !kDense) {
       const __nv_bfloat16* gp = a.gates + (((size_t)b * a.R + row) * a.H + head) * 3;
       g_c = __bfloat162float(gp[0]);
       g_w = __bfloat162float(gp[2]);
@@ -523,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // zero the block-score rows
-    if (!a.dense) {
+    if (!kDense) {
       for (int i = wg * 128 + r; i < QT * a.nbs; i += 256) scores[i] = 0.f;
       sync8();
     }
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---------------- top-n selection (one warp per query)
     sync8();
-    if (ok && !a.dense) {
+    if (ok && !kDense) {
       for (int qq = warp; qq < QT; qq += 8) {
         const int tq = p0 + qq;
         if (t0 + qq >= a.R) continue;
@@ -707,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[16];
         tmem_ld16(tmem_o + lane_base + cc, rr);
         tmem_ld_wait(rr);
-        if (row_ok && a.dense) {
+        if (row_ok && kDense) {
           uint32_t pk[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(__uint_as_float(rr[2 * k]), __uint_as_float(rr[2 * k + 1]));
@@ -751,14 +753,19 @@ int scores_stride(int T, int Nc) {
   return (s + 3) & ~3;
 }
 
-template <int HPG>
-int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
-  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&cmp_win_kernel<HPG>), smem_max())) return rc;
+template <int HPG, bool kDense>
+int launch_inst(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&cmp_win_kernel<HPG, kDense>), smem_max())) return rc;
   dim3 grid((a0.R + a0.QT - 1) / a0.QT, a0.G, B);
-  prof::begin(a0.dense ? "full_attn" : "cmp_win", s);
-  cmp_win_kernel<HPG><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
+  prof::begin(kDense ? "full_attn" : "cmp_win", s);
+  cmp_win_kernel<HPG, kDense><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a0);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+}
+
+template <int HPG>
+int launch_hpg(const CmpWinArgs& a0, int B, const CUtensorMap* maps, size_t smem, cudaStream_t s) {
+  return a0.dense ? launch_inst<HPG, true>(a0, B, maps, smem, s) : launch_inst<HPG, false>(a0, B, maps, smem, s);
 }
 
 }  // namespace

@@ -114,13 +114,16 @@ def test_dsa_latent_values_argument_checks(nsa):
     need = nsa.dsa_decode_workspace_size(c)
     assert need > 0
     bad = nsa.make_dsa_cfg(8, 131072, 4, 64, 16, 64, 128, 2048)   # dv > dk
-    assert f(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE,
+    assert f(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE,
              nsa.dsa_decode_workspace_size(bad), None) == 1
-    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, None, FAKE, need, None) == 3
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None, FAKE, None, FAKE, need, None) == 3
+    # per-row context lengths: an int32 array, 4-byte aligned
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, None, FAKE, need, None) == 3
     if not torch.cuda.is_available():
-        # valid arguments, latent or not: the no-device status
-        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 7
-        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None) == 7
+        # valid arguments, latent or not, with or without lengths: the no-device status
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, FAKE, need, None) == 7
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 7
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE, need, None) == 7
 
 
 def _prefill_args(nsa, c, **kw):

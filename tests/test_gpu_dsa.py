@@ -28,8 +28,9 @@ def _nsa():
     return nsa
 
 
-def run_dsa(inp, topk, latent_dv=None):
-    """inp["v"] None: latent values, the first latent_dv columns of k."""
+def run_dsa(inp, topk, latent_dv=None, seq_lens=None, expect_status=0):
+    """inp["v"] None: latent values, the first latent_dv columns of k.
+    seq_lens: per-row context lengths (device int32), None for all T."""
     nsa = _nsa()
     d = {k: t.cuda() for k, t in inp.items() if t is not None}
     B, T, dI = inp["kI"].shape
@@ -41,9 +42,10 @@ def run_dsa(inp, topk, latent_dv=None):
     out = torch.full((B, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
     idx = torch.full((B, kk), -7, dtype=torch.int32, device="cuda")
     ws = nsa.workspace(nsa.dsa_decode_workspace_size(cfg))
-    nsa.dsa_decode_step(cfg, d["qI"], d["wI"], d["kI"], d["q"], d["k"], d.get("v"), out, idx, ws)
+    lens = None if seq_lens is None else torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    nsa.dsa_decode_step(cfg, d["qI"], d["wI"], d["kI"], d["q"], d["k"], d.get("v"), out, idx, ws, seq_lens=lens)
     torch.cuda.synchronize()
-    assert nsa.nsa_device_status(ws) == 0
+    assert nsa.nsa_device_status(ws) == expect_status
     return out, idx
 
 
@@ -55,13 +57,17 @@ def check_dsa(inp, ref, out, idx, topk, label="", exact_idx=False):
     gidx = idx[torch.as_tensor(batches)].cpu().numpy()
     expect = ref["out"].copy()
     near = 0
+    lens = [int(x) for x in ref["lens"]]
     for si, b in enumerate(batches):
-        row = gidx[si]
+        Tb = lens[si]
+        kk = min(topk, Tb)
+        assert (gidx[si, kk:] == -1).all(), f"{label} b={b}: -1 padding past the kept positions"
+        row = gidx[si, :kk]
         assert list(row) == sorted(set(row.tolist())), f"{label} b={b}: positions not ascending/distinct"
-        if np.array_equal(row, ref["idx"][si]):
+        if np.array_equal(row, ref["idx"][si, :kk]):
             continue
         assert not exact_idx, f"{label} b={b}: kept set differs from the oracle's"
-        ok, gap = D.topk_set_valid(ref["I32"][si], row, topk, NEAR_TIE)
+        ok, gap = D.topk_set_valid(ref["I32"][si, :Tb], row, topk, NEAR_TIE)
         assert ok, f"{label} b={b}: GPU set is not a valid top-{topk} (gap {gap:.3g})"
         near += 1
         ti = torch.as_tensor(row.astype(np.int64))
@@ -153,3 +159,25 @@ def test_dsa_latent_values_full_size():
     out, idx = run_dsa(inp, wl.topk, latent_dv=wl.dv)
     ref = D.dsa_decode_reference(inp, wl.topk, latent_dv=wl.dv)
     check_dsa(inp, ref, out, idx, wl.topk, label="dsa latent 8x128k")
+
+
+def test_dsa_rows_with_different_lengths():
+    """One batch whose rows hold different context lengths (seq_lens): each
+    row scores and keeps among its own positions only."""
+    wl = DSAWorkload("dsa_ragged", 6, 5000, 4, 64, 16, 576, 512, 256, 17)
+    inp = make_dsa(wl)
+    lens = [5000, 1, 255, 256, 257, 3001]
+    ref = D.dsa_decode_reference(inp, wl.topk, seq_lens=lens)
+    out, idx = run_dsa(inp, wl.topk, seq_lens=lens)
+    check_dsa(inp, ref, out, idx, wl.topk, label="dsa ragged")
+
+
+def test_dsa_invalid_lengths_are_reported_and_skipped():
+    wl = DSAWorkload("dsa_ragged_bad", 4, 3000, 4, 64, 16, 576, 512, 256, 18)
+    inp = make_dsa(wl)
+    lens = [0, 3000, 3001, 700]
+    out, idx = run_dsa(inp, wl.topk, seq_lens=lens, expect_status=1)   # 1 = NSA_ERR_INVALID_ARG
+    bad = torch.as_tensor([0, 2])
+    assert torch.all(out[bad].float() == 0) and torch.all(idx[bad] == -1)
+    ref = D.dsa_decode_reference(inp, wl.topk, batches=[1, 3], seq_lens=[3000, 3000, 3000, 700])
+    check_dsa(inp, ref, out, idx, wl.topk, label="dsa with invalid lengths")

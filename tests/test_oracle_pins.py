@@ -490,6 +490,27 @@ def test_selection_set_valid_rejects_planted_invalid_rows():
     assert not O.selection_set_valid(S, 2 * 64, [0, 2, -1, -1], n, lsel, 1e-5)[0]
 
 
+def test_dsa_with_lengths_equals_cropped_context():
+    """A row whose context holds T_b tokens is the same step on the first T_b
+    tokens alone; nothing past T_b is read."""
+    wl = dsa_config()
+    inp = make_dsa(wl, B=3, T=900)
+    lens = [900, 37, 512]
+    res = D.dsa_decode_reference(inp, topk=64, seq_lens=lens)
+    for b, L in enumerate(lens):
+        one = {key: (t[b:b + 1, :L] if key in ("kI", "k", "v") else t[b:b + 1]) for key, t in inp.items()}
+        ref = D.dsa_decode_reference(one, topk=64)
+        np.testing.assert_array_equal(res["out"][b], ref["out"][0])
+        kk = min(64, L)
+        np.testing.assert_array_equal(res["idx"][b, :kk], ref["idx"][0])
+        assert (res["idx"][b, kk:] == -1).all()
+    for key in ("kI", "k", "v"):
+        for b, L in enumerate(lens):
+            inp[key][b, L:] = 50.0
+    res2 = D.dsa_decode_reference(inp, topk=64, seq_lens=lens)
+    np.testing.assert_array_equal(res["out"], res2["out"])
+
+
 def test_dsa_full_when_k_covers_context():
     wl = dsa_config()
     inp = make_dsa(wl, B=2, T=300)
