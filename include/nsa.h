@@ -254,8 +254,10 @@ typedef struct dsa_cfg {
   int topk;    /* positions kept per query (pages: 2048)              */
   float scale; /* <= 0 -> 1/sqrt(dk)                                  */
 } dsa_cfg;
-/* Supported: HI <= 16, dI a multiple of 8 up to 256, dk and dv multiples of 8
-   up to 1024, 1 <= topk, H <= 32. */
+/* Supported: 1 <= HI <= 8, dI in {64, 128, 256}, 1 <= H <= 16, dk a multiple
+   of 64 up to 640, dv in {64, 128, 256, 512}, 1 <= topk, B <= 65535,
+   T <= 2^28; every device pointer 16-byte aligned.  Anything else returns
+   NSA_ERR_UNSUPPORTED (shape) or NSA_ERR_INVALID_ARG (pointer). */
 
 size_t dsa_decode_workspace_size(const dsa_cfg* cfg);
 

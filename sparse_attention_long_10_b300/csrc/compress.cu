@@ -67,25 +67,14 @@ __global__ void __cluster_dims__(1, kBiasSplit, 1) __launch_bounds__(32 * kBiasR
     part[threadIdx.x] = sum;
   }
   // every CTA's partial is in its shared memory before CTA 0 reads them
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  cluster_sync();
   if (blockIdx.y == 0 && threadIdx.y == 0) {
     float sum = 0.f;
-    const uint32_t local = smem_u32(&part[threadIdx.x]);
-    for (int c = 0; c < kBiasSplit; ++c) {
-      uint32_t remote;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(c));
-      float v;
-      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-      sum += v;
-    }
+    for (int c = 0; c < kBiasSplit; ++c) sum += __uint_as_float(dsmem_ld_u32(dsmem_addr(&part[threadIdx.x], c)));
     if (n < N) bias[n] = sum;
   }
   // no CTA leaves while CTA 0 may still read its shared memory
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  cluster_sync();
 }
 
 __global__ void __launch_bounds__(128, 1)

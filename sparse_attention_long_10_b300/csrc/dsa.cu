@@ -5,23 +5,21 @@
 // are kept, independently per query; attention runs over the kept tokens only,
 // its softmax normalised over that set].
 //
-// One query token per batch row b at position T-1.  Five launches:
+// One query token per batch row b at position T-1.  Four launches:
 //   dsa_index   I[s] = sum_h w_h * max(0, qI_h . kI_s) for every s (warp MMA,
 //               kI streamed by TMA); writes an order-preserving 32-bit key of
 //               the fp32 score and a 4096-bin histogram of the key's top 12
 //               bits per row.
-//   dsa_thresh  exact radix select of the kk-th best (key, position) pair,
-//               ties to the lower position: the first level comes from the
-//               histogram, the boundary bin's candidates are collected and the
-//               last CTA of the row resolves them (12 + 8 more key bits, then
-//               the position); it also counts the kept positions per part.
-//   dsa_compact ordered compaction of the kept positions (ascending).
-//   dsa_attn    softmax(q K_sel^T * scale) V_sel over the kept positions:
-//               rows gathered by untiled bulk copies, warp MMA, split over
-//               CTAs of 64 kept positions, each leaving (max, sum, O);
+//   dsa_select  one thread-block cluster per row: exact radix select of the
+//               kk-th best (key, position) pair, ties to the lower position
+//               (first level from the histogram, the boundary bin's candidates
+//               resolved on 12 + 8 more key bits, then the position), and the
+//               ordered compaction of the kept positions (ascending); counts
+//               and candidates move through distributed shared memory.
+//   dsa_attn    softmax(q K_sel^T * scale) V_sel over the kept positions on
+//               tcgen05: rows gathered by TMA tile::gather4, split over CTAs of
+//               128 kept positions, each leaving (max, sum, O);
 //   dsa_merge   merges a row's splits, one CTA per (head, row).
-// The last indexer CTA of a row finds the first radix cut from the row's
-// histogram.
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -37,19 +35,13 @@ constexpr int kIdxTile = 128;       // keys per indexer tile
 constexpr int kIdxStages = 4;
 constexpr int kIdxPartMax = 4096;   // most positions per indexer CTA
 constexpr int kBins = 4096;         // first radix level: top 12 bits
-constexpr int kSelThreads = 256;
-constexpr int kSelPart = 2048;      // positions per threshold / compaction CTA
-constexpr int kCandCap = 8192;      // boundary-bin candidates kept per row
-constexpr int kAttnThreads = 160;   // 4 compute warps + 1 gather warp
-constexpr int kAttnTile = 32;       // kept tokens per attention tile
-constexpr int kAttnTilesPerCta = 2;
-constexpr int kAttnStages = 2;
+constexpr int kSelThreads = 512;
+constexpr int kCandCap = 4096;      // boundary-bin candidates resolved in shared memory per row
 
 struct DsaArgs {
   int B, T, HI, dI, H, dk, dv, kk;  // T: context capacity; kk = min(topk, T) (row stride of idx)
   int topk;
   const int32_t* lens;              // nullable [B]: context length of each row (query at len-1)
-  int nparts;                       // threshold / compaction parts per row
   int idx_part;                     // positions per indexer CTA (a multiple of kIdxTile)
   int attn_ctas;                    // attention CTAs per row
   int all;                          // kk == T: every position is kept
@@ -62,25 +54,15 @@ struct DsaArgs {
   int v_from_k;                     // values are the first dv columns of k (latent KV)
   __nv_bfloat16* out;               // [B,H,dv]
   int32_t* idx_out;                 // nullable [B,kk]
-  uint32_t* keys;                   // [B,T]
+  uint32_t* keys;                   // [B,kstride]
+  int kstride;                      // T rounded up to 64 keys
   uint32_t* hist;                   // [B,kBins]
-  uint32_t* cand;                   // [B,kCandCap,2] (key, position)
-  uint32_t* cand_n;                 // [B]
-  uint32_t* gtcnt;                  // [B,nparts] keys above the boundary bin
-  uint32_t* offs;                   // [B,nparts] output offset of each part
-  uint32_t* thr;                    // [B,2] (K*, I*): the kk-th kept pair
-  uint32_t* cut1;                   // [B,2] first-level cut: boundary bin B1, count above it
   int32_t* idx;                     // [B,kk] kept positions, ascending
   float* pm;                        // [B,attn_ctas,16]
   float* pl;                        // [B,attn_ctas,16]
   float* po;                        // [B,attn_ctas,16,dv]
-  int* cnt;                         // [3,B] last-CTA counters (threshold, indexer, unused)
   DeviceStatus* st;
 };
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
 
 // Order-preserving key of an fp32 score: unsigned order of keys = numeric
 // order of scores; -0 is folded into +0 so the two compare equal.
@@ -209,7 +191,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
           const int pos = e ? pb : pa;
           const uint32_t key = e ? kb : ka;
           const bool mine = tq == 0 && pos < rg.T;
-          if (mine) a.keys[(size_t)b * a.T + pos] = key;
+          if (mine) a.keys[(size_t)b * a.kstride + pos] = key;
           const uint32_t bin = mine ? (key >> 20) : 0xffffffffu;
           const unsigned same = __match_any_sync(0xffffffffu, bin);
           if (mine && (__ffs(same) - 1) == lane) atomicAdd(&hs[bin], (uint32_t)__popc(same));
@@ -223,79 +205,27 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   if (*abort_flag) return;
   for (int i = threadIdx.x; i < kBins; i += kIdxThreads)
     if (hs[i]) atomicAdd(&a.hist[(size_t)b * kBins + i], hs[i]);
-  // the last CTA of the row finds the boundary bin of the first radix level
-  __threadfence();
-  __syncthreads();
-  __shared__ int s_last;
-  if (threadIdx.x == 0) s_last = (atomicAdd(&a.cnt[a.B + b], 1) == (int)gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (!s_last || rg.all) return;   // a row that keeps every position needs no cut
-  __threadfence();
-  // suffix counts over the bins, 16 per thread for the first 256 threads' worth
-  uint32_t* hg = hs;   // reuse: copy of the row's histogram
-  {
-    constexpr int kPer = (kBins + kIdxThreads - 1) / kIdxThreads;
-    uint32_t v[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * kIdxThreads;
-      v[k] = i < kBins ? __ldcg(a.hist + (size_t)b * kBins + i) : 0u;
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * kIdxThreads;
-      if (i < kBins) hg[i] = v[k];
-    }
-  }
-  __syncthreads();
-  // 128 threads, 32 bins each from the top: warp scans, then the thread whose
-  // range holds the kk-th best key walks its bins
-  __shared__ uint32_t wtot[4];
-  const int t = threadIdx.x;
-  uint32_t sum = 0, incl = 0;
-  if (t < 128) {
-    for (int i = 0; i < 32; ++i) sum += hg[kBins - 32 * t - 1 - i];
-    incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) wtot[warp] = incl;
-  }
-  __syncthreads();
-  if (t < 128) {
-    for (int k = 0; k < warp; ++k) incl += wtot[k];
-    const uint32_t excl = incl - sum;
-    if (excl < (uint32_t)rg.kk && incl >= (uint32_t)rg.kk) {
-      uint32_t cum = excl;
-      for (int i = 0; i < 32; ++i) {
-        const int bin = kBins - 32 * t - 1 - i;
-        if (cum + hg[bin] >= (uint32_t)rg.kk) {
-          a.cut1[(size_t)b * 2] = (uint32_t)bin;
-          a.cut1[(size_t)b * 2 + 1] = cum;
-          break;
-        }
-        cum += hg[bin];
-      }
-    }
-  }
 }
 
-// ============================================================ threshold
-// Block-wide cut over a histogram of ``nbins`` (a multiple of 256) bins read
-// through get(i).  from_top: the highest bin B with count(bins >= B) >= need,
-// and count(bins > B); otherwise the lowest bin B with count(bins <= B) >=
-// need, and count(bins < B).  Needs 256 threads; scan has 256 + 2 words.
+// ============================================================ radix select helpers
+// Block-wide cut over a histogram of ``nbins`` bins (a multiple of
+// kSelThreads, or fewer) read through get(i).  from_top: the highest bin B with
+// count(bins >= B) >= need, and count(bins > B); otherwise the lowest bin B
+// with count(bins <= B) >= need, and count(bins < B).  Needs kSelThreads
+// threads; scan has 258 words (warp totals, then the result in 256 and 257).
 template <class Get>
 __device__ void block_cut(Get get, int nbins, uint32_t need, bool from_top, uint32_t* scan, uint32_t& bin,
                           uint32_t& before) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int per = nbins / 256;
+  const int per = (nbins + kSelThreads - 1) / kSelThreads;
   auto bin_of = [&](int i) { return from_top ? nbins - per * t - 1 - i : per * t + i; };
+  auto count = [&](int i) -> uint32_t {
+    const int x = bin_of(i);
+    return (x >= 0 && x < nbins) ? get(x) : 0u;
+  };
   uint32_t sum = 0;
-  for (int i = 0; i < per; ++i) sum += get(bin_of(i));
-  // inclusive scan over the 256 threads: within warps by shuffles, then warp totals
+  for (int i = 0; i < per; ++i) sum += count(i);
+  // inclusive scan over the threads: within warps by shuffles, then warp totals
   uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -311,7 +241,7 @@ __device__ void block_cut(Get get, int nbins, uint32_t need, bool from_top, uint
   if (excl < need && incl >= need) {
     uint32_t cum = excl;
     for (int i = 0; i < per; ++i) {
-      const uint32_t c = get(bin_of(i));
+      const uint32_t c = count(i);
       if (cum + c >= need) {
         scan[256] = (uint32_t)bin_of(i);
         scan[257] = cum;
@@ -328,35 +258,74 @@ __device__ void block_cut(Get get, int nbins, uint32_t need, bool from_top, uint
 
 // Exact radix select over ``n`` (key, position) elements read through
 // elem(i, key, pos) that all share the top-12-bit bin B1: the need-th best
-// pair under (key descending, position ascending).  hist: 4096 words.
+// pair under (key descending, position ascending).  hist: 4096 words.  Once a
+// level leaves at most kRankMax elements in the chosen bin, they are ranked
+// by direct comparison (positions break key ties), which ends the select.
+constexpr uint32_t kRankMax = 256;
+
 template <class Elem>
 __device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need, uint32_t max_pos, uint32_t* hist,
                               uint32_t* scan, uint32_t& Ks, uint32_t& Is) {
   const int t = threadIdx.x;
   uint32_t prefix = B1 << 20, mask = 0xFFF00000u;
-  // key bits 19..8 (4096 bins), then 7..0 (256 bins), from the top
-  const int shifts[2] = {8, 0};
-  const int widths[2] = {12, 8};
-  for (int lv = 0; lv < 2; ++lv) {
-    const int nb = 1 << widths[lv];
+  // key bits 19..12, 11..4 (256 bins each), then 3..0 (16 bins), from the top
+  constexpr int kLevels = 3;
+  uint32_t last = 0;
+  for (int lv = 0; lv < kLevels; ++lv) {
+    const int shift = lv == 0 ? 12 : (lv == 1 ? 4 : 0);
+    const int nb = lv < 2 ? 256 : 16;
     const uint32_t dmask = (uint32_t)nb - 1;
-    for (int i = t; i < nb; i += 256) hist[i] = 0;
+    for (int i = t; i < nb; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (uint32_t i = t; i < n; i += 256) {
+    for (uint32_t i = t; i < n; i += kSelThreads) {
       uint32_t key, pos;
       elem(i, key, pos);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shifts[lv]) & dmask], 1u);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
     }
     __syncthreads();
     uint32_t bin, before;
     block_cut([&](int i) { return hist[i]; }, nb, need, true, scan, bin, before);
-    prefix |= bin << shifts[lv];
-    mask |= dmask << shifts[lv];
+    const uint32_t in_bin = hist[bin];
+    prefix |= bin << shift;
+    mask |= dmask << shift;
     need -= before;
+    last = bin;
+    if (in_bin <= kRankMax) {
+      // the need-th best of the few left: the one with need-1 better pairs
+      uint32_t* sk = hist + 1024;
+      uint32_t* sp = sk + kRankMax;
+      if (t == 0) scan[255] = 0;
+      __syncthreads();
+      for (uint32_t i = t; i < n; i += kSelThreads) {
+        uint32_t key, pos;
+        elem(i, key, pos);
+        if ((key & mask) == prefix) {
+          const uint32_t slot = atomicAdd(&scan[255], 1u);
+          sk[slot] = key;
+          sp[slot] = pos;
+        }
+      }
+      __syncthreads();
+      const uint32_t m = scan[255];
+      if ((uint32_t)t < m) {
+        const uint32_t k0 = sk[t], p0 = sp[t];
+        uint32_t r = 0;
+        for (uint32_t u = 0; u < m; ++u) r += (sk[u] > k0 || (sk[u] == k0 && sp[u] < p0)) ? 1u : 0u;
+        if (r == need - 1) {
+          scan[256] = k0;
+          scan[257] = p0;
+        }
+      }
+      __syncthreads();
+      Ks = scan[256];
+      Is = scan[257];
+      __syncthreads();
+      return;
+    }
   }
   Ks = prefix;
   // every element equal to K* is kept: no position cut needed
-  const uint32_t n_eq = hist[Ks & 255u];
+  const uint32_t n_eq = hist[last];
   __syncthreads();
   if (n_eq == need) {
     Is = 0xffffffffu;
@@ -368,9 +337,9 @@ __device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need,
   while (top < 24 && (max_pos >> (top + 8)) != 0) top += 8;
   uint32_t pprefix = 0, pmask = 0;
   for (int sh = top; sh >= 0; sh -= 8) {
-    for (int i = t; i < 256; i += 256) hist[i] = 0;
+    for (int i = t; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (uint32_t i = t; i < n; i += 256) {
+    for (uint32_t i = t; i < n; i += kSelThreads) {
       uint32_t key, pos;
       elem(i, key, pos);
       if (key == Ks && (pos & pmask) == pprefix) atomicAdd(&hist[(pos >> sh) & 255u], 1u);
@@ -385,383 +354,614 @@ __device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need,
   Is = pprefix;
 }
 
-__global__ void __launch_bounds__(kSelThreads) dsa_thresh_kernel(const DsaArgs a) {
-  extern __shared__ uint8_t dyn[];
-  __shared__ uint32_t scan[258];
-  __shared__ uint32_t red[8];
-  __shared__ int s_last;
-  const int part = blockIdx.x, b = blockIdx.y;
+// ============================================================ selection
+// One cluster of kSelCluster CTAs per row turns the row's keys into its kept
+// positions, ascending.  Each CTA owns a contiguous range of positions, staged
+// in shared memory by bulk copies together with the row's histogram; each
+// warp owns a contiguous segment of the staged range:
+//   1. every CTA finds the boundary bin B1 of the row's 4096-bin histogram
+//      (the bin holding the kk-th best key) and the count above it;
+//   2. each warp lists, in position order, its keys at or above B1 (a few
+//      per cent of the keys: every kept key and the boundary candidates);
+//   3. every CTA stores the boundary candidates of its lists into CTA 0's
+//      shared memory (distributed shared memory); CTA 0 resolves the exact
+//      kk-th pair (K*, I*) and stores it into every CTA;
+//   4. every CTA counts its kept list entries, stores the count into the CTAs
+//      after it (their output offsets) and writes its kept positions in order.
+// A list that overflows, or a range longer than one staged chunk, switches the
+// row to the general path: (K*, I*) resolved over the whole row, then counts
+// and writes from full scans of the staged keys.  Every CTA reaches every
+// cluster barrier, also after a failed wait.
+constexpr int kSelCluster = 8;
+constexpr int kSelChunk = 16384;    // keys staged in shared memory at a time
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kWarpList = 256;      // keys at or above B1 listed per warp segment
+static_assert(kSelCluster <= kSelThreads, "one thread per cluster CTA stores the shared values");
+static_assert(2 * kCandCap >= (kBins / 16) * 17, "the padded histogram fits the candidate buffers");
+
+struct SelShared {
+  uint64_t bar;
+  uint32_t scan[258];
+  uint32_t wcnt[kSelWarps];         // kept positions per warp segment
+  uint32_t pre[kSelCluster];        // kept positions of each CTA before this one (stored by them)
+  uint32_t gtotal;                  // CTA 0: the row's boundary candidates (stored by every CTA)
+  uint32_t spill;                   // CTA 0 collects, then every CTA holds: 1 = general path
+  uint32_t ks, is;                  // stored by CTA 0: the kk-th kept pair (K*, I*)
+  int abort;
+};
+
+size_t select_smem() {
+  return sizeof(uint32_t) * ((size_t)kSelChunk + kBins + 2 * (size_t)kCandCap + 2 * kSelWarps * kWarpList) + 1024;
+}
+
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kSelThreads) dsa_select_kernel(const DsaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t* kc = reinterpret_cast<uint32_t*>(align1024(smem_raw));   // [kSelChunk] staged keys
+  uint32_t* h2 = kc + kSelChunk;                       // [kBins] the row's histogram, then radix scratch
+  uint32_t* ck = h2 + kBins;                           // [kCandCap] CTA 0: the row's candidates (keys)
+  uint32_t* cp = ck + kCandCap;                        // [kCandCap] their positions
+  uint32_t* lk = cp + kCandCap;                        // [kSelWarps][kWarpList] keys >= B1 per warp
+  uint32_t* lp = lk + kSelWarps * kWarpList;           // their positions
+  __shared__ SelShared sh;
+  const uint32_t rank = cluster_rank(), nr = cluster_size();
+  const int b = blockIdx.y;
   const int t = threadIdx.x, lane = lane_id(), warp = warp_id();
-  if (t == 0) s_last = prior_error(a.st);
-  __syncthreads();
-  if (s_last) return;
-  __syncthreads();
-  const RowGeom rg = row_geom(a, b, nullptr);
-  if (rg.all) return;   // every position kept (or an empty row): no threshold
-  const uint32_t* hist = a.hist + (size_t)b * kBins;
-  const uint32_t B1 = __ldcg(a.cut1 + (size_t)b * 2), above = __ldcg(a.cut1 + (size_t)b * 2 + 1);
-  // this part's keys: count those above the boundary bin, collect the boundary bin
-  const int p0 = part * kSelPart, p1 = min(rg.T, p0 + kSelPart);
-  const uint32_t* keys = a.keys + (size_t)b * a.T;
-  uint32_t gt = 0;
-  constexpr int kChunks = kSelPart / kSelThreads;
-  uint32_t kv[kChunks];
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const int pos = p0 + c * kSelThreads + t;
-    kv[c] = pos < p1 ? __ldcg(keys + pos) : 0u;
+  const uint32_t lt = (1u << lane) - 1u;
+  // this CTA's share of the row by capacity: known before the row's length is
+  // read, so the first copy starts at once
+  const int per = ((a.T + (int)nr - 1) / (int)nr + 255) / 256 * 256;
+  const int c0 = min(a.T, (int)rank * per), c1 = min(a.T, c0 + per);
+  const uint32_t* keys = a.keys + (size_t)b * a.kstride;
+  if (t == 0) {
+    mbar_init(&sh.bar, 1);
+    sh.gtotal = 0;
+    sh.spill = 0;
+    sh.abort = 0;
+    fence_barrier_init();
   }
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const int pos = p0 + c * kSelThreads + t;
-    const uint32_t key = kv[c];
-    bool cand = false;
-    if (pos < p1) {
-      const uint32_t bin = key >> 20;
-      gt += bin > B1 ? 1u : 0u;
-      cand = bin == B1;
+  if (t < kSelCluster) sh.pre[t] = 0;
+  __syncthreads();
+  // chunk c of the share (with the first, the histogram), copied in whole
+  // 16-byte groups (the row stride is a multiple of 64 keys, so the copy stays
+  // inside the row); issued by thread 0
+  auto issue = [&](int c, bool with_hist) {
+    const int s = c0 + c * kSelChunk;
+    const int n = max(0, min(kSelChunk, c1 - s));
+    const uint32_t bytes = (uint32_t)((n + 3) / 4) * 16u;
+    mbar_arrive_expect_tx(&sh.bar, bytes + (with_hist ? kBins * 4u : 0u));
+    if (with_hist) bulk_load(h2, a.hist + (size_t)b * kBins, kBins * 4u, &sh.bar);
+    for (uint32_t off = 0; off < bytes; off += 16384u)
+      bulk_load(kc + off / 4, keys + s + off / 4, min(16384u, bytes - off), &sh.bar);
+  };
+  if (t == 0) issue(0, true);
+  // the status cannot change while this kernel runs (nothing in it records a
+  // fail-fast error before its last barrier), so all CTAs of a cluster agree
+  const int err = prior_error(a.st);
+  const RowGeom rg = row_geom(a, b, rank == 0 && t == 0 ? a.st : nullptr);
+  int32_t* dst = a.idx + (size_t)b * a.kk;
+  int32_t* dst2 = a.idx_out != nullptr ? a.idx_out + (size_t)b * a.kk : nullptr;
+  if (!err) {
+    // a row that keeps fewer than kk positions: its index row ends in -1
+    if (rank == 0)
+      for (int e = rg.kk + t; e < a.kk; e += kSelThreads) {
+        dst[e] = -1;
+        if (dst2) dst2[e] = -1;
+      }
+    // a row that keeps every position
+    if (rg.all)
+      for (int pos = min(rg.T, c0) + t; pos < min(rg.T, c1); pos += kSelThreads) {
+        dst[pos] = pos;
+        if (dst2) dst2[pos] = pos;
+      }
+  }
+  if (err || rg.all) {
+    // the copy lands before the shared memory is released
+    if (t == 0) mbar_wait_plain(&sh.bar, 0, kWaitLimitNs);
+    return;
+  }
+  // every CTA's counters are initialised before any CTA stores into them (the
+  // matching wait comes before the first remote access)
+  cluster_arrive();
+  const int p0 = min(rg.T, c0), p1 = min(rg.T, c1);
+  const int nchunks = (p1 - p0 + kSelChunk - 1) / kSelChunk;
+  bool ok = true;
+  uint32_t phase = 0;
+  auto wait_copy = [&]() {
+    const bool got = mbar_wait(&sh.bar, phase, &sh.abort, a.st, 541);
+    // every thread continues on the same verdict; a copy still in flight
+    // keeps ``phase`` for the drain at the end
+    ok = __syncthreads_and(got ? 1 : 0) != 0;
+    if (ok) phase ^= 1u;
+  };
+  // stage chunk c >= 1 of [p0, p1); returns its valid keys
+  auto stage = [&](int c, bool) -> int {
+    __syncthreads();   // the previous chunk is no longer read
+    if (ok) {
+      if (t == 0) issue(c, false);
+      wait_copy();
     }
-    const unsigned m = __ballot_sync(0xffffffffu, cand);
-    if (m) {
-      const int leader = __ffs(m) - 1;
-      uint32_t base_i = 0;
-      if (lane == leader) base_i = atomicAdd(&a.cand_n[b], (uint32_t)__popc(m));
-      base_i = __shfl_sync(0xffffffffu, base_i, leader);
-      if (cand) {
-        const uint32_t r = base_i + __popc(m & ((1u << lane) - 1u));
-        if (r < (uint32_t)kCandCap) {
-          uint32_t* c = a.cand + ((size_t)b * kCandCap + r) * 2;
-          c[0] = key;
-          c[1] = (uint32_t)pos;
+    return min(kSelChunk, p1 - (p0 + c * kSelChunk));
+  };
+  // warp w's segment of a chunk of n keys: [w*S, min(n, (w+1)*S)), S a multiple of 128
+  auto seg_len = [&](int n) { return (n + kSelWarps * 128 - 1) / (kSelWarps * 128) * 128; };
+  // the four keys of this lane at chunk index i (i < i1 checked per key; the
+  // staged copy covers whole 16-byte groups, so the vector load stays inside it)
+  auto load4 = [&](int i, int i1, uint32_t (&k4)[4]) {
+    const uint4 v = (ok && i < i1) ? *reinterpret_cast<const uint4*>(kc + i) : make_uint4(0u, 0u, 0u, 0u);
+    k4[0] = v.x;
+    k4[1] = v.y;
+    k4[2] = v.z;
+    k4[3] = v.w;
+  };
+
+  // ---- 1. boundary bin of the first radix level (through a copy of the
+  // histogram padded to 17 words per 16 bins: conflict-free for the cut)
+  wait_copy();
+  int n_last = nchunks > 0 ? min(kSelChunk, p1 - p0) : 0;
+  uint32_t* hp = ck;   // spans ck and cp, both unused until step 3
+  for (int j = 0; j < kBins / kSelThreads; ++j) {
+    const int f = j * kSelThreads + t;
+    hp[(f >> 4) * 17 + (f & 15)] = h2[f];
+  }
+  __syncthreads();
+  uint32_t B1, above;
+  block_cut([&](int i) { return hp[(i >> 4) * 17 + (i & 15)]; }, kBins, (uint32_t)rg.kk, true, sh.scan, B1, above);
+  // ---- 2. each warp lists its keys at or above B1, in position order
+  uint32_t wn = 0;
+  for (int c = 0; c < nchunks; ++c) {
+    const int n = c == 0 ? n_last : stage(c, false);
+    n_last = n;
+    const int s = p0 + c * kSelChunk;
+    const int S = seg_len(n);
+    const int i0 = min(n, warp * S), i1 = min(n, i0 + S);
+    for (int base = i0; base < i1; base += 128) {
+      const int i = base + 4 * lane;
+      uint32_t k4[4];
+      load4(i, i1, k4);
+      unsigned m[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m[j] = __ballot_sync(0xffffffffu, ok && i + j < i1 && (k4[j] >> 20) >= B1);
+      if (m[0] | m[1] | m[2] | m[3]) {
+        uint32_t slot = wn + __popc(m[0] & lt) + __popc(m[1] & lt) + __popc(m[2] & lt) + __popc(m[3] & lt);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((m[j] >> lane) & 1u) {
+            if (slot < (uint32_t)kWarpList) {
+              lk[warp * kWarpList + slot] = k4[j];
+              lp[warp * kWarpList + slot] = (uint32_t)(s + i + j);
+            }
+            ++slot;
+          }
+        wn += __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+      }
+    }
+  }
+  // ---- 3. boundary candidates into CTA 0, which resolves (K*, I*)
+  cluster_wait();
+  {
+    const uint32_t a_tot = dsmem_addr(&sh.gtotal, 0), a_ck = dsmem_addr(ck, 0), a_cp = dsmem_addr(cp, 0);
+    if (wn > (uint32_t)kWarpList) {
+      if (lane == 0) dsmem_atomic_or_u32(dsmem_addr(&sh.spill, 0), 1u);
+    } else {
+      for (uint32_t i0 = 0; i0 < wn; i0 += 32) {
+        const uint32_t i = i0 + lane;
+        const uint32_t key = i < wn ? lk[warp * kWarpList + i] : 0u;
+        const bool cand = i < wn && (key >> 20) == B1;
+        const unsigned m = __ballot_sync(0xffffffffu, cand);
+        if (!m) continue;
+        uint32_t slot = 0;
+        if (lane == 0) slot = dsmem_atomic_add_u32(a_tot, (uint32_t)__popc(m));
+        slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(m & lt);
+        if (cand && slot < (uint32_t)kCandCap) {
+          dsmem_st_u32(a_ck + 4 * slot, key);
+          dsmem_st_u32(a_cp + 4 * slot, lp[warp * kWarpList + i]);
         }
       }
     }
   }
+  cluster_sync();
+  if (rank == 0) {
+    const uint32_t total = sh.gtotal;
+    const uint32_t spill = (sh.spill || nchunks > 1 || total > (uint32_t)kCandCap) ? 1u : 0u;
+    const uint32_t need1 = (uint32_t)rg.kk - above;
+    uint32_t Ks, Is;
+    if (!spill) {
+      radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = ck[i]; pos = cp[i]; }, total, B1, need1,
+                    (uint32_t)(rg.T - 1), h2, sh.scan, Ks, Is);
+    } else {
+      radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = __ldcg(keys + i); pos = i; },
+                    (uint32_t)rg.T, B1, need1, (uint32_t)(rg.T - 1), h2, sh.scan, Ks, Is);
+    }
+    if (t < (int)nr) {
+      dsmem_st_u32(dsmem_addr(&sh.ks, t), Ks);
+      dsmem_st_u32(dsmem_addr(&sh.is, t), Is);
+      dsmem_st_u32(dsmem_addr(&sh.spill, t), spill);
+    }
+  }
+  cluster_sync();
+  const uint32_t Ks = sh.ks, Is = sh.is;
+  const bool general = sh.spill != 0;
+  // ---- 4. kept positions per warp segment
+  // general path: a full scan of a staged chunk
+  auto count_chunk = [&](int c, int n) {
+    const int s = p0 + c * kSelChunk;
+    const int S = seg_len(n);
+    const int i0 = min(n, warp * S), i1 = min(n, i0 + S);
+    uint32_t cnt = 0;
+    for (int base = i0; base < i1; base += 128) {
+      const int i = base + 4 * lane;
+      uint32_t k4[4];
+      load4(i, i1, k4);
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
-  if (lane == 0) red[warp] = gt;
-  __syncthreads();
-  if (t == 0) {
-    uint32_t s = 0;
-    for (int w = 0; w < kSelThreads / 32; ++w) s += red[w];
-    a.gtcnt[(size_t)b * a.nparts + part] = s;
-  }
-  __threadfence();
-  __syncthreads();
-  if (t == 0) s_last = (atomicAdd(&a.cnt[b], 1) == (int)gridDim.x - 1) ? 1 : 0;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // ---------------------------------------------------------- last CTA of the row
-  uint32_t* ck = reinterpret_cast<uint32_t*>(dyn);   // [kCandCap]
-  uint32_t* cp = ck + kCandCap;                        // [kCandCap]
-  uint32_t* h2 = cp + kCandCap;                        // [4096]
-  uint32_t* pc = h2 + 4096;                            // [nparts]
-  const uint32_t c1 = __ldcg(hist + B1);
-  const uint32_t need1 = (uint32_t)rg.kk - above;
-  uint32_t Ks, Is;
-  const bool fast = c1 <= (uint32_t)kCandCap;
-  if (fast) {
-    for (uint32_t i = t; i < c1; i += kSelThreads) {
-      ck[i] = __ldcg(a.cand + ((size_t)b * kCandCap + i) * 2);
-      cp[i] = __ldcg(a.cand + ((size_t)b * kCandCap + i) * 2 + 1);
+      for (int j = 0; j < 4; ++j) cnt += (ok && i + j < i1 && kept(k4[j], (uint32_t)(s + i + j), Ks, Is)) ? 1u : 0u;
     }
+    cnt = warp_sum_u32(cnt);
     __syncthreads();
-    radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = ck[i]; pos = cp[i]; }, c1, B1, need1,
-                  (uint32_t)(rg.T - 1), h2, scan, Ks, Is);
+    if (lane == 0) sh.wcnt[warp] = cnt;
+    __syncthreads();
+  };
+  uint32_t kept_total = 0;
+  if (!general) {
+    uint32_t cnt = 0;
+    for (uint32_t i = lane; i < wn; i += 32)
+      cnt += kept(lk[warp * kWarpList + i], lp[warp * kWarpList + i], Ks, Is) ? 1u : 0u;
+    cnt = warp_sum_u32(cnt);
+    if (lane == 0) sh.wcnt[warp] = cnt;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) kept_total += sh.wcnt[w];
   } else {
-    // more boundary candidates than the buffer holds: resolve over the whole row
-    radix_resolve([&](uint32_t i, uint32_t& key, uint32_t& pos) { key = __ldcg(keys + i); pos = i; },
-                  (uint32_t)rg.T, B1, need1, (uint32_t)(rg.T - 1), h2, scan, Ks, Is);
-  }
-  // kept positions per part: above the boundary bin + kept boundary candidates
-  for (int p = t; p < a.nparts; p += kSelThreads) pc[p] = __ldcg(a.gtcnt + (size_t)b * a.nparts + p);
-  __syncthreads();
-  if (fast) {
-    for (uint32_t i = t; i < c1; i += kSelThreads)
-      if (kept(ck[i], cp[i], Ks, Is)) atomicAdd(&pc[cp[i] / kSelPart], 1u);
-  } else {
-    for (uint32_t i = t; i < (uint32_t)rg.T; i += kSelThreads) {
-      const uint32_t key = __ldcg(keys + i);
-      if ((key >> 20) == B1 && kept(key, i, Ks, Is)) atomicAdd(&pc[i / kSelPart], 1u);
+    for (int c = 0; c < nchunks; ++c) {
+      const int n = nchunks > 1 ? stage(c, false) : n_last;
+      count_chunk(c, n);
+#pragma unroll
+      for (int w = 0; w < kSelWarps; ++w) kept_total += sh.wcnt[w];
     }
   }
-  __syncthreads();
-  if (t == 0) {
-    uint32_t run = 0;
-    for (int p = 0; p < a.nparts; ++p) {
-      a.offs[(size_t)b * a.nparts + p] = run;
-      run += pc[p];
+  // this CTA's count into the offsets of the CTAs after it
+  if (t > (int)rank && t < (int)nr) dsmem_st_u32(dsmem_addr(&sh.pre[rank], t), kept_total);
+  cluster_sync();
+  uint32_t run = 0;
+  for (uint32_t r = 0; r < rank; ++r) run += sh.pre[r];
+  // ---- kept positions in order: warp w writes its segment after the segments before it
+  auto put = [&](uint32_t e, int pos) {
+    if (e < (uint32_t)rg.kk) {
+      dst[e] = pos;
+      if (dst2) dst2[e] = pos;
     }
-    a.thr[(size_t)b * 2 + 0] = Ks;
-    a.thr[(size_t)b * 2 + 1] = Is;
+  };
+  if (!general) {
+    uint32_t o = run;
+    for (int w = 0; w < warp; ++w) o += sh.wcnt[w];
+    for (uint32_t i0 = 0; i0 < wn; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      const bool k = i < wn && kept(lk[warp * kWarpList + i], lp[warp * kWarpList + i], Ks, Is);
+      const unsigned m = __ballot_sync(0xffffffffu, k);
+      if (k) put(o + __popc(m & lt), (int)lp[warp * kWarpList + i]);
+      o += __popc(m);
+    }
+  } else {
+    for (int c = 0; c < nchunks; ++c) {
+      int n = n_last;
+      if (nchunks > 1) {
+        n = stage(c, false);
+        count_chunk(c, n);
+      }
+      const int s = p0 + c * kSelChunk;
+      const int S = seg_len(n);
+      const int i0 = min(n, warp * S), i1 = min(n, i0 + S);
+      uint32_t o = run;
+      for (int w = 0; w < warp; ++w) o += sh.wcnt[w];
+      for (int base = i0; base < i1; base += 128) {
+        const int i = base + 4 * lane;
+        uint32_t k4[4];
+        load4(i, i1, k4);
+        bool f[4];
+        unsigned m[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[j] = ok && i + j < i1 && kept(k4[j], (uint32_t)(s + i + j), Ks, Is);
+          m[j] = __ballot_sync(0xffffffffu, f[j]);
+        }
+        uint32_t e = o + __popc(m[0] & lt) + __popc(m[1] & lt) + __popc(m[2] & lt) + __popc(m[3] & lt);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (f[j]) put(e++, s + i + j);
+        o += __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+      }
+#pragma unroll
+      for (int w = 0; w < kSelWarps; ++w) run += sh.wcnt[w];
+    }
   }
+  // a failed copy: wait (bounded) for it before the shared memory is released
+  if (!ok && t == 0) mbar_wait_plain(&sh.bar, phase, kWaitLimitNs);
 }
 
-// ============================================================ compaction
-__global__ void __launch_bounds__(kSelThreads) dsa_compact_kernel(const DsaArgs a) {
-  __shared__ uint32_t wc[kSelThreads / 32];
-  __shared__ int s_abort;
-  const int part = blockIdx.x, b = blockIdx.y;
-  const int t = threadIdx.x, lane = lane_id(), warp = warp_id();
-  if (t == 0) s_abort = prior_error(a.st);
-  __syncthreads();
-  if (s_abort) return;
-  const RowGeom rg = row_geom(a, b, part == 0 && t == 0 ? a.st : nullptr);
-  const int p0 = part * kSelPart, p1 = min(rg.T, p0 + kSelPart);
-  uint32_t run = rg.all ? (uint32_t)p0 : __ldcg(a.offs + (size_t)b * a.nparts + part);
-  const uint32_t Ks = rg.all ? 0u : __ldcg(a.thr + (size_t)b * 2);
-  const uint32_t Is = rg.all ? 0u : __ldcg(a.thr + (size_t)b * 2 + 1);
-  const uint32_t* keys = a.keys + (size_t)b * a.T;
-  int32_t* dst = a.idx + (size_t)b * a.kk;
-  int32_t* dst2 = a.idx_out != nullptr ? a.idx_out + (size_t)b * a.kk : nullptr;
-  // a row that keeps fewer than kk positions: its index row ends in -1
-  if (part == 0)
-    for (int e = rg.kk + t; e < a.kk; e += kSelThreads) {
-      dst[e] = -1;
-      if (dst2) dst2[e] = -1;
-    }
-  constexpr int kChunks = kSelPart / kSelThreads;
-  bool selv[kChunks];
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const int pos = p0 + c * kSelThreads + t;
-    selv[c] = pos < p1 && (rg.all || kept(__ldcg(keys + pos), (uint32_t)pos, Ks, Is));
-  }
-#pragma unroll
-  for (int c = 0; c < kChunks; ++c) {
-    const int base = p0 + c * kSelThreads;
-    const int pos = base + t;
-    const bool sel = selv[c];
-    const unsigned m = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) wc[warp] = (uint32_t)__popc(m);
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kSelThreads / 32; ++w) {
-      before += w < warp ? wc[w] : 0u;
-      total += wc[w];
-    }
-    if (sel) {
-      const uint32_t o = run + before + __popc(m & ((1u << lane) - 1u));
-      dst[o] = pos;
-      if (dst2) dst2[o] = pos;
-    }
-    run += total;
-    __syncthreads();
-  }
-}
+// ============================================================ attention (tcgen05)
+// One CTA = 128 kept positions of one row: the gather-attention design of the
+// selected-block branch, with keys as the M = 128 side and the (up to 16)
+// heads as N:
+//     S^T[key, head] = K_sel[key, :] . q[head, :]           (dk/64 chunks x 4 MMAs)
+//     exact softmax of the tile per head (max, exp, sum), P^T bf16 in smem
+//     O^T[dv, head] = V_sel^T[dv, key] . P^T[key, head]     (dv/128 tiles x 8 MMAs)
+// The kept rows are gathered four at a time by TMA tile::gather4 into the
+// 128-byte-swizzled K-major layout the MMAs read; every 64-column chunk of the
+// tile's keys stays resident.  Values reuse the key slots once the QK^T MMAs
+// have drained them (latent KV: the first dv/64 key chunks are the values, so
+// nothing more is fetched).  The tile's (max, sum, O^T) goes to the merge.
+constexpr int kTcThreads = 192;         // warps 0-3 softmax + epilogue, 4 gather, 5 MMA issuer
+constexpr int kTcKeys = 128;            // kept positions per CTA
+constexpr int kTcMaxChunks = 10;        // resident 64-column chunks: dk <= 640
+constexpr int kTcChunk = kTcKeys * 128; // 16 KB
 
-// ============================================================ attention
-struct AttnBars {
-  uint64_t full[kAttnStages];
-  uint64_t empty[kAttnStages];
+struct TcBars {
+  uint64_t q_full;
+  uint64_t k_full[kTcMaxChunks];
+  uint64_t v_full;
+  uint64_t s_full;     // QK^T done: softmax may read S^T
+  uint64_t qk_done;    // QK^T done: the gather may overwrite key slots with values
+  uint64_t p_full;     // P^T written (4 softmax warps)
+  uint64_t o_full;
+  uint64_t wg;         // softmax warps' rendezvous
+  uint64_t drain;
+  uint32_t tmem;
   int abort_flag;
-  int last;
 };
 
-struct AttnLayout {
-  uint32_t qs, kst, vst, stage, ks_off, vs_off, p_off, red_off, bar_off, total;
+struct TcLayout {
+  uint32_t k_off, p_off, red_off, rows_off, bar_off, total;
 };
 
-__host__ __device__ inline AttnLayout attn_layout(int dk, int dv) {
-  AttnLayout L;
-  L.qs = 2u * dk + 16u;    // padded row strides (bytes): 8 ldmatrix rows hit 8 bank groups
-  L.kst = 2u * dk + 16u;
-  L.vst = 2u * dv + 16u;
-  L.stage = (uint32_t)kAttnTile * (L.kst + L.vst);
-  L.ks_off = 16u * L.qs;
-  L.vs_off = L.ks_off + (uint32_t)kAttnTile * L.kst;
-  L.p_off = L.ks_off + kAttnStages * L.stage;
-  L.red_off = L.p_off + 16u * 80u;
-  L.bar_off = L.red_off + 2u * 4u * 16u * 4u;
-  L.total = L.bar_off + 128u;
+__host__ __device__ inline int tc_value_chunks(int dv) { return dv / 64 < 2 ? 2 : dv / 64; }
+
+__host__ __device__ inline TcLayout tc_layout(int dk, int dv) {
+  const int nk = dk / 64;
+  const int nslots = nk > tc_value_chunks(dv) ? nk : tc_value_chunks(dv);
+  TcLayout L;
+  L.k_off = (uint32_t)(((nk * 2048) + 1023) / 1024 * 1024);   // q: nk chunks of 16 rows x 128 B
+  L.p_off = L.k_off + (uint32_t)nslots * kTcChunk;              // P^T: 2 chunks of 16 rows x 128 B
+  L.red_off = L.p_off + 4096;                                   // [2 m/l][4 warps][16] floats
+  L.rows_off = L.red_off + 2 * 4 * 16 * 4;                      // [128] gathered row indices
+  L.bar_off = L.rows_off + kTcKeys * 4;
+  L.total = L.bar_off + 256 + 1024;                             // + alignment slack
   return L;
 }
 
+// Four rows (global row indices r0..r3, out of range reads zeros) of 64
+// columns starting at column col, into 4 consecutive 128-byte swizzled rows.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 template <int DV>
-__global__ void __launch_bounds__(kAttnThreads, 1) dsa_attn_kernel(const DsaArgs a) {
-  constexpr int DV4 = DV / 4;   // value columns per compute warp
-  extern __shared__ __align__(16) uint8_t smem[];
-  const AttnLayout L = attn_layout(a.dk, DV);
-  uint8_t* Qs = smem;
-  uint8_t* Ps = smem + L.p_off;
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dsa_attn_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                    const __grid_constant__ CUtensorMap mapV, const DsaArgs a) {
+  constexpr int kVC = DV / 64 < 2 ? 2 : DV / 64;   // value chunks, padded to one M = 128 pair
+  constexpr int kVT = kVC / 2;                        // 128-row value tiles
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const TcLayout L = tc_layout(a.dk, DV);
+  uint8_t* qs = smem;
+  uint8_t* ks = smem + L.k_off;
+  uint8_t* ps = smem + L.p_off;
   float* red_m = reinterpret_cast<float*>(smem + L.red_off);   // [4][16]
   float* red_l = red_m + 64;                                     // [4][16]
-  AttnBars* bars = reinterpret_cast<AttnBars*>(smem + L.bar_off);
+  int* rows_s = reinterpret_cast<int*>(smem + L.rows_off);
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + L.bar_off);
   volatile int* abort_flag = &bars->abort_flag;
   const int x = blockIdx.x, b = blockIdx.y;
   const int warp = warp_id(), lane = lane_id();
-  const int e0 = x * kAttnTile * kAttnTilesPerCta;
-  const int nent = min(kAttnTile * kAttnTilesPerCta, row_geom(a, b, nullptr).kk - e0);
-  const int ntiles = nent > 0 ? (nent + kAttnTile - 1) / kAttnTile : 0;
-  const int dk = a.dk;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 4);
+  const int nk = a.dk / 64;
+  const RowGeom rg = row_geom(a, b, nullptr);
+  const int e0 = x * kTcKeys;
+  const int nent = min(kTcKeys, rg.kk - e0);
+  const size_t pb = (size_t)b * a.attn_ctas + x;
+  if (nent <= 0) {
+    // a row that keeps fewer positions than this tile starts at: empty partial
+    if (threadIdx.x < 16) {
+      a.pm[pb * 16 + threadIdx.x] = -INFINITY;
+      a.pl[pb * 16 + threadIdx.x] = 0.f;
     }
+    for (int i = threadIdx.x; i < 16 * DV; i += kTcThreads) a.po[pb * 16 * DV + i] = 0.f;
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int c = 0; c < kTcMaxChunks; ++c) mbar_init(&bars->k_full[c], 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->qk_done, 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->wg, 4);
+    mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
-    bars->last = 0;
     fence_barrier_init();
   }
-  // query rows (heads past H are zero)
-  for (int i = threadIdx.x; i < 16 * dk / 8; i += kAttnThreads) {
-    const int h = i / (dk / 8), c = i % (dk / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (h < a.H) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.H + h) * dk + 8 * c);
-    *reinterpret_cast<uint4*>(Qs + h * L.qs + 16 * c) = v;
-  }
-  __syncthreads();
+  // query rows H..15 are never loaded: keep them finite (zero)
+  if (a.H < 16)
+    for (int i = threadIdx.x; i < nk * 2048 / 16; i += kTcThreads) {
+      const int row = (i % 128) / 8;
+      if (row >= a.H) reinterpret_cast<uint4*>(qs)[i] = make_uint4(0, 0, 0, 0);
+    }
+  // the tile's global row indices; entries past the row's last kept position
+  // repeat its first one (finite data, masked out of the softmax)
   const int32_t* sel = a.idx + (size_t)b * a.kk + e0;
+  for (int j = threadIdx.x; j < kTcKeys; j += kTcThreads) rows_s[j] = b * a.T + __ldg(sel + (j < nent ? j : 0));
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;          // S^T at columns 0..15, O^T tile t at 16 + 16 t
   bool ok = *abort_flag == 0;
-  const int gq = lane >> 2, tq = lane & 3;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[DV4 / 8][4];
-#pragma unroll
-  for (int i = 0; i < DV4 / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ gather warp
-    if (ok) {
-      int i = 0;
-      for (; i < ntiles; ++i) {
-        const int slot = i % kAttnStages;
-        if (!mbar_wait(&bars->empty[slot], (uint32_t)(((i / kAttnStages) & 1) ^ 1), abort_flag, a.st, 521)) {
-          ok = false;
+  if (!ok) {
+    // an earlier CTA failed: do nothing
+  } else if (warp == 4) {
+    // ============================================================ gather (one warp)
+    // lane 0 arms every barrier; lane j then gathers rows 4j .. 4j+3 of each chunk
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(nk * a.H * 128));
+      for (int c = 0; c < nk; ++c) tma_load_2d(qs + c * 2048, &mapQ, &bars->q_full, c * 64, b * a.H);
+      for (int c = 0; c < nk; ++c) mbar_arrive_expect_tx(&bars->k_full[c], kTcChunk);
+    }
+    __syncwarp();
+    const int4 rw = *reinterpret_cast<const int4*>(rows_s + 4 * lane);
+    for (int c = 0; c < nk; ++c)
+      tma_gather4(ks + c * kTcChunk + lane * 512, &mapK, &bars->k_full[c], c * 64, rw.x, rw.y, rw.z, rw.w);
+    bool vok = true;
+    if (!a.v_from_k) {
+      // the value chunks overwrite key slots 0 .. DV/64-1 once QK^T has read them
+      if (lane == 0) {
+        vok = mbar_wait(&bars->qk_done, 0, abort_flag, a.st, 531);
+        if (vok) mbar_arrive_expect_tx(&bars->v_full, (uint32_t)(DV / 64) * kTcChunk);
+      }
+      vok = __shfl_sync(0xffffffffu, vok ? 1 : 0, 0) != 0;
+      if (vok)
+        for (int c = 0; c < DV / 64; ++c)
+          tma_gather4(ks + c * kTcChunk + lane * 512, &mapV, &bars->v_full, c * 64, rw.x, rw.y, rw.z, rw.w);
+    }
+    if (lane == 0 && (!vok || *abort_flag)) {
+      // drain every copy issued before the CTA releases its shared memory
+      mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
+      for (int c = 0; c < nk; ++c) mbar_wait_plain(&bars->k_full[c], 0, kWaitLimitNs);
+      if (!a.v_from_k && vok) mbar_wait_plain(&bars->v_full, 0, kWaitLimitNs);
+    }
+  } else if (warp == 5) {
+    // ============================================================ MMA issuer (one thread)
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, 16, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 16, true, false);
+      const uint32_t q_a = smem_u32(qs), k_a = smem_u32(ks), p_a = smem_u32(ps);
+      bool mok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 532);
+      for (int c = 0; c < nk && mok; ++c) {
+        if (!mbar_wait(&bars->k_full[c], 0, abort_flag, a.st, 533)) {
+          mok = false;
           break;
         }
-        uint8_t* ks = smem + L.ks_off + slot * L.stage;
-        uint8_t* vs = ks + kAttnTile * L.kst;
-        const int nv = min(kAttnTile, nent - i * kAttnTile);
-        const int e = i * kAttnTile + lane;
-        // with latent KV the value rows are the first DV columns of the key
-        // rows: only the keys are fetched
-        const uint32_t vbytes = a.v_from_k ? 0u : 2u * DV;
-        if (lane >= nv) {   // absent rows read as zeros
-          for (int c = 0; c < dk / 8; ++c) *reinterpret_cast<uint4*>(ks + lane * L.kst + 16 * c) = make_uint4(0, 0, 0, 0);
-          if (!a.v_from_k)
-            for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(vs + lane * L.vst + 16 * c) = make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&bars->full[slot], (uint32_t)nv * (2u * dk + vbytes));
-        __syncwarp();
-        if (lane < nv) {
-          const int pos = __ldg(sel + e);
-          bulk_load(ks + lane * L.kst, a.k + ((size_t)b * a.T + pos) * dk, 2u * dk, &bars->full[slot]);
-          if (!a.v_from_k)
-            bulk_load(vs + lane * L.vst, a.v + ((size_t)b * a.T + pos) * DV, 2u * DV, &bars->full[slot]);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = sdesc_sw128(k_a + c * kTcChunk + k * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(q_a + c * 2048 + k * 32, 16, 1024);
+          umma_bf16(tmem, ad, bd, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
         }
       }
-      if (lane == 0 && (!ok || *abort_flag))
-        for (int y = (i > kAttnStages ? i - kAttnStages : 0); y < i; ++y)
-          mbar_wait_plain(&bars->full[y % kAttnStages], (uint32_t)((y / kAttnStages) & 1), kWaitLimitNs);
+      if (mok) {
+        umma_commit(&bars->s_full);
+        umma_commit(&bars->qk_done);
+      }
+      if (mok && !mbar_wait(&bars->p_full, 0, abort_flag, a.st, 534)) mok = false;
+      if (mok && !a.v_from_k && !mbar_wait(&bars->v_full, 0, abort_flag, a.st, 535)) mok = false;
+      if (mok) {
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < kVT; ++t)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            // A = V^T: value columns 128 t .. 128 t + 127 as two 64-column
+            // chunks one slot apart, keys 16 k .. 16 k + 15 along K
+            const uint64_t ad = sdesc_sw128(k_a + 2 * t * kTcChunk + k * 2048, kTcChunk, 1024);
+            const uint64_t bd = sdesc_sw128(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+            umma_bf16(tmem + 16 + 16 * t, ad, bd, idesc_pv, k > 0 ? 1u : 0u);
+          }
+        umma_commit(&bars->o_full);
+      }
+      if (!mok || *abort_flag) {
+        umma_commit(&bars->drain);
+        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
+      }
     }
-  } else if (ok) {
-    // ------------------------------------------------------------ compute warps
-    const uint32_t q_a = smem_u32(Qs);
-    for (int i = 0; i < ntiles; ++i) {
-      const int slot = i % kAttnStages;
-      if (!mbar_wait(&bars->full[slot], (uint32_t)((i / kAttnStages) & 1), abort_flag, a.st, 522)) {
-        ok = false;
-        break;
-      }
-      const uint32_t k_a = smem_u32(smem + L.ks_off + slot * L.stage);
-      const uint32_t v_a = a.v_from_k ? k_a : k_a + kAttnTile * L.kst;
-      const uint32_t vst = a.v_from_k ? L.kst : L.vst;
-      const int nv = min(kAttnTile, nent - i * kAttnTile);
-      // S[16 heads x 8 keys] for keys 8*warp .. 8*warp+7
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k0 = 0; k0 < dk; k0 += 32) {
-        uint32_t b0, b1, b2, b3, x0[4], x1[4];
-        ldsm_x4(k_a + (uint32_t)(8 * warp + (lane & 7)) * L.kst + (uint32_t)(k0 + (lane >> 3) * 8) * 2, b0, b1, b2,
-                b3);
-        ldsm_x4(q_a + (uint32_t)(lane & 15) * L.qs + (uint32_t)(k0 + (lane >> 4) * 8) * 2, x0[0], x0[1], x0[2],
-                x0[3]);
-        ldsm_x4(q_a + (uint32_t)(lane & 15) * L.qs + (uint32_t)(k0 + 16 + (lane >> 4) * 8) * 2, x1[0], x1[1],
-                x1[2], x1[3]);
-        mma_16816(s, x0, b0, b1);
-        mma_16816(s, x1, b2, b3);
-      }
-      const int key0 = 8 * warp + 2 * tq;
-      s[0] = key0 < nv ? s[0] * a.sc2 : -INFINITY;
-      s[1] = key0 + 1 < nv ? s[1] * a.sc2 : -INFINITY;
-      s[2] = key0 < nv ? s[2] * a.sc2 : -INFINITY;
-      s[3] = key0 + 1 < nv ? s[3] * a.sc2 : -INFINITY;
-      const float mx0 = quad_max(fmaxf(s[0], s[1])), mx1 = quad_max(fmaxf(s[2], s[3]));
-      if (tq == 0) {
-        red_m[warp * 16 + gq] = mx0;
-        red_m[warp * 16 + gq + 8] = mx1;
-      }
-      named_bar(1, 128);
-      const float tm0 = fmaxf(fmaxf(red_m[gq], red_m[16 + gq]), fmaxf(red_m[32 + gq], red_m[48 + gq]));
-      const float tm1 =
-          fmaxf(fmaxf(red_m[gq + 8], red_m[16 + gq + 8]), fmaxf(red_m[32 + gq + 8], red_m[48 + gq + 8]));
-      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-      const float us0 = mn0 == -INFINITY ? 0.f : mn0, us1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m0 - us0), al1 = fast_exp2(m1 - us1);
-      const float p0 = fast_exp2(s[0] - us0), p1 = fast_exp2(s[1] - us0);
-      const float p2 = fast_exp2(s[2] - us1), p3 = fast_exp2(s[3] - us1);
-      const float ps0 = quad_sum(p0 + p1), ps1 = quad_sum(p2 + p3);
-      if (tq == 0) {
-        red_l[warp * 16 + gq] = ps0;
-        red_l[warp * 16 + gq + 8] = ps1;
-      }
-      *reinterpret_cast<uint32_t*>(Ps + gq * 80 + key0 * 2) = pack_bf16x2(p0, p1);
-      *reinterpret_cast<uint32_t*>(Ps + (gq + 8) * 80 + key0 * 2) = pack_bf16x2(p2, p3);
-      named_bar(1, 128);
-      l0 = l0 * al0 + (red_l[gq] + red_l[16 + gq] + red_l[32 + gq] + red_l[48 + gq]);
-      l1 = l1 * al1 + (red_l[gq + 8] + red_l[16 + gq + 8] + red_l[32 + gq + 8] + red_l[48 + gq + 8]);
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int j = 0; j < DV4 / 8; ++j) {
-        o[j][0] *= al0;
-        o[j][1] *= al0;
-        o[j][2] *= al1;
-        o[j][3] *= al1;
-      }
-      const uint32_t p_a = smem_u32(Ps);
-#pragma unroll
-      for (int kk2 = 0; kk2 < 2; ++kk2) {
-        uint32_t pa[4];
-        ldsm_x4(p_a + (uint32_t)(lane & 15) * 80u + (uint32_t)(16 * kk2 + (lane >> 4) * 8) * 2, pa[0], pa[1], pa[2],
-                pa[3]);
-#pragma unroll
-        for (int np = 0; np < DV4 / 16; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(v_a + (uint32_t)(16 * kk2 + (lane & 7) + ((lane >> 3) & 1) * 8) * vst +
-                        (uint32_t)(warp * DV4 + 16 * np + (lane >> 4) * 8) * 2,
-                    b0, b1, b2, b3);
-          mma_16816(o[2 * np], pa, b0, b1);
-          mma_16816(o[2 * np + 1], pa, b2, b3);
-        }
-      }
+  } else {
+    // ============================================================ softmax + epilogue (warps 0-3)
+    const int r = warp * 32 + lane;           // TMEM lane: a key of the tile, later a value row
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const bool valid = r < nent;
+    uint32_t wg_phase = 0;
+    auto wg_sync = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->empty[slot]);
-    }
-  }
-  __syncthreads();
-  if (*abort_flag) return;
-  // ---------------------------------------------------------------- partial of this CTA
-  const size_t pb = (size_t)b * a.attn_ctas + x;
-  if (warp < 4) {
-    if (warp == 0 && tq == 0) {
-      a.pm[pb * 16 + gq] = m0;
-      a.pm[pb * 16 + gq + 8] = m1;
-      a.pl[pb * 16 + gq] = l0;
-      a.pl[pb * 16 + gq + 8] = l1;
-    }
+      if (lane == 0) mbar_arrive(&bars->wg);
+      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 536)) ok = false;
+      ++wg_phase;
+    };
+    uint32_t sr[16];
+    if (!mbar_wait(&bars->s_full, 0, abort_flag, a.st, 537)) ok = false;
+    tc_fence_after();
+    tmem_ld16(tmem + lane_base, sr);
+    tmem_ld_wait(sr);
+    float m[16];
 #pragma unroll
-    for (int j = 0; j < DV4 / 8; ++j) {
-      float* r = a.po + (pb * 16 + gq) * DV + warp * DV4 + 8 * j + 2 * tq;
-      r[0] = o[j][0];
-      r[1] = o[j][1];
-      r[8 * DV] = o[j][2];
-      r[8 * DV + 1] = o[j][3];
+    for (int h = 0; h < 16; ++h) m[h] = warp_max_f32(valid ? __uint_as_float(sr[h]) * a.sc2 : -INFINITY);
+    if (lane == 0)
+#pragma unroll
+      for (int h = 0; h < 16; ++h) red_m[warp * 16 + h] = m[h];
+    wg_sync();
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      m[h] = fmaxf(fmaxf(red_m[h], red_m[16 + h]), fmaxf(red_m[32 + h], red_m[48 + h]));
+      if (m[h] == -INFINITY) m[h] = 0.f;
+    }
+    // p = exp2(s * scale - max) as P^T (bf16, key-major rows of heads), sums
+    float ls[16];
+    uint8_t* chunk = ps + (r >> 6) * 2048 + (r & 7) * 2;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      const float e = valid ? fast_exp2(fmaf(__uint_as_float(sr[h]), a.sc2, -m[h])) : 0.f;
+      ls[h] = e;
+      *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, (r & 63) >> 3)) = __float2bfloat16_rn(e);
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_full);
+    const float ws = warp_sum16(ls, lane);
+    if ((lane & 1) == 0) red_l[warp * 16 + head_of_lane(lane)] = ws;
+    wg_sync();
+    if (ok && threadIdx.x < 16) {
+      const int h = threadIdx.x;
+      const float mh = fmaxf(fmaxf(red_m[h], red_m[16 + h]), fmaxf(red_m[32 + h], red_m[48 + h]));
+      a.pm[pb * 16 + h] = mh == -INFINITY ? 0.f : mh;
+      a.pl[pb * 16 + h] = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+    }
+    // unnormalised O^T of the tile: lane r holds value row 128 t + r, 16 heads
+    if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 538)) {
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kVT; ++t) {
+        uint32_t orr[16];
+        tmem_ld16(tmem + lane_base + 16 + 16 * t, orr);
+        tmem_ld_wait(orr);
+        const int d = 128 * t + r;
+        if (d < DV) {
+          float* dst = a.po + pb * 16 * DV + d;
+#pragma unroll
+          for (int h = 0; h < 16; ++h) dst[(size_t)h * DV] = __uint_as_float(orr[h]);
+        }
+      }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // Merge of a row's attention splits: out[b,h,:] = sum_c w_c O_c / sum_c w_c l_c,
@@ -839,19 +1039,19 @@ __global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const 
 
 // ============================================================ host side
 struct DsaWs {
-  size_t cnt, hist, cand_n, zero_end, keys, cand, gtcnt, offs, thr, cut1, idx, pm, pl, po, end;
+  size_t hist, zero_end, keys, idx, pm, pl, po, end;
 };
 
 struct DsaShape {
-  int kk, nparts, attn_ctas, all;
+  int kk, attn_ctas, all, kstride;
 };
 
 DsaShape dsa_shape(const dsa_cfg& c) {
   DsaShape s;
   s.kk = c.topk < c.T ? c.topk : c.T;
   s.all = s.kk == c.T ? 1 : 0;
-  s.nparts = (c.T + kSelPart - 1) / kSelPart;
-  s.attn_ctas = (s.kk + kAttnTile * kAttnTilesPerCta - 1) / (kAttnTile * kAttnTilesPerCta);
+  s.attn_ctas = (s.kk + kTcKeys - 1) / kTcKeys;
+  s.kstride = (c.T + 63) / 64 * 64;
   return s;
 }
 
@@ -859,26 +1059,15 @@ DsaWs dsa_ws(const dsa_cfg& c) {
   const DsaShape s = dsa_shape(c);
   const size_t B = (size_t)c.B;
   DsaWs w;
-  w.cnt = sizeof(DeviceStatus);
-  w.cand_n = align_up(w.cnt + sizeof(int) * 3 * B, 256);
-  w.hist = align_up(w.cand_n + sizeof(uint32_t) * B, 256);
+  w.hist = align_up(sizeof(DeviceStatus), 256);
   w.zero_end = align_up(w.hist + sizeof(uint32_t) * B * kBins, 256);
   w.keys = w.zero_end;
-  w.cand = align_up(w.keys + sizeof(uint32_t) * B * (size_t)c.T, 256);
-  w.gtcnt = align_up(w.cand + sizeof(uint32_t) * B * kCandCap * 2, 256);
-  w.offs = align_up(w.gtcnt + sizeof(uint32_t) * B * s.nparts, 256);
-  w.thr = align_up(w.offs + sizeof(uint32_t) * B * s.nparts, 256);
-  w.cut1 = align_up(w.thr + sizeof(uint32_t) * B * 2, 256);
-  w.idx = align_up(w.cut1 + sizeof(uint32_t) * B * 2, 256);
+  w.idx = align_up(w.keys + sizeof(uint32_t) * B * (size_t)s.kstride, 256);
   w.pm = align_up(w.idx + sizeof(int32_t) * B * (size_t)s.kk, 256);
   w.pl = align_up(w.pm + sizeof(float) * B * s.attn_ctas * 16, 256);
   w.po = align_up(w.pl + sizeof(float) * B * s.attn_ctas * 16, 256);
   w.end = align_up(w.po + sizeof(float) * B * s.attn_ctas * 16 * (size_t)c.dv, 256);
   return w;
-}
-
-size_t thresh_smem(const DsaShape& s) {
-  return sizeof(uint32_t) * (2 * (size_t)kCandCap + 4096 + (size_t)s.nparts);
 }
 
 template <int DI>
@@ -891,12 +1080,61 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
+int launch_select(const DsaArgs& a, cudaStream_t s) {
+  const size_t smem = select_smem();
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_select_kernel), smem)) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSelCluster, a.B);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSelCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof::begin("dsa_select", s);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa_select_kernel, a);
+  prof::end(s);
+  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+}
+
 template <int DV>
 int launch_attn(const DsaArgs& a, cudaStream_t s) {
-  const AttnLayout L = attn_layout(a.dk, DV);
-  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_attn_kernel<DV>), smem_max())) return rc;
+  const TcLayout L = tc_layout(a.dk, DV);
+  // each CTA holds 128 TMEM columns: at most 4 may share an SM, so a small
+  // layout asks for enough shared memory to keep the count there
+  size_t smem = L.total;
+  const size_t floor4 = (size_t)smem_max() / 4 + 1024;
+  if (smem < floor4) smem = floor4;
+  if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_attn_kernel<DV>), smem)) return rc;
+  // q as [B*H, dk] in boxes of 64 columns x H heads; k and v as [B*T, d] rows
+  // fetched one row per gathered coordinate
+  CUtensorMap mq, mk, mv;
+  {
+    const uint64_t dims[2] = {(uint64_t)a.dk, (uint64_t)a.B * a.H};
+    const uint64_t str[1] = {(uint64_t)a.dk * 2};
+    const uint32_t box[2] = {64, (uint32_t)a.H};
+    if (!make_tmap_bf16(&mq, a.q, 2, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)a.dk, (uint64_t)a.B * a.T};
+    const uint64_t str[1] = {(uint64_t)a.dk * 2};
+    const uint32_t box[2] = {64, 1};
+    if (!make_tmap_bf16(&mk, a.k, 2, dims, str, box)) return NSA_ERR_CUDA;
+  }
+  if (a.v_from_k) {
+    mv = mk;
+  } else {
+    const uint64_t dims[2] = {(uint64_t)DV, (uint64_t)a.B * a.T};
+    const uint64_t str[1] = {(uint64_t)DV * 2};
+    const uint32_t box[2] = {64, 1};
+    if (!make_tmap_bf16(&mv, a.v, 2, dims, str, box)) return NSA_ERR_CUDA;
+  }
   prof::begin("dsa_attn", s);
-  dsa_attn_kernel<DV><<<dim3(a.attn_ctas, a.B), kAttnThreads, L.total, s>>>(a);
+  dsa_attn_kernel<DV><<<dim3(a.attn_ctas, a.B), kTcThreads, smem, s>>>(mq, mk, mv, a);
   prof::end(s);
   if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
   prof::begin("dsa_merge", s);
@@ -911,12 +1149,11 @@ int dsa_supported(const dsa_cfg& c) {
   if (c.HI < 1 || c.HI > 8) return NSA_ERR_UNSUPPORTED;
   if (c.dI != 64 && c.dI != 128 && c.dI != 256) return NSA_ERR_UNSUPPORTED;
   if (c.H < 1 || c.H > 16) return NSA_ERR_UNSUPPORTED;
-  if (c.dk % 64 != 0 || c.dk > 1024) return NSA_ERR_UNSUPPORTED;
+  if (c.dk % 64 != 0 || c.dk > 64 * kTcMaxChunks) return NSA_ERR_UNSUPPORTED;
   if (c.dv != 64 && c.dv != 128 && c.dv != 256 && c.dv != 512) return NSA_ERR_UNSUPPORTED;
   if (c.B > 65535 || c.T > (1 << 28)) return NSA_ERR_UNSUPPORTED;
-  const DsaShape s = dsa_shape(c);
-  if (attn_layout(c.dk, c.dv).total > smem_max()) return NSA_ERR_UNSUPPORTED;
-  if (thresh_smem(s) + 2048 > smem_max()) return NSA_ERR_UNSUPPORTED;
+  if (tc_layout(c.dk, c.dv).total > smem_max()) return NSA_ERR_UNSUPPORTED;
+  if (select_smem() + sizeof(SelShared) + 1024 > smem_max()) return NSA_ERR_UNSUPPORTED;
   return NSA_OK;
 }
 
@@ -938,7 +1175,6 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.kk = sh.kk;
   a.topk = c.topk;
   a.lens = lens;
-  a.nparts = sh.nparts;
   {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -962,18 +1198,12 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   a.out = static_cast<__nv_bfloat16*>(out);
   a.idx_out = idx_out;
   a.keys = reinterpret_cast<uint32_t*>(ws + w.keys);
+  a.kstride = sh.kstride;
   a.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
-  a.cand = reinterpret_cast<uint32_t*>(ws + w.cand);
-  a.cand_n = reinterpret_cast<uint32_t*>(ws + w.cand_n);
-  a.gtcnt = reinterpret_cast<uint32_t*>(ws + w.gtcnt);
-  a.offs = reinterpret_cast<uint32_t*>(ws + w.offs);
-  a.thr = reinterpret_cast<uint32_t*>(ws + w.thr);
-  a.cut1 = reinterpret_cast<uint32_t*>(ws + w.cut1);
   a.idx = reinterpret_cast<int32_t*>(ws + w.idx);
   a.pm = reinterpret_cast<float*>(ws + w.pm);
   a.pl = reinterpret_cast<float*>(ws + w.pl);
   a.po = reinterpret_cast<float*>(ws + w.po);
-  a.cnt = reinterpret_cast<int*>(ws + w.cnt);
   a.st = reinterpret_cast<DeviceStatus*>(ws);
   int rc = NSA_OK;
   if (!sh.all) {
@@ -989,18 +1219,8 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
       default: return NSA_ERR_UNSUPPORTED;
     }
     if (rc != NSA_OK) return rc;
-    // dynamic size actually needed (the kernel also has ~1 KB of static shared memory)
-    if ((rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_thresh_kernel), thresh_smem(sh))) != NSA_OK)
-      return rc;
-    prof::begin("dsa_thresh", s);
-    dsa_thresh_kernel<<<dim3(sh.nparts, c.B), kSelThreads, thresh_smem(sh), s>>>(a);
-    prof::end(s);
-    if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
   }
-  prof::begin("dsa_compact", s);
-  dsa_compact_kernel<<<dim3(sh.nparts, c.B), kSelThreads, 0, s>>>(a);
-  prof::end(s);
-  if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  if ((rc = launch_select(a, s)) != NSA_OK) return rc;
   switch (c.dv) {
     case 64: return launch_attn<64>(a, s);
     case 128: return launch_attn<128>(a, s);

@@ -84,10 +84,6 @@ struct Bars {
   int abort_flag;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __device__ __forceinline__ int visible_cmp(int t, int Nc) {
   // compressed block i is visible once its last token 16*i+31 <= t
   if (t < 31) return 0;
@@ -114,11 +110,6 @@ __device__ __forceinline__ int reduce_scatter16(float (&v)[16], int lane) {
   return base;
 }
 
-__device__ __forceinline__ float warp_max_f32(float x) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-  return r;
-}
 __device__ __forceinline__ uint32_t warp_min_u32(uint32_t x) {
   uint32_t r;
   asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));

@@ -68,10 +68,6 @@ struct Bars {
   int abort_flag;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 // token coordinate of block ``blk`` for a TMA load; an absent block reads
 // zeros from a negative coordinate
 __device__ __forceinline__ int block_token(int blk) { return blk >= 0 ? blk * 64 : -128; }
@@ -100,31 +96,6 @@ __device__ __forceinline__ void load_blocks(const int32_t* blk, int n, int (&bk)
 #pragma unroll
     for (int k = 0; k < 16; ++k) bk[k] = k < n ? __ldg(blk + k) : -1;
   }
-}
-
-__device__ __forceinline__ float warp_max_f32(float x) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-// Warp sums of 16 per-lane values: afterwards lane holds the sum over the warp
-// of v[h] for h = head_of_lane(lane) (butterfly reduce-scatter, 16 shuffles).
-__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
-#pragma unroll
-  for (int m = 16, n = 8; m >= 2; m >>= 1, n >>= 1) {
-    const bool up = (lane & m) != 0;
-#pragma unroll
-    for (int k = 0; k < n; ++k) {
-      const float send = up ? v[k] : v[k + n];
-      const float keep = up ? v[k + n] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-    }
-  }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-__device__ __forceinline__ int head_of_lane(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
 
 // kMulti: query rows at positions qoff + row against head-major caches (a
