@@ -57,6 +57,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel in the stream ends; it
+// must call pdl_wait() before it reads anything that kernel writes (without
+// the launch attribute both are no-ops)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // thread-block clusters and distributed shared memory
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {

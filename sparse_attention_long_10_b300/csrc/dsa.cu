@@ -18,8 +18,10 @@
 //               and candidates move through distributed shared memory.
 //   dsa_attn    softmax(q K_sel^T * scale) V_sel over the kept positions on
 //               tcgen05: rows gathered by TMA tile::gather4, split over CTAs of
-//               128 kept positions, each leaving (max, sum, O);
+//               64 kept positions (two per SM), each leaving (max, sum, O);
 //   dsa_merge   merges a row's splits, one CTA per (head, row).
+#include <utility>
+
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -30,7 +32,8 @@ namespace nsa {
 
 namespace {
 
-constexpr int kIdxThreads = 160;    // 4 compute warps + 1 TMA producer warp
+constexpr int kIdxWarps = 8;        // compute warps: 16 keys of each tile each
+constexpr int kIdxThreads = 32 * (kIdxWarps + 1);   // + 1 TMA producer warp
 constexpr int kIdxTile = 128;       // keys per indexer tile
 constexpr int kIdxStages = 4;
 constexpr int kIdxPartMax = 4096;   // most positions per indexer CTA
@@ -119,10 +122,11 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   const int npos = min(a.idx_part, rg.T - s0);
   const int ntiles = npos > 0 ? (npos + kIdxTile - 1) / kIdxTile : 0;
   const int warp = warp_id(), lane = lane_id();
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kIdxStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 4);
+      mbar_init(&bars->empty[s], kIdxWarps);
     }
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
@@ -130,7 +134,7 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
   for (int i = threadIdx.x; i < kBins; i += kIdxThreads) hs[i] = 0;
   __syncthreads();
   bool ok = *abort_flag == 0;
-  if (warp == 4) {
+  if (warp == kIdxWarps) {
     if (lane == 0 && ok) {
       tma_prefetch_desc(&mapKI);
       int i = 0;
@@ -166,9 +170,8 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
       const int slot = i % kIdxStages;
       if (!mbar_wait(&bars->full[slot], (uint32_t)((i / kIdxStages) & 1), abort_flag, a.st, 502)) break;
       const uint32_t base = smem_u32(smem + slot * kStage);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int r0 = warp * 32 + mt * 16;
+      {
+        const int r0 = warp * 16;
         float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < DI / 16; ++ks) {
@@ -182,19 +185,18 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
         float sb = w0 * fmaxf(c[2], 0.f) + w1 * fmaxf(c[3], 0.f);
         sa = quad_sum(sa);
         sb = quad_sum(sb);
-        // lanes with tq == 0 own keys r0+gq and r0+gq+8; equal bins within the
-        // warp are counted with one shared-memory atomic
+        // lanes with tq == 0 own keys r0+gq and r0+gq+8
         const int pa = s0 + i * kIdxTile + r0 + gq, pb = pa + 8;
-        const uint32_t ka = order_key(sa), kb = order_key(sb);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int pos = e ? pb : pa;
-          const uint32_t key = e ? kb : ka;
-          const bool mine = tq == 0 && pos < rg.T;
-          if (mine) a.keys[(size_t)b * a.kstride + pos] = key;
-          const uint32_t bin = mine ? (key >> 20) : 0xffffffffu;
-          const unsigned same = __match_any_sync(0xffffffffu, bin);
-          if (mine && (__ffs(same) - 1) == lane) atomicAdd(&hs[bin], (uint32_t)__popc(same));
+        if (tq == 0) {
+          const uint32_t ka = order_key(sa), kb = order_key(sb);
+          if (pa < rg.T) {
+            a.keys[(size_t)b * a.kstride + pa] = ka;
+            atomicAdd(&hs[ka >> 20], 1u);
+          }
+          if (pb < rg.T) {
+            a.keys[(size_t)b * a.kstride + pb] = kb;
+            atomicAdd(&hs[kb >> 20], 1u);
+          }
         }
       }
       __syncwarp();
@@ -426,6 +428,9 @@ __global__ void __launch_bounds__(kSelThreads) dsa_select_kernel(const DsaArgs a
     fence_barrier_init();
   }
   if (t < kSelCluster) sh.pre[t] = 0;
+  pdl_launch_dependents();
+  // the keys and the histogram come from the indexer
+  pdl_wait();
   __syncthreads();
   // chunk c of the share (with the first, the histogram), copied in whole
   // 16-byte groups (the row stride is a multiple of 64 keys, so the copy stays
@@ -684,21 +689,24 @@ __global__ void __launch_bounds__(kSelThreads) dsa_select_kernel(const DsaArgs a
 }
 
 // ============================================================ attention (tcgen05)
-// One CTA = 128 kept positions of one row: the gather-attention design of the
-// selected-block branch, with keys as the M = 128 side and the (up to 16)
-// heads as N:
+// One CTA = 64 kept positions of one row, two CTAs per SM: the gather-attention
+// design of the selected-block branch, with keys as the M side and the (up to
+// 16) heads as N:
 //     S^T[key, head] = K_sel[key, :] . q[head, :]           (dk/64 chunks x 4 MMAs)
 //     exact softmax of the tile per head (max, exp, sum), P^T bf16 in smem
-//     O^T[dv, head] = V_sel^T[dv, key] . P^T[key, head]     (dv/128 tiles x 8 MMAs)
+//     O^T[dv, head] = V_sel^T[dv, key] . P^T[key, head]     (dv/128 tiles x 4 MMAs)
 // The kept rows are gathered four at a time by TMA tile::gather4 into the
 // 128-byte-swizzled K-major layout the MMAs read; every 64-column chunk of the
-// tile's keys stays resident.  Values reuse the key slots once the QK^T MMAs
-// have drained them (latent KV: the first dv/64 key chunks are the values, so
-// nothing more is fetched).  The tile's (max, sum, O^T) goes to the merge.
-constexpr int kTcThreads = 192;         // warps 0-3 softmax + epilogue, 4 gather, 5 MMA issuer
-constexpr int kTcKeys = 128;            // kept positions per CTA
+// tile's keys stays resident, 8 KB apart.  The QK^T MMAs keep M = 128: rows
+// 64..127 of a chunk's operand are the next chunk's rows (the last chunk is
+// followed by a spare slot), and their S^T lanes are never read.  Values reuse
+// the key slots once the QK^T MMAs have drained them (latent KV: the first
+// dv/64 key chunks are the values, so nothing more is fetched).  The tile's
+// (max, sum, O^T) goes to the merge.
+constexpr int kTcThreads = 192;         // warps 0-1 softmax, 0-3 epilogue, 4 gather, 5 MMA issuer
+constexpr int kTcKeys = 64;             // kept positions per CTA
 constexpr int kTcMaxChunks = 10;        // resident 64-column chunks: dk <= 640
-constexpr int kTcChunk = kTcKeys * 128; // 16 KB
+constexpr int kTcChunk = kTcKeys * 128; // 8 KB
 
 struct TcBars {
   uint64_t q_full;
@@ -706,7 +714,7 @@ struct TcBars {
   uint64_t v_full;
   uint64_t s_full;     // QK^T done: softmax may read S^T
   uint64_t qk_done;    // QK^T done: the gather may overwrite key slots with values
-  uint64_t p_full;     // P^T written (4 softmax warps)
+  uint64_t p_full;     // P^T written (2 softmax warps)
   uint64_t o_full;
   uint64_t wg;         // softmax warps' rendezvous
   uint64_t drain;
@@ -722,19 +730,21 @@ __host__ __device__ inline int tc_value_chunks(int dv) { return dv / 64 < 2 ? 2 
 
 __host__ __device__ inline TcLayout tc_layout(int dk, int dv) {
   const int nk = dk / 64;
-  const int nslots = nk > tc_value_chunks(dv) ? nk : tc_value_chunks(dv);
+  // key chunks (or value chunks, padded to a pair) plus the spare slot the
+  // last chunk's M = 128 operand reads into
+  const int nslots = (nk > tc_value_chunks(dv) ? nk : tc_value_chunks(dv)) + 1;
   TcLayout L;
   L.k_off = (uint32_t)(((nk * 2048) + 1023) / 1024 * 1024);   // q: nk chunks of 16 rows x 128 B
-  L.p_off = L.k_off + (uint32_t)nslots * kTcChunk;              // P^T: 2 chunks of 16 rows x 128 B
-  L.red_off = L.p_off + 4096;                                   // [2 m/l][4 warps][16] floats
-  L.rows_off = L.red_off + 2 * 4 * 16 * 4;                      // [128] gathered row indices
+  L.p_off = L.k_off + (uint32_t)nslots * kTcChunk;              // P^T: 16 rows x 128 B
+  L.red_off = L.p_off + 2048;                                   // [2 m/l][2 warps][16] floats
+  L.rows_off = L.red_off + 2 * 2 * 16 * 4;                      // [64] gathered row indices
   L.bar_off = L.rows_off + kTcKeys * 4;
   L.total = L.bar_off + 256 + 1024;                             // + alignment slack
   return L;
 }
 
-// Four rows (global row indices r0..r3, out of range reads zeros) of 64
-// columns starting at column col, into 4 consecutive 128-byte swizzled rows.
+// Four rows (global row indices r0..r3) of 64 columns starting at column col,
+// into 4 consecutive 128-byte swizzled rows.
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int col, int r0, int r1,
                                             int r2, int r3) {
   asm volatile(
@@ -745,19 +755,20 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
 }
 
 template <int DV>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     dsa_attn_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                     const __grid_constant__ CUtensorMap mapV, const DsaArgs a) {
   constexpr int kVC = DV / 64 < 2 ? 2 : DV / 64;   // value chunks, padded to one M = 128 pair
   constexpr int kVT = kVC / 2;                        // 128-row value tiles
+  constexpr int kG4 = kTcKeys / 4;                    // gather4 copies per chunk
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const TcLayout L = tc_layout(a.dk, DV);
   uint8_t* qs = smem;
   uint8_t* ks = smem + L.k_off;
   uint8_t* ps = smem + L.p_off;
-  float* red_m = reinterpret_cast<float*>(smem + L.red_off);   // [4][16]
-  float* red_l = red_m + 64;                                     // [4][16]
+  float* red_m = reinterpret_cast<float*>(smem + L.red_off);   // [2][16]
+  float* red_l = red_m + 32;                                     // [2][16]
   int* rows_s = reinterpret_cast<int*>(smem + L.rows_off);
   TcBars* bars = reinterpret_cast<TcBars*>(smem + L.bar_off);
   volatile int* abort_flag = &bars->abort_flag;
@@ -777,34 +788,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = threadIdx.x; i < 16 * DV; i += kTcThreads) a.po[pb * 16 * DV + i] = 0.f;
     return;
   }
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    for (int c = 0; c < kTcMaxChunks; ++c) mbar_init(&bars->k_full[c], 1);
-    mbar_init(&bars->v_full, 1);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->qk_done, 1);
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->wg, 4);
-    mbar_init(&bars->drain, 1);
-    bars->abort_flag = prior_error(a.st);
-    fence_barrier_init();
-  }
+  pdl_launch_dependents();
   // query rows H..15 are never loaded: keep them finite (zero)
   if (a.H < 16)
     for (int i = threadIdx.x; i < nk * 2048 / 16; i += kTcThreads) {
       const int row = (i % 128) / 8;
       if (row >= a.H) reinterpret_cast<uint4*>(qs)[i] = make_uint4(0, 0, 0, 0);
     }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int c = 0; c < kTcMaxChunks; ++c) mbar_init(&bars->k_full[c], 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->qk_done, 1);
+    mbar_init(&bars->p_full, 2);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->wg, 2);
+    mbar_init(&bars->drain, 1);
+    fence_barrier_init();
+    // the query is an input: its load overlaps the previous kernel's tail
+    tma_prefetch_desc(&mapQ);
+    tma_prefetch_desc(&mapK);
+    mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(nk * a.H * 128));
+    for (int c = 0; c < nk; ++c) tma_load_2d(qs + c * 2048, &mapQ, &bars->q_full, c * 64, b * a.H);
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 128);
+    tmem_relinquish();
+  }
+  // the kept positions and the status come from the previous kernels
+  pdl_wait();
+  if (threadIdx.x == 0) bars->abort_flag = prior_error(a.st);
   // the tile's global row indices; entries past the row's last kept position
   // repeat its first one (finite data, masked out of the softmax)
   const int32_t* sel = a.idx + (size_t)b * a.kk + e0;
   for (int j = threadIdx.x; j < kTcKeys; j += kTcThreads) rows_s[j] = b * a.T + __ldg(sel + (j < nent ? j : 0));
   fence_proxy_async_smem();
-  if (warp == 0) {
-    tmem_alloc(&bars->tmem, 128);
-    tmem_relinquish();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -812,21 +831,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   bool ok = *abort_flag == 0;
 
   if (!ok) {
-    // an earlier CTA failed: do nothing
+    // an earlier CTA failed: only the query load is in flight
+    if (threadIdx.x == 0) mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
   } else if (warp == 4) {
     // ============================================================ gather (one warp)
-    // lane 0 arms every barrier; lane j then gathers rows 4j .. 4j+3 of each chunk
-    if (lane == 0) {
-      tma_prefetch_desc(&mapQ);
-      tma_prefetch_desc(&mapK);
-      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(nk * a.H * 128));
-      for (int c = 0; c < nk; ++c) tma_load_2d(qs + c * 2048, &mapQ, &bars->q_full, c * 64, b * a.H);
+    // lane 0 arms every barrier; lane j < kG4 then gathers rows 4j .. 4j+3 of each chunk
+    if (lane == 0)
       for (int c = 0; c < nk; ++c) mbar_arrive_expect_tx(&bars->k_full[c], kTcChunk);
-    }
     __syncwarp();
-    const int4 rw = *reinterpret_cast<const int4*>(rows_s + 4 * lane);
-    for (int c = 0; c < nk; ++c)
-      tma_gather4(ks + c * kTcChunk + lane * 512, &mapK, &bars->k_full[c], c * 64, rw.x, rw.y, rw.z, rw.w);
+    int4 rw = make_int4(0, 0, 0, 0);
+    if (lane < kG4) rw = *reinterpret_cast<const int4*>(rows_s + 4 * lane);
+    if (lane < kG4)
+      for (int c = 0; c < nk; ++c)
+        tma_gather4(ks + c * kTcChunk + lane * 512, &mapK, &bars->k_full[c], c * 64, rw.x, rw.y, rw.z, rw.w);
     bool vok = true;
     if (!a.v_from_k) {
       // the value chunks overwrite key slots 0 .. DV/64-1 once QK^T has read them
@@ -835,7 +852,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (vok) mbar_arrive_expect_tx(&bars->v_full, (uint32_t)(DV / 64) * kTcChunk);
       }
       vok = __shfl_sync(0xffffffffu, vok ? 1 : 0, 0) != 0;
-      if (vok)
+      if (vok && lane < kG4)
         for (int c = 0; c < DV / 64; ++c)
           tma_gather4(ks + c * kTcChunk + lane * 512, &mapV, &bars->v_full, c * 64, rw.x, rw.y, rw.z, rw.w);
     }
@@ -876,11 +893,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int t = 0; t < kVT; ++t)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < kTcKeys / 16; ++k) {
             // A = V^T: value columns 128 t .. 128 t + 127 as two 64-column
             // chunks one slot apart, keys 16 k .. 16 k + 15 along K
             const uint64_t ad = sdesc_sw128(k_a + 2 * t * kTcChunk + k * 2048, kTcChunk, 1024);
-            const uint64_t bd = sdesc_sw128(p_a + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(p_a + k * 32, 16, 1024);
             umma_bf16(tmem + 16 + 16 * t, ad, bd, idesc_pv, k > 0 ? 1u : 0u);
           }
         umma_commit(&bars->o_full);
@@ -891,55 +908,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
-    // ============================================================ softmax + epilogue (warps 0-3)
-    const int r = warp * 32 + lane;           // TMEM lane: a key of the tile, later a value row
+    // ============================================================ softmax (warps 0-1) + epilogue (warps 0-3)
+    const int r = warp * 32 + lane;           // TMEM lane: a key of the tile (warps 0-1), a value row
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const bool valid = r < nent;
-    uint32_t wg_phase = 0;
-    auto wg_sync = [&]() {
+    if (warp < 2) {
+      const bool valid = r < nent;
+      uint32_t wg_phase = 0;
+      auto wg_sync = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->wg);
+        if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 536)) ok = false;
+        ++wg_phase;
+      };
+      uint32_t sr[16];
+      if (!mbar_wait(&bars->s_full, 0, abort_flag, a.st, 537)) ok = false;
+      tc_fence_after();
+      tmem_ld16(tmem + lane_base, sr);
+      tmem_ld_wait(sr);
+      float m[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) m[h] = warp_max_f32(valid ? __uint_as_float(sr[h]) * a.sc2 : -INFINITY);
+      if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < 16; ++h) red_m[warp * 16 + h] = m[h];
+      wg_sync();
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        m[h] = fmaxf(red_m[h], red_m[16 + h]);
+        if (m[h] == -INFINITY) m[h] = 0.f;
+      }
+      // p = exp2(s * scale - max) as P^T (bf16, key-major rows of heads), sums
+      float ls[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float e = valid ? fast_exp2(fmaf(__uint_as_float(sr[h]), a.sc2, -m[h])) : 0.f;
+        ls[h] = e;
+        *reinterpret_cast<__nv_bfloat16*>(ps + sw128_offset(h, r >> 3) + (r & 7) * 2) = __float2bfloat16_rn(e);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->wg);
-      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 536)) ok = false;
-      ++wg_phase;
-    };
-    uint32_t sr[16];
-    if (!mbar_wait(&bars->s_full, 0, abort_flag, a.st, 537)) ok = false;
-    tc_fence_after();
-    tmem_ld16(tmem + lane_base, sr);
-    tmem_ld_wait(sr);
-    float m[16];
-#pragma unroll
-    for (int h = 0; h < 16; ++h) m[h] = warp_max_f32(valid ? __uint_as_float(sr[h]) * a.sc2 : -INFINITY);
-    if (lane == 0)
-#pragma unroll
-      for (int h = 0; h < 16; ++h) red_m[warp * 16 + h] = m[h];
-    wg_sync();
-#pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      m[h] = fmaxf(fmaxf(red_m[h], red_m[16 + h]), fmaxf(red_m[32 + h], red_m[48 + h]));
-      if (m[h] == -INFINITY) m[h] = 0.f;
-    }
-    // p = exp2(s * scale - max) as P^T (bf16, key-major rows of heads), sums
-    float ls[16];
-    uint8_t* chunk = ps + (r >> 6) * 2048 + (r & 7) * 2;
-#pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      const float e = valid ? fast_exp2(fmaf(__uint_as_float(sr[h]), a.sc2, -m[h])) : 0.f;
-      ls[h] = e;
-      *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, (r & 63) >> 3)) = __float2bfloat16_rn(e);
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->p_full);
-    const float ws = warp_sum16(ls, lane);
-    if ((lane & 1) == 0) red_l[warp * 16 + head_of_lane(lane)] = ws;
-    wg_sync();
-    if (ok && threadIdx.x < 16) {
-      const int h = threadIdx.x;
-      const float mh = fmaxf(fmaxf(red_m[h], red_m[16 + h]), fmaxf(red_m[32 + h], red_m[48 + h]));
-      a.pm[pb * 16 + h] = mh == -INFINITY ? 0.f : mh;
-      a.pl[pb * 16 + h] = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      const float ws = warp_sum16(ls, lane);
+      if ((lane & 1) == 0) red_l[warp * 16 + head_of_lane(lane)] = ws;
+      wg_sync();
+      if (ok && threadIdx.x < 16) {
+        const int h = threadIdx.x;
+        const float mh = fmaxf(red_m[h], red_m[16 + h]);
+        a.pm[pb * 16 + h] = mh == -INFINITY ? 0.f : mh;
+        a.pl[pb * 16 + h] = red_l[h] + red_l[16 + h];
+      }
     }
     // unnormalised O^T of the tile: lane r holds value row 128 t + r, 16 heads
     if (ok && mbar_wait(&bars->o_full, 0, abort_flag, a.st, 538)) {
@@ -976,6 +994,8 @@ __global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const 
   __shared__ float Ms, iLs;
   __shared__ int s_abort;
   __shared__ float4 part[kMergeGroups - 1][C4];
+  // the partials come from the attention kernel
+  pdl_wait();
   if (threadIdx.x == 0) s_abort = prior_error(a.st);
   __syncthreads();
   if (s_abort) return;
@@ -1080,25 +1100,42 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialisation (the kernel may start before
+// the previous kernel in the stream ends; it waits with pdl_wait() before it
+// reads that kernel's outputs), and optionally as clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+}
+
 int launch_select(const DsaArgs& a, cudaStream_t s) {
   const size_t smem = select_smem();
   if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_select_kernel), smem)) return rc;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kSelCluster, a.B);
-  cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kSelCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   prof::begin("dsa_select", s);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dsa_select_kernel, a);
+  const int rc = launch_dependent(dsa_select_kernel, dim3(kSelCluster, a.B), dim3(kSelThreads), smem, s, kSelCluster, a);
   prof::end(s);
-  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+  return rc;
 }
 
 template <int DV>
@@ -1134,13 +1171,13 @@ int launch_attn(const DsaArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16(&mv, a.v, 2, dims, str, box)) return NSA_ERR_CUDA;
   }
   prof::begin("dsa_attn", s);
-  dsa_attn_kernel<DV><<<dim3(a.attn_ctas, a.B), kTcThreads, smem, s>>>(mq, mk, mv, a);
+  int rc = launch_dependent(dsa_attn_kernel<DV>, dim3(a.attn_ctas, a.B), dim3(kTcThreads), smem, s, 1, mq, mk, mv, a);
   prof::end(s);
-  if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  if (rc != NSA_OK) return rc;
   prof::begin("dsa_merge", s);
-  dsa_merge_kernel<DV><<<dim3(a.H, a.B), DV / 4 * kMergeGroups, 0, s>>>(a);
+  rc = launch_dependent(dsa_merge_kernel<DV>, dim3(a.H, a.B), dim3(DV / 4 * kMergeGroups), 0, s, 1, a);
   prof::end(s);
-  return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+  return rc;
 }
 
 }  // namespace
