@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "nsa.h"
 
@@ -402,6 +403,38 @@ __device__ __forceinline__ int head_of_lane(int lane) {
 // 128-byte-swizzled tile (rows of 128 B, 1024-byte aligned base).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// host: launches with programmatic stream serialisation
+// ---------------------------------------------------------------------------
+// Launch with programmatic stream serialisation (the kernel may start before
+// the previous kernel in the stream ends; it waits with pdl_wait() before it
+// reads that kernel's outputs), and optionally as clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
 }  // namespace nsa

@@ -481,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     return blk >= 0 ? 64 * blk : -1;
   };
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < kRingK; ++i) {
@@ -496,7 +497,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->wg, 4);
     mbar_init(&bars->drain, 1);
-    bars->abort_flag = prior_error(a.st);
     bars->last = 0;
     fence_barrier_init();
   }
@@ -511,6 +511,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the query is an input: its load overlaps the previous kernel's tail
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&mapQ);
+    tma_prefetch_desc(mapK);
+    tma_prefetch_desc(mapV);
+    mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * a.hpg * 128));
+    for (int c = 0; c < kcs; ++c) tma_load_3d(qbuf + c * kQBuf, &mapQ, &bars->q_full, c * 64, g * a.hpg, b);
+  }
+  // the kept blocks, the partials and the status come from the previous kernel
+  pdl_wait();
+  if (threadIdx.x == 0) bars->abort_flag = prior_error(a.st);
+  __syncthreads();
   const uint32_t tmem = bars->tmem;
   const uint32_t tmem_s = tmem;                 // kPairs x NP columns
   const uint32_t tmem_o = tmem + kPairs * NP;   // NP columns
@@ -518,16 +530,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool ok = *abort_flag == 0;
 
   if (!ok) {
-    // an earlier CTA failed: do nothing
+    // an earlier CTA failed: only the query load is in flight
+    if (threadIdx.x == 0) mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
   } else if (warp == 4) {
     // =============================================================== producer
     if (lane == 0) {
-      tma_prefetch_desc(&mapQ);
-      tma_prefetch_desc(mapK);
-      tma_prefetch_desc(mapV);
       int kv = 0, vv = 0;
-      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kcs * a.hpg * 128));
-      for (int c = 0; c < kcs; ++c) tma_load_3d(qbuf + c * kQBuf, &mapQ, &bars->q_full, c * 64, g * a.hpg, b);
       for (int p = 0; p < npairs && ok; ++p) {
         const int r0 = block_row(p, 0), r1 = block_row(p, 1);
         for (int c = 0; c < kcs; ++c) {
@@ -847,9 +855,17 @@ int launch_one(const DecArgs& a, dim3 grid, const CUtensorMap* maps, uint32_t sm
                const char* name) {
   if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dec_kernel<DK, DV, MODE>), smem_max())) return rc;
   prof::begin(name, s);
-  dec_kernel<DK, DV, MODE><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+  int rc = NSA_OK;
+  if (MODE == 0) {
+    dec_kernel<DK, DV, MODE><<<grid, kThreads, smem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    rc = cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+  } else {
+    // may start while the compressed / window kernel finishes (pdl_wait)
+    rc = launch_dependent(dec_kernel<DK, DV, MODE>, grid, dim3(kThreads), smem, s, 1, maps[0], maps[1], maps[2],
+                          maps[3], maps[4], a);
+  }
   prof::end(s);
-  return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
+  return rc;
 }
 
 template <int DK, int DV>

@@ -20,8 +20,6 @@
 //               tcgen05: rows gathered by TMA tile::gather4, split over CTAs of
 //               64 kept positions (two per SM), each leaving (max, sum, O);
 //   dsa_merge   merges a row's splits, one CTA per (head, row).
-#include <utility>
-
 #include "common.cuh"
 #include "kernels.hpp"
 #include "profiler.hpp"
@@ -1098,35 +1096,6 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
   dsa_index_kernel<DI><<<dim3((a.T + a.idx_part - 1) / a.idx_part, a.B), kIdxThreads, smem, s>>>(map, a);
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
-}
-
-// Launch with programmatic stream serialisation (the kernel may start before
-// the previous kernel in the stream ends; it waits with pdl_wait() before it
-// reads that kernel's outputs), and optionally as clusters of cluster_x CTAs.
-template <typename... KArgs, typename... Args>
-int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_x,
-                     Args&&... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int n = 0;
-  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[n].val.programmaticStreamSerializationAllowed = 1;
-  ++n;
-  if (cluster_x > 1) {
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)cluster_x;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = (unsigned)n;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;
 }
 
 int launch_select(const DsaArgs& a, cudaStream_t s) {
