@@ -158,19 +158,19 @@ def whole_job_rate(units_per_rank: float, ms_max: float, ws: int) -> float:
 # (sha256 prefix of the listed files); otherwise the bench line says null.
 _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
-    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "daee54b7ef57bd80",
-                "bytes": (1858.56 + 2115.71) * 1e6, "how": "full-size capture (one pass)"},
-    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "14a40cd57cf681c4",
-            "bytes": (4426.66 + 1073.95) * 1e6, "how": "full-size capture (one pass)"},
+    "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "e959ad480b14df14",
+                "bytes": (1857.92 + 2115.24) * 1e6, "how": "full-size capture (one pass)"},
+    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "2ebb744aa7a991a6",
+            "bytes": (4453.29 + 1072.77) * 1e6, "how": "full-size capture (one pass)"},
     # both kernels of one decode step
-    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "bb2bfdd8c4b6194f",
-               "bytes": (189.27 + 10.00 + 52.02 + 0.01) * 1e6, "how": "full-size capture, both kernels"},
-    # the five kernels of one DSA step (captured before per-row context lengths)
-    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "recapture-needed",
-            "bytes": (134.39 + 4.10 + 4.25 + 4.21 + 35.90 + 8.43) * 1e6, "how": "full-size capture, five kernels"},
-    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "recapture-needed",
-                   "bytes": (134.38 + 4.10 + 4.25 + 4.21 + 19.12 + 8.44) * 1e6,
-                   "how": "full-size capture, five kernels"},
+    "decode": {"files": ["decode.cu", "common.cuh"], "sha": "e50108f99388e6fe",
+               "bytes": (189.29 + 9.81 + 52.01 + 0.01) * 1e6, "how": "full-size capture, both kernels"},
+    # the four kernels of one DSA step
+    "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "a56a44edfcb094ac",
+            "bytes": (134.25 + 4.61 + 4.40 + 36.96 + 8.43) * 1e6, "how": "full-size capture, four kernels"},
+    "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "a56a44edfcb094ac",
+                   "bytes": (134.25 + 3.98 + 4.40 + 20.18 + 8.44) * 1e6,
+                   "how": "full-size capture, four kernels"},
 }
 
 def ncu_traffic(key: str):
@@ -658,7 +658,7 @@ def run_dsa_leg(args, ws, latent=False):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
                      "frac": gbs / pk["hbm"], "peak_kind": f"HBM copy ({pk['src']})",
                      "traffic": ncu_traffic("dsa_latent" if latent else "dsa"),
-                     "note": "whole step (memset + 5 kernels, CUDA graph replay), L2 flushed before each step; "
+                     "note": "whole step (memset + 4 kernels, CUDA graph replay), L2 flushed before each step; "
                              "traffic: " + NCU_TRAFFIC["dsa_latent" if latent else "dsa"]["how"]},
         "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
                     for k, (c, t) in prof.items()},
