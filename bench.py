@@ -33,8 +33,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from workloads import NSAParams, PREFILL_CONFIGS, decode_config, dsa_config, make_prefill, \
-    make_decode, make_dsa  # noqa: E402
+from workloads import NSAParams, PREFILL_CONFIGS, decode_config, dsa_config, dsa_prefill_config, \
+    make_prefill, make_decode, make_dsa, make_dsa_prefill  # noqa: E402
 
 PARAMS = NSAParams()
 
@@ -577,6 +577,95 @@ def run_decode_multi_leg(args, ws, m=4):
 
 
 # ---------------------------------------------------------------- DSA decode leg
+def run_dsa_prefill_leg(args, ws):
+    """DSA over a whole sequence: one 8,192-token sequence, every position a
+    query with its own indexer query and weights, keeping min(2048, t+1)
+    positions of its causal prefix; latent keys (576 columns, the first 512
+    are the values)."""
+    import sparse_attention_long_10_b300 as nsa
+    wl = dsa_prefill_config()
+    inp = make_dsa_prefill(wl)
+    inp["v"] = None
+    dev = {k: v.cuda() for k, v in inp.items() if v is not None}
+    cfg = nsa.make_dsa_cfg(wl.B, wl.T, wl.HI, wl.dI, wl.H, wl.dk, wl.dv, wl.topk)
+    out = torch.empty(wl.B, wl.T, wl.H, wl.dv, dtype=torch.bfloat16, device="cuda")
+    wsp = nsa.workspace(nsa.dsa_prefill_workspace_size(cfg))
+
+    def step():
+        nsa.dsa_prefill_fwd(cfg, dev["qI"], dev["wI"], dev["kI"], dev["q"], dev["k"], None, out, None, wsp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("dsa prefill: device status set during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    flush = L2Flush()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = max_over_ranks(statistics.mean(time_graph_steps(graph, args.steps, flush)), ws)
+    if nsa.nsa_device_status(wsp) != 0:
+        raise RuntimeError("dsa prefill: device status set in the timed region")
+    nsa.nsa_profile_enable(True)
+    for _ in range(args.steps):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    prof = nsa.nsa_profile_read()
+    nsa.nsa_profile_enable(False)
+    # end to end: the sequence's inputs in, out back
+    host = {k: inp[k].pin_memory() for k in ("qI", "wI", "kI", "q", "k")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step_e2e():
+        for k, t in host.items():
+            dev[k].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    e_times = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step_e2e()
+        e1.record()
+        e_times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e_times), ws)
+    # useful work: the indexer over every causal prefix, the attention over the kept positions
+    t1 = torch.arange(1, wl.T + 1, dtype=torch.float64)
+    idx_flop = float(t1.sum()) * wl.HI * wl.dI * 2 * wl.B
+    att_flop = float(torch.clamp(t1, max=wl.topk).sum()) * wl.H * (wl.dk + wl.dv) * 2 * wl.B
+    pk = peaks()
+    tf = (idx_flop + att_flop) / (ms * 1e-3) / 1e12
+    return {
+        "metric": "DSA prefill (1 x 8,192 tokens, every position a query, top-2048, latent KV)",
+        "value": wl.B * wl.T / (ms * 1e-3), "unit": "tokens/s", "higher_is_better": True,
+        "ms_per_step": ms, "workload": wl.name, "steps": args.steps, "l2_flush": L2_FLUSH_NOTE,
+        "useful_tflop_per_step": (idx_flop + att_flop) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                     "frac": tf / pk["bf16_sus"], "peak_kind": f"bf16 dense sustained ({pk['src']})",
+                     "traffic": None,
+                     "note": "indexer + attention FLOPs over the step (memset + 4 kernels, CUDA graph replay); "
+                             "the attention's MMAs have N = 16 heads"},
+        "kernels": {k: {"launches_per_step": c / args.steps, "us_per_step": 1e3 * t / args.steps}
+                    for k, (c, t) in prof.items()},
+        "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
+        "e2e": {"value": wl.B * wl.T / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+    }
+
+
 def run_dsa_leg(args, ws, latent=False):
     """One DSA-style decode step: batch 8, 131,072-token context, indexer of 4
     heads x 64 dims, top-2048 positions, attention of 16 heads (dk=576,
@@ -677,9 +766,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and DSA decode legs")
     ap.add_argument("--workload", default="prefill_64k",
-                    choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k", "dsa_latent_128k"],
+                    choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k", "dsa_latent_128k",
+                                                       "dsa_prefill_8k"],
                     help="prefill workload (the headline is prefill_64k; smaller ones serve profiling) or "
-                         "decode_64k / dsa_128k: one decode leg alone")
+                         "decode_64k / dsa_128k / dsa_latent_128k / dsa_prefill_8k: one of the other legs alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, _ = dist_setup()
@@ -706,9 +796,11 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
-    if args.workload in ("decode_64k", "dsa_128k", "dsa_latent_128k"):
+    if args.workload in ("decode_64k", "dsa_128k", "dsa_latent_128k", "dsa_prefill_8k"):
         if args.workload == "decode_64k":
             res = run_decode_leg(args, ws)
+        elif args.workload == "dsa_prefill_8k":
+            res = run_dsa_prefill_leg(args, ws)
         else:
             res = run_dsa_leg(args, ws, latent=args.workload == "dsa_latent_128k")
         if rank == 0:
@@ -724,6 +816,8 @@ def main():
         res["gpu_launches"] += res["dsa"]["gpu_launches_per_step"] * args.steps
         res["dsa_latent"] = run_dsa_leg(args, ws, latent=True)
         res["gpu_launches"] += res["dsa_latent"]["gpu_launches_per_step"] * args.steps
+        res["dsa_prefill"] = run_dsa_prefill_leg(args, ws)
+        res["gpu_launches"] += res["dsa_prefill"]["gpu_launches_per_step"] * args.steps
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         blas, ncpu = cpu_cores()
         rate, info = oracle_prefill_rate(inp, rows_per_step=16, steps=2)

@@ -285,6 +285,28 @@ int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const vo
                     const void* q, const void* k, const void* v, const int32_t* seq_lens,
                     void* out, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * dsa_prefill_fwd -- DSA over whole sequences [P4, "쉽게 이해하기": the
+ * selection is made independently for every query token]: every position t of
+ * sequence b is a query with its own indexer query and weights, scoring and
+ * keeping among its causal prefix s <= t (itself included):
+ *   I[b,t,s]   = sum_h wI[b,t,h] * max(0, qI[b,t,h,:] . kI[b,s,:])     s <= t
+ *   keep(b,t)  = the min(topk, t+1) positions of largest fp32 I, ties to the lower s
+ *   out[b,t,h] = softmax_{s in keep}(q[b,t,h,:] . k[b,s,:] * scale) @ v[b,keep,:]
+ *   qI [B,T,HI,dI]   wI [B,T,HI]   kI [B,T,dI]   q [B,T,H,dk]   k [B,T,dk]
+ *   v [B,T,dv] (or NULL: the first dv columns of k, as in dsa_decode_step)
+ *   out [B,T,H,dv]
+ *   idx_out (nullable): [B,T,min(topk,T)] int32, ascending, -1 past min(topk,t+1)
+ *   ws     : dsa_prefill_workspace_size(cfg) bytes
+ * The rows run through the decode step's kernels (row b*T + t reads the keys
+ * of sequence b with context t+1), so B*T <= 65535 and the shapes of
+ * dsa_decode_step apply; anything else returns NSA_ERR_UNSUPPORTED.
+ */
+size_t dsa_prefill_workspace_size(const dsa_cfg* cfg);
+int dsa_prefill_fwd(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI,
+                    const void* q, const void* k, const void* v, void* out, int32_t* idx_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- profiling */
 /* No counterpart on the pages: measurement support.  When enabled, every
    kernel launch of the library is bracketed by two CUDA events on its

@@ -72,6 +72,9 @@ def _load() -> ctypes.CDLL:
         "nsa_prefill_workspace_size": (_c_size, [P(NsaCfg)]),
         "nsa_decode_workspace_size": (_c_size, [P(NsaCfg)]),
         "dsa_decode_workspace_size": (_c_size, [P(DsaCfg)]),
+        "dsa_prefill_workspace_size": (_c_size, [P(DsaCfg)]),
+        "dsa_prefill_fwd": (_c_int, [P(DsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     _c_vp, _c_size, _c_vp]),
         "nsa_compress_kv": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_size,
                                      _c_vp]),
         "nsa_prefill_fwd": (_c_int, [P(NsaCfg), _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -250,6 +253,18 @@ def dsa_decode_step(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=N
                                _ptr(v), _ptr(seq_lens), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "dsa_decode_step")
+
+
+def dsa_prefill_workspace_size(cfg: DsaCfg) -> int:
+    return _lib().dsa_prefill_workspace_size(ctypes.byref(cfg))
+
+
+def dsa_prefill_fwd(cfg: DsaCfg, qI, wI, kI, q, k, v, out, idx_out, ws, stream=None):
+    """Every position of every sequence a query; v None: latent values."""
+    _check(_lib().dsa_prefill_fwd(ctypes.byref(cfg), _ptr(qI), _ptr(wI), _ptr(kI), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(out), _ptr(idx_out), _ptr(ws),
+                               ws.numel() if ws is not None else 0, _stream(stream)),
+           "dsa_prefill_fwd")
 
 
 def nsa_device_status(ws, stream=None) -> int:

@@ -356,6 +356,38 @@ int dsa_decode_step(const dsa_cfg* cfg, const void* qI, const void* wI, const vo
   return launch_dsa(*cfg, qI, wI, kI, q, k, v, seq_lens, out, idx_out, static_cast<uint8_t*>(ws), s);
 }
 
+// The prefill form runs the decode kernels over B*T query rows.
+static bool prefill_rows_cfg(const dsa_cfg* cfg, dsa_cfg* rows) {
+  if (cfg == nullptr || cfg->B < 1 || cfg->T < 1 || (long long)cfg->B * cfg->T > 65535) return false;
+  *rows = *cfg;
+  rows->B = cfg->B * cfg->T;
+  return true;
+}
+
+size_t dsa_prefill_workspace_size(const dsa_cfg* cfg) {
+  dsa_cfg rc;
+  if (!prefill_rows_cfg(cfg, &rc) || validate_dsa(&rc) != NSA_OK) return 0;
+  return dsa_ws_bytes(rc);
+}
+
+int dsa_prefill_fwd(const dsa_cfg* cfg, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
+                    const void* v, void* out, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = validate_dsa(cfg);
+  if (rc != NSA_OK) return rc;
+  dsa_cfg rows;
+  if (!prefill_rows_cfg(cfg, &rows)) return NSA_ERR_UNSUPPORTED;
+  if ((rc = validate_dsa(&rows)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({qI, wI, kI, q, k, out})) != NSA_OK) return rc;
+  // v == NULL: values are the first dv columns of the key rows (latent KV)
+  if (v == nullptr ? cfg->dv > cfg->dk : !aligned16(v)) return v == nullptr ? NSA_ERR_INVALID_ARG : NSA_ERR_MISALIGNED;
+  if (idx_out != nullptr && !aligned16(idx_out)) return NSA_ERR_MISALIGNED;
+  if ((rc = check_ws(ws, ws_bytes, dsa_ws_bytes(rows))) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, dsa_zero_bytes(rows), s) != cudaSuccess) return NSA_ERR_CUDA;
+  return launch_dsa(rows, qI, wI, kI, q, k, v, nullptr, out, idx_out, static_cast<uint8_t*>(ws), s, cfg->T);
+}
+
 int nsa_device_status(void* ws, void* stream) {
   if (ws == nullptr) return NSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

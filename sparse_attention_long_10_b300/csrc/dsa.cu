@@ -40,7 +40,9 @@ constexpr int kSelThreads = 512;
 constexpr int kCandCap = 4096;      // boundary-bin candidates resolved in shared memory per row
 
 struct DsaArgs {
-  int B, T, HI, dI, H, dk, dv, kk;  // T: context capacity; kk = min(topk, T) (row stride of idx)
+  int B, T, HI, dI, H, dk, dv, kk;  // B: query rows; T: context capacity; kk = min(topk, T) (row stride of idx)
+  int nseq;                         // sequences whose keys the rows read
+  int rows_per_seq;                 // 1: one query per sequence (decode); T: every position (prefill)
   int topk;
   const int32_t* lens;              // nullable [B]: context length of each row (query at len-1)
   int idx_part;                     // positions per indexer CTA (a multiple of kIdxTile)
@@ -81,10 +83,15 @@ struct RowGeom {
   int T, kk, all;
 };
 __device__ __forceinline__ RowGeom row_geom(const DsaArgs& a, int b, DeviceStatus* st) {
-  int T = a.lens != nullptr ? __ldg(a.lens + b) : a.T;
-  if (T < 1 || T > a.T) {
-    record_arg_error(st, NSA_ERR_INVALID_ARG, 500);
-    T = 0;
+  int T;
+  if (a.rows_per_seq > 1) {
+    T = b % a.rows_per_seq + 1;   // prefill: row b is position b mod T of its sequence
+  } else {
+    T = a.lens != nullptr ? __ldg(a.lens + b) : a.T;
+    if (T < 1 || T > a.T) {
+      record_arg_error(st, NSA_ERR_INVALID_ARG, 500);
+      T = 0;
+    }
   }
   RowGeom r;
   r.T = T;
@@ -146,7 +153,8 @@ __global__ void __launch_bounds__(kIdxThreads, 2)
         mbar_arrive_expect_tx(&bars->full[slot], kStage);
 #pragma unroll
         for (int c = 0; c < KB; ++c)
-          tma_load_3d(dst + c * kIdxTile * 128, &mapKI, &bars->full[slot], c * 64, s0 + i * kIdxTile, b);
+          tma_load_3d(dst + c * kIdxTile * 128, &mapKI, &bars->full[slot], c * 64, s0 + i * kIdxTile,
+                      b / a.rows_per_seq);
       }
       if (!ok || *abort_flag)
         for (int y = (i > kIdxStages ? i - kIdxStages : 0); y < i; ++y)
@@ -777,15 +785,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int e0 = x * kTcKeys;
   const int nent = min(kTcKeys, rg.kk - e0);
   const size_t pb = (size_t)b * a.attn_ctas + x;
-  if (nent <= 0) {
-    // a row that keeps fewer positions than this tile starts at: empty partial
-    if (threadIdx.x < 16) {
-      a.pm[pb * 16 + threadIdx.x] = -INFINITY;
-      a.pl[pb * 16 + threadIdx.x] = 0.f;
-    }
-    for (int i = threadIdx.x; i < 16 * DV; i += kTcThreads) a.po[pb * 16 * DV + i] = 0.f;
-    return;
-  }
+  // a row that keeps fewer positions than this tile starts at has no
+  // partial here (the merge reads only a row's own tiles)
+  if (nent <= 0) return;
   pdl_launch_dependents();
   // query rows H..15 are never loaded: keep them finite (zero)
   if (a.H < 16)
@@ -820,7 +822,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // the tile's global row indices; entries past the row's last kept position
   // repeat its first one (finite data, masked out of the softmax)
   const int32_t* sel = a.idx + (size_t)b * a.kk + e0;
-  for (int j = threadIdx.x; j < kTcKeys; j += kTcThreads) rows_s[j] = b * a.T + __ldg(sel + (j < nent ? j : 0));
+  const int seq_row0 = (b / a.rows_per_seq) * a.T;   // the sequence's first key row
+  for (int j = threadIdx.x; j < kTcKeys; j += kTcThreads) rows_s[j] = seq_row0 + __ldg(sel + (j < nent ? j : 0));
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -988,7 +991,8 @@ template <int DV>
 __global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const DsaArgs a) {
   constexpr int C4 = DV / 4;            // float4 columns
   const int h = blockIdx.x, b = blockIdx.y;
-  const int NC = a.attn_ctas;
+  const int NC = a.attn_ctas;                                   // partial stride per row
+  const int NR = (row_geom(a, b, nullptr).kk + kTcKeys - 1) / kTcKeys;   // this row's partials
   __shared__ float Ms, iLs;
   __shared__ int s_abort;
   __shared__ float4 part[kMergeGroups - 1][C4];
@@ -1001,12 +1005,12 @@ __global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const 
   const float* pl = a.pl + (size_t)b * NC * 16 + h;
   if (threadIdx.x < 32) {
     float M = -INFINITY;
-    for (int c = threadIdx.x; c < NC; c += 32) M = fmaxf(M, __ldcg(pm + (size_t)c * 16));
+    for (int c = threadIdx.x; c < NR; c += 32) M = fmaxf(M, __ldcg(pm + (size_t)c * 16));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Mu = M == -INFINITY ? 0.f : M;
     float L = 0.f;
-    for (int c = threadIdx.x; c < NC; c += 32)
+    for (int c = threadIdx.x; c < NR; c += 32)
       L += __ldcg(pl + (size_t)c * 16) * fast_exp2(__ldcg(pm + (size_t)c * 16) - Mu);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -1019,14 +1023,14 @@ __global__ void __launch_bounds__(DV / 4 * kMergeGroups) dsa_merge_kernel(const 
   const int col = threadIdx.x % C4, grp = threadIdx.x / C4;
   const float* po = a.po + ((size_t)b * NC * 16 + h) * DV + 4 * col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c0 = grp * 8; c0 < NC; c0 += 8 * kMergeGroups) {
+  for (int c0 = grp * 8; c0 < NR; c0 += 8 * kMergeGroups) {
     float4 v[8];
     float f[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = c0 + k;
-      v[k] = c < NC ? __ldcg(reinterpret_cast<const float4*>(po + (size_t)c * 16 * DV)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      f[k] = c < NC ? __ldcg(pm + (size_t)c * 16) : -INFINITY;
+      v[k] = c < NR ? __ldcg(reinterpret_cast<const float4*>(po + (size_t)c * 16 * DV)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      f[k] = c < NR ? __ldcg(pm + (size_t)c * 16) : -INFINITY;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -1126,7 +1130,7 @@ int launch_attn(const DsaArgs& a, cudaStream_t s) {
     if (!make_tmap_bf16(&mq, a.q, 2, dims, str, box)) return NSA_ERR_CUDA;
   }
   {
-    const uint64_t dims[2] = {(uint64_t)a.dk, (uint64_t)a.B * a.T};
+    const uint64_t dims[2] = {(uint64_t)a.dk, (uint64_t)a.nseq * a.T};
     const uint64_t str[1] = {(uint64_t)a.dk * 2};
     const uint32_t box[2] = {64, 1};
     if (!make_tmap_bf16(&mk, a.k, 2, dims, str, box)) return NSA_ERR_CUDA;
@@ -1134,7 +1138,7 @@ int launch_attn(const DsaArgs& a, cudaStream_t s) {
   if (a.v_from_k) {
     mv = mk;
   } else {
-    const uint64_t dims[2] = {(uint64_t)DV, (uint64_t)a.B * a.T};
+    const uint64_t dims[2] = {(uint64_t)DV, (uint64_t)a.nseq * a.T};
     const uint64_t str[1] = {(uint64_t)DV * 2};
     const uint32_t box[2] = {64, 1};
     if (!make_tmap_bf16(&mv, a.v, 2, dims, str, box)) return NSA_ERR_CUDA;
@@ -1167,11 +1171,14 @@ size_t dsa_ws_bytes(const dsa_cfg& c) { return dsa_ws(c).end; }
 size_t dsa_zero_bytes(const dsa_cfg& c) { return dsa_ws(c).zero_end; }
 
 int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
-               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s) {
+               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s,
+               int rows_per_seq) {
   const DsaShape sh = dsa_shape(c);
   const DsaWs w = dsa_ws(c);
   DsaArgs a;
   a.B = c.B;
+  a.rows_per_seq = rows_per_seq;
+  a.nseq = c.B / rows_per_seq;
   a.T = c.T;
   a.HI = c.HI;
   a.dI = c.dI;
@@ -1214,7 +1221,7 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
   int rc = NSA_OK;
   if (!sh.all) {
     CUtensorMap map;
-    const uint64_t dims[3] = {(uint64_t)c.dI, (uint64_t)c.T, (uint64_t)c.B};
+    const uint64_t dims[3] = {(uint64_t)c.dI, (uint64_t)c.T, (uint64_t)a.nseq};
     const uint64_t str[2] = {(uint64_t)c.dI * 2, (uint64_t)c.T * c.dI * 2};
     const uint32_t box[3] = {64, (uint32_t)kIdxTile, 1};
     if (!make_tmap_bf16(&map, kI, 3, dims, str, box)) return NSA_ERR_CUDA;

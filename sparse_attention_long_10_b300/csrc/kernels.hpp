@@ -75,7 +75,11 @@ int dsa_supported(const dsa_cfg& c);
 size_t dsa_ws_bytes(const dsa_cfg& c);
 size_t dsa_zero_bytes(const dsa_cfg& c);
 // lens: nullable device array [B] of context lengths (each in [1, c.T])
+// c.B is the number of query rows; rows_per_seq = 1 for the decode step (one
+// row per sequence), T for the prefill (row r is position r mod T of sequence
+// r / T).
 int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI, const void* q, const void* k,
-               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s);
+               const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s,
+               int rows_per_seq = 1);
 
 }  // namespace nsa

@@ -28,7 +28,7 @@ import torch
 
 __all__ = [
     "NSAParams", "PrefillWorkload", "DecodeWorkload", "DSAWorkload",
-    "prefill_config", "decode_config", "dsa_config",
+    "prefill_config", "decode_config", "dsa_config", "dsa_prefill_config",
     "make_prefill", "make_prefill_dout", "make_decode", "make_decode_multi", "make_dsa",
     "make_dsa_prefill", "PREFILL_CONFIGS",
 ]
@@ -104,6 +104,14 @@ def dsa_config() -> DSAWorkload:
     """Batch 8, context 131,072, indexer 4x64, 16 heads, dk=576, dv=512, top-2048."""
     return DSAWorkload("dsa_decode_B8_T131072_HI4_dI64_H16_dk576_dv512_top2048",
                        8, 131072, 4, 64, 16, 576, 512, 2048, 4)
+
+
+def dsa_prefill_config() -> DSAWorkload:
+    """DSA prefill: one 8,192-token sequence, every position a query; indexer
+    4x64, 16 heads, latent keys of 576 columns whose first 512 are the values,
+    top-2048 (the decode step's heads and selection over a whole sequence)."""
+    return DSAWorkload("dsa_prefill_B1_T8192_HI4_dI64_H16_dk576_dv512_top2048_latent",
+                       1, 8192, 4, 64, 16, 576, 512, 2048, 13)
 
 
 def _draw(gen: torch.Generator, shape, std: float) -> torch.Tensor:
