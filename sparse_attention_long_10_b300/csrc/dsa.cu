@@ -363,7 +363,7 @@ __device__ void radix_resolve(Elem elem, uint32_t n, uint32_t B1, uint32_t need,
 }
 
 // ============================================================ selection
-// One cluster of kSelCluster CTAs per row turns the row's keys into its kept
+// One cluster of up to kSelCluster CTAs per row turns the row's keys into its kept
 // positions, ascending.  Each CTA owns a contiguous range of positions, staged
 // in shared memory by bulk copies together with the row's histogram; each
 // warp owns a contiguous segment of the staged range:
@@ -1105,8 +1105,12 @@ int launch_index(const DsaArgs& a, const CUtensorMap& map, cudaStream_t s) {
 int launch_select(const DsaArgs& a, cudaStream_t s) {
   const size_t smem = select_smem();
   if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&dsa_select_kernel), smem)) return rc;
+  // one CTA per staged chunk of the row, at most kSelCluster: a row that fits
+  // one chunk (the prefill's short rows) runs on a single CTA
+  int cl = (a.T + kSelChunk - 1) / kSelChunk;
+  cl = cl < 1 ? 1 : (cl > kSelCluster ? kSelCluster : cl);
   prof::begin("dsa_select", s);
-  const int rc = launch_dependent(dsa_select_kernel, dim3(kSelCluster, a.B), dim3(kSelThreads), smem, s, kSelCluster, a);
+  const int rc = launch_dependent(dsa_select_kernel, dim3(cl, a.B), dim3(kSelThreads), smem, s, cl, a);
   prof::end(s);
   return rc;
 }
