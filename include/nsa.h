@@ -94,7 +94,7 @@ typedef struct nsa_cfg {
   const void* w_v;   /* [l*dv, dv]                                       */
 } nsa_cfg;
 
-/* Supported by this build: l=32, d=16, lsel=64, 3 <= n <= 32, 1 <= w,
+/* Supported shapes: l=32, d=16, lsel=64, 3 <= n <= 32, 1 <= w,
    dk and dv multiples of 64 with dk <= 256 and dv <= 256, H/G a power of two
    between 1 and 128, T >= 1, B >= 1.  Anything else -> NSA_ERR_UNSUPPORTED. */
 

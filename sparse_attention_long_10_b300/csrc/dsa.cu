@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kSelThreads) dsa_select_kernel(const DsaArgs a
   uint32_t phase = 0;
   auto wait_copy = [&]() {
     const bool got = mbar_wait(&sh.bar, phase, &sh.abort, a.st, 541);
-    // every thread continues on the same verdict; a copy still in flight
+    // every thread continues on the same outcome; a copy still in flight
     // keeps ``phase`` for the drain at the end
     ok = __syncthreads_and(got ? 1 : 0) != 0;
     if (ok) phase ^= 1u;
