@@ -126,6 +126,32 @@ def test_dsa_latent_values_argument_checks(nsa):
         assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE, need, None) == 7
 
 
+def test_dsa_prefill_argument_checks(nsa):
+    """dsa_prefill_fwd: every position of every sequence is a query row, so
+    B*T rows must fit the launch grid (<= 65535, else UNSUPPORTED); the
+    pointer rules are those of dsa_decode_step."""
+    f = nsa.lib.dsa_prefill_fwd
+    c = nsa.make_dsa_cfg(1, 8192, 4, 64, 16, 576, 512, 2048)
+    need = nsa.dsa_prefill_workspace_size(c)
+    assert need > nsa.dsa_decode_workspace_size(nsa.make_dsa_cfg(1, 8192, 4, 64, 16, 576, 512, 2048))
+    # B*T = 65,536 rows: unsupported, and no workspace size
+    big = nsa.make_dsa_cfg(2, 32768, 4, 64, 16, 576, 512, 2048)
+    assert nsa.dsa_prefill_workspace_size(big) == 0
+    assert f(ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, 1 << 40, None) == 2
+    # latent values need dv <= dk; a given v must be 16-byte aligned
+    bad = nsa.make_dsa_cfg(1, 4096, 4, 64, 16, 64, 128, 2048)
+    assert f(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE,
+             nsa.dsa_prefill_workspace_size(bad), None) == 1
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, None, FAKE, need, None) == 3
+    # null inputs, misaligned idx_out, a short workspace
+    assert f(ctypes.byref(c), None, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 1
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE + 4, FAKE, need, None) == 3
+    assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need - 256, None) == 4
+    if not torch.cuda.is_available():
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE, need, None) == 7
+        assert f(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None) == 7
+
+
 def _prefill_args(nsa, c, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, gates=FAKE, kc=FAKE, vc=FAKE, out=FAKE, idx=None, ws=FAKE,
              ws_bytes=nsa.nsa_prefill_workspace_size(c))
