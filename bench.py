@@ -294,47 +294,21 @@ def run_ours(args, ws, rank):
     cfgs = [cfg, nsa.make_cfg(B, T, H, G, dk, dv, phi=sets[1])]
     outs = [out, torch.empty_like(out)]
     outs_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    in_free = [torch.cuda.Event() for _ in range(2)]
-    out_ready = [torch.cuda.Event() for _ in range(2)]
-    out_free = [torch.cuda.Event() for _ in range(2)]
 
-    def run_e2e(n):
-        for ev in in_free + out_free:
-            ev.record(stream)
-        s_in.wait_stream(stream)
-        s_out.wait_stream(stream)
-        for i in range(n):
-            j = i & 1
-            s_in.wait_event(in_free[j])            # step i-2 has read set j
-            with torch.cuda.stream(s_in):
-                for k in keys_in:
-                    sets[j][k].copy_(host[k], non_blocking=True)
-            in_ready[j].record(s_in)
-            stream.wait_event(in_ready[j])
-            stream.wait_event(out_free[j])         # step i-2's output is downloaded
-            nsa.nsa_prefill_fwd(cfgs[j], sets[j]["q"], sets[j]["k"], sets[j]["v"], sets[j]["gates"], kc, vc,
-                                outs[j], idx, wsp, stream)
-            in_free[j].record(stream)
-            out_ready[j].record(stream)
-            s_out.wait_event(out_ready[j])
-            with torch.cuda.stream(s_out):
-                outs_h[j].copy_(outs[j], non_blocking=True)
-            out_free[j].record(s_out)
-        stream.wait_stream(s_in)
-        stream.wait_stream(s_out)
+    def upload(j):
+        for k in keys_in:
+            sets[j][k].copy_(host[k], non_blocking=True)
 
-    run_e2e(2)
-    torch.cuda.synchronize()
-    e_steps = max(3, args.steps)
+    def compute(j):
+        nsa.nsa_prefill_fwd(cfgs[j], sets[j]["q"], sets[j]["k"], sets[j]["v"], sets[j]["gates"], kc, vc,
+                            outs[j], idx, wsp, stream)
+
+    def download(j):
+        outs_h[j].copy_(outs[j], non_blocking=True)
+
     barrier(ws)
     torch.cuda.synchronize()
-    e0.record(stream)
-    run_e2e(e_steps)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e_steps, ws)
+    ms_e2e = max_over_ranks(pipelined_e2e(upload, compute, download, max(3, args.steps), stream), ws)
     if nsa.nsa_device_status(wsp) != 0:
         raise RuntimeError("device status set in the end-to-end region")
 
@@ -378,10 +352,7 @@ def run_ours(args, ws, rank):
         "gpu_launches": int(launches),
         "dense": dense,
         "e2e": {"value": whole_job_rate(B * T, ms_e2e, ws), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e,
-                "how": "per step: inputs uploaded from pinned host memory, nsa_prefill_fwd, output downloaded; "
-                       "uploads and downloads on their own streams overlap the neighbouring steps' compute "
-                       "(two device input / output sets)"},
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e, "how": PIPELINE_HOW},
         "clocks": clk.summary(),
     }
     return res, inp
@@ -452,6 +423,76 @@ def time_graph_steps(graph, steps, flush):
     return [a.elapsed_time(b) for a, b in times]
 
 
+def pipelined_e2e(upload, compute, download, n_steps, stream):
+    """Per-step time (ms) of ``n_steps`` end-to-end steps run as a serving loop
+    runs them, over two device input / output sets j = i % 2: upload(j) on
+    one copy stream, compute(j) on ``stream``, download(j) on another copy
+    stream; step i+1's upload and step i-1's download overlap step i's
+    compute, and events order every reuse of a set."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in_ready", "in_free", "out_ready", "out_free")}
+
+    def run(n):
+        for e in ev["in_free"] + ev["out_free"]:
+            e.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(n):
+            j = i & 1
+            s_in.wait_event(ev["in_free"][j])       # step i-2 has read set j
+            with torch.cuda.stream(s_in):
+                upload(j)
+            ev["in_ready"][j].record(s_in)
+            stream.wait_event(ev["in_ready"][j])
+            stream.wait_event(ev["out_free"][j])    # step i-2's output is downloaded
+            compute(j)
+            ev["in_free"][j].record(stream)
+            ev["out_ready"][j].record(stream)
+            s_out.wait_event(ev["out_ready"][j])
+            with torch.cuda.stream(s_out):
+                download(j)
+            ev["out_free"][j].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    run(2)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(n_steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
+PIPELINE_HOW = ("per step: inputs uploaded from pinned host memory, the C-ABI call, output downloaded; uploads and "
+                "downloads on their own streams overlap the neighbouring steps' compute (two device input / output "
+                "sets)")
+
+
+class PackedInputs:
+    """A step's small inputs packed into one pinned host buffer, uploaded with
+    one copy into one device buffer whose slices (256-byte aligned) are the
+    tensors the C-ABI call reads."""
+
+    def __init__(self, tensors):
+        offs, off = [], 0
+        for t in tensors:
+            offs.append(off)
+            off = (off + t.numel() * t.element_size() + 255) // 256 * 256
+        self.host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(off, dtype=torch.uint8, device="cuda")
+        self.views = []
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            self.host[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+            self.views.append(self.dev[o:o + n].view(t.dtype).view(t.shape))
+        self.nbytes = sum(t.numel() * t.element_size() for t in tensors)
+
+    def upload(self):
+        self.dev.copy_(self.host, non_blocking=True)
+
+
 def time_e2e_graph(step_e2e, steps, flush, ws):
     """End-to-end time of a decode-type step (ms): the step's host-to-device
     input copies, the C-ABI call and the device-to-host copy of its result,
@@ -470,7 +511,8 @@ def time_e2e_graph(step_e2e, steps, flush, ws):
     return max_over_ranks(statistics.mean(time_graph_steps(g, steps, flush)), ws)
 
 
-E2E_HOW = "CUDA graph replay of the step's input copies from pinned host memory, the C-ABI call and the result copy back"
+E2E_HOW = ("CUDA graph replay of the step's input upload from pinned host memory (one packed copy), the C-ABI "
+           "call and the result copy back")
 
 
 def run_decode_leg(args, ws):
@@ -521,21 +563,19 @@ def run_decode_leg(args, ws):
     torch.cuda.synchronize()
     prof = nsa.nsa_profile_read()
     nsa.nsa_profile_enable(False)
-    # end to end: the new token's q, gates and K/V row copied in, out copied back
-    host_q = inp["q"].pin_memory()
-    host_g = inp["gates"].pin_memory()
-    host_k = inp["kcache"][:, :, T - 1].contiguous().pin_memory()
-    host_v = inp["vcache"][:, :, T - 1].contiguous().pin_memory()
+    # end to end: the new token's q, gates and K/V row uploaded in one copy
+    # (the rows then placed into the caches on the device), out copied back
+    pk_in = PackedInputs([inp["q"], inp["gates"], inp["kcache"][:, :, T - 1], inp["vcache"][:, :, T - 1]])
+    q_v, g_v, krow_v, vrow_v = pk_in.views
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_g, host_k, host_v))
+    h2d = pk_in.nbytes
     d2h = out_h.numel() * out_h.element_size()
 
     def step_e2e():
-        dev["q"].copy_(host_q, non_blocking=True)
-        dev["gates"].copy_(host_g, non_blocking=True)
-        dev["kcache"][:, :, T - 1].copy_(host_k, non_blocking=True)
-        dev["vcache"][:, :, T - 1].copy_(host_v, non_blocking=True)
-        step()
+        pk_in.upload()
+        dev["kcache"][:, :, T - 1].copy_(krow_v, non_blocking=True)
+        dev["vcache"][:, :, T - 1].copy_(vrow_v, non_blocking=True)
+        nsa.nsa_decode_step(cfg, q_v, dev["kcache"], dev["vcache"], kc, vc, g_v, out, None, wsp, None)
         out_h.copy_(out, non_blocking=True)
 
     ms_e2e = time_e2e_graph(step_e2e, args.steps, flush, ws)
@@ -659,19 +699,24 @@ def run_dsa_prefill_leg(args, ws):
     torch.cuda.synchronize()
     prof = nsa.nsa_profile_read()
     nsa.nsa_profile_enable(False)
-    # end to end: the sequence's inputs in, out back
-    host = {k: inp[k].pin_memory() for k in ("qI", "wI", "kI", "q", "k")}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size()
+    # end to end: the sequence's inputs uploaded (one packed copy), out back,
+    # pipelined over two device sets
+    packs = [PackedInputs([inp["qI"], inp["wI"], inp["kI"], inp["q"], inp["k"]]) for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
+    outs_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = packs[0].nbytes
+    d2h = out.numel() * out.element_size()
+    stream = torch.cuda.current_stream()
 
-    def step_e2e():
-        for k, t in host.items():
-            dev[k].copy_(t, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
+    def compute(j):
+        qI_v, wI_v, kI_v, q_v, k_v = packs[j].views
+        nsa.dsa_prefill_fwd(cfg, qI_v, wI_v, kI_v, q_v, k_v, None, outs[j], None, wsp, stream)
 
-    ms_e2e = time_e2e_graph(step_e2e, args.steps, flush, ws)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(pipelined_e2e(lambda j: packs[j].upload(), compute,
+                                          lambda j: outs_h[j].copy_(outs[j], non_blocking=True),
+                                          max(3, args.steps), stream), ws)
     # useful work: the indexer over every causal prefix, the attention over the kept positions
     t1 = torch.arange(1, wl.T + 1, dtype=torch.float64)
     idx_flop = float(t1.sum()) * wl.HI * wl.dI * 2 * wl.B
@@ -692,7 +737,7 @@ def run_dsa_prefill_leg(args, ws):
                     for k, (c, t) in prof.items()},
         "gpu_launches_per_step": int(sum(c for c, _ in prof.values()) / args.steps),
         "e2e": {"value": wl.B * wl.T / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "how": E2E_HOW},
+                "d2h_bytes_per_step": int(d2h), "how": PIPELINE_HOW},
     }
 
 
@@ -739,16 +784,17 @@ def run_dsa_leg(args, ws, latent=False):
     torch.cuda.synchronize()
     prof = nsa.nsa_profile_read()
     nsa.nsa_profile_enable(False)
-    # end to end: the new token's queries and indexer weights in, out back
-    host = {k: inp[k].pin_memory() for k in ("qI", "wI", "q")}
+    # end to end: the new token's queries and indexer weights uploaded in one
+    # copy, out copied back
+    pk_in = PackedInputs([inp["qI"], inp["wI"], inp["q"]])
+    qI_v, wI_v, q_v = pk_in.views
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = pk_in.nbytes
     d2h = out_h.numel() * out_h.element_size()
 
     def step_e2e():
-        for k, t in host.items():
-            dev[k].copy_(t, non_blocking=True)
-        step()
+        pk_in.upload()
+        nsa.dsa_decode_step(cfg, qI_v, wI_v, dev["kI"], q_v, dev["k"], dev.get("v"), out, None, wsp)
         out_h.copy_(out, non_blocking=True)
 
     ms_e2e = time_e2e_graph(step_e2e, args.steps, flush, ws)
