@@ -741,6 +741,81 @@ def run_dsa_prefill_leg(args, ws):
     }
 
 
+def run_backward_leg(args, ws):
+    """NSA backward over the 64k prefill (B=1, T=65,536, H=64, G=4, dk=192,
+    dv=128): gradients of every input (q, k, v, gates, W_c, PE) given the
+    forward's compressed cache and kept blocks and a bf16 upstream gradient.
+    The forward runs once before the timed region; every step is one
+    nsa_prefill_bwd call (inputs far above the L2 size, so no flush)."""
+    import sparse_attention_long_10_b300 as nsa
+    from workloads import make_prefill_dout
+    wl = PREFILL_CONFIGS["prefill_64k"]
+    inp = make_prefill(wl)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    dout = make_prefill_dout(wl).cuda()
+    B, T, H, G, dk, dv = wl.B, wl.T, wl.H, wl.G, wl.dk, wl.dv
+    cfg = nsa.make_cfg(B, T, H, G, dk, dv, phi=dev)
+    Nc = nsa.nsa_num_compressed(cfg)
+    kc = torch.empty(B, G, Nc, dk, dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty(B, G, Nc, dv, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(B, T, G, PARAMS.n, dtype=torch.int32, device="cuda")
+    wsf = nsa.workspace(nsa.nsa_prefill_workspace_size(cfg))
+    nsa.nsa_prefill_fwd(cfg, dev["q"], dev["k"], dev["v"], dev["gates"], kc, vc, out, idx, wsf)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    grads = [torch.empty(B, T, H, dk, **f32), torch.empty(B, T, G, dk, **f32), torch.empty(B, T, G, dv, **f32),
+             torch.empty(B, T, H, 3, **f32), torch.empty(32 * dk, dk, **f32), torch.empty(32 * dv, dv, **f32),
+             torch.empty(32, dk, **f32), torch.empty(32, dv, **f32)]
+    wsb = nsa.workspace(nsa.nsa_prefill_bwd_workspace_size(cfg))
+
+    def step():
+        nsa.nsa_prefill_bwd(cfg, dev["q"], dev["k"], dev["v"], dev["gates"], kc, vc, idx, dout, *grads, wsb)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if nsa.nsa_device_status(wsb) != 0:
+        raise RuntimeError("backward: device status set during warm-up")
+    steps = max(2, min(args.steps, 5))
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, ws)
+    if nsa.nsa_device_status(wsb) != 0:
+        raise RuntimeError("backward: device status set in the timed region")
+    nsa.nsa_profile_enable(True)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    prof = nsa.nsa_profile_read()
+    nsa.nsa_profile_enable(False)
+    # algorithmic work: 2.5x the forward's attention FLOPs (S recomputed, dP,
+    # dV, dK, dq) plus twice the compression GEMM (dX and dW)
+    f, _ = prefill_counts(T, H, G, dk, dv, B)
+    att_fwd = f["cmp"] + f["sel"] + f["win"]
+    flops = 2.5 * att_fwd + 2 * f["phi"]
+    pk = peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "NSA 64k backward tokens/s", "value": B * T / (ms * 1e-3), "unit": "tokens/s",
+        "higher_is_better": True, "ms_per_step": ms, "workload": wl.name + "_backward", "steps": steps,
+        "useful_tflop_per_step": flops / 1e12,
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                     "frac": tf / pk["bf16_sus"], "peak_kind": f"bf16 dense sustained ({pk['src']})",
+                     "traffic": None,
+                     "note": "2.5 x the forward's attention FLOPs + 2 x the compression GEMM over the whole call"},
+        "kernels": {k: {"launches_per_step": c / steps, "ms_per_step": t / steps} for k, (c, t) in prof.items()},
+        # profiled spans: the list building is 3 kernels, the compression backward 8
+        "gpu_launches_per_step": int(sum(c * {"bwd_lists": 3, "bwd_compress": 8}.get(k, 1)
+                                         for k, (c, _) in prof.items()) / steps),
+    }
+
+
 def run_dsa_leg(args, ws, latent=False):
     """One DSA-style decode step: batch 8, 131,072-token context, indexer of 4
     heads x 64 dims, top-2048 positions, attention of 16 heads (dk=576,
@@ -831,9 +906,10 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and DSA decode legs")
     ap.add_argument("--workload", default="prefill_64k",
                     choices=sorted(PREFILL_CONFIGS) + ["decode_64k", "dsa_128k", "dsa_latent_128k",
-                                                       "dsa_prefill_8k"],
+                                                       "dsa_prefill_8k", "backward_64k"],
                     help="prefill workload (the headline is prefill_64k; smaller ones serve profiling) or "
-                         "decode_64k / dsa_128k / dsa_latent_128k / dsa_prefill_8k: one of the other legs alone")
+                         "decode_64k / dsa_128k / dsa_latent_128k / dsa_prefill_8k / backward_64k: one of the other legs "
+                         "alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, _ = dist_setup()
@@ -860,9 +936,11 @@ def main():
         print(json.dumps(res), flush=True)
         return
 
-    if args.workload in ("decode_64k", "dsa_128k", "dsa_latent_128k", "dsa_prefill_8k"):
+    if args.workload in ("decode_64k", "dsa_128k", "dsa_latent_128k", "dsa_prefill_8k", "backward_64k"):
         if args.workload == "decode_64k":
             res = run_decode_leg(args, ws)
+        elif args.workload == "backward_64k":
+            res = run_backward_leg(args, ws)
         elif args.workload == "dsa_prefill_8k":
             res = run_dsa_prefill_leg(args, ws)
         else:
@@ -882,6 +960,8 @@ def main():
         res["gpu_launches"] += res["dsa_latent"]["gpu_launches_per_step"] * args.steps
         res["dsa_prefill"] = run_dsa_prefill_leg(args, ws)
         res["gpu_launches"] += res["dsa_prefill"]["gpu_launches_per_step"] * args.steps
+        res["backward"] = run_backward_leg(args, ws)
+        res["gpu_launches"] += res["backward"]["gpu_launches_per_step"] * res["backward"]["steps"]
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         blas, ncpu = cpu_cores()
         rate, info = oracle_prefill_rate(inp, rows_per_step=16, steps=2)

@@ -182,6 +182,38 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * nsa_prefill_bwd -- NSA backward pass over whole sequences: the gradients of
+ * sum(dout * out) for out = nsa_prefill_fwd(...) [P2 II; the pages' training
+ * figure, 6.0x faster than full attention at 64k, P2 III.3].  The pages give
+ * no backward formula; these are the gradients of the forward under three
+ * readings: the kept blocks idx are constants (top-n has no gradient), the
+ * bf16 rounding of the compressed cache passes gradients unchanged, and the
+ * gradients of pe_k / pe_v / w_k / w_v sum over every sequence and KV head.
+ * Per branch (softmax attention, P = softmax(scale q K^T), dO_b = g_b dout):
+ *   dV_j += P_j dO_b,  dS_j = P_j (dO_b . V_j - dO_b . O_b),
+ *   dq += scale sum_j dS_j K_j,  dK_j += scale dS_j q,  dgates_b = dout . O_b,
+ * and the compressed branch's dKc / dVc flow through the compression map
+ * (dW += flatten(X_i + PE)^T dXc_i, dX[16 i + r] += (dXc_i W^T)[r], dPE).
+ *   q, k, v, gates, kc, vc : the forward's inputs and its compressed cache
+ *   idx   : [B,T,G,n] int32, the forward's kept blocks (its idx_out)
+ *   dout  : [B,T,H,dv] bf16, the upstream gradient
+ *   dq    : out, fp32 [B,T,H,dk]      dk, dv : out, fp32 [B,T,G,dk] / [B,T,G,dv]
+ *   dgates: out, fp32 [B,T,H,3]       dw_k, dw_v : out, fp32 [l*dk,dk] / [l*dv,dv]
+ *   dpe_k, dpe_v : out, fp32 [l,dk] / [l,dv]
+ *   ws    : nsa_prefill_bwd_workspace_size(cfg) bytes
+ * Every output is overwritten.  dk, dv, dw_* are sums of fp32 reductions in
+ * an order that varies between runs (the last bits can differ).
+ * Supported: H/G <= 16, n <= 16, dk 128 or 192, dv 64 or 128, T <= 65536,
+ * 16*B*G <= 65535 (cfg rules as nsa_prefill_fwd).
+ */
+size_t nsa_prefill_bwd_workspace_size(const nsa_cfg* cfg);
+int nsa_prefill_bwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v,
+                    const void* gates, const void* kc, const void* vc, const int32_t* idx,
+                    const void* dout, float* dq, float* dk, float* dv, float* dgates,
+                    float* dw_k, float* dw_v, float* dpe_k, float* dpe_v,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * nsa_decode_step -- one new token per sequence [P2 II, III.3]: row t = len-1
  * of the prefill definition, read from the caches (the cache already holds
  * the new token).  Per KV head it reads the visible compressed entries, the

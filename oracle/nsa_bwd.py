@@ -171,7 +171,9 @@ def nsa_prefill_backward(inp: Dict[str, torch.Tensor], dout: np.ndarray, b: int 
     instead, the differentiable function of ``nsa_prefill_forward_fixed``.
     Returns dq [T, H, dk], dk [T, G, dk],
     dv [T, G, dv], dgates [T, H, 3], dw_k, dw_v, dpe_k, dpe_v, the forward
-    out [T, H, dv] and idx.
+    out [T, H, dv] and idx, and the compressed cache's gradients dkc
+    [G, Nc, dk], dvc [G, Nc, dv] (what the compression map's backward
+    receives).
     """
     x = _inputs_f64(inp, b)
     T, H, dk = x["q"].shape
@@ -197,6 +199,8 @@ def nsa_prefill_backward(inp: Dict[str, torch.Tensor], dout: np.ndarray, b: int 
                           dout[:, hs])
         dKx, dpk, dwk = compress_bwd(K, x["pe_k"], x["w_k"], params.l, params.d, r["dKc"])
         dVx, dpv, dwv = compress_bwd(V, x["pe_v"], x["w_v"], params.l, params.d, r["dVc"])
+        res.setdefault("dkc", []).append(r["dKc"])
+        res.setdefault("dvc", []).append(r["dVc"])
         res["dq"][:, hs] = r["dq"]
         res["dk"][:, g] = r["dK"] + dKx
         res["dv"][:, g] = r["dV"] + dVx
@@ -207,6 +211,8 @@ def nsa_prefill_backward(inp: Dict[str, torch.Tensor], dout: np.ndarray, b: int 
         res["dpe_v"] += dpv
         res["out"][:, hs] = r["out"]
         res["idx"][:, g] = ig
+    res["dkc"] = np.stack(res["dkc"])
+    res["dvc"] = np.stack(res["dvc"])
     return res
 
 

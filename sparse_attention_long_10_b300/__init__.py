@@ -23,7 +23,8 @@ __all__ = [
     "nsa_compress_workspace_size", "nsa_prefill_workspace_size", "nsa_decode_workspace_size",
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
     "nsa_compress_kv_noalloc_status", "nsa_full_attn_workspace_size", "nsa_full_attn_fwd",
-    "nsa_decode_multi_workspace_size", "nsa_decode_multi", "nsa_prefill_fwd", "nsa_decode_step",
+    "nsa_decode_multi_workspace_size", "nsa_decode_multi", "nsa_prefill_fwd",
+    "nsa_prefill_bwd_workspace_size", "nsa_prefill_bwd", "nsa_decode_step",
     "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
@@ -85,6 +86,8 @@ def _load() -> ctypes.CDLL:
                                      _c_vp, _c_vp, _c_vp, _c_size, _c_vp]),
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
         "nsa_full_attn_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_prefill_bwd_workspace_size": (_c_size, [P(NsaCfg)]),
+        "nsa_prefill_bwd": (_c_int, [P(NsaCfg)] + [_c_vp] * 16 + [_c_vp, _c_size, _c_vp]),
         "nsa_decode_multi_workspace_size": (_c_size, [P(NsaCfg), _c_int]),
         "nsa_decode_multi": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                       _c_vp, _c_size, _c_vp]),
@@ -215,6 +218,21 @@ def nsa_prefill_fwd(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, ws, strea
                                _ptr(kc), _ptr(vc), _ptr(out), _ptr(idx_out), _ptr(ws),
                                ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_prefill_fwd")
+
+
+def nsa_prefill_bwd_workspace_size(cfg: NsaCfg) -> int:
+    return int(_lib().nsa_prefill_bwd_workspace_size(ctypes.byref(cfg)))
+
+
+def nsa_prefill_bwd(cfg: NsaCfg, q, k, v, gates, kc, vc, idx, dout, dq, dk, dv, dgates, dw_k, dw_v,
+                    dpe_k, dpe_v, ws, stream=None):
+    """Gradients of sum(dout * out) for the forward on the same inputs; the
+    outputs are fp32 tensors (see include/nsa.h)."""
+    _check(_lib().nsa_prefill_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates), _ptr(kc),
+                                  _ptr(vc), _ptr(idx), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgates),
+                                  _ptr(dw_k), _ptr(dw_v), _ptr(dpe_k), _ptr(dpe_v), _ptr(ws),
+                                  ws.numel() if ws is not None else 0, _stream(stream)),
+           "nsa_prefill_bwd")
 
 
 def nsa_full_attn_workspace_size(cfg: NsaCfg) -> int:

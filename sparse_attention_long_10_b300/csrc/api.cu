@@ -251,6 +251,32 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
   return launch_sel(c, q, k, v, gates, idx, part, out, st, s);
 }
 
+size_t nsa_prefill_bwd_workspace_size(const nsa_cfg* cfg) {
+  if (validate_cfg(cfg) != NSA_OK || bwd_supported(*cfg) != NSA_OK) return 0;
+  return bwd_ws(*cfg, kHeader).end;
+}
+
+int nsa_prefill_bwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, const void* gates,
+                    const void* kc, const void* vc, const int32_t* idx, const void* dout, float* dq, float* dk,
+                    float* dv, float* dgates, float* dw_k, float* dw_v, float* dpe_k, float* dpe_v, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  const nsa_cfg& c = *cfg;
+  if ((rc = bwd_supported(c)) != NSA_OK) return rc;
+  if ((rc = validate_phi(cfg)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, k, v, gates, idx, dout, dq, dk, dv, dgates, dw_k, dw_v, dpe_k, dpe_v})) != NSA_OK)
+    return rc;
+  if (num_compressed(c) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  const BwdWs w = bwd_ws(c, kHeader);
+  if ((rc = check_ws(ws, ws_bytes, w.end)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  BwdPtrs p{q, k, v, gates, kc, vc, dout, idx, dq, dk, dv, dgates, dw_k, dw_v, dpe_k, dpe_v};
+  return launch_prefill_bwd(c, p, static_cast<uint8_t*>(ws), w, s);
+}
+
 size_t nsa_full_attn_workspace_size(const nsa_cfg* cfg) {
   if (validate_cfg(cfg) != NSA_OK || full_attn_supported(*cfg) != NSA_OK) return 0;
   return kHeader;

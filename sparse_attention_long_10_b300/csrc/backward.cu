@@ -1,0 +1,1485 @@
+// backward.cu -- NSA backward pass over whole sequences: gradients of
+// <dout, out> for the prefill forward (three branches and the gated combine
+// [P2 II; P3 token compression / selection / sliding window], the pages'
+// 6.0x training-speed figure [P2 III.3]).
+//
+// The pages give no backward formula; the gradients are those of the forward
+// under three readings: the kept blocks are constants (top-n has no
+// gradient), the bf16 rounding of the compressed cache passes gradients
+// unchanged, and W_c / PE gradients sum over the KV heads.  Each branch is
+// softmax attention, so its backward is the textbook one: with
+// P = softmax(s), dO_b = g_b * dout,
+//     dV_j += P_j dO_b,   dS_j = P_j (dO_b . V_j - dO_b . O_b),
+//     dq += scale sum_j dS_j K_j,   dK_j += scale dS_j q,
+// and dg_b = dout . O_b = sum_j P_j (dout . V_j).
+//
+// Kernels (in launch order):
+//  1. bwd_dq_kernel     one item = one query t of one KV group g (the group's
+//                       16 heads on the MMA N side, keys on M, as in the
+//                       forward's selected-block kernel).  Per branch: pass 0
+//                       streams the keys once for the log-sum-exp and dg_b
+//                       (per-thread online max / sum, merged across the 128
+//                       key lanes at the end); pass 1 streams them again for
+//                       dS and accumulates dQ^T = K^T dS^T in TMEM over all
+//                       three branches.  Writes dq, dgates and, per branch,
+//                       the log-sum-exp and dg of every (t, h) row.
+//  2. slc_count / build_units / slc_fill: for the selected branch the
+//                       inverse of the kept-block lists (per (b, g, block):
+//                       the queries that kept it); for every branch a list of
+//                       work units (b, g, key tile, query range).
+//  3. bwd_dkv_kernel<BR> key-outer, one CTA per unit at a time: a 128-key tile
+//                       (K and V loaded once) against chunks of 4 queries x 16
+//                       heads (64 MMA columns):
+//                           S^T  = K Q^T,   dP'^T = V dout^T          (tcgen05, TMEM)
+//                           P^T g, dS^T  -> bf16 in TMEM
+//                           dV  += (g P)^T dout,  dK += dS^T Q         (A from TMEM)
+//                       The unit's dK / dV are added to global memory with
+//                       fp32 reductions (units of one key tile may overlap).
+//  4. compression backward on CUDA cores in fp32: dX overlap-add of
+//     dB_i = dXc_i W^T into dk / dv, dPE = (sum_i dXc_i) W_r^T per offset r,
+//     dW = sum_i flatten(X_i + PE)^T dXc_i.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.hpp"
+#include "profiler.hpp"
+#include "tmap.hpp"
+
+namespace nsa {
+
+namespace {
+
+constexpr int NP = 16;              // MMA N of one item: the group's heads, padded
+constexpr int kQB = 2048;           // one 64-column chunk of NP rows (bf16, 128-B swizzle)
+constexpr int kChunk = 16384;       // one 64-column chunk of 128 key rows
+constexpr int kRowsPerUnit = 1024;  // queries per key-outer work unit
+
+constexpr int kBrCmp = 0, kBrSlc = 1, kBrWin = 2;
+
+// ============================================================================
+// branch key lists of one query (shared by every role of bwd_dq_kernel)
+// ============================================================================
+struct BranchKeys {
+  int np;      // 128-row key tiles ("pairs")
+  int start;   // cmp: visible entries nc; win: first token of the window
+};
+
+__device__ __forceinline__ int visible_compressed(int t, int Nc) {
+  // entries i with 16 i + 31 <= t (l = 32, d = 16)
+  return t >= 31 ? min(Nc, (t - 31) / 16 + 1) : 0;
+}
+
+__device__ __forceinline__ BranchKeys branch_keys(int br, int t, int Nc, int n, int w) {
+  BranchKeys k;
+  if (br == kBrCmp) {
+    k.start = visible_compressed(t, Nc);
+    k.np = (k.start + 127) / 128;
+  } else if (br == kBrSlc) {
+    k.start = 0;
+    k.np = (n + 1) / 2;
+  } else {
+    k.start = max(0, t - w + 1);
+    k.np = (t - k.start + 1 + 127) / 128;
+  }
+  return k;
+}
+
+// The n (<= 16) kept blocks of query t, -1 past n.
+__device__ __forceinline__ void load_kept(const int32_t* blk, int n, int (&bk)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) bk[k] = k < n ? __ldg(blk + k) : -1;
+}
+
+__device__ __forceinline__ int block_token(int blk) { return blk >= 0 ? blk * 64 : -128; }
+
+// ============================================================================
+// 1. dQ, dgates, per-branch log-sum-exp and dg
+// ============================================================================
+struct DqArgs {
+  int T, H, G, dk, dv, n, w, hpg, Nc, QPC;
+  float sc2, scale;
+  const int32_t* idx;              // [B,T,G,n]
+  const __nv_bfloat16* gates;      // [B,T,H,3]
+  float* dq;                       // [B,T,H,dk]
+  float* dgates;                   // [B,T,H,3]
+  float* lse;                      // [3][B,T,H]  log2-domain log-sum-exp of s*scale
+  float* dgw;                      // [3][B,T,H]  dout . O_b
+  DeviceStatus* st;
+  uint32_t off_kv, off_ds, off_red, off_bar;
+};
+
+struct DqBars {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[4], s_free[4];
+  uint64_t ds_full[2], ds_free[2];
+  uint64_t dq_full[2], dq_free[2];
+  uint64_t wg;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort_flag;
+};
+
+constexpr int kDqThreads = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
+
+__global__ void __launch_bounds__(kDqThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                  const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                  const __grid_constant__ CUtensorMap mapKc, const __grid_constant__ CUtensorMap mapVc,
+                  const DqArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int kcs = a.dk / 64, vcs = a.dv / 64, cs = kcs + vcs;
+  const int slot_bytes = cs * kChunk;
+  uint8_t* qbuf = smem;                         // 2 items x (kcs Q + vcs dout) chunks x 2 KB
+  uint8_t* kvring = smem + a.off_kv;            // 2 slots x (kcs K + vcs V) chunks x 16 KB
+  uint8_t* dsbuf = smem + a.off_ds;             // 2 x dS^T (2 chunks x 2 KB)
+  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [4 warps][3][NP]
+  DqBars* bars = reinterpret_cast<DqBars*>(smem + a.off_bar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int t0 = blockIdx.x * a.QPC;
+  const int nitems = min(a.QPC, a.T - t0);
+  const int warp = warp_id(), lane = lane_id();
+  const int nm = (a.dk + 127) / 128;            // M=128 tiles of dQ^T (dk rows)
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->ds_full[i], 4);
+      mbar_init(&bars->ds_free[i], 1);
+      mbar_init(&bars->dq_full[i], 1);
+      mbar_init(&bars->dq_free[i], 4);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 4);
+    }
+    mbar_init(&bars->wg, 4);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = prior_error(a.st);
+    fence_barrier_init();
+  }
+  // query / dout rows hpg..NP-1 are never loaded: keep them zero
+  for (int i = threadIdx.x; i < 2 * cs * kQB / 16; i += kDqThreads)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tmem_sd = tmem;          // 4 x (S^T 16 + dP'^T 16) columns
+  const uint32_t tmem_dq = tmem + 128;    // 2 x (nm x 16) columns
+
+  if (*abort_flag) {
+  } else if (warp == 4) {
+    // ===================================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapDO);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      bool ok = true;
+      int jp = 0, nq = 0;
+      for (int i = 0; i < nitems && ok; ++i) {
+        const int t = t0 + i;
+        const int qb = i & 1;
+        if (!mbar_wait(&bars->q_empty[qb], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag, a.st, 801)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->q_full[qb], (uint32_t)(cs * a.hpg * 128));
+        for (int c = 0; c < kcs; ++c)
+          tma_load_4d(qbuf + (qb * cs + c) * kQB, &mapQ, &bars->q_full[qb], c * 64, g * a.hpg, t, b);
+        for (int c = 0; c < vcs; ++c)
+          tma_load_4d(qbuf + (qb * cs + kcs + c) * kQB, &mapDO, &bars->q_full[qb], c * 64, g * a.hpg, t, b);
+        ++nq;
+        int bks[16];
+        load_kept(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
+        for (int br = 0; br < 3 && ok; ++br) {
+          const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
+          for (int pass = 0; pass < 2 && ok; ++pass) {
+            for (int p = 0; p < bk.np; ++p) {
+              const int slot = jp & 1;
+              if (!mbar_wait(&bars->kv_empty[slot], (uint32_t)(((jp >> 1) & 1) ^ 1), abort_flag, a.st, 802)) {
+                ok = false;
+                break;
+              }
+              uint8_t* dst = kvring + slot * slot_bytes;
+              uint64_t* bar = &bars->kv_full[slot];
+              mbar_arrive_expect_tx(bar, (uint32_t)slot_bytes);
+              if (br == kBrCmp) {
+                const int r0 = 128 * p;
+                for (int c = 0; c < kcs; ++c) {
+                  tma_load_4d(dst + c * kChunk, &mapKc, bar, c * 64, r0, g, b);
+                  tma_load_4d(dst + c * kChunk + 8192, &mapKc, bar, c * 64, r0 + 64, g, b);
+                }
+                for (int c = 0; c < vcs; ++c) {
+                  tma_load_4d(dst + (kcs + c) * kChunk, &mapVc, bar, c * 64, r0, g, b);
+                  tma_load_4d(dst + (kcs + c) * kChunk + 8192, &mapVc, bar, c * 64, r0 + 64, g, b);
+                }
+              } else {
+                int tk0, tk1;
+                if (br == kBrSlc) {
+                  int b0 = -1, b1 = -1;
+#pragma unroll
+                  for (int q = 0; q < 8; ++q)
+                    if (q == p) {
+                      b0 = bks[2 * q];
+                      b1 = bks[2 * q + 1];
+                    }
+                  tk0 = block_token(b0);
+                  tk1 = block_token(b1);
+                } else {
+                  tk0 = bk.start + 128 * p;
+                  tk1 = tk0 + 64;
+                }
+                for (int c = 0; c < kcs; ++c) {
+                  tma_load_4d(dst + c * kChunk, &mapK, bar, c * 64, g, tk0, b);
+                  tma_load_4d(dst + c * kChunk + 8192, &mapK, bar, c * 64, g, tk1, b);
+                }
+                for (int c = 0; c < vcs; ++c) {
+                  tma_load_4d(dst + (kcs + c) * kChunk, &mapV, bar, c * 64, g, tk0, b);
+                  tma_load_4d(dst + (kcs + c) * kChunk + 8192, &mapV, bar, c * 64, g, tk1, b);
+                }
+              }
+              ++jp;
+            }
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        for (int x = (nq > 2 ? nq - 2 : 0); x < nq; ++x)
+          mbar_wait_plain(&bars->q_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+        for (int x = (jp > 2 ? jp - 2 : 0); x < jp; ++x)
+          mbar_wait_plain(&bars->kv_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ===================================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, NP, false, false);
+      const uint32_t idesc_dq = idesc_bf16_f32(128, NP, true, false);
+      const uint32_t q_a = smem_u32(qbuf), kv_a = smem_u32(kvring), ds_a = smem_u32(dsbuf);
+      // first 64-row chunk of each dQ^T tile: 0, then dk - 128 (overlapping rows discarded)
+      const int mchunk1 = (a.dk - 128) / 64;
+      bool ok = true;
+      int jp = 0, jd = 0;
+      for (int i = 0; i < nitems && ok; ++i) {
+        const int t = t0 + i;
+        const int qb = i & 1;
+        const int qq = i & 1;
+        if (!mbar_wait(&bars->q_full[qb], (uint32_t)((i >> 1) & 1), abort_flag, a.st, 811) ||
+            !mbar_wait(&bars->dq_free[qq], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag, a.st, 812)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bool dq_started = false;
+        for (int br = 0; br < 3 && ok; ++br) {
+          const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
+          for (int pass = 0; pass < 2 && ok; ++pass) {
+            for (int p = 0; p < bk.np; ++p) {
+              const int slot = jp & 1, sb = jp & 3;
+              if (!mbar_wait(&bars->kv_full[slot], (uint32_t)((jp >> 1) & 1), abort_flag, a.st, 813) ||
+                  !mbar_wait(&bars->s_free[sb], (uint32_t)(((jp >> 2) & 1) ^ 1), abort_flag, a.st, 814)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t kvs = kv_a + slot * slot_bytes;
+              for (int c = 0; c < kcs; ++c) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = sdesc_sw128(kvs + c * kChunk + k * 32, 16, 1024);
+                  const uint64_t bd = sdesc_sw128(q_a + (qb * cs + c) * kQB + k * 32, 16, 1024);
+                  umma_bf16(tmem_sd + sb * 32, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+                }
+              }
+              for (int c = 0; c < vcs; ++c) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = sdesc_sw128(kvs + (kcs + c) * kChunk + k * 32, 16, 1024);
+                  const uint64_t bd = sdesc_sw128(q_a + (qb * cs + kcs + c) * kQB + k * 32, 16, 1024);
+                  umma_bf16(tmem_sd + sb * 32 + 16, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+                }
+              }
+              umma_commit(&bars->s_full[sb]);
+              if (pass == 1) {
+                const int db = jd & 1;
+                if (!mbar_wait(&bars->ds_full[db], (uint32_t)((jd >> 1) & 1), abort_flag, a.st, 815)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                for (int m = 0; m < nm; ++m) {
+                  const int mc = m == 0 ? 0 : mchunk1;
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) {
+                    // A = K^T (dk-major rows of keys), B = dS^T (head rows, keys along K)
+                    const uint64_t ad = sdesc_sw128(kvs + mc * kChunk + k * 2048, kChunk, 1024);
+                    const uint64_t bd = sdesc_sw128(ds_a + db * 2 * kQB + (k >> 2) * kQB + (k & 3) * 32, 16, 1024);
+                    umma_bf16(tmem_dq + qq * 32 + m * 16, ad, bd, idesc_dq, (dq_started || k > 0) ? 1u : 0u);
+                  }
+                }
+                dq_started = true;
+                umma_commit(&bars->ds_free[db]);
+                ++jd;
+              }
+              umma_commit(&bars->kv_empty[slot]);
+              ++jp;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(&bars->q_empty[qb]);
+        umma_commit(&bars->dq_full[qq]);
+      }
+      if (!ok || *abort_flag) {
+        umma_commit(&bars->drain);
+        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ===================================================================== softmax + epilogue
+    const int r = warp * 32 + lane;           // TMEM lane: key row of a tile / dk row of dQ^T
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float* red_m = red;                       // [4][NP]
+    float* red_l = red + 4 * NP;              // [4][NP]
+    float* red_a = red + 8 * NP;              // [4][NP]
+    bool ok = true;
+    uint32_t wg_phase = 0;
+    auto wg_sync = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->wg);
+      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 821)) ok = false;
+      ++wg_phase;
+    };
+    const int mchunk1 = (a.dk - 128) / 64;
+    int jp = 0, jd = 0;
+    for (int i = 0; i < nitems && ok; ++i) {
+      const int t = t0 + i;
+      const int qq = i & 1;
+      const size_t rowbase = ((size_t)b * a.T + t) * a.H + g * a.hpg;
+      int bks[16];
+      load_kept(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
+      bool any = false;
+      for (int br = 0; br < 3 && ok; ++br) {
+        const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
+        float gs[NP];
+#pragma unroll
+        for (int h = 0; h < NP; ++h) gs[h] = h < a.hpg ? __bfloat162float(a.gates[(rowbase + h) * 3 + br]) : 0.f;
+        float lse2[NP], dg[NP];
+        // ---- pass 0: per-thread online max / sum / sum of p * dP' over this lane's keys
+        {
+          float m[NP], l[NP], s1[NP];
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+            s1[h] = 0.f;
+          }
+          for (int p = 0; p < bk.np; ++p) {
+            const int sb = jp & 3;
+            if (!mbar_wait(&bars->s_full[sb], (uint32_t)((jp >> 2) & 1), abort_flag, a.st, 822)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t sr[16], dr[16];
+            tmem_ld16(tmem_sd + lane_base + sb * 32, sr);
+            tmem_ld16(tmem_sd + lane_base + sb * 32 + 16, dr);
+            tmem_ld_wait(sr);
+            tmem_reg_fence(dr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+            ++jp;
+            bool valid;
+            if (br == kBrCmp) {
+              valid = 128 * p + r < bk.start;
+            } else if (br == kBrSlc) {
+              int blk = -1;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (q == p) blk = (r >> 6) ? bks[2 * q + 1] : bks[2 * q];
+              valid = blk >= 0 && blk * 64 + (r & 63) <= t;
+            } else {
+              valid = bk.start + 128 * p + r <= t;
+            }
+            if (valid) {
+#pragma unroll
+              for (int h = 0; h < NP; ++h) {
+                const float s = __uint_as_float(sr[h]) * a.sc2;
+                const float dp = __uint_as_float(dr[h]);
+                if (s > m[h]) {
+                  const float f = fast_exp2(m[h] - s);   // 0 when m = -inf
+                  l[h] = fmaf(l[h], f, 1.f);
+                  s1[h] = fmaf(s1[h], f, dp);
+                  m[h] = s;
+                } else {
+                  const float e = fast_exp2(s - m[h]);
+                  l[h] += e;
+                  s1[h] = fmaf(e, dp, s1[h]);
+                }
+              }
+            }
+          }
+          if (!ok) break;
+          // merge across the 128 key lanes: per warp, then across the 4 warps
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            const float mw = warp_max_f32(m[h]);
+            const float f = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - mw);
+            m[h] = mw;
+            l[h] *= f;
+            s1[h] *= f;
+          }
+          const float lw = warp_sum16(l, lane);
+          const float aw = warp_sum16(s1, lane);
+          if (lane == 0)
+#pragma unroll
+            for (int h = 0; h < NP; ++h) red_m[warp * NP + h] = m[h];
+          if ((lane & 1) == 0) {
+            red_l[warp * NP + head_of_lane(lane)] = lw;
+            red_a[warp * NP + head_of_lane(lane)] = aw;
+          }
+          wg_sync();
+          if (!ok) break;
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) M = fmaxf(M, red_m[x * NP + h]);
+            float L = 0.f, A = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const float mx = red_m[x * NP + h];
+                const float f = (mx == -INFINITY) ? 0.f : fast_exp2(mx - M);
+                L = fmaf(red_l[x * NP + h], f, L);
+                A = fmaf(red_a[x * NP + h], f, A);
+              }
+            }
+            lse2[h] = L > 0.f ? M + __log2f(L) : INFINITY;
+            dg[h] = L > 0.f ? __fdividef(A, L) : 0.f;
+          }
+          // rows of this (t, group): thread h < hpg writes head h
+          if (r < a.hpg) {
+            float M = -INFINITY;
+            for (int x = 0; x < 4; ++x) M = fmaxf(M, red_m[x * NP + r]);
+            float L = 0.f, A = 0.f;
+            if (M != -INFINITY)
+              for (int x = 0; x < 4; ++x) {
+                const float mx = red_m[x * NP + r];
+                const float f = (mx == -INFINITY) ? 0.f : fast_exp2(mx - M);
+                L = fmaf(red_l[x * NP + r], f, L);
+                A = fmaf(red_a[x * NP + r], f, A);
+              }
+            // the same operations as the per-head values above, so the rows
+            // written here equal the ones this kernel's pass 1 uses
+            const float lv = L > 0.f ? M + __log2f(L) : INFINITY;
+            const float dv = L > 0.f ? __fdividef(A, L) : 0.f;
+            const size_t row = rowbase + r;
+            a.dgates[row * 3 + br] = dv;
+            a.lse[(size_t)br * a.T * a.H * gridDim.z + row] = lv;
+            a.dgw[(size_t)br * a.T * a.H * gridDim.z + row] = dv;
+          }
+          wg_sync();   // the reduction arrays are reused by the next branch
+          if (!ok) break;
+        }
+        // ---- pass 1: dS^T -> shared memory (bf16) for dQ^T += K^T dS^T
+        for (int p = 0; p < bk.np; ++p) {
+          const int sb = jp & 3;
+          const int db = jd & 1;
+          if (!mbar_wait(&bars->s_full[sb], (uint32_t)((jp >> 2) & 1), abort_flag, a.st, 823)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sr[16], dr[16];
+          tmem_ld16(tmem_sd + lane_base + sb * 32, sr);
+          tmem_ld16(tmem_sd + lane_base + sb * 32 + 16, dr);
+          tmem_ld_wait(sr);
+          tmem_reg_fence(dr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+          ++jp;
+          bool valid;
+          if (br == kBrCmp) {
+            valid = 128 * p + r < bk.start;
+          } else if (br == kBrSlc) {
+            int blk = -1;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q == p) blk = (r >> 6) ? bks[2 * q + 1] : bks[2 * q];
+            valid = blk >= 0 && blk * 64 + (r & 63) <= t;
+          } else {
+            valid = bk.start + 128 * p + r <= t;
+          }
+          if (!mbar_wait(&bars->ds_free[db], (uint32_t)(((jd >> 1) & 1) ^ 1), abort_flag, a.st, 824)) {
+            ok = false;
+            break;
+          }
+          const int kk = r & 63;
+          uint8_t* chunk = dsbuf + db * 2 * kQB + (r >> 6) * kQB + (kk & 7) * 2;
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            float ds = 0.f;
+            if (valid) {
+              const float pr = fast_exp2(fmaf(__uint_as_float(sr[h]), a.sc2, -lse2[h]));
+              ds = gs[h] * a.scale * pr * (__uint_as_float(dr[h]) - dg[h]);
+            }
+            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, kk >> 3)) = __float2bfloat16_rn(ds);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ds_full[db]);
+          ++jd;
+          any = true;
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: dq rows of this item (fp32)
+      if (!mbar_wait(&bars->dq_full[qq], (uint32_t)((i >> 1) & 1), abort_flag, a.st, 825)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int m = 0; m < nm; ++m) {
+        uint32_t rr[16];
+        tmem_ld16(tmem_dq + lane_base + qq * 32 + m * 16, rr);
+        tmem_ld_wait(rr);
+        const int drow = (m == 0 ? 0 : mchunk1 * 64) + r;
+        const bool own = drow < a.dk && (m == 0 || drow >= 128);
+        if (own) {
+#pragma unroll
+          for (int h = 0; h < NP; ++h)
+            if (h < a.hpg) a.dq[(rowbase + h) * a.dk + drow] = any ? __uint_as_float(rr[h]) : 0.f;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_free[qq]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// 2. selected-branch inverse lists and work units
+// ============================================================================
+// one thread per kept-block entry of idx [B,T,G,n]
+__global__ void slc_count_kernel(const int32_t* __restrict__ idx, int B, int T, int G, int n, int nblk,
+                                 int* __restrict__ cnt) {
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)B * T * G * n;
+  if (e >= total) return;
+  const int blk = idx[e];
+  const size_t btg = e / n;
+  const int g = (int)(btg % G);
+  const int b = (int)(btg / ((size_t)T * G));
+  if (blk >= 0 && blk < nblk) atomicAdd(&cnt[((size_t)b * G + g) * nblk + blk], 1);
+}
+
+__global__ void slc_fill_kernel(const int32_t* __restrict__ idx, int B, int T, int G, int n, int nblk,
+                                const int* __restrict__ offs, int* __restrict__ fill, int* __restrict__ inv) {
+  const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)B * T * G * n;
+  if (e >= total) return;
+  const int blk = idx[e];
+  const size_t btg = e / n;
+  const int g = (int)(btg % G);
+  const int t = (int)((btg / G) % T);
+  const int b = (int)(btg / ((size_t)T * G));
+  if (blk < 0 || blk >= nblk) return;
+  const size_t list = ((size_t)b * G + g) * nblk + blk;
+  const int pos = atomicAdd(&fill[list], 1);
+  inv[offs[list] + pos] = t;
+}
+
+struct UnitArgs {
+  int B, T, G, Nc, w, nblk;
+  int ntc, ntw;                 // 128-entry tiles of the compressed cache / 128-token tiles
+  const int* cnt;               // [B*G*nblk] selected-branch list lengths
+  int* offs;                    // [B*G*nblk] out: list starts in inv
+  int4* units[3];               // out: {b*G+g, first key, query lo, query hi}
+  int cap[3];
+  int* nunits;                  // out: [3]
+};
+
+// Exclusive scan of one value per thread over the CTA (1024 threads); returns
+// the thread's prefix and writes the CTA total to *total.
+__device__ int cta_exclusive_scan(int v, int* sh, int* total) {
+  const int lane = lane_id(), warp = warp_id();
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sh[32 + lane] = s;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? sh[32 + warp - 1] : 0) + x - v;
+  *total = sh[32 + (blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+// One CTA of 1024 threads: list starts of the selected branch, and the work
+// units of all three branches (each list cut into pieces of kRowsPerUnit).
+__global__ void __launch_bounds__(1024) build_units_kernel(const UnitArgs a) {
+  __shared__ int sh[64];
+  // selected-branch list starts
+  const int nl_s = a.B * a.G * a.nblk;
+  int carry = 0;
+  for (int base = 0; base < nl_s; base += blockDim.x) {
+    const int l = base + threadIdx.x;
+    const int v = l < nl_s ? a.cnt[l] : 0;
+    int tot;
+    const int pre = cta_exclusive_scan(v, sh, &tot);
+    if (l < nl_s) a.offs[l] = carry + pre;
+    carry += tot;
+  }
+  __syncthreads();
+  for (int br = 0; br < 3; ++br) {
+    const int per = br == kBrCmp ? a.ntc : (br == kBrWin ? a.ntw : a.nblk);
+    const int nl = a.B * a.G * per;
+    int ucarry = 0;
+    for (int base = 0; base < nl; base += blockDim.x) {
+      const int l = base + threadIdx.x;
+      int key0 = 0, lo = 0, hi = 0;
+      if (l < nl) {
+        const int tile = l % per;
+        if (br == kBrCmp) {
+          key0 = 128 * tile;
+          lo = min(a.T, 16 * key0 + 31);
+          hi = a.T;
+        } else if (br == kBrWin) {
+          key0 = 128 * tile;
+          lo = key0;
+          hi = min(a.T, key0 + 127 + a.w);
+        } else {
+          key0 = 64 * tile;
+          lo = a.offs[l];
+          hi = lo + a.cnt[l];
+        }
+      }
+      const int nu = hi > lo ? (hi - lo + kRowsPerUnit - 1) / kRowsPerUnit : 0;
+      int tot;
+      const int pre = cta_exclusive_scan(nu, sh, &tot);
+      for (int k = 0; k < nu; ++k) {
+        const int u = ucarry + pre + k;
+        if (u < a.cap[br])
+          a.units[br][u] = make_int4(l / per, key0, lo + k * kRowsPerUnit, min(hi, lo + (k + 1) * kRowsPerUnit));
+      }
+      ucarry += tot;
+    }
+    if (threadIdx.x == 0) a.nunits[br] = min(ucarry, a.cap[br]);
+    __syncthreads();
+  }
+}
+
+// ============================================================================
+// 3. key-outer dK / dV of one branch
+// ============================================================================
+struct DkvArgs {
+  int T, H, G, dk, dv, w, hpg, Nc;
+  float sc2, scale;
+  const __nv_bfloat16* gates;  // [B,T,H,3]
+  const float* lse;            // [B,T,H] of this branch
+  const float* dgw;            // [B,T,H] of this branch
+  const int* inv;              // selected branch: query lists
+  const int4* units;
+  const int* nunits;           // device count of this branch's units
+  float* dK;                   // cmp: [B,G,Nc,dk]; slc/win: [B,T,G,dk]  (fp32, reduced into)
+  float* dV;
+  DeviceStatus* st;
+  uint32_t off_q, off_col, off_bar;
+};
+
+struct DkvBars {
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t col_full[2], col_free[2];
+  uint64_t s_full, s_free;
+  uint64_t p_full, p_free;
+  uint64_t acc_full, acc_free;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort_flag;
+};
+
+struct ColInfo {
+  int t;        // query position, -1 for a padded column
+  float lse2;   // log2-domain log-sum-exp of the row
+  float dg;     // dout . O_b of the row
+  float gs;     // gate of the branch
+};
+
+constexpr int kDkvThreads = 192;   // warps 0-3 softmax / epilogue, 4 producer, 5 MMA
+constexpr int kQChunk = 8192;      // one 64-column chunk of 4 queries x 16 heads
+
+template <int BR>
+__global__ void __launch_bounds__(kDkvThreads, 1)
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                   const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                   const DkvArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int kcs = a.dk / 64, vcs = a.dv / 64, cs = kcs + vcs;
+  uint8_t* kv = smem;                                   // kcs K + vcs V chunks x 16 KB
+  uint8_t* qb_base = smem + a.off_q;                    // 2 x (kcs Q + vcs dout) chunks x 8 KB
+  ColInfo* cols = reinterpret_cast<ColInfo*>(smem + a.off_col);   // [2][64]
+  DkvBars* bars = reinterpret_cast<DkvBars*>(smem + a.off_bar);
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = warp_id(), lane = lane_id();
+  const int nunits = *a.nunits;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    mbar_init(&bars->kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->col_full[i], 32);
+      mbar_init(&bars->col_free[i], 4);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 4);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_free, 4);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = prior_error(a.st);
+    fence_barrier_init();
+  }
+  // key rows never loaded (the upper half of a selected-branch tile) and query
+  // rows hpg..15 stay zero
+  for (int i = threadIdx.x; i < (int)(a.off_col / 16); i += kDkvThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tm_s = tmem, tm_dp = tmem + 64, tm_pg = tmem + 128, tm_ds = tmem + 160;
+  const uint32_t tm_dk = tmem + 192, tm_dv = tmem + 192 + a.dk;
+
+  if (*abort_flag) {
+  } else if (warp == 4) {
+    // ===================================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapDO);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+    }
+    bool ok = true;
+    int jc = 0, ju = 0;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ju) {
+      const int4 un = a.units[u];
+      const int b = un.x / a.G, g = un.x % a.G, key0 = un.y;
+      const int nq = un.w - un.z;
+      const int nch = (nq + 3) / 4;
+      if (lane == 0) {
+        if (!mbar_wait(&bars->kv_empty, (uint32_t)((ju & 1) ^ 1), abort_flag, a.st, 831)) ok = false;
+        if (ok) {
+          const uint32_t rows_bytes = BR == kBrSlc ? 8192u : 16384u;
+          mbar_arrive_expect_tx(&bars->kv_full, (uint32_t)cs * rows_bytes);
+          for (int c = 0; c < cs; ++c) {
+            const CUtensorMap* m = c < kcs ? &mapK : &mapV;
+            const int col = (c < kcs ? c : c - kcs) * 64;
+            uint8_t* dst = kv + c * kChunk;
+            if (BR == kBrCmp) {
+              tma_load_4d(dst, m, &bars->kv_full, col, key0, g, b);
+              tma_load_4d(dst + 8192, m, &bars->kv_full, col, key0 + 64, g, b);
+            } else {
+              tma_load_4d(dst, m, &bars->kv_full, col, g, key0, b);
+              if (BR != kBrSlc) tma_load_4d(dst + 8192, m, &bars->kv_full, col, g, key0 + 64, b);
+            }
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      for (int ci = 0; ci < nch && ok; ++ci, ++jc) {
+        const int qb = jc & 1;
+        const uint32_t par = (uint32_t)(((jc >> 1) & 1) ^ 1);
+        if (lane == 0) {
+          if (!mbar_wait(&bars->q_empty[qb], par, abort_flag, a.st, 832) ||
+              !mbar_wait(&bars->col_free[qb], par, abort_flag, a.st, 833))
+            ok = false;
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        // the chunk's 4 query positions
+        int tq[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = un.z + 4 * ci + k;
+          tq[k] = e < un.w ? (BR == kBrSlc ? __ldg(a.inv + e) : e) : -1;
+        }
+        if (lane == 0) {
+          uint8_t* qd = qb_base + qb * cs * kQChunk;
+          mbar_arrive_expect_tx(&bars->q_full[qb], (uint32_t)(4 * cs * a.hpg * 128));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            for (int c = 0; c < kcs; ++c)
+              tma_load_4d(qd + c * kQChunk + k * kQB, &mapQ, &bars->q_full[qb], c * 64, g * a.hpg, tq[k], b);
+            for (int c = 0; c < vcs; ++c)
+              tma_load_4d(qd + (kcs + c) * kQChunk + k * kQB, &mapDO, &bars->q_full[qb], c * 64, g * a.hpg,
+                          tq[k], b);
+          }
+        }
+        // per-column data: column 16 k + h is head h of query k
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int col = lane + 32 * x;
+          const int k = col >> 4, h = col & 15;
+          int tk = -1;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            if (kk == k) tk = tq[kk];
+          ColInfo ci_;
+          ci_.t = -1;
+          ci_.lse2 = INFINITY;
+          ci_.dg = 0.f;
+          ci_.gs = 0.f;
+          if (tk >= 0 && h < a.hpg) {
+            const size_t row = ((size_t)b * a.T + tk) * a.H + g * a.hpg + h;
+            ci_.t = tk;
+            ci_.lse2 = a.lse[row];
+            ci_.dg = a.dgw[row];
+            ci_.gs = __bfloat162float(a.gates[row * 3 + BR]);
+          }
+          cols[qb * 64 + col] = ci_;
+        }
+        mbar_arrive(&bars->col_full[qb]);
+      }
+    }
+    if (lane == 0 && (!ok || *abort_flag)) {
+      for (int x = (jc > 2 ? jc - 2 : 0); x < jc; ++x)
+        mbar_wait_plain(&bars->q_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+      if (ju > 0) mbar_wait_plain(&bars->kv_full, (uint32_t)((ju - 1) & 1), kWaitLimitNs);
+    }
+  } else if (warp == 5) {
+    // ===================================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
+      const uint32_t idesc_dv = idesc_bf16_f32(128, a.dv, false, true);
+      const uint32_t idesc_dk = idesc_bf16_f32(128, a.dk, false, true);
+      const uint32_t kv_a = smem_u32(kv), q_a = smem_u32(qb_base);
+      bool ok = true;
+      int jc = 0, ju = 0;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ju) {
+        const int4 un = a.units[u];
+        const int nch = (un.w - un.z + 3) / 4;
+        if (!mbar_wait(&bars->kv_full, (uint32_t)(ju & 1), abort_flag, a.st, 841) ||
+            !mbar_wait(&bars->acc_free, (uint32_t)((ju & 1) ^ 1), abort_flag, a.st, 842)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ci = 0; ci < nch; ++ci, ++jc) {
+          const int qb = jc & 1;
+          const uint32_t qd = q_a + qb * cs * kQChunk;
+          if (!mbar_wait(&bars->q_full[qb], (uint32_t)((jc >> 1) & 1), abort_flag, a.st, 843) ||
+              !mbar_wait(&bars->s_free, (uint32_t)((jc & 1) ^ 1), abort_flag, a.st, 844)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int c = 0; c < kcs; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(kv_a + c * kChunk + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(qd + c * kQChunk + k * 32, 16, 1024);
+              umma_bf16(tm_s, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          for (int c = 0; c < vcs; ++c) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(kv_a + (kcs + c) * kChunk + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(qd + (kcs + c) * kQChunk + k * 32, 16, 1024);
+              umma_bf16(tm_dp, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&bars->s_full);
+          if (!mbar_wait(&bars->p_full, (uint32_t)(jc & 1), abort_flag, a.st, 845)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // B = dout / Q rows (t, h) along K, head dims along N (N-major, 8 KB per 64 columns)
+            const uint64_t bdo = sdesc_sw128(qd + kcs * kQChunk + k * 2048, kQChunk, 1024);
+            umma_bf16_ts(tm_dv, tm_pg + 8 * k, bdo, idesc_dv, (ci > 0 || k > 0) ? 1u : 0u);
+            const uint64_t bq = sdesc_sw128(qd + k * 2048, kQChunk, 1024);
+            umma_bf16_ts(tm_dk, tm_ds + 8 * k, bq, idesc_dk, (ci > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&bars->q_empty[qb]);
+          umma_commit(&bars->p_free);
+        }
+        if (!ok) break;
+        umma_commit(&bars->kv_empty);
+        umma_commit(&bars->acc_full);
+      }
+      if (!ok || *abort_flag) {
+        umma_commit(&bars->drain);
+        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ===================================================================== softmax + epilogue
+    const int r = warp * 32 + lane;           // TMEM lane = key row of the tile
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    int jc = 0, ju = 0;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ju) {
+      const int4 un = a.units[u];
+      const int b = un.x / a.G, g = un.x % a.G, key0 = un.y;
+      const int nch = (un.w - un.z + 3) / 4;
+      // this lane's key: compressed entry or token position
+      const int key = key0 + r;
+      const bool key_ok = BR == kBrCmp ? key < a.Nc : (BR == kBrSlc ? (r < 64 && key < a.T) : key < a.T);
+      const int vis_from = BR == kBrCmp ? 16 * key + 31 : key;   // first query that sees the key
+      for (int ci = 0; ci < nch; ++ci, ++jc) {
+        const int qb = jc & 1;
+        const uint32_t par = (uint32_t)((jc >> 1) & 1);
+        if (!mbar_wait(&bars->col_full[qb], par, abort_flag, a.st, 851) ||
+            !mbar_wait(&bars->s_full, (uint32_t)(jc & 1), abort_flag, a.st, 852)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const ColInfo* cc = cols + qb * 64;
+        uint32_t pg[32], dsv[32];
+#pragma unroll
+        for (int grp = 0; grp < 4; ++grp) {
+          uint32_t sr[16], dr[16];
+          tmem_ld16(tm_s + lane_base + grp * 16, sr);
+          tmem_ld16(tm_dp + lane_base + grp * 16, dr);
+          tmem_ld_wait(sr);
+          tmem_reg_fence(dr);
+#pragma unroll
+          for (int h = 0; h < 16; h += 2) {
+            float pv[2], dv2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const ColInfo c = cc[grp * 16 + h + e];
+              bool vis = key_ok && c.t >= 0 && c.t >= vis_from;
+              if (BR == kBrWin) vis = vis && key > c.t - a.w;
+              float p = 0.f, d = 0.f;
+              if (vis) {
+                p = fast_exp2(fmaf(__uint_as_float(sr[h + e]), a.sc2, -c.lse2));
+                d = c.gs * a.scale * p * (__uint_as_float(dr[h + e]) - c.dg);
+                p *= c.gs;
+              }
+              pv[e] = p;
+              dv2[e] = d;
+            }
+            pg[grp * 8 + h / 2] = pack_bf16x2(pv[0], pv[1]);
+            dsv[grp * 8 + h / 2] = pack_bf16x2(dv2[0], dv2[1]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->s_free);
+          mbar_arrive(&bars->col_free[qb]);
+        }
+        if (!mbar_wait(&bars->p_free, (uint32_t)((jc & 1) ^ 1), abort_flag, a.st, 853)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          uint32_t x0[16], x1[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            x0[e] = pg[e];
+            x1[e] = pg[16 + e];
+          }
+          tmem_st16(tm_pg + lane_base, x0);
+          tmem_st16(tm_pg + lane_base + 16, x1);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            x0[e] = dsv[e];
+            x1[e] = dsv[16 + e];
+          }
+          tmem_st16(tm_ds + lane_base, x0);
+          tmem_st16(tm_ds + lane_base + 16, x1);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue: this unit's dK / dV rows reduced into global memory
+      if (!mbar_wait(&bars->acc_full, (uint32_t)(ju & 1), abort_flag, a.st, 854)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float* dkrow = nullptr;
+      float* dvrow = nullptr;
+      if (key_ok) {
+        if (BR == kBrCmp) {
+          dkrow = a.dK + (((size_t)b * a.G + g) * a.Nc + key) * a.dk;
+          dvrow = a.dV + (((size_t)b * a.G + g) * a.Nc + key) * a.dv;
+        } else {
+          dkrow = a.dK + (((size_t)b * a.T + key) * a.G + g) * a.dk;
+          dvrow = a.dV + (((size_t)b * a.T + key) * a.G + g) * a.dv;
+        }
+      }
+      for (int c0 = 0; c0 < a.dk; c0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tm_dk + lane_base + c0, rr);
+        tmem_ld_wait(rr);
+        if (dkrow != nullptr)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) atomicAdd(dkrow + c0 + e, __uint_as_float(rr[e]));
+      }
+      for (int c0 = 0; c0 < a.dv; c0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tm_dv + lane_base + c0, rr);
+        tmem_ld_wait(rr);
+        if (dvrow != nullptr)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) atomicAdd(dvrow + c0 + e, __uint_as_float(rr[e]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_free);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================
+// 4. compression backward (fp32, CUDA cores)
+// ============================================================================
+// s[e] = sum over (b, g, i) of dXc[b,g,i,e]
+__global__ void colsum_kernel(const float* __restrict__ dxc, size_t rows, int D, float* __restrict__ s) {
+  const int e = threadIdx.x;   // blockDim.x == D
+  float acc = 0.f;
+  for (size_t r = blockIdx.x; r < rows; r += gridDim.x) acc += dxc[r * D + e];
+  atomicAdd(s + e, acc);
+}
+
+// dPE[r, c] = sum_e s[e] W[r*D + c, e]   (one CTA per offset r, one thread per c)
+__global__ void dpe_kernel(const float* __restrict__ s, const __nv_bfloat16* __restrict__ W, int D,
+                           float* __restrict__ dpe) {
+  const int r = blockIdx.x, c = threadIdx.x;
+  const __nv_bfloat16* wr = W + ((size_t)r * D + c) * D;
+  float acc = 0.f;
+  for (int e = 0; e < D; ++e) acc = fmaf(s[e], __bfloat162float(wr[e]), acc);
+  dpe[(size_t)r * D + c] = acc;
+}
+
+// dX[b, 16 i + rr, g, c] += sum_{q in {0,1}} sum_e dXc[b,g,i-q,e] W[(rr + 16 q) D + c, e]
+// for rr in [0,16): tile of 64 entries i x 64 columns c, 256 threads x (4 x 4).
+// X is token-major [B,T,G,D] (fp32, the dk / dv output, added into).
+__global__ void __launch_bounds__(256) dx_kernel(const float* __restrict__ dxc, const __nv_bfloat16* __restrict__ W,
+                                                 int B, int T, int G, int Nc, int D, float* __restrict__ dX) {
+  __shared__ float sa[16][65];   // [e][i]
+  __shared__ float sw[16][65];   // [e][c]
+  const int i0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  const int rr = blockIdx.z % 16, bg = blockIdx.z / 16;
+  const int b = bg / G, g = bg % G;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+  const float* base = dxc + (size_t)bg * Nc * D;
+  for (int q = 0; q < 2; ++q) {
+    const int wrow = (rr + 16 * q) * D;
+    for (int e0 = 0; e0 < D; e0 += 16) {
+      for (int x = threadIdx.x; x < 16 * 64; x += 256) {
+        const int ii = x / 16, e = x % 16;
+        const int ent = i0 + ii - q;
+        sa[e][ii] = (ent >= 0 && ent < Nc) ? base[(size_t)ent * D + e0 + e] : 0.f;
+        sw[e][ii] = __bfloat162float(W[(size_t)(wrow + c0 + ii) * D + e0 + e]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float av[4], wv[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) av[x] = sa[e][ty * 4 + x];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) wv[y] = sw[e][tx * 4 + y];
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+          for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], wv[y], acc[x][y]);
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int tok = 16 * (i0 + ty * 4 + x) + rr;
+    if (tok >= T) continue;
+    float* o = dX + (((size_t)b * T + tok) * G + g) * D + c0 + tx * 4;
+#pragma unroll
+    for (int y = 0; y < 4; ++y) o[y] += acc[x][y];
+  }
+}
+
+// dW[r*D + c, e] += sum over rows rho = (b, g, i) of (X[b, 16 i + r, g, c] + PE[r, c]) dXc[rho, e]:
+// tile 64 c x 64 e, rows split in pieces of 256, fp32 reductions into dW.
+__global__ void __launch_bounds__(256) dw_kernel(const __nv_bfloat16* __restrict__ X,
+                                                 const __nv_bfloat16* __restrict__ PE,
+                                                 const float* __restrict__ dxc, int B, int T, int G, int Nc, int D,
+                                                 float* __restrict__ dW) {
+  __shared__ float sx[16][65];   // [row][c]
+  __shared__ float sd[16][65];   // [row][e]
+  const int c0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int r = blockIdx.z % 32, piece = blockIdx.z / 32;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const size_t rows = (size_t)B * G * Nc;
+  const size_t r_lo = (size_t)piece * 256, r_hi = min(rows, r_lo + 256);
+  float acc[4][4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y) acc[x][y] = 0.f;
+  for (size_t rb = r_lo; rb < r_hi; rb += 16) {
+    for (int x = threadIdx.x; x < 16 * 64; x += 256) {
+      const int rw = x / 64, cc = x % 64;
+      const size_t rho = rb + rw;
+      float xv = 0.f, dv = 0.f;
+      if (rho < r_hi) {
+        const int i = (int)(rho % Nc);
+        const size_t bg = rho / Nc;
+        const int g = (int)(bg % G), b = (int)(bg / G);
+        xv = __bfloat162float(X[(((size_t)b * T + 16 * i + r) * G + g) * D + c0 + cc]) +
+             __bfloat162float(PE[(size_t)r * D + c0 + cc]);
+        dv = dxc[rho * D + e0 + cc];
+      }
+      sx[rw][cc] = xv;
+      sd[rw][cc] = dv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int rw = 0; rw < 16; ++rw) {
+      float xv[4], dv[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) xv[x] = sx[rw][ty * 4 + x];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) dv[y] = sd[rw][tx * 4 + y];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(xv[x], dv[y], acc[x][y]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+#pragma unroll
+    for (int y = 0; y < 4; ++y)
+      atomicAdd(dW + ((size_t)r * D + c0 + ty * 4 + x) * D + e0 + tx * 4 + y, acc[x][y]);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+struct DqLayout {
+  uint32_t off_kv, off_ds, off_red, off_bar, total;
+};
+DqLayout dq_layout(int dk, int dv) {
+  const int cs = dk / 64 + dv / 64;
+  DqLayout L;
+  L.off_kv = (uint32_t)align_up((size_t)2 * cs * kQB, 1024);
+  L.off_ds = L.off_kv + 2 * cs * kChunk;
+  L.off_red = L.off_ds + 2 * 2 * kQB;
+  L.off_bar = (uint32_t)align_up(L.off_red + 3 * 4 * NP * sizeof(float), 256);
+  L.total = L.off_bar + (uint32_t)align_up(sizeof(DqBars), 256) + 1024;
+  return L;
+}
+
+struct DkvLayout {
+  uint32_t off_q, off_col, off_bar, total;
+};
+DkvLayout dkv_layout(int dk, int dv) {
+  const int cs = dk / 64 + dv / 64;
+  DkvLayout L;
+  L.off_q = (uint32_t)(cs * kChunk);
+  L.off_col = L.off_q + 2 * cs * kQChunk;
+  L.off_bar = (uint32_t)align_up(L.off_col + 2 * 64 * sizeof(ColInfo), 256);
+  L.total = L.off_bar + (uint32_t)align_up(sizeof(DkvBars), 256) + 1024;
+  return L;
+}
+
+// q-like tensor [B,T,H,d]: boxes of 64 columns x hpg heads x 1 row
+bool make_rows_map(CUtensorMap* m, const void* p, int B, int T, int H, int d, int hpg) {
+  const uint64_t e = 2;
+  const uint64_t dims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+  const uint64_t str[3] = {d * e, (uint64_t)H * d * e, (uint64_t)T * H * d * e};
+  const uint32_t box[4] = {64, (uint32_t)hpg, 1, 1};
+  return make_tmap_bf16(m, p, 4, dims, str, box);
+}
+
+}  // namespace
+
+int bwd_supported(const nsa_cfg& c) {
+  const int hpg = c.H / c.G;
+  if (hpg > NP || c.n > 16 || (c.dk != 128 && c.dk != 192) || (c.dv != 64 && c.dv != 128)) return NSA_ERR_UNSUPPORTED;
+  if (c.T > 65536 || c.B > 65535) return NSA_ERR_UNSUPPORTED;
+  // grid limits of the compression-backward launches
+  const long long Nc = c.T < 32 ? 0 : (c.T - 32) / 16 + 1;
+  if (16ll * c.B * c.G > 65535 || 32ll * ((c.B * c.G * Nc + 255) / 256) > 65535) return NSA_ERR_UNSUPPORTED;
+  if (dq_layout(c.dk, c.dv).total > smem_max() || dkv_layout(c.dk, c.dv).total > smem_max())
+    return NSA_ERR_UNSUPPORTED;
+  return NSA_OK;
+}
+
+BwdWs bwd_ws(const nsa_cfg& c, size_t header) {
+  const int Nc = c.T < 32 ? 0 : (c.T - 32) / 16 + 1;
+  const int nblk = (c.T + 63) / 64;
+  const size_t rows = (size_t)c.B * c.T * c.H;
+  const size_t lists = (size_t)c.B * c.G * nblk;
+  const int ntc = (Nc + 127) / 128, ntw = (c.T + 127) / 128;
+  const size_t per_list = (size_t)(c.T + kRowsPerUnit - 1) / kRowsPerUnit + 1;
+  BwdWs w;
+  w.cap[kBrCmp] = (size_t)c.B * c.G * ntc * per_list;
+  w.cap[kBrWin] = (size_t)c.B * c.G * ntw * ((127 + c.w + kRowsPerUnit - 1) / kRowsPerUnit + 1);
+  w.cap[kBrSlc] = lists + (size_t)c.B * c.T * c.G * c.n / kRowsPerUnit + 1;
+  size_t o = header;
+  w.lse = o;   o = align_up(o + 3 * rows * sizeof(float), 256);
+  w.dgw = o;   o = align_up(o + 3 * rows * sizeof(float), 256);
+  w.dkc = o;   o = align_up(o + (size_t)c.B * c.G * Nc * c.dk * sizeof(float), 256);
+  w.dvc = o;   o = align_up(o + (size_t)c.B * c.G * Nc * c.dv * sizeof(float), 256);
+  w.zero_begin = o;
+  w.cnt = o;   o = align_up(o + lists * sizeof(int), 256);
+  w.fill = o;  o = align_up(o + lists * sizeof(int), 256);
+  w.csum = o;  o = align_up(o + (size_t)(c.dk + c.dv) * sizeof(float), 256);
+  w.zero_end = o;
+  w.offs = o;  o = align_up(o + lists * sizeof(int), 256);
+  w.nunits = o; o = align_up(o + 4 * sizeof(int), 256);
+  w.inv = o;   o = align_up(o + (size_t)c.B * c.T * c.G * c.n * sizeof(int), 256);
+  for (int br = 0; br < 3; ++br) {
+    w.units[br] = o;
+    o = align_up(o + w.cap[br] * sizeof(int4), 256);
+  }
+  w.end = o;
+  return w;
+}
+
+int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const BwdWs& w, cudaStream_t s) {
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(ws);
+  const int hpg = c.H / c.G;
+  const int Nc = c.T < 32 ? 0 : (c.T - 32) / 16 + 1;
+  const int nblk = (c.T + 63) / 64;
+  const float scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.dk);
+  const float sc2 = scale * 1.4426950408889634f;
+  float* lse = reinterpret_cast<float*>(ws + w.lse);
+  float* dgw = reinterpret_cast<float*>(ws + w.dgw);
+  float* dkc = reinterpret_cast<float*>(ws + w.dkc);
+  float* dvc = reinterpret_cast<float*>(ws + w.dvc);
+  const size_t rows = (size_t)c.B * c.T * c.H;
+
+  // zeroed outputs and counters
+  if (cudaMemsetAsync(p.dk, 0, sizeof(float) * (size_t)c.B * c.T * c.G * c.dk, s) != cudaSuccess ||
+      cudaMemsetAsync(p.dv, 0, sizeof(float) * (size_t)c.B * c.T * c.G * c.dv, s) != cudaSuccess ||
+      cudaMemsetAsync(p.dw_k, 0, sizeof(float) * (size_t)32 * c.dk * c.dk, s) != cudaSuccess ||
+      cudaMemsetAsync(p.dw_v, 0, sizeof(float) * (size_t)32 * c.dv * c.dv, s) != cudaSuccess ||
+      cudaMemsetAsync(p.dpe_k, 0, sizeof(float) * (size_t)32 * c.dk, s) != cudaSuccess ||
+      cudaMemsetAsync(p.dpe_v, 0, sizeof(float) * (size_t)32 * c.dv, s) != cudaSuccess ||
+      cudaMemsetAsync(ws + w.dkc, 0, w.zero_begin - w.dkc, s) != cudaSuccess ||
+      cudaMemsetAsync(ws + w.zero_begin, 0, w.zero_end - w.zero_begin, s) != cudaSuccess)
+    return NSA_ERR_CUDA;
+
+  CUtensorMap mq, mdo, mk, mv, mkc, mvc;
+  if (!make_rows_map(&mq, p.q, c.B, c.T, c.H, c.dk, hpg) || !make_rows_map(&mdo, p.dout, c.B, c.T, c.H, c.dv, hpg) ||
+      !make_kv_map(&mk, p.k, c.B, c.T, c.G, c.dk, 64, false) || !make_kv_map(&mv, p.v, c.B, c.T, c.G, c.dv, 64, false))
+    return NSA_ERR_CUDA;
+  // the compressed cache as a head-major [B,G,Nc,d] tensor (a 1-row stand-in when empty)
+  const int ncr = Nc > 0 ? Nc : 1;
+  if (!make_kv_map(&mkc, Nc > 0 ? p.kc : p.k, c.B, ncr, c.G, c.dk, 64, true) ||
+      !make_kv_map(&mvc, Nc > 0 ? p.vc : p.v, c.B, ncr, c.G, c.dv, 64, true))
+    return NSA_ERR_CUDA;
+
+  // ---- 1. dq, dgates, per-branch statistics
+  {
+    const DqLayout L = dq_layout(c.dk, c.dv);
+    DqArgs a;
+    a.T = c.T;
+    a.H = c.H;
+    a.G = c.G;
+    a.dk = c.dk;
+    a.dv = c.dv;
+    a.n = c.n;
+    a.w = c.w;
+    a.hpg = hpg;
+    a.Nc = Nc;
+    a.QPC = 16;
+    a.sc2 = sc2;
+    a.scale = scale;
+    a.idx = p.idx;
+    a.gates = static_cast<const __nv_bfloat16*>(p.gates);
+    a.dq = p.dq;
+    a.dgates = p.dgates;
+    a.lse = lse;
+    a.dgw = dgw;
+    a.st = st;
+    a.off_kv = L.off_kv;
+    a.off_ds = L.off_ds;
+    a.off_red = L.off_red;
+    a.off_bar = L.off_bar;
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dq_kernel), L.total)) return rc;
+    dim3 grid((c.T + a.QPC - 1) / a.QPC, c.G, c.B);
+    prof::begin("bwd_dq", s);
+    bwd_dq_kernel<<<grid, kDqThreads, L.total, s>>>(mq, mdo, mk, mv, mkc, mvc, a);
+    prof::end(s);
+    if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  }
+
+  // ---- 2. selected-branch inverse lists, work units
+  int* cnt = reinterpret_cast<int*>(ws + w.cnt);
+  int* fill = reinterpret_cast<int*>(ws + w.fill);
+  int* offs = reinterpret_cast<int*>(ws + w.offs);
+  int* inv = reinterpret_cast<int*>(ws + w.inv);
+  int* nunits = reinterpret_cast<int*>(ws + w.nunits);
+  {
+    const size_t entries = (size_t)c.B * c.T * c.G * c.n;
+    const unsigned nb = (unsigned)((entries + 255) / 256);
+    prof::begin("bwd_lists", s);
+    slc_count_kernel<<<nb, 256, 0, s>>>(p.idx, c.B, c.T, c.G, c.n, nblk, cnt);
+    UnitArgs ua;
+    ua.B = c.B;
+    ua.T = c.T;
+    ua.G = c.G;
+    ua.Nc = Nc;
+    ua.w = c.w;
+    ua.nblk = nblk;
+    ua.ntc = (Nc + 127) / 128;
+    ua.ntw = (c.T + 127) / 128;
+    ua.cnt = cnt;
+    ua.offs = offs;
+    for (int br = 0; br < 3; ++br) {
+      ua.units[br] = reinterpret_cast<int4*>(ws + w.units[br]);
+      ua.cap[br] = (int)w.cap[br];
+    }
+    ua.nunits = nunits;
+    build_units_kernel<<<1, 1024, 0, s>>>(ua);
+    slc_fill_kernel<<<nb, 256, 0, s>>>(p.idx, c.B, c.T, c.G, c.n, nblk, offs, fill, inv);
+    prof::end(s);
+    if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  }
+
+  // ---- 3. key-outer dK / dV per branch
+  {
+    const DkvLayout L = dkv_layout(c.dk, c.dv);
+    int nsm = 148;
+    {
+      int dev = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    }
+    for (int br = 0; br < 3; ++br) {
+      if (br == kBrCmp && Nc == 0) continue;
+      DkvArgs a;
+      a.T = c.T;
+      a.H = c.H;
+      a.G = c.G;
+      a.dk = c.dk;
+      a.dv = c.dv;
+      a.w = c.w;
+      a.hpg = hpg;
+      a.Nc = Nc;
+      a.sc2 = sc2;
+      a.scale = scale;
+      a.gates = static_cast<const __nv_bfloat16*>(p.gates);
+      a.lse = lse + (size_t)br * rows;
+      a.dgw = dgw + (size_t)br * rows;
+      a.inv = inv;
+      a.units = reinterpret_cast<const int4*>(ws + w.units[br]);
+      a.nunits = nunits + br;
+      a.dK = br == kBrCmp ? dkc : p.dk;
+      a.dV = br == kBrCmp ? dvc : p.dv;
+      a.st = st;
+      a.off_q = L.off_q;
+      a.off_col = L.off_col;
+      a.off_bar = L.off_bar;
+      const unsigned grid = (unsigned)std::min<size_t>((size_t)nsm, std::max<size_t>(1, w.cap[br]));
+      if (br == kBrCmp) {
+        if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dkv_kernel<kBrCmp>), L.total)) return rc;
+        prof::begin("bwd_dkv_cmp", s);
+        bwd_dkv_kernel<kBrCmp><<<grid, kDkvThreads, L.total, s>>>(mq, mdo, mkc, mvc, a);
+      } else if (br == kBrSlc) {
+        if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dkv_kernel<kBrSlc>), L.total)) return rc;
+        prof::begin("bwd_dkv_slc", s);
+        bwd_dkv_kernel<kBrSlc><<<grid, kDkvThreads, L.total, s>>>(mq, mdo, mk, mv, a);
+      } else {
+        if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dkv_kernel<kBrWin>), L.total)) return rc;
+        prof::begin("bwd_dkv_win", s);
+        bwd_dkv_kernel<kBrWin><<<grid, kDkvThreads, L.total, s>>>(mq, mdo, mk, mv, a);
+      }
+      prof::end(s);
+      if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+    }
+  }
+
+  // ---- 4. compression backward
+  if (Nc > 0) {
+    float* csum = reinterpret_cast<float*>(ws + w.csum);
+    const size_t crow = (size_t)c.B * c.G * Nc;
+    prof::begin("bwd_compress", s);
+    for (int kvs = 0; kvs < 2; ++kvs) {
+      const int D = kvs == 0 ? c.dk : c.dv;
+      const float* dxc = kvs == 0 ? dkc : dvc;
+      float* sv = csum + (kvs == 0 ? 0 : c.dk);
+      const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(kvs == 0 ? c.w_k : c.w_v);
+      const __nv_bfloat16* PE = static_cast<const __nv_bfloat16*>(kvs == 0 ? c.pe_k : c.pe_v);
+      const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(kvs == 0 ? p.k : p.v);
+      colsum_kernel<<<(unsigned)std::min<size_t>(crow, 1184), D, 0, s>>>(dxc, crow, D, sv);
+      dpe_kernel<<<32, D, 0, s>>>(sv, W, D, kvs == 0 ? p.dpe_k : p.dpe_v);
+      dim3 gx((unsigned)((c.T + 16 * 64 - 1) / (16 * 64)), (unsigned)(D / 64), (unsigned)(16 * c.B * c.G));
+      dx_kernel<<<gx, 256, 0, s>>>(dxc, W, c.B, c.T, c.G, Nc, D, kvs == 0 ? p.dk : p.dv);
+      dim3 gw((unsigned)(D / 64), (unsigned)(D / 64), (unsigned)(32 * ((crow + 255) / 256)));
+      dw_kernel<<<gw, 256, 0, s>>>(X, PE, dxc, c.B, c.T, c.G, Nc, D, kvs == 0 ? p.dw_k : p.dw_v);
+    }
+    prof::end(s);
+    if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  }
+  return NSA_OK;
+}
+
+}  // namespace nsa

@@ -82,4 +82,20 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
                const void* v, const int32_t* lens, void* out, int32_t* idx_out, uint8_t* ws, cudaStream_t s,
                int rows_per_seq = 1);
 
+// ---- prefill backward (backward.cu)
+struct BwdPtrs {
+  const void *q, *k, *v, *gates, *kc, *vc, *dout;
+  const int32_t* idx;
+  float *dq, *dk, *dv, *dgates, *dw_k, *dw_v, *dpe_k, *dpe_v;
+};
+// byte offsets of the backward's scratch inside the workspace; [zero_begin,
+// zero_end) and [dkc, zero_begin) are cleared by every call
+struct BwdWs {
+  size_t lse, dgw, dkc, dvc, zero_begin, cnt, fill, csum, zero_end, offs, nunits, inv, units[3], end;
+  size_t cap[3];
+};
+int bwd_supported(const nsa_cfg& c);
+BwdWs bwd_ws(const nsa_cfg& c, size_t header);
+int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const BwdWs& w, cudaStream_t s);
+
 }  // namespace nsa

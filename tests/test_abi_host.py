@@ -294,3 +294,38 @@ def test_decode_multi_argument_checks(nsa):
     assert call(ws_bytes=need - 1) == 4
     if not torch.cuda.is_available():
         assert call() == 7
+
+
+def test_prefill_backward_argument_checks(nsa):
+    c = nsa.make_cfg(1, 65536, 64, 4, 192, 128)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    need = nsa.nsa_prefill_bwd_workspace_size(c)
+    # the per-branch log-sum-exp and dg rows alone: 2 x 3 x T x H fp32
+    assert need >= 256 + 2 * 3 * 65536 * 64 * 4
+    f = nsa.lib.nsa_prefill_bwd
+
+    def call(cfg=c, **kw):
+        names = ["q", "k", "v", "gates", "kc", "vc", "idx", "dout", "dq", "dk", "dv", "dgates", "dw_k", "dw_v",
+                 "dpe_k", "dpe_v"]
+        a = {n: FAKE for n in names}
+        a.update(ws=FAKE, ws_bytes=need)
+        a.update(kw)
+        return f(ctypes.byref(cfg), *[a[n] for n in names], a["ws"], a["ws_bytes"], None)
+    assert call(q=None) == 1
+    assert call(idx=None) == 1
+    assert call(dpe_v=None) == 1
+    assert call(dout=FAKE + 2) == 3
+    assert call(ws=FAKE + 16) == 3                      # workspace must be 256-byte aligned
+    assert call(ws_bytes=need - 1) == 4
+    wide = nsa.make_cfg(1, 4096, 64, 2, 192, 128)       # 32 heads per group
+    wide.pe_k = wide.pe_v = wide.w_k = wide.w_v = FAKE
+    assert nsa.nsa_prefill_bwd_workspace_size(wide) == 0
+    assert call(cfg=wide) == 2
+    small_dk = nsa.make_cfg(1, 4096, 64, 4, 64, 128)    # dk 64 is not implemented by the backward
+    small_dk.pe_k = small_dk.pe_v = small_dk.w_k = small_dk.w_v = FAKE
+    assert call(cfg=small_dk) == 2
+    c.w_v = None
+    assert call() == 1
+    c.w_v = FAKE
+    if not torch.cuda.is_available():
+        assert call() == 7

@@ -162,3 +162,28 @@ def test_compress_backward_mean_pool_closed_form():
                 ref[s] += dXc[i] / l
     np.testing.assert_allclose(dX, ref, rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(dPE, np.broadcast_to(dXc.sum(axis=0) / l, (l, dx)), rtol=1e-13)
+
+
+def test_key_shift_invariance_gives_zero_dpe_k(case):
+    """Softmax is unchanged when one vector is added to every key of a branch
+    (each score of a row moves by the same q . c), so the gradients of a
+    branch's keys sum to zero for every query: sum_j dS_j = sum_j P_j (dP_j -
+    dO . O) = dO . O - dO . O = 0.  Summed over the compressed cache this
+    makes sum_i dKc_i = 0, hence dPE_K = sum_i dKc_i W_r^T = 0, while dPE_V
+    (values carry no such invariance) is not."""
+    inp, dout, idx, _ = case
+    g = BW.nsa_prefill_backward(inp, dout, params=PARAMS, idx=idx)
+    assert g["dkc"].shape[1] > 0
+    scale_k = np.abs(g["dkc"]).sum(axis=1).max()
+    assert np.abs(g["dkc"].sum(axis=1)).max() <= 1e-12 * scale_k
+    assert np.abs(g["dpe_k"]).max() <= 1e-12 * np.abs(g["dw_k"]).max()
+    assert np.abs(g["dpe_v"]).max() > 1e-3 * np.abs(g["dw_v"]).max()
+    # selected and window keys: each row's gradient over its own keys sums to
+    # zero too, so the token-level dk summed over all tokens (minus the part
+    # that reaches the tokens through the compression map) vanishes
+    K = BW._inputs_f64(inp, 0)["k"]
+    for gg in range(WL.G):
+        dKx, _, _ = BW.compress_bwd(K[:, gg], BW._inputs_f64(inp, 0)["pe_k"], BW._inputs_f64(inp, 0)["w_k"],
+                                    PARAMS.l, PARAMS.d, g["dkc"][gg])
+        direct = g["dk"][:, gg] - dKx
+        assert np.abs(direct.sum(axis=0)).max() <= 1e-10 * np.abs(direct).sum(axis=0).max()
