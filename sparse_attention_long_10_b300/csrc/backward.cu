@@ -97,6 +97,8 @@ __device__ __forceinline__ int block_token(int blk) { return blk >= 0 ? blk * 64
 // ============================================================================
 struct DqArgs {
   int T, H, G, dk, dv, n, w, hpg, Nc, QPC;
+  int br_lo, br_hi;                // branches handled (cmp 0, slc 1, win 2)
+  int acc_dq;                      // add to dq (another kernel wrote the other branches)
   float sc2, scale;
   const int32_t* idx;              // [B,T,G,n]
   const __nv_bfloat16* gates;      // [B,T,H,3]
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         ++nq;
         int bks[16];
         load_kept(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
-        for (int br = 0; br < 3 && ok; ++br) {
+        for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
           const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
           for (int pass = 0; pass < 2 && ok; ++pass) {
             for (int p = 0; p < bk.np; ++p) {
@@ -284,7 +286,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         tc_fence_after();
         bool dq_started = false;
-        for (int br = 0; br < 3 && ok; ++br) {
+        for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
           const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
           for (int pass = 0; pass < 2 && ok; ++pass) {
             for (int p = 0; p < bk.np; ++p) {
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       int bks[16];
       load_kept(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
       bool any = false;
-      for (int br = 0; br < 3 && ok; ++br) {
+      for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
         const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
         float gs[NP];
 #pragma unroll
@@ -564,7 +566,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (own) {
 #pragma unroll
           for (int h = 0; h < NP; ++h)
-            if (h < a.hpg) a.dq[(rowbase + h) * a.dk + drow] = any ? __uint_as_float(rr[h]) : 0.f;
+            if (h < a.hpg) {
+              float* o = a.dq + (rowbase + h) * a.dk + drow;
+              const float v = any ? __uint_as_float(rr[h]) : 0.f;
+              *o = a.acc_dq ? *o + v : v;
+            }
         }
       }
       tc_fence_before();
@@ -576,6 +582,392 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ============================================================================
+// 1b. dQ of the compressed and window branches, query-tile form
+// ============================================================================
+// One CTA = 8 consecutive queries of one KV group: 128 rows (query, head) on
+// the MMA M side against 128-key tiles, so every key tile is read once for 8
+// queries (the compressed and window keys of neighbouring queries coincide):
+//     S   = Q K^T,  dP' = dout V^T                  (M=128 rows, N=128 keys)
+//     dQ += dS K      (dS bf16 in tensor memory as the A operand, N = dk)
+// Thread = TMEM lane = one (query, head) row, so a row's statistics need no
+// cross-thread reduction.  Per branch a statistics pass and a dS pass, as in
+// bwd_dq_kernel.  Writes dq (fp32, overwritten), dgates and the branch rows
+// of lse / dg.
+constexpr int kTileQ = 8;
+constexpr int kTileThreads = 192;     // warps 0-3 rows, 4 producer, 5 MMA
+
+struct TileArgs {
+  int T, H, G, dk, dv, w, hpg, Nc;
+  float sc2, scale;
+  const __nv_bfloat16* gates;     // [B,T,H,3]
+  float* dq;                      // [B,T,H,dk]
+  float* dgates;                  // [B,T,H,3]
+  float* lse;                     // [3][B,T,H]
+  float* dgw;                     // [3][B,T,H]
+  DeviceStatus* st;
+  uint32_t off_do, off_k, off_v, off_bar;
+};
+
+struct TileBars {
+  uint64_t q_full;
+  uint64_t k_full[2], k_empty[2];
+  uint64_t v_full, v_empty;
+  uint64_t s_full, s_free;
+  uint64_t ds_full, ds_free;
+  uint64_t dq_full;
+  uint64_t drain;
+  uint32_t tmem;
+  int abort_flag;
+};
+
+struct TileKeys {
+  int ntiles;   // 128-key tiles of the CTA's 8 queries
+  int base;     // cmp: first entry (0); win: first token
+};
+
+__device__ __forceinline__ TileKeys tile_keys(int br, int t0, int t_last, int Nc, int w) {
+  TileKeys k;
+  if (br == kBrCmp) {
+    k.base = 0;
+    k.ntiles = (visible_compressed(t_last, Nc) + 127) / 128;
+  } else {
+    k.base = max(0, t0 - w + 1);
+    k.ntiles = (t_last - k.base + 1 + 127) / 128;
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(kTileThreads, 1)
+    bwd_dq_tile_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
+                       const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                       const __grid_constant__ CUtensorMap mapKc, const __grid_constant__ CUtensorMap mapVc,
+                       const TileArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int kcs = a.dk / 64, vcs = a.dv / 64;
+  uint8_t* qt = smem;                       // Q tile: kcs chunks x 16 KB (128 rows x 64 columns)
+  uint8_t* dot = smem + a.off_do;           // dout tile: vcs chunks x 16 KB
+  uint8_t* kring = smem + a.off_k;          // 2 x kcs chunks x 16 KB
+  uint8_t* vbuf = smem + a.off_v;           // vcs chunks x 16 KB
+  TileBars* bars = reinterpret_cast<TileBars*>(smem + a.off_bar);
+  volatile int* abort_flag = &bars->abort_flag;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int t0 = blockIdx.x * kTileQ;
+  const int t_last = min(a.T - 1, t0 + kTileQ - 1);
+  const int warp = warp_id(), lane = lane_id();
+  const int kslot = kcs * kChunk;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 4);
+    mbar_init(&bars->ds_full, 4);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort_flag = prior_error(a.st);
+    fence_barrier_init();
+  }
+  // query / dout rows of heads hpg..15 are never loaded: keep them zero
+  for (int i = threadIdx.x; i < (int)(a.off_k / 16); i += kTileThreads)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const uint32_t tm_s = tmem, tm_dp = tmem + 128, tm_ds = tmem + 256, tm_dq = tmem + 320;
+
+  if (*abort_flag) {
+  } else if (warp == 4) {
+    // ===================================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapDO);
+      bool ok = true;
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(kTileQ * (kcs + vcs) * a.hpg * 128));
+      for (int k = 0; k < kTileQ; ++k) {
+        for (int c = 0; c < kcs; ++c)
+          tma_load_4d(qt + c * kChunk + k * kQB, &mapQ, &bars->q_full, c * 64, g * a.hpg, t0 + k, b);
+        for (int c = 0; c < vcs; ++c)
+          tma_load_4d(dot + c * kChunk + k * kQB, &mapDO, &bars->q_full, c * 64, g * a.hpg, t0 + k, b);
+      }
+      int jk = 0, jv = 0;
+      for (int br = kBrCmp; br <= kBrWin && ok; br += kBrWin - kBrCmp) {
+        const TileKeys tk = tile_keys(br, t0, t_last, a.Nc, a.w);
+        const CUtensorMap* mk = br == kBrCmp ? &mapKc : &mapK;
+        const CUtensorMap* mv = br == kBrCmp ? &mapVc : &mapV;
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int kt = 0; kt < tk.ntiles; ++kt) {
+            const int r0 = tk.base + 128 * kt;
+            const int slot = jk & 1;
+            if (!mbar_wait(&bars->k_empty[slot], (uint32_t)(((jk >> 1) & 1) ^ 1), abort_flag, a.st, 861)) {
+              ok = false;
+              break;
+            }
+            uint8_t* kd = kring + slot * kslot;
+            mbar_arrive_expect_tx(&bars->k_full[slot], (uint32_t)kslot);
+            for (int c = 0; c < kcs; ++c) {
+              if (br == kBrCmp) {
+                tma_load_4d(kd + c * kChunk, mk, &bars->k_full[slot], c * 64, r0, g, b);
+                tma_load_4d(kd + c * kChunk + 8192, mk, &bars->k_full[slot], c * 64, r0 + 64, g, b);
+              } else {
+                tma_load_4d(kd + c * kChunk, mk, &bars->k_full[slot], c * 64, g, r0, b);
+                tma_load_4d(kd + c * kChunk + 8192, mk, &bars->k_full[slot], c * 64, g, r0 + 64, b);
+              }
+            }
+            ++jk;
+            if (!mbar_wait(&bars->v_empty, (uint32_t)((jv & 1) ^ 1), abort_flag, a.st, 862)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars->v_full, (uint32_t)(vcs * kChunk));
+            for (int c = 0; c < vcs; ++c) {
+              if (br == kBrCmp) {
+                tma_load_4d(vbuf + c * kChunk, mv, &bars->v_full, c * 64, r0, g, b);
+                tma_load_4d(vbuf + c * kChunk + 8192, mv, &bars->v_full, c * 64, r0 + 64, g, b);
+              } else {
+                tma_load_4d(vbuf + c * kChunk, mv, &bars->v_full, c * 64, g, r0, b);
+                tma_load_4d(vbuf + c * kChunk + 8192, mv, &bars->v_full, c * 64, g, r0 + 64, b);
+              }
+            }
+            ++jv;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        mbar_wait_plain(&bars->q_full, 0, kWaitLimitNs);
+        for (int x = (jk > 2 ? jk - 2 : 0); x < jk; ++x)
+          mbar_wait_plain(&bars->k_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+        if (jv > 0) mbar_wait_plain(&bars->v_full, (uint32_t)((jv - 1) & 1), kWaitLimitNs);
+      }
+    }
+  } else if (warp == 5) {
+    // ===================================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idesc_dq = idesc_bf16_f32(128, a.dk, false, true);
+      const uint32_t q_a = smem_u32(qt), do_a = smem_u32(dot), k_a = smem_u32(kring), v_a = smem_u32(vbuf);
+      bool ok = mbar_wait(&bars->q_full, 0, abort_flag, a.st, 871);
+      tc_fence_after();
+      int jk = 0, jv = 0, jt = 0, jd = 0;
+      bool dq_started = false;
+      for (int br = kBrCmp; br <= kBrWin && ok; br += kBrWin - kBrCmp) {
+        const TileKeys tk = tile_keys(br, t0, t_last, a.Nc, a.w);
+        for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int kt = 0; kt < tk.ntiles; ++kt) {
+            const int slot = jk & 1;
+            const uint32_t ks = k_a + slot * kslot;
+            if (!mbar_wait(&bars->k_full[slot], (uint32_t)((jk >> 1) & 1), abort_flag, a.st, 872) ||
+                !mbar_wait(&bars->s_free, (uint32_t)((jt & 1) ^ 1), abort_flag, a.st, 873)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < kcs; ++c) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = sdesc_sw128(q_a + c * kChunk + k * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(ks + c * kChunk + k * 32, 16, 1024);
+                umma_bf16(tm_s, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+              }
+            }
+            if (!mbar_wait(&bars->v_full, (uint32_t)(jv & 1), abort_flag, a.st, 874)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < vcs; ++c) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = sdesc_sw128(do_a + c * kChunk + k * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(v_a + c * kChunk + k * 32, 16, 1024);
+                umma_bf16(tm_dp, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
+              }
+            }
+            umma_commit(&bars->v_empty);
+            umma_commit(&bars->s_full);
+            ++jv;
+            ++jt;
+            if (pass == 1) {
+              if (!mbar_wait(&bars->ds_full, (uint32_t)(jd & 1), abort_flag, a.st, 875)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                // B = K rows (keys) along K, head dims along N (N-major, 16 KB per 64 columns)
+                const uint64_t bd = sdesc_sw128(ks + k * 2048, kChunk, 1024);
+                umma_bf16_ts(tm_dq, tm_ds + 8 * k, bd, idesc_dq, (dq_started || k > 0) ? 1u : 0u);
+              }
+              dq_started = true;
+              umma_commit(&bars->ds_free);
+              ++jd;
+            }
+            umma_commit(&bars->k_empty[slot]);
+            ++jk;
+          }
+        }
+      }
+      if (ok) umma_commit(&bars->dq_full);
+      if (!ok || *abort_flag) {
+        umma_commit(&bars->drain);
+        mbar_wait_plain(&bars->drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ===================================================================== rows
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int t = t0 + (r >> 4), h = r & 15;
+    const bool row_ok = t < a.T && h < a.hpg;
+    const size_t row = ((size_t)b * a.T + (row_ok ? t : 0)) * a.H + g * a.hpg + (row_ok ? h : 0);
+    const size_t plane = (size_t)gridDim.z * a.T * a.H;
+    bool ok = true;
+    int jt = 0, jd = 0;
+    bool any = false;
+    for (int br = kBrCmp; br <= kBrWin && ok; br += kBrWin - kBrCmp) {
+      const TileKeys tk = tile_keys(br, t0, t_last, a.Nc, a.w);
+      const float gs = row_ok ? __bfloat162float(a.gates[row * 3 + br]) : 0.f;
+      // visible keys of this row, as positions inside the branch's key range
+      int lo, hi;
+      if (br == kBrCmp) {
+        lo = 0;
+        hi = t >= 31 ? min(a.Nc - 1, (t - 31) / 16) : -1;
+      } else {
+        lo = max(0, t - a.w + 1) - tk.base;
+        hi = t - tk.base;
+      }
+      float lse2 = INFINITY, dg = 0.f;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        float m = -INFINITY, l = 0.f, s1 = 0.f;
+        for (int kt = 0; kt < tk.ntiles; ++kt) {
+          if (!mbar_wait(&bars->s_full, (uint32_t)(jt & 1), abort_flag, a.st, 881)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (pass == 1 && !mbar_wait(&bars->ds_free, (uint32_t)((jd & 1) ^ 1), abort_flag, a.st, 882)) {
+            ok = false;
+            break;
+          }
+          const int kb = 128 * kt;
+          for (int grp = 0; grp < 8; ++grp) {
+            uint32_t sr[16], dr[16];
+            tmem_ld16(tm_s + lane_base + grp * 16, sr);
+            tmem_ld16(tm_dp + lane_base + grp * 16, dr);
+            tmem_ld_wait(sr);
+            tmem_reg_fence(dr);
+            const int j0 = kb + grp * 16;
+            if (pass == 0) {
+              float gm = -INFINITY;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const bool vis = j0 + e >= lo && j0 + e <= hi;
+                if (vis) gm = fmaxf(gm, __uint_as_float(sr[e]) * a.sc2);
+              }
+              if (gm != -INFINITY) {
+                const float mn = fmaxf(m, gm);
+                const float f = fast_exp2(m - mn);
+                l *= f;
+                s1 *= f;
+                m = mn;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const bool vis = j0 + e >= lo && j0 + e <= hi;
+                  if (vis) {
+                    const float p = fast_exp2(fmaf(__uint_as_float(sr[e]), a.sc2, -m));
+                    l += p;
+                    s1 = fmaf(p, __uint_as_float(dr[e]), s1);
+                  }
+                }
+              }
+            } else {
+              uint32_t pk[8];
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                float d2[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const bool vis = j0 + e + u >= lo && j0 + e + u <= hi;
+                  float d = 0.f;
+                  if (vis) {
+                    const float p = fast_exp2(fmaf(__uint_as_float(sr[e + u]), a.sc2, -lse2));
+                    d = gs * a.scale * p * (__uint_as_float(dr[e + u]) - dg);
+                  }
+                  d2[u] = d;
+                }
+                pk[e / 2] = pack_bf16x2(d2[0], d2[1]);
+              }
+              // 8 columns of packed bf16 pairs per 16 keys
+              asm volatile(
+                  "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                      tm_ds + lane_base + grp * 8),
+                  "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
+                  : "memory");
+            }
+          }
+          if (pass == 1) tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->s_free);
+            if (pass == 1) mbar_arrive(&bars->ds_full);
+          }
+          ++jt;
+          if (pass == 1) {
+            ++jd;
+            any = true;
+          }
+        }
+        if (!ok) break;
+        if (pass == 0) {
+          lse2 = l > 0.f ? m + __log2f(l) : INFINITY;
+          dg = l > 0.f ? __fdividef(s1, l) : 0.f;
+          if (row_ok) {
+            a.dgates[row * 3 + br] = dg;
+            a.lse[(size_t)br * plane + row] = lse2;
+            a.dgw[(size_t)br * plane + row] = dg;
+          }
+        }
+      }
+    }
+    // ---- epilogue: this row's dq (cmp + win), fp32
+    if (ok && mbar_wait(&bars->dq_full, 0, abort_flag, a.st, 883)) {
+      tc_fence_after();
+      for (int c0 = 0; c0 < a.dk; c0 += 16) {
+        uint32_t rr[16];
+        tmem_ld16(tm_dq + lane_base + c0, rr);
+        tmem_ld_wait(rr);
+        if (row_ok) {
+          float4* o = reinterpret_cast<float4*>(a.dq + row * a.dk + c0);
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            o[e / 4] = any ? make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]),
+                                         __uint_as_float(rr[e + 2]), __uint_as_float(rr[e + 3]))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ============================================================================
@@ -1235,6 +1627,19 @@ DqLayout dq_layout(int dk, int dv) {
   return L;
 }
 
+struct TileLayout {
+  uint32_t off_do, off_k, off_v, off_bar, total;
+};
+TileLayout tile_layout(int dk, int dv) {
+  TileLayout L;
+  L.off_do = (uint32_t)(dk / 64 * kChunk);
+  L.off_k = L.off_do + (uint32_t)(dv / 64 * kChunk);
+  L.off_v = L.off_k + (uint32_t)(2 * (dk / 64) * kChunk);
+  L.off_bar = L.off_v + (uint32_t)(dv / 64 * kChunk);
+  L.total = L.off_bar + (uint32_t)align_up(sizeof(TileBars), 256) + 1024;
+  return L;
+}
+
 struct DkvLayout {
   uint32_t off_q, off_col, off_bar, total;
 };
@@ -1266,7 +1671,8 @@ int bwd_supported(const nsa_cfg& c) {
   // grid limits of the compression-backward launches
   const long long Nc = c.T < 32 ? 0 : (c.T - 32) / 16 + 1;
   if (16ll * c.B * c.G > 65535 || 32ll * ((c.B * c.G * Nc + 255) / 256) > 65535) return NSA_ERR_UNSUPPORTED;
-  if (dq_layout(c.dk, c.dv).total > smem_max() || dkv_layout(c.dk, c.dv).total > smem_max())
+  if (dq_layout(c.dk, c.dv).total > smem_max() || dkv_layout(c.dk, c.dv).total > smem_max() ||
+      tile_layout(c.dk, c.dv).total > smem_max())
     return NSA_ERR_UNSUPPORTED;
   return NSA_OK;
 }
@@ -1337,10 +1743,44 @@ int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const Bw
       !make_kv_map(&mvc, Nc > 0 ? p.vc : p.v, c.B, ncr, c.G, c.dv, 64, true))
     return NSA_ERR_CUDA;
 
-  // ---- 1. dq, dgates, per-branch statistics
+  // ---- 1. dq, dgates, per-branch statistics: the compressed and window
+  // branches in query tiles, then the selected branch per (query, group)
+  {
+    const TileLayout L = tile_layout(c.dk, c.dv);
+    TileArgs a;
+    a.T = c.T;
+    a.H = c.H;
+    a.G = c.G;
+    a.dk = c.dk;
+    a.dv = c.dv;
+    a.w = c.w;
+    a.hpg = hpg;
+    a.Nc = Nc;
+    a.sc2 = sc2;
+    a.scale = scale;
+    a.gates = static_cast<const __nv_bfloat16*>(p.gates);
+    a.dq = p.dq;
+    a.dgates = p.dgates;
+    a.lse = lse;
+    a.dgw = dgw;
+    a.st = st;
+    a.off_do = L.off_do;
+    a.off_k = L.off_k;
+    a.off_v = L.off_v;
+    a.off_bar = L.off_bar;
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dq_tile_kernel), L.total)) return rc;
+    dim3 grid((c.T + kTileQ - 1) / kTileQ, c.G, c.B);
+    prof::begin("bwd_dq_tile", s);
+    bwd_dq_tile_kernel<<<grid, kTileThreads, L.total, s>>>(mq, mdo, mk, mv, mkc, mvc, a);
+    prof::end(s);
+    if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
+  }
   {
     const DqLayout L = dq_layout(c.dk, c.dv);
     DqArgs a;
+    a.br_lo = kBrSlc;
+    a.br_hi = kBrSlc;
+    a.acc_dq = 1;
     a.T = c.T;
     a.H = c.H;
     a.G = c.G;
@@ -1366,7 +1806,7 @@ int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const Bw
     a.off_bar = L.off_bar;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dq_kernel), L.total)) return rc;
     dim3 grid((c.T + a.QPC - 1) / a.QPC, c.G, c.B);
-    prof::begin("bwd_dq", s);
+    prof::begin("bwd_dq_slc", s);
     bwd_dq_kernel<<<grid, kDqThreads, L.total, s>>>(mq, mdo, mk, mv, mkc, mvc, a);
     prof::end(s);
     if (cudaPeekAtLastError() != cudaSuccess) return NSA_ERR_CUDA;
