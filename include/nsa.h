@@ -182,6 +182,21 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * nsa_prefill_fwd_train -- nsa_prefill_fwd that also saves what the backward
+ * pass reads of the selected branch: its log-sum-exp and its output before
+ * the gate.
+ *   idx_out : [B,T,G,n] int32 (required here)
+ *   slc_lse : out, fp32 [B,T,H]: the row's log-sum-exp in base 2 over its
+ *             kept keys, m + log2(sum_j 2^(u_j - m)) with u_j = s_j * scale *
+ *             log2(e) and m = max_j u_j
+ *   slc_o   : out, fp32 [B,T,H,dv]: O_slc = sum_j P_j v_j
+ * Everything else as nsa_prefill_fwd (same workspace size).
+ */
+int nsa_prefill_fwd_train(const nsa_cfg* cfg, const void* q, const void* k, const void* v,
+                          const void* gates, void* kc, void* vc, void* out, int32_t* idx_out,
+                          float* slc_lse, float* slc_o, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * nsa_prefill_bwd -- NSA backward pass over whole sequences: the gradients of
  * sum(dout * out) for out = nsa_prefill_fwd(...) [P2 II; the pages' training
  * figure, 6.0x faster than full attention at 64k, P2 III.3].  The pages give
@@ -196,6 +211,10 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
  * (dW += flatten(X_i + PE)^T dXc_i, dX[16 i + r] += (dXc_i W^T)[r], dPE).
  *   q, k, v, gates, kc, vc : the forward's inputs and its compressed cache
  *   idx   : [B,T,G,n] int32, the forward's kept blocks (its idx_out)
+ *   slc_lse, slc_o (nullable, both or neither): the selected branch's
+ *           statistics saved by nsa_prefill_fwd_train; given, the backward
+ *           skips its own statistics pass over the kept blocks (dgates of
+ *           that branch is then dout . slc_o, with the forward's bf16 P)
  *   dout  : [B,T,H,dv] bf16, the upstream gradient
  *   dq    : out, fp32 [B,T,H,dk]      dk, dv : out, fp32 [B,T,G,dk] / [B,T,G,dv]
  *   dgates: out, fp32 [B,T,H,3]       dw_k, dw_v : out, fp32 [l*dk,dk] / [l*dv,dv]
@@ -209,6 +228,7 @@ int nsa_prefill_fwd(const nsa_cfg* cfg, const void* q, const void* k, const void
 size_t nsa_prefill_bwd_workspace_size(const nsa_cfg* cfg);
 int nsa_prefill_bwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v,
                     const void* gates, const void* kc, const void* vc, const int32_t* idx,
+                    const float* slc_lse, const float* slc_o,
                     const void* dout, float* dq, float* dk, float* dv, float* dgates,
                     float* dw_k, float* dw_v, float* dpe_k, float* dpe_v,
                     void* ws, size_t ws_bytes, void* stream);

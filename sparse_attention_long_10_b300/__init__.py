@@ -24,7 +24,7 @@ __all__ = [
     "dsa_decode_workspace_size", "nsa_compress_kv", "nsa_compress_kv_noalloc",
     "nsa_compress_kv_noalloc_status", "nsa_full_attn_workspace_size", "nsa_full_attn_fwd",
     "nsa_decode_multi_workspace_size", "nsa_decode_multi", "nsa_prefill_fwd",
-    "nsa_prefill_bwd_workspace_size", "nsa_prefill_bwd", "nsa_decode_step",
+    "nsa_prefill_bwd_workspace_size", "nsa_prefill_bwd", "nsa_prefill_fwd_train", "nsa_decode_step",
     "dsa_decode_step", "nsa_device_status", "nsa_profile_enable", "nsa_profile_read", "workspace",
 ]
 
@@ -87,7 +87,8 @@ def _load() -> ctypes.CDLL:
         "nsa_device_status": (_c_int, [_c_vp, _c_vp]),
         "nsa_full_attn_workspace_size": (_c_size, [P(NsaCfg)]),
         "nsa_prefill_bwd_workspace_size": (_c_size, [P(NsaCfg)]),
-        "nsa_prefill_bwd": (_c_int, [P(NsaCfg)] + [_c_vp] * 16 + [_c_vp, _c_size, _c_vp]),
+        "nsa_prefill_bwd": (_c_int, [P(NsaCfg)] + [_c_vp] * 18 + [_c_vp, _c_size, _c_vp]),
+        "nsa_prefill_fwd_train": (_c_int, [P(NsaCfg)] + [_c_vp] * 10 + [_c_vp, _c_size, _c_vp]),
         "nsa_decode_multi_workspace_size": (_c_size, [P(NsaCfg), _c_int]),
         "nsa_decode_multi": (_c_int, [P(NsaCfg), _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                       _c_vp, _c_size, _c_vp]),
@@ -224,12 +225,21 @@ def nsa_prefill_bwd_workspace_size(cfg: NsaCfg) -> int:
     return int(_lib().nsa_prefill_bwd_workspace_size(ctypes.byref(cfg)))
 
 
+def nsa_prefill_fwd_train(cfg: NsaCfg, q, k, v, gates, kc, vc, out, idx_out, slc_lse, slc_o, ws, stream=None):
+    _check(_lib().nsa_prefill_fwd_train(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates), _ptr(kc),
+                                        _ptr(vc), _ptr(out), _ptr(idx_out), _ptr(slc_lse), _ptr(slc_o), _ptr(ws),
+                                        ws.numel() if ws is not None else 0, _stream(stream)),
+           "nsa_prefill_fwd_train")
+
+
 def nsa_prefill_bwd(cfg: NsaCfg, q, k, v, gates, kc, vc, idx, dout, dq, dk, dv, dgates, dw_k, dw_v,
-                    dpe_k, dpe_v, ws, stream=None):
+                    dpe_k, dpe_v, ws, stream=None, slc_lse=None, slc_o=None):
     """Gradients of sum(dout * out) for the forward on the same inputs; the
-    outputs are fp32 tensors (see include/nsa.h)."""
+    outputs are fp32 tensors (see include/nsa.h).  slc_lse / slc_o: the
+    statistics nsa_prefill_fwd_train saved (optional)."""
     _check(_lib().nsa_prefill_bwd(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gates), _ptr(kc),
-                                  _ptr(vc), _ptr(idx), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgates),
+                                  _ptr(vc), _ptr(idx), _ptr(slc_lse), _ptr(slc_o), _ptr(dout), _ptr(dq),
+                                  _ptr(dk), _ptr(dv), _ptr(dgates),
                                   _ptr(dw_k), _ptr(dw_v), _ptr(dpe_k), _ptr(dpe_v), _ptr(ws),
                                   ws.numel() if ws is not None else 0, _stream(stream)),
            "nsa_prefill_bwd")

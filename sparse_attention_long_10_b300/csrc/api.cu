@@ -257,9 +257,9 @@ size_t nsa_prefill_bwd_workspace_size(const nsa_cfg* cfg) {
 }
 
 int nsa_prefill_bwd(const nsa_cfg* cfg, const void* q, const void* k, const void* v, const void* gates,
-                    const void* kc, const void* vc, const int32_t* idx, const void* dout, float* dq, float* dk,
-                    float* dv, float* dgates, float* dw_k, float* dw_v, float* dpe_k, float* dpe_v, void* ws,
-                    size_t ws_bytes, void* stream) {
+                    const void* kc, const void* vc, const int32_t* idx, const float* slc_lse, const float* slc_o,
+                    const void* dout, float* dq, float* dk, float* dv, float* dgates, float* dw_k, float* dw_v,
+                    float* dpe_k, float* dpe_v, void* ws, size_t ws_bytes, void* stream) {
   int rc = validate_cfg(cfg);
   if (rc != NSA_OK) return rc;
   const nsa_cfg& c = *cfg;
@@ -268,13 +268,40 @@ int nsa_prefill_bwd(const nsa_cfg* cfg, const void* q, const void* k, const void
   if ((rc = check_ptrs({q, k, v, gates, idx, dout, dq, dk, dv, dgates, dw_k, dw_v, dpe_k, dpe_v})) != NSA_OK)
     return rc;
   if (num_compressed(c) > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  if ((slc_lse == nullptr) != (slc_o == nullptr)) return NSA_ERR_INVALID_ARG;
+  if (slc_lse != nullptr && (rc = check_ptrs({slc_lse, slc_o})) != NSA_OK) return rc;
   const BwdWs w = bwd_ws(c, kHeader);
   if ((rc = check_ws(ws, ws_bytes, w.end)) != NSA_OK) return rc;
   if ((rc = check_device()) != NSA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
-  BwdPtrs p{q, k, v, gates, kc, vc, dout, idx, dq, dk, dv, dgates, dw_k, dw_v, dpe_k, dpe_v};
+  BwdPtrs p{q, k, v, gates, kc, vc, dout, idx, slc_lse, slc_o, dq, dk, dv, dgates, dw_k, dw_v, dpe_k, dpe_v};
   return launch_prefill_bwd(c, p, static_cast<uint8_t*>(ws), w, s);
+}
+
+int nsa_prefill_fwd_train(const nsa_cfg* cfg, const void* q, const void* k, const void* v, const void* gates,
+                          void* kc, void* vc, void* out, int32_t* idx_out, float* slc_lse, float* slc_o, void* ws,
+                          size_t ws_bytes, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc != NSA_OK) return rc;
+  const nsa_cfg& c = *cfg;
+  if ((rc = prefill_supported(c)) != NSA_OK) return rc;
+  const bool given = (c.flags & NSA_FLAG_KC_GIVEN) != 0;
+  const int Nc = num_compressed(c);
+  if (!given && (rc = validate_phi(cfg)) != NSA_OK) return rc;
+  if ((rc = check_ptrs({q, k, v, gates, out, idx_out, slc_lse, slc_o})) != NSA_OK) return rc;
+  if (Nc > 0 && (rc = check_ptrs({kc, vc})) != NSA_OK) return rc;
+  const PrefillWs w = prefill_ws(c);
+  if ((rc = check_ws(ws, ws_bytes, w.end)) != NSA_OK) return rc;
+  if ((rc = check_device()) != NSA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DeviceStatus* st = reinterpret_cast<DeviceStatus*>(wsb);
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return NSA_ERR_CUDA;
+  if (!given && Nc > 0 && (rc = run_compress(c, NSA_LAYOUT_BTGD, k, v, kc, vc, wsb, s)) != NSA_OK) return rc;
+  void* part = wsb + w.part;
+  if ((rc = launch_cmp_win(c, q, k, v, kc, vc, gates, part, idx_out, st, s)) != NSA_OK) return rc;
+  return launch_sel(c, q, k, v, gates, idx_out, part, out, st, s, QueryRows(), slc_lse, slc_o);
 }
 
 size_t nsa_full_attn_workspace_size(const nsa_cfg* cfg) {

@@ -53,6 +53,7 @@ constexpr int NP = 16;              // MMA N of one item: the group's heads, pad
 constexpr int kQB = 2048;           // one 64-column chunk of NP rows (bf16, 128-B swizzle)
 constexpr int kChunk = 16384;       // one 64-column chunk of 128 key rows
 constexpr int kRowsPerUnit = 1024;  // queries per key-outer work unit
+constexpr int kDqRingK = 3;         // bwd_dq_kernel: key-pair slots (held until the dQ MMA)
 
 constexpr int kBrCmp = 0, kBrSlc = 1, kBrWin = 2;
 
@@ -101,6 +102,9 @@ struct DqArgs {
   int acc_dq;                      // add to dq (another kernel wrote the other branches)
   float sc2, scale;
   const int32_t* idx;              // [B,T,G,n]
+  const float* slc_lse;            // nullable: the forward's selected-branch log-sum-exp [B,T,H]
+  const float* slc_o;              // and O_slc [B,T,H,dv]: the statistics pass is skipped
+  const __nv_bfloat16* dout;       // [B,T,H,dv]
   const __nv_bfloat16* gates;      // [B,T,H,3]
   float* dq;                       // [B,T,H,dk]
   float* dgates;                   // [B,T,H,3]
@@ -112,7 +116,8 @@ struct DqArgs {
 
 struct DqBars {
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[kDqRingK], k_empty[kDqRingK];
+  uint64_t v_full, v_empty;
   uint64_t s_full[4], s_free[4];
   uint64_t ds_full[2], ds_free[2];
   uint64_t dq_full[2], dq_free[2];
@@ -132,9 +137,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int kcs = a.dk / 64, vcs = a.dv / 64, cs = kcs + vcs;
-  const int slot_bytes = cs * kChunk;
+  const int kslot_bytes = kcs * kChunk;
   uint8_t* qbuf = smem;                         // 2 items x (kcs Q + vcs dout) chunks x 2 KB
-  uint8_t* kvring = smem + a.off_kv;            // 2 slots x (kcs K + vcs V) chunks x 16 KB
+  uint8_t* kring = smem + a.off_kv;             // kDqRingK slots x kcs K chunks x 16 KB
+  uint8_t* vbuf = kring + kDqRingK * kslot_bytes;   // vcs V chunks x 16 KB
   uint8_t* dsbuf = smem + a.off_ds;             // 2 x dS^T (2 chunks x 2 KB)
   float* red = reinterpret_cast<float*>(smem + a.off_red);   // [4 warps][3][NP]
   DqBars* bars = reinterpret_cast<DqBars*>(smem + a.off_bar);
@@ -150,8 +156,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
       mbar_init(&bars->ds_full[i], 4);
       mbar_init(&bars->ds_free[i], 1);
       mbar_init(&bars->dq_full[i], 1);
@@ -161,6 +165,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);
     }
+    for (int i = 0; i < kDqRingK; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+    }
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
     mbar_init(&bars->wg, 4);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
@@ -190,7 +200,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
       bool ok = true;
-      int jp = 0, nq = 0;
+      int jp = 0, nq = 0, nv = 0;
       for (int i = 0; i < nitems && ok; ++i) {
         const int t = t0 + i;
         const int qb = i & 1;
@@ -208,52 +218,60 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         load_kept(a.idx + (((size_t)b * a.T + t) * a.G + g) * a.n, a.n, bks);
         for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
           const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
-          for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int pass = (br == kBrSlc && a.slc_lse != nullptr) ? 1 : 0; pass < 2 && ok; ++pass) {
             for (int p = 0; p < bk.np; ++p) {
-              const int slot = jp & 1;
-              if (!mbar_wait(&bars->kv_empty[slot], (uint32_t)(((jp >> 1) & 1) ^ 1), abort_flag, a.st, 802)) {
+              const int ks = jp % kDqRingK;
+              if (!mbar_wait(&bars->k_empty[ks], (uint32_t)(((jp / kDqRingK) & 1) ^ 1), abort_flag, a.st, 802)) {
                 ok = false;
                 break;
               }
-              uint8_t* dst = kvring + slot * slot_bytes;
-              uint64_t* bar = &bars->kv_full[slot];
-              mbar_arrive_expect_tx(bar, (uint32_t)slot_bytes);
+              int tk0, tk1;   // first row of each 64-row half (entries for cmp, tokens otherwise)
               if (br == kBrCmp) {
-                const int r0 = 128 * p;
-                for (int c = 0; c < kcs; ++c) {
-                  tma_load_4d(dst + c * kChunk, &mapKc, bar, c * 64, r0, g, b);
-                  tma_load_4d(dst + c * kChunk + 8192, &mapKc, bar, c * 64, r0 + 64, g, b);
-                }
-                for (int c = 0; c < vcs; ++c) {
-                  tma_load_4d(dst + (kcs + c) * kChunk, &mapVc, bar, c * 64, r0, g, b);
-                  tma_load_4d(dst + (kcs + c) * kChunk + 8192, &mapVc, bar, c * 64, r0 + 64, g, b);
-                }
-              } else {
-                int tk0, tk1;
-                if (br == kBrSlc) {
-                  int b0 = -1, b1 = -1;
+                tk0 = 128 * p;
+                tk1 = tk0 + 64;
+              } else if (br == kBrSlc) {
+                int b0 = -1, b1 = -1;
 #pragma unroll
-                  for (int q = 0; q < 8; ++q)
-                    if (q == p) {
-                      b0 = bks[2 * q];
-                      b1 = bks[2 * q + 1];
-                    }
-                  tk0 = block_token(b0);
-                  tk1 = block_token(b1);
-                } else {
-                  tk0 = bk.start + 128 * p;
-                  tk1 = tk0 + 64;
-                }
+                for (int q = 0; q < 8; ++q)
+                  if (q == p) {
+                    b0 = bks[2 * q];
+                    b1 = bks[2 * q + 1];
+                  }
+                tk0 = block_token(b0);
+                tk1 = block_token(b1);
+              } else {
+                tk0 = bk.start + 128 * p;
+                tk1 = tk0 + 64;
+              }
+              auto load_half = [&](uint8_t* dst, const CUtensorMap* m, uint64_t* bar, int col, int row) {
+                if (br == kBrCmp) tma_load_4d(dst, m, bar, col, row, g, b);
+                else tma_load_4d(dst, m, bar, col, g, row, b);
+              };
+              {
+                uint8_t* dst = kring + ks * kslot_bytes;
+                uint64_t* bar = &bars->k_full[ks];
+                const CUtensorMap* m = br == kBrCmp ? &mapKc : &mapK;
+                mbar_arrive_expect_tx(bar, (uint32_t)kslot_bytes);
                 for (int c = 0; c < kcs; ++c) {
-                  tma_load_4d(dst + c * kChunk, &mapK, bar, c * 64, g, tk0, b);
-                  tma_load_4d(dst + c * kChunk + 8192, &mapK, bar, c * 64, g, tk1, b);
+                  load_half(dst + c * kChunk, m, bar, c * 64, tk0);
+                  load_half(dst + c * kChunk + 8192, m, bar, c * 64, tk1);
                 }
+              }
+              if (!mbar_wait(&bars->v_empty, (uint32_t)((jp & 1) ^ 1), abort_flag, a.st, 803)) {
+                ok = false;
+                ++jp;
+                break;
+              }
+              {
+                const CUtensorMap* m = br == kBrCmp ? &mapVc : &mapV;
+                mbar_arrive_expect_tx(&bars->v_full, (uint32_t)(vcs * kChunk));
                 for (int c = 0; c < vcs; ++c) {
-                  tma_load_4d(dst + (kcs + c) * kChunk, &mapV, bar, c * 64, g, tk0, b);
-                  tma_load_4d(dst + (kcs + c) * kChunk + 8192, &mapV, bar, c * 64, g, tk1, b);
+                  load_half(vbuf + c * kChunk, m, &bars->v_full, c * 64, tk0);
+                  load_half(vbuf + c * kChunk + 8192, m, &bars->v_full, c * 64, tk1);
                 }
               }
               ++jp;
+              ++nv;
             }
           }
         }
@@ -261,8 +279,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!ok || *abort_flag) {
         for (int x = (nq > 2 ? nq - 2 : 0); x < nq; ++x)
           mbar_wait_plain(&bars->q_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
-        for (int x = (jp > 2 ? jp - 2 : 0); x < jp; ++x)
-          mbar_wait_plain(&bars->kv_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+        for (int x = (jp > kDqRingK ? jp - kDqRingK : 0); x < jp; ++x)
+          mbar_wait_plain(&bars->k_full[x % kDqRingK], (uint32_t)((x / kDqRingK) & 1), kWaitLimitNs);
+        if (nv > 0) mbar_wait_plain(&bars->v_full, (uint32_t)((nv - 1) & 1), kWaitLimitNs);
       }
     }
   } else if (warp == 5) {
@@ -270,7 +289,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, NP, false, false);
       const uint32_t idesc_dq = idesc_bf16_f32(128, NP, true, false);
-      const uint32_t q_a = smem_u32(qbuf), kv_a = smem_u32(kvring), ds_a = smem_u32(dsbuf);
+      const uint32_t q_a = smem_u32(qbuf), k_a = smem_u32(kring), v_a = smem_u32(vbuf), ds_a = smem_u32(dsbuf);
       // first 64-row chunk of each dQ^T tile: 0, then dk - 128 (overlapping rows discarded)
       const int mchunk1 = (a.dk - 128) / 64;
       bool ok = true;
@@ -286,18 +305,42 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         tc_fence_after();
         bool dq_started = false;
+        // dQ^T of a dS pass pair is issued after the next pair's S^T / dP'^T,
+        // so those run while the rows form this pair's dS
+        int pend_slot = -1, pend_db = 0;
+        auto issue_dq = [&]() -> bool {
+          if (!mbar_wait(&bars->ds_full[pend_db], (uint32_t)((jd >> 1) & 1), abort_flag, a.st, 815)) return false;
+          tc_fence_after();
+          const uint32_t kvs = k_a + pend_slot * kslot_bytes;
+          for (int m = 0; m < nm; ++m) {
+            const int mc = m == 0 ? 0 : mchunk1;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              // A = K^T (dk-major rows of keys), B = dS^T (head rows, keys along K)
+              const uint64_t ad = sdesc_sw128(kvs + mc * kChunk + k * 2048, kChunk, 1024);
+              const uint64_t bd = sdesc_sw128(ds_a + pend_db * 2 * kQB + (k >> 2) * kQB + (k & 3) * 32, 16, 1024);
+              umma_bf16(tmem_dq + qq * 32 + m * 16, ad, bd, idesc_dq, (dq_started || k > 0) ? 1u : 0u);
+            }
+          }
+          dq_started = true;
+          umma_commit(&bars->ds_free[pend_db]);
+          umma_commit(&bars->k_empty[pend_slot]);
+          ++jd;
+          pend_slot = -1;
+          return true;
+        };
         for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
           const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
-          for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int pass = (br == kBrSlc && a.slc_lse != nullptr) ? 1 : 0; pass < 2 && ok; ++pass) {
             for (int p = 0; p < bk.np; ++p) {
-              const int slot = jp & 1, sb = jp & 3;
-              if (!mbar_wait(&bars->kv_full[slot], (uint32_t)((jp >> 1) & 1), abort_flag, a.st, 813) ||
+              const int slot = jp % kDqRingK, sb = jp & 3;
+              if (!mbar_wait(&bars->k_full[slot], (uint32_t)((jp / kDqRingK) & 1), abort_flag, a.st, 813) ||
                   !mbar_wait(&bars->s_free[sb], (uint32_t)(((jp >> 2) & 1) ^ 1), abort_flag, a.st, 814)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t kvs = kv_a + slot * slot_bytes;
+              const uint32_t kvs = k_a + slot * kslot_bytes;
               for (int c = 0; c < kcs; ++c) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -306,41 +349,36 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                   umma_bf16(tmem_sd + sb * 32, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
                 }
               }
+              if (!mbar_wait(&bars->v_full, (uint32_t)(jp & 1), abort_flag, a.st, 816)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
               for (int c = 0; c < vcs; ++c) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const uint64_t ad = sdesc_sw128(kvs + (kcs + c) * kChunk + k * 32, 16, 1024);
+                  const uint64_t ad = sdesc_sw128(v_a + c * kChunk + k * 32, 16, 1024);
                   const uint64_t bd = sdesc_sw128(q_a + (qb * cs + kcs + c) * kQB + k * 32, 16, 1024);
                   umma_bf16(tmem_sd + sb * 32 + 16, ad, bd, idesc_s, (c > 0 || k > 0) ? 1u : 0u);
                 }
               }
+              umma_commit(&bars->v_empty);
               umma_commit(&bars->s_full[sb]);
-              if (pass == 1) {
-                const int db = jd & 1;
-                if (!mbar_wait(&bars->ds_full[db], (uint32_t)((jd >> 1) & 1), abort_flag, a.st, 815)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                for (int m = 0; m < nm; ++m) {
-                  const int mc = m == 0 ? 0 : mchunk1;
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) {
-                    // A = K^T (dk-major rows of keys), B = dS^T (head rows, keys along K)
-                    const uint64_t ad = sdesc_sw128(kvs + mc * kChunk + k * 2048, kChunk, 1024);
-                    const uint64_t bd = sdesc_sw128(ds_a + db * 2 * kQB + (k >> 2) * kQB + (k & 3) * 32, 16, 1024);
-                    umma_bf16(tmem_dq + qq * 32 + m * 16, ad, bd, idesc_dq, (dq_started || k > 0) ? 1u : 0u);
-                  }
-                }
-                dq_started = true;
-                umma_commit(&bars->ds_free[db]);
-                ++jd;
+              if (pend_slot >= 0 && !issue_dq()) {
+                ok = false;
+                break;
               }
-              umma_commit(&bars->kv_empty[slot]);
+              if (pass == 1) {
+                pend_slot = slot;
+                pend_db = jd & 1;
+              } else {
+                umma_commit(&bars->k_empty[slot]);
+              }
               ++jp;
             }
           }
         }
+        if (ok && pend_slot >= 0 && !issue_dq()) ok = false;
         if (!ok) break;
         umma_commit(&bars->q_empty[qb]);
         umma_commit(&bars->dq_full[qq]);
@@ -380,8 +418,33 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int h = 0; h < NP; ++h) gs[h] = h < a.hpg ? __bfloat162float(a.gates[(rowbase + h) * 3 + br]) : 0.f;
         float lse2[NP], dg[NP];
+        if (br == kBrSlc && a.slc_lse != nullptr) {
+          // ---- the forward's statistics: lse as saved, dg = dout . O_slc
+          // (thread r takes value dim r of every head; sums over the 128 lanes)
+          float v[NP];
+#pragma unroll
+          for (int h = 0; h < NP; ++h) {
+            const size_t e = (rowbase + h) * a.dv + r;
+            v[h] = (h < a.hpg && r < a.dv) ? __bfloat162float(a.dout[e]) * a.slc_o[e] : 0.f;
+            lse2[h] = h < a.hpg ? a.slc_lse[rowbase + h] : INFINITY;
+          }
+          const float vw = warp_sum16(v, lane);
+          if ((lane & 1) == 0) red_a[warp * NP + head_of_lane(lane)] = vw;
+          wg_sync();
+          if (!ok) break;
+#pragma unroll
+          for (int h = 0; h < NP; ++h) dg[h] = red_a[h] + red_a[NP + h] + red_a[2 * NP + h] + red_a[3 * NP + h];
+          if (r < a.hpg) {
+            const float dv = red_a[r] + red_a[NP + r] + red_a[2 * NP + r] + red_a[3 * NP + r];
+            const size_t row = rowbase + r;
+            a.dgates[row * 3 + br] = dv;
+            a.lse[(size_t)br * a.T * a.H * gridDim.z + row] = a.slc_lse[row];
+            a.dgw[(size_t)br * a.T * a.H * gridDim.z + row] = dv;
+          }
+          wg_sync();   // the reduction array is reused by the next item
+          if (!ok) break;
+        } else {
         // ---- pass 0: per-thread online max / sum / sum of p * dP' over this lane's keys
-        {
           float m[NP], l[NP], s1[NP];
 #pragma unroll
           for (int h = 0; h < NP; ++h) {
@@ -1299,14 +1362,15 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int ci = 0; ci < nch; ++ci, ++jc) {
-          const int qb = jc & 1;
+        // S^T / dP'^T of chunk j into the (single) score buffer once the rows
+        // have read chunk j-1's scores, so they run while the rows compute
+        // chunk j-1's gP / dS; then dV / dK of chunk j-1
+        auto issue_s = [&](int j) -> bool {
+          const int qb = j & 1;
           const uint32_t qd = q_a + qb * cs * kQChunk;
-          if (!mbar_wait(&bars->q_full[qb], (uint32_t)((jc >> 1) & 1), abort_flag, a.st, 843) ||
-              !mbar_wait(&bars->s_free, (uint32_t)((jc & 1) ^ 1), abort_flag, a.st, 844)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&bars->q_full[qb], (uint32_t)((j >> 1) & 1), abort_flag, a.st, 843) ||
+              !mbar_wait(&bars->s_free, (uint32_t)((j & 1) ^ 1), abort_flag, a.st, 844))
+            return false;
           tc_fence_after();
           for (int c = 0; c < kcs; ++c) {
 #pragma unroll
@@ -1325,6 +1389,19 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             }
           }
           umma_commit(&bars->s_full);
+          return true;
+        };
+        if (nch > 0 && !issue_s(jc)) {
+          ok = false;
+          break;
+        }
+        for (int ci = 0; ci < nch; ++ci, ++jc) {
+          const int qb = jc & 1;
+          const uint32_t qd = q_a + qb * cs * kQChunk;
+          if (ci + 1 < nch && !issue_s(jc + 1)) {
+            ok = false;
+            break;
+          }
           if (!mbar_wait(&bars->p_full, (uint32_t)(jc & 1), abort_flag, a.st, 845)) {
             ok = false;
             break;
@@ -1620,7 +1697,7 @@ DqLayout dq_layout(int dk, int dv) {
   const int cs = dk / 64 + dv / 64;
   DqLayout L;
   L.off_kv = (uint32_t)align_up((size_t)2 * cs * kQB, 1024);
-  L.off_ds = L.off_kv + 2 * cs * kChunk;
+  L.off_ds = L.off_kv + (kDqRingK * (dk / 64) + dv / 64) * kChunk;
   L.off_red = L.off_ds + 2 * 2 * kQB;
   L.off_bar = (uint32_t)align_up(L.off_red + 3 * 4 * NP * sizeof(float), 256);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(DqBars), 256) + 1024;
@@ -1781,6 +1858,9 @@ int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const Bw
     a.br_lo = kBrSlc;
     a.br_hi = kBrSlc;
     a.acc_dq = 1;
+    a.slc_lse = p.slc_lse;
+    a.slc_o = p.slc_o;
+    a.dout = static_cast<const __nv_bfloat16*>(p.dout);
     a.T = c.T;
     a.H = c.H;
     a.G = c.G;

@@ -54,10 +54,12 @@ size_t sel_smem_bytes(const nsa_cfg& c);
 int launch_cmp_win(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* kc, const void* vc,
                    const void* gates, void* part, int32_t* idx, DeviceStatus* st, cudaStream_t s,
                    bool dense = false, const QueryRows& rows = QueryRows());
-// selected attention; out = part + g_slc*O_slc
+// selected attention; out = part + g_slc*O_slc.  slc_lse / slc_o (both or
+// neither, token-major prefill only): also write the branch's log2-domain
+// log-sum-exp [B,T,H] and O_slc [B,T,H,dv] (fp32) for the backward pass.
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
                const void* part, void* out, DeviceStatus* st, cudaStream_t s,
-               const QueryRows& rows = QueryRows());
+               const QueryRows& rows = QueryRows(), float* slc_lse = nullptr, float* slc_o = nullptr);
 
 // ---- decode (decode.cu)
 int decode_supported(const nsa_cfg& c);
@@ -86,6 +88,7 @@ int launch_dsa(const dsa_cfg& c, const void* qI, const void* wI, const void* kI,
 struct BwdPtrs {
   const void *q, *k, *v, *gates, *kc, *vc, *dout;
   const int32_t* idx;
+  const float *slc_lse, *slc_o;   // nullable: the forward's saved selected-branch statistics
   float *dq, *dk, *dv, *dgates, *dw_k, *dw_v, *dpe_k, *dpe_v;
 };
 // byte offsets of the backward's scratch inside the workspace; [zero_begin,

@@ -51,6 +51,8 @@ struct SelArgs {
   const __nv_bfloat16* gates;      // [B,T,H,3]
   const float* part;               // [B,R,H,dv] fp32
   __nv_bfloat16* out;              // [B,T,H,dv]
+  float* slc_lse;                  // kSave: [B,R,H] log2-domain log-sum-exp of s*scale
+  float* slc_o;                    // kSave: [B,R,H,dv] O_slc (fp32, before the gate)
   DeviceStatus* st;
   uint32_t off_kring, off_vring, off_pt, off_red, off_bar;
 };
@@ -100,8 +102,10 @@ __device__ __forceinline__ void load_blocks(const int32_t* blk, int n, int (&bk)
 
 // kMulti: query rows at positions qoff + row against head-major caches (a
 // multi-token decode); otherwise one row per position of token-major inputs
-// (the prefill), with those values known at compile time.
-template <bool kMulti>
+// (the prefill), with those values known at compile time.  kSave: also write
+// the branch's log-sum-exp and its output O_slc, which the backward pass
+// reads instead of recomputing them.
+template <bool kMulti, bool kSave>
 __global__ void __launch_bounds__(kThreads, 1)
     sel_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const SelArgs a) {
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++wg_phase;
     };
     float coef[NP];   // g_slc / sum of the item whose epilogue is pending
+    float linv[NP];   // kSave: 1 / sum of that item
 
     // softmax of item i: P^T (unnormalised) into this warpgroup's buffer and
     // coef[h] = g_slc[h] / sum[h]
@@ -449,10 +454,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < NP; ++h) {
         const float l = red_l[h] + red_l[NP + h] + red_l[2 * NP + h] + red_l[3 * NP + h];
         coef[h] = (l > 0.f) ? __fdividef(gsl[h], l) : 0.f;
+        if constexpr (kSave) linv[h] = (l > 0.f) ? __fdividef(1.f, l) : 0.f;
+      }
+      if constexpr (kSave) {
+        // thread r < hpg: head r's log-sum-exp, m * sc2 + log2(l) in the
+        // exp2 domain the kernel uses (the max and the sums as above)
+        // (the maxima come from this thread's registers: the red_m rows may
+        // already hold a later item's maxima)
+        if (lw == 0 && lane < a.hpg) {
+          const int hh = lane;
+          float mm = 0.f;
+#pragma unroll
+          for (int h = 0; h < NP; ++h)
+            if (h == hh) mm = mx[h];
+          const float l = red_l[hh] + red_l[NP + hh] + red_l[2 * NP + hh] + red_l[3 * NP + hh];
+          a.slc_lse[((size_t)b * R + row) * a.H + g * a.hpg + hh] = l > 0.f ? mm + __log2f(l) : INFINITY;
+        }
       }
     };
 
-    auto epilogue = [&](int i, const float (&cf)[NP]) {
+    auto epilogue = [&](int i, const float (&cf)[NP], const float (&li)[NP]) {
       if (!ok) return;
       const int ob = i & 3;
       const int d = r;
@@ -476,25 +497,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (d < a.dv) {
 #pragma unroll
         for (int h = 0; h < NP; ++h) {
-          if (h < a.hpg)
+          if (h < a.hpg) {
             a.out[(rowbase + h) * a.dv + d] = __float2bfloat16_rn(fmaf(cf[h], __uint_as_float(rr[h]), prt[h]));
+            if constexpr (kSave) a.slc_o[(rowbase + h) * a.dv + d] = li[h] * __uint_as_float(rr[h]);
+          }
         }
       }
     };
 
     // items wg, wg+2, ...: softmax(next) overlaps the PV of the current item,
     // whose epilogue follows
-    float cprev[NP];
+    float cprev[NP], lprev[NP];
     if (wg < nitems) {
       softmax(wg);
 #pragma unroll
-      for (int h = 0; h < NP; ++h) cprev[h] = coef[h];
+      for (int h = 0; h < NP; ++h) {
+        cprev[h] = coef[h];
+        if constexpr (kSave) lprev[h] = linv[h];
+      }
     }
     for (int i = wg; i < nitems; i += 2) {
       if (i + 2 < nitems) softmax(i + 2);
-      epilogue(i, cprev);
+      epilogue(i, cprev, lprev);
 #pragma unroll
-      for (int h = 0; h < NP; ++h) cprev[h] = coef[h];
+      for (int h = 0; h < NP; ++h) {
+        cprev[h] = coef[h];
+        if constexpr (kSave) lprev[h] = linv[h];
+      }
     }
   }
   tc_fence_before();
@@ -524,7 +553,8 @@ Layout layout_for(int dk, int n) {
 size_t sel_smem_bytes(const nsa_cfg& c) { return layout_for(c.dk, c.n).total; }
 
 int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, const void* gates, const int32_t* idx,
-               const void* part, void* out, DeviceStatus* st, cudaStream_t s, const QueryRows& rows) {
+               const void* part, void* out, DeviceStatus* st, cudaStream_t s, const QueryRows& rows, float* slc_lse,
+               float* slc_o) {
   const int R = rows.R > 0 ? rows.R : c.T;
   const int hpg = c.H / c.G;
   if (hpg > NP || c.n > 16 || (c.dv != 64 && c.dv != 128)) return NSA_ERR_UNSUPPORTED;
@@ -559,6 +589,8 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.gates = static_cast<const __nv_bfloat16*>(gates);
   a.part = static_cast<const float*>(part);
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.slc_lse = slc_lse;
+  a.slc_o = slc_o;
   a.st = st;
   a.off_kring = L.off_kring;
   a.off_vring = L.off_vring;
@@ -566,15 +598,23 @@ int launch_sel(const nsa_cfg& c, const void* q, const void* k, const void* v, co
   a.off_red = L.off_red;
   a.off_bar = L.off_bar;
   dim3 grid((R + a.QPC - 1) / a.QPC, c.G, c.B);
+  const bool save = slc_lse != nullptr && slc_o != nullptr;
   if (rows.head_major) {
-    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<true>), smem_max())) return rc;
+    if (save) return NSA_ERR_UNSUPPORTED;
+    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<true, false>), smem_max())) return rc;
     prof::begin("sel_multi", s);
-    sel_kernel<true><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+    sel_kernel<true, false><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
   } else {
     if (rows.R > 0 && rows.R != c.T) return NSA_ERR_UNSUPPORTED;   // token-major rows are positions
-    if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<false>), smem_max())) return rc;
-    prof::begin("sel", s);
-    sel_kernel<false><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+    if (save) {
+      if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<false, true>), smem_max())) return rc;
+      prof::begin("sel_save", s);
+      sel_kernel<false, true><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+    } else {
+      if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&sel_kernel<false, false>), smem_max())) return rc;
+      prof::begin("sel", s);
+      sel_kernel<false, false><<<grid, kThreads, L.total, s>>>(mq, mk, mv, a);
+    }
   }
   prof::end(s);
   return cudaPeekAtLastError() == cudaSuccess ? NSA_OK : NSA_ERR_CUDA;

@@ -305,8 +305,8 @@ def test_prefill_backward_argument_checks(nsa):
     f = nsa.lib.nsa_prefill_bwd
 
     def call(cfg=c, **kw):
-        names = ["q", "k", "v", "gates", "kc", "vc", "idx", "dout", "dq", "dk", "dv", "dgates", "dw_k", "dw_v",
-                 "dpe_k", "dpe_v"]
+        names = ["q", "k", "v", "gates", "kc", "vc", "idx", "slc_lse", "slc_o", "dout", "dq", "dk", "dv", "dgates",
+                 "dw_k", "dw_v", "dpe_k", "dpe_v"]
         a = {n: FAKE for n in names}
         a.update(ws=FAKE, ws_bytes=need)
         a.update(kw)
@@ -315,6 +315,8 @@ def test_prefill_backward_argument_checks(nsa):
     assert call(idx=None) == 1
     assert call(dpe_v=None) == 1
     assert call(dout=FAKE + 2) == 3
+    assert call(slc_o=None) == 1                         # the saved statistics come as a pair
+    assert call(slc_lse=FAKE + 4) == 3
     assert call(ws=FAKE + 16) == 3                      # workspace must be 256-byte aligned
     assert call(ws_bytes=need - 1) == 4
     wide = nsa.make_cfg(1, 4096, 64, 2, 192, 128)       # 32 heads per group
@@ -327,5 +329,25 @@ def test_prefill_backward_argument_checks(nsa):
     c.w_v = None
     assert call() == 1
     c.w_v = FAKE
+    if not torch.cuda.is_available():
+        assert call() == 7
+
+
+def test_prefill_fwd_train_argument_checks(nsa):
+    c = nsa.make_cfg(1, 4096, 64, 4, 192, 128)
+    c.pe_k = c.pe_v = c.w_k = c.w_v = FAKE
+    need = nsa.nsa_prefill_workspace_size(c)
+    f = nsa.lib.nsa_prefill_fwd_train
+
+    def call(**kw):
+        names = ["q", "k", "v", "gates", "kc", "vc", "out", "idx", "slc_lse", "slc_o"]
+        a = {n: FAKE for n in names}
+        a.update(ws=FAKE, ws_bytes=need)
+        a.update(kw)
+        return f(ctypes.byref(c), *[a[n] for n in names], a["ws"], a["ws_bytes"], None)
+    assert call(idx=None) == 1                           # the kept blocks are required here
+    assert call(slc_lse=None) == 1
+    assert call(slc_o=FAKE + 8) == 3
+    assert call(ws_bytes=need - 1) == 4
     if not torch.cuda.is_available():
         assert call() == 7

@@ -50,7 +50,9 @@ def oracle_cache(inp):
     return out
 
 
-def run_fwd_bwd(inp, dout, params=NSAParams(), caches=None):
+def run_fwd_bwd(inp, dout, params=NSAParams(), caches=None, saved=False):
+    """saved: the forward saves the selected branch's statistics
+    (nsa_prefill_fwd_train) and the backward reads them."""
     nsa = _nsa()
     d = {k: t.cuda() for k, t in inp.items()}
     B, T, H, dk = inp["q"].shape
@@ -68,22 +70,28 @@ def run_fwd_bwd(inp, dout, params=NSAParams(), caches=None):
     out = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device="cuda")
     idx = torch.full((B, T, G, params.n), -7, dtype=torch.int32, device="cuda")
     ws = nsa.workspace(nsa.nsa_prefill_workspace_size(cfg))
-    nsa.nsa_prefill_fwd(cfg, d["q"], d["k"], d["v"], d["gates"], kc, vc, out, idx, ws)
     f32 = dict(device="cuda", dtype=torch.float32)
+    lse = o = None
+    if saved:
+        lse = torch.full((B, T, H), float("nan"), **f32)
+        o = torch.full((B, T, H, dv), float("nan"), **f32)
+        nsa.nsa_prefill_fwd_train(cfg, d["q"], d["k"], d["v"], d["gates"], kc, vc, out, idx, lse, o, ws)
+    else:
+        nsa.nsa_prefill_fwd(cfg, d["q"], d["k"], d["v"], d["gates"], kc, vc, out, idx, ws)
     g = dict(dq=torch.full((B, T, H, dk), float("nan"), **f32), dk=torch.full((B, T, G, dk), float("nan"), **f32),
              dv=torch.full((B, T, G, dv), float("nan"), **f32), dgates=torch.full((B, T, H, 3), float("nan"), **f32),
              dw_k=torch.full((32 * dk, dk), float("nan"), **f32), dw_v=torch.full((32 * dv, dv), float("nan"), **f32),
              dpe_k=torch.full((32, dk), float("nan"), **f32), dpe_v=torch.full((32, dv), float("nan"), **f32))
     wsb = nsa.workspace(nsa.nsa_prefill_bwd_workspace_size(cfg))
     nsa.nsa_prefill_bwd(cfg, d["q"], d["k"], d["v"], d["gates"], kc, vc, idx, dout.cuda(), g["dq"], g["dk"],
-                        g["dv"], g["dgates"], g["dw_k"], g["dw_v"], g["dpe_k"], g["dpe_v"], wsb)
+                        g["dv"], g["dgates"], g["dw_k"], g["dw_v"], g["dpe_k"], g["dpe_v"], wsb, slc_lse=lse, slc_o=o)
     torch.cuda.synchronize()
     assert nsa.nsa_device_status(ws) == 0
     assert nsa.nsa_device_status(wsb) == 0
     return {k: v.cpu().numpy().astype(np.float64) for k, v in g.items()}, idx.cpu().numpy()
 
 
-def compare(name, got, ref, label, scale=None):
+def compare(name, got, ref, label, scale=None, lim=None):
     """``scale``: the magnitude to measure errors against when the reference
     itself cancels to (near) zero."""
     assert np.isfinite(got).all(), f"{label} {name}: non-finite values"
@@ -94,15 +102,27 @@ def compare(name, got, ref, label, scale=None):
     rel_max = float(err.max()) / mx if mx > 0 else float(err.max())
     rel_mean = float(err.mean()) / mn if mn > 0 else float(err.mean())
     print(f"{label} {name}: max|ref|={mx:.3e} rel_max={rel_max:.2e} rel_mean={rel_mean:.2e}")
-    lim = REL_MAX_GATES if name == "dgates" else REL_MAX
+    if lim is None:
+        lim = REL_MAX_GATES if name == "dgates" else REL_MAX
     assert rel_max <= lim, f"{label} {name}: rel max error {rel_max:.3e} > {lim}"
     assert rel_mean <= REL_MEAN, f"{label} {name}: rel mean error {rel_mean:.3e} > {REL_MEAN}"
 
 
-def check_case(wl, label, T=None):
+def check_dgates(got, ref, label, saved):
+    """With the forward's saved statistics the selected branch's dgates is
+    dout . O_slc, where O_slc was formed with the forward's bf16 P (a 2^-9
+    relative rounding of each term): that column is held to 2^-9."""
+    if saved:
+        compare("dgates[cmp,win]", got[..., [0, 2]], ref[..., [0, 2]], label, lim=REL_MAX_GATES)
+        compare("dgates[slc]", got[..., 1], ref[..., 1], label, lim=2.0 ** -9)
+    else:
+        compare("dgates", got, ref, label)
+
+
+def check_case(wl, label, T=None, saved=False):
     inp = make_prefill(wl, T=T)
     dout = make_prefill_dout(wl, T=T)
-    got, gidx = run_fwd_bwd(inp, dout, wl.params)
+    got, gidx = run_fwd_bwd(inp, dout, wl.params, saved=saved)
     B = inp["q"].shape[0]
     acc = {k: np.zeros_like(got[k]) for k in ("dw_k", "dw_v", "dpe_k", "dpe_v")}
     # dPE_K = (sum_i dKc_i) W_r^T cancels to zero (softmax is invariant to a
@@ -114,8 +134,9 @@ def check_case(wl, label, T=None):
     for b in range(B):
         ref = BW.nsa_prefill_backward(inp, O.to_f64(dout[b]), b=b, params=wl.params)
         assert np.array_equal(gidx[b], ref["idx"]), f"{label} b={b}: kept blocks differ from the oracle's"
-        for name in ("dq", "dk", "dv", "dgates"):
+        for name in ("dq", "dk", "dv"):
             compare(name, got[name][b], ref[name], f"{label} b={b}")
+        check_dgates(got["dgates"][b], ref["dgates"], f"{label} b={b}", saved)
         for k in acc:
             acc[k] += ref[k]
         if ref["dkc"].shape[1]:
@@ -128,6 +149,16 @@ def check_case(wl, label, T=None):
 def test_backward_bench_group_shapes():
     wl = PrefillWorkload("bwd_T1000_H16_G1_dk192_dv128", 1, 1000, 16, 1, 192, 128, 21)
     check_case(wl, "bwd T=1000 dk192")
+
+
+def test_backward_with_saved_forward_statistics():
+    wl = PrefillWorkload("bwd_T1000_H16_G1_dk192_dv128", 1, 1000, 16, 1, 192, 128, 21)
+    check_case(wl, "bwd saved T=1000 dk192", saved=True)
+
+
+def test_backward_saved_statistics_batch_few_heads():
+    wl = PrefillWorkload("bwd_B2_T700_H8_G2", 2, 700, 8, 2, 128, 128, 23, NSAParams(n=4, w=96))
+    check_case(wl, "bwd saved B=2 hpg=4", saved=True)
 
 
 def test_backward_two_groups_dk128_dv64():
@@ -151,16 +182,17 @@ def test_backward_short_sequences(T):
 
 
 def test_backward_full_size_sampled_rows():
-    """The 64k benchmark shape (B=1, H=64, G=4, dk=192, dv=128): dq and dgates
-    of 24 sampled rows per group against the oracle's per-row backward (the
-    rows' own kept blocks from the oracle forward); dk, dv and the parameter
-    gradients must be finite."""
+    """The 64k benchmark shape (B=1, H=64, G=4, dk=192, dv=128), run as the
+    benchmark runs it (the forward saves the selected branch's statistics):
+    dq and dgates of 24 sampled rows per group against the oracle's per-row
+    backward (the rows' own kept blocks from the oracle forward); dk, dv and
+    the parameter gradients must be finite."""
     from workloads import PREFILL_CONFIGS
     wl = PREFILL_CONFIGS["prefill_64k"]
     inp = make_prefill(wl)
     dout = make_prefill_dout(wl)
     kc64, vc64 = oracle_cache(inp)
-    got, gidx = run_fwd_bwd(inp, dout, wl.params, caches=(kc64, vc64))
+    got, gidx = run_fwd_bwd(inp, dout, wl.params, caches=(kc64, vc64), saved=True)
     for k in ("dk", "dv", "dw_k", "dw_v", "dpe_k", "dpe_v"):
         assert np.isfinite(got[k]).all(), k
     x = BW._inputs_f64(inp, 0)
@@ -180,4 +212,4 @@ def test_backward_full_size_sampled_rows():
         r = BW.nsa_group_bwd(x["q"][rows][:, hs], rows, K, V, Kc, Vc, x["gates"][rows][:, hs], fw["idx"],
                              wl.params, scale, dout64[rows][:, hs])
         compare("dq", got["dq"][0, rows][:, hs], r["dq"], f"64k g={g}")
-        compare("dgates", got["dgates"][0, rows][:, hs], r["dgates"], f"64k g={g}")
+        check_dgates(got["dgates"][0, rows][:, hs], r["dgates"], f"64k g={g}", True)
