@@ -121,13 +121,13 @@ struct DqBars {
   uint64_t s_full[4], s_free[4];
   uint64_t ds_full[2], ds_free[2];
   uint64_t dq_full[2], dq_free[2];
-  uint64_t wg;
+  uint64_t wg[2];
   uint64_t drain;
   uint32_t tmem;
   int abort_flag;
 };
 
-constexpr int kDqThreads = 192;   // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kDqThreads = 320;   // warps 0-7 softmax (two warpgroups), 8 producer, 9 MMA
 
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapDO,
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   uint8_t* kring = smem + a.off_kv;             // kDqRingK slots x kcs K chunks x 16 KB
   uint8_t* vbuf = kring + kDqRingK * kslot_bytes;   // vcs V chunks x 16 KB
   uint8_t* dsbuf = smem + a.off_ds;             // 2 x dS^T (2 chunks x 2 KB)
-  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [4 warps][3][NP]
+  float* red = reinterpret_cast<float*>(smem + a.off_red);   // [2 warpgroups][3][4 warps][NP / 2]
   DqBars* bars = reinterpret_cast<DqBars*>(smem + a.off_bar);
   volatile int* abort_flag = &bars->abort_flag;
 
@@ -156,14 +156,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
-      mbar_init(&bars->ds_full[i], 4);
+      mbar_init(&bars->ds_full[i], 8);
       mbar_init(&bars->ds_free[i], 1);
       mbar_init(&bars->dq_full[i], 1);
-      mbar_init(&bars->dq_free[i], 4);
+      mbar_init(&bars->dq_free[i], 8);
+      mbar_init(&bars->wg[i], 4);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 4);
+      mbar_init(&bars->s_free[i], 8);
     }
     for (int i = 0; i < kDqRingK; ++i) {
       mbar_init(&bars->k_full[i], 1);
@@ -171,7 +172,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mbar_init(&bars->v_full, 1);
     mbar_init(&bars->v_empty, 1);
-    mbar_init(&bars->wg, 4);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const uint32_t tmem_dq = tmem + 128;    // 2 x (nm x 16) columns
 
   if (*abort_flag) {
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ===================================================================== producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (nv > 0) mbar_wait_plain(&bars->v_full, (uint32_t)((nv - 1) & 1), kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ===================================================================== MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, NP, false, false);
@@ -390,18 +390,46 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
   } else {
     // ===================================================================== softmax + epilogue
-    const int r = warp * 32 + lane;           // TMEM lane: key row of a tile / dk row of dQ^T
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* red_m = red;                       // [4][NP]
-    float* red_l = red + 4 * NP;              // [4][NP]
-    float* red_a = red + 8 * NP;              // [4][NP]
+    // two warpgroups on the same 128 lanes, warpgroup wg taking heads
+    // 8 wg .. 8 wg + 7 of every tile (the heads' statistics are independent)
+    constexpr int HW = NP / 2;
+    const int wg = warp >> 2, lw = warp & 3;
+    const int h0 = wg * HW;
+    const int r = lw * 32 + lane;             // TMEM lane: key row of a tile / dk row of dQ^T
+    const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
+    float* red_m = red + wg * 3 * 4 * HW;     // [4][HW]
+    float* red_l = red_m + 4 * HW;            // [4][HW]
+    float* red_a = red_l + 4 * HW;            // [4][HW]
     bool ok = true;
     uint32_t wg_phase = 0;
     auto wg_sync = [&]() {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->wg);
-      if (!mbar_wait(&bars->wg, wg_phase & 1, abort_flag, a.st, 821)) ok = false;
+      if (lane == 0) mbar_arrive(&bars->wg[wg]);
+      if (!mbar_wait(&bars->wg[wg], wg_phase & 1, abort_flag, a.st, 821)) ok = false;
       ++wg_phase;
+    };
+    auto warp_sum = [](float x) {
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      return x;
+    };
+    // this warpgroup's 8 columns of S^T and dP'^T in score buffer sb
+    auto load_sd = [&](int sb, uint32_t (&sr)[HW], uint32_t (&dr)[HW]) {
+      const uint32_t base = tmem_sd + lane_base + sb * 32 + h0;
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                   : "=r"(sr[0]), "=r"(sr[1]), "=r"(sr[2]), "=r"(sr[3]), "=r"(sr[4]), "=r"(sr[5]), "=r"(sr[6]),
+                     "=r"(sr[7])
+                   : "r"(base));
+      asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                   : "=r"(dr[0]), "=r"(dr[1]), "=r"(dr[2]), "=r"(dr[3]), "=r"(dr[4]), "=r"(dr[5]), "=r"(dr[6]),
+                     "=r"(dr[7])
+                   : "r"(base + 16));
+      asm volatile("tcgen05.wait::ld.sync.aligned;"
+                   : "+r"(sr[0]), "+r"(sr[1]), "+r"(sr[2]), "+r"(sr[3]), "+r"(sr[4]), "+r"(sr[5]), "+r"(sr[6]),
+                     "+r"(sr[7]), "+r"(dr[0]), "+r"(dr[1]), "+r"(dr[2]), "+r"(dr[3]), "+r"(dr[4]), "+r"(dr[5]),
+                     "+r"(dr[6]), "+r"(dr[7])
+                   :
+                   : "memory");
     };
     const int mchunk1 = (a.dk - 128) / 64;
     int jp = 0, jd = 0;
@@ -414,43 +442,53 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       bool any = false;
       for (int br = a.br_lo; br <= a.br_hi && ok; ++br) {
         const BranchKeys bk = branch_keys(br, t, a.Nc, a.n, a.w);
-        float gs[NP];
+        float gs[HW];
 #pragma unroll
-        for (int h = 0; h < NP; ++h) gs[h] = h < a.hpg ? __bfloat162float(a.gates[(rowbase + h) * 3 + br]) : 0.f;
-        float lse2[NP], dg[NP];
-        if (br == kBrSlc && a.slc_lse != nullptr) {
-          // ---- the forward's statistics: lse as saved, dg = dout . O_slc
-          // (thread r takes value dim r of every head; sums over the 128 lanes)
-          float v[NP];
-#pragma unroll
-          for (int h = 0; h < NP; ++h) {
-            const size_t e = (rowbase + h) * a.dv + r;
-            v[h] = (h < a.hpg && r < a.dv) ? __bfloat162float(a.dout[e]) * a.slc_o[e] : 0.f;
-            lse2[h] = h < a.hpg ? a.slc_lse[rowbase + h] : INFINITY;
-          }
-          const float vw = warp_sum16(v, lane);
-          if ((lane & 1) == 0) red_a[warp * NP + head_of_lane(lane)] = vw;
-          wg_sync();
-          if (!ok) break;
-#pragma unroll
-          for (int h = 0; h < NP; ++h) dg[h] = red_a[h] + red_a[NP + h] + red_a[2 * NP + h] + red_a[3 * NP + h];
-          if (r < a.hpg) {
-            const float dv = red_a[r] + red_a[NP + r] + red_a[2 * NP + r] + red_a[3 * NP + r];
-            const size_t row = rowbase + r;
+        for (int hh = 0; hh < HW; ++hh)
+          gs[hh] = h0 + hh < a.hpg ? __bfloat162float(a.gates[(rowbase + h0 + hh) * 3 + br]) : 0.f;
+        float lse2[HW], dg[HW];
+        // head h0 + lane (lane < HW) writes its row's statistics
+        auto write_row = [&](float lv, float dv) {
+          if (lw == 0 && lane < HW && h0 + lane < a.hpg) {
+            const size_t row = rowbase + h0 + lane;
             a.dgates[row * 3 + br] = dv;
-            a.lse[(size_t)br * a.T * a.H * gridDim.z + row] = a.slc_lse[row];
+            a.lse[(size_t)br * a.T * a.H * gridDim.z + row] = lv;
             a.dgw[(size_t)br * a.T * a.H * gridDim.z + row] = dv;
           }
+        };
+        if (br == kBrSlc && a.slc_lse != nullptr) {
+          // ---- the forward's statistics: lse as saved, dg = dout . O_slc
+          // (thread r takes value dim r of each head; sums over the 128 lanes)
+#pragma unroll
+          for (int hh = 0; hh < HW; ++hh) {
+            const size_t e = (rowbase + h0 + hh) * a.dv + r;
+            const float v = (h0 + hh < a.hpg && r < a.dv) ? __bfloat162float(a.dout[e]) * a.slc_o[e] : 0.f;
+            const float vw = warp_sum(v);
+            if (lane == 0) red_a[lw * HW + hh] = vw;
+            lse2[hh] = h0 + hh < a.hpg ? a.slc_lse[rowbase + h0 + hh] : INFINITY;
+          }
+          wg_sync();
+          if (!ok) break;
+          float mine_l = 0.f, mine_d = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < HW; ++hh) {
+            dg[hh] = red_a[hh] + red_a[HW + hh] + red_a[2 * HW + hh] + red_a[3 * HW + hh];
+            if (hh == lane) {
+              mine_l = lse2[hh];
+              mine_d = dg[hh];
+            }
+          }
+          write_row(mine_l, mine_d);
           wg_sync();   // the reduction array is reused by the next item
           if (!ok) break;
         } else {
-        // ---- pass 0: per-thread online max / sum / sum of p * dP' over this lane's keys
-          float m[NP], l[NP], s1[NP];
+          // ---- pass 0: per-thread online max / sum / sum of p * dP' over this lane's keys
+          float m[HW], l[HW], s1[HW];
 #pragma unroll
-          for (int h = 0; h < NP; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-            s1[h] = 0.f;
+          for (int hh = 0; hh < HW; ++hh) {
+            m[hh] = -INFINITY;
+            l[hh] = 0.f;
+            s1[hh] = 0.f;
           }
           for (int p = 0; p < bk.np; ++p) {
             const int sb = jp & 3;
@@ -459,11 +497,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
               break;
             }
             tc_fence_after();
-            uint32_t sr[16], dr[16];
-            tmem_ld16(tmem_sd + lane_base + sb * 32, sr);
-            tmem_ld16(tmem_sd + lane_base + sb * 32 + 16, dr);
-            tmem_ld_wait(sr);
-            tmem_reg_fence(dr);
+            uint32_t sr[HW], dr[HW];
+            load_sd(sb, sr, dr);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->s_free[sb]);
@@ -482,18 +517,18 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             if (valid) {
 #pragma unroll
-              for (int h = 0; h < NP; ++h) {
-                const float s = __uint_as_float(sr[h]) * a.sc2;
-                const float dp = __uint_as_float(dr[h]);
-                if (s > m[h]) {
-                  const float f = fast_exp2(m[h] - s);   // 0 when m = -inf
-                  l[h] = fmaf(l[h], f, 1.f);
-                  s1[h] = fmaf(s1[h], f, dp);
-                  m[h] = s;
+              for (int hh = 0; hh < HW; ++hh) {
+                const float sv = __uint_as_float(sr[hh]) * a.sc2;
+                const float dp = __uint_as_float(dr[hh]);
+                if (sv > m[hh]) {
+                  const float f = fast_exp2(m[hh] - sv);   // 0 when m = -inf
+                  l[hh] = fmaf(l[hh], f, 1.f);
+                  s1[hh] = fmaf(s1[hh], f, dp);
+                  m[hh] = sv;
                 } else {
-                  const float e = fast_exp2(s - m[h]);
-                  l[h] += e;
-                  s1[h] = fmaf(e, dp, s1[h]);
+                  const float e = fast_exp2(sv - m[hh]);
+                  l[hh] += e;
+                  s1[hh] = fmaf(e, dp, s1[hh]);
                 }
               }
             }
@@ -501,63 +536,43 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!ok) break;
           // merge across the 128 key lanes: per warp, then across the 4 warps
 #pragma unroll
-          for (int h = 0; h < NP; ++h) {
-            const float mw = warp_max_f32(m[h]);
-            const float f = (m[h] == -INFINITY) ? 0.f : fast_exp2(m[h] - mw);
-            m[h] = mw;
-            l[h] *= f;
-            s1[h] *= f;
-          }
-          const float lw = warp_sum16(l, lane);
-          const float aw = warp_sum16(s1, lane);
-          if (lane == 0)
-#pragma unroll
-            for (int h = 0; h < NP; ++h) red_m[warp * NP + h] = m[h];
-          if ((lane & 1) == 0) {
-            red_l[warp * NP + head_of_lane(lane)] = lw;
-            red_a[warp * NP + head_of_lane(lane)] = aw;
+          for (int hh = 0; hh < HW; ++hh) {
+            const float mw = warp_max_f32(m[hh]);
+            const float f = (m[hh] == -INFINITY) ? 0.f : fast_exp2(m[hh] - mw);
+            const float lw_ = warp_sum(l[hh] * f);
+            const float aw_ = warp_sum(s1[hh] * f);
+            if (lane == 0) {
+              red_m[lw * HW + hh] = mw;
+              red_l[lw * HW + hh] = lw_;
+              red_a[lw * HW + hh] = aw_;
+            }
           }
           wg_sync();
           if (!ok) break;
+          float mine_l = 0.f, mine_d = 0.f;
 #pragma unroll
-          for (int h = 0; h < NP; ++h) {
+          for (int hh = 0; hh < HW; ++hh) {
             float M = -INFINITY;
 #pragma unroll
-            for (int x = 0; x < 4; ++x) M = fmaxf(M, red_m[x * NP + h]);
+            for (int x = 0; x < 4; ++x) M = fmaxf(M, red_m[x * HW + hh]);
             float L = 0.f, A = 0.f;
             if (M != -INFINITY) {
 #pragma unroll
               for (int x = 0; x < 4; ++x) {
-                const float mx = red_m[x * NP + h];
+                const float mx = red_m[x * HW + hh];
                 const float f = (mx == -INFINITY) ? 0.f : fast_exp2(mx - M);
-                L = fmaf(red_l[x * NP + h], f, L);
-                A = fmaf(red_a[x * NP + h], f, A);
+                L = fmaf(red_l[x * HW + hh], f, L);
+                A = fmaf(red_a[x * HW + hh], f, A);
               }
             }
-            lse2[h] = L > 0.f ? M + __log2f(L) : INFINITY;
-            dg[h] = L > 0.f ? __fdividef(A, L) : 0.f;
+            lse2[hh] = L > 0.f ? M + __log2f(L) : INFINITY;
+            dg[hh] = L > 0.f ? __fdividef(A, L) : 0.f;
+            if (hh == lane) {
+              mine_l = lse2[hh];
+              mine_d = dg[hh];
+            }
           }
-          // rows of this (t, group): thread h < hpg writes head h
-          if (r < a.hpg) {
-            float M = -INFINITY;
-            for (int x = 0; x < 4; ++x) M = fmaxf(M, red_m[x * NP + r]);
-            float L = 0.f, A = 0.f;
-            if (M != -INFINITY)
-              for (int x = 0; x < 4; ++x) {
-                const float mx = red_m[x * NP + r];
-                const float f = (mx == -INFINITY) ? 0.f : fast_exp2(mx - M);
-                L = fmaf(red_l[x * NP + r], f, L);
-                A = fmaf(red_a[x * NP + r], f, A);
-              }
-            // the same operations as the per-head values above, so the rows
-            // written here equal the ones this kernel's pass 1 uses
-            const float lv = L > 0.f ? M + __log2f(L) : INFINITY;
-            const float dv = L > 0.f ? __fdividef(A, L) : 0.f;
-            const size_t row = rowbase + r;
-            a.dgates[row * 3 + br] = dv;
-            a.lse[(size_t)br * a.T * a.H * gridDim.z + row] = lv;
-            a.dgw[(size_t)br * a.T * a.H * gridDim.z + row] = dv;
-          }
+          write_row(mine_l, mine_d);
           wg_sync();   // the reduction arrays are reused by the next branch
           if (!ok) break;
         }
@@ -570,11 +585,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t sr[16], dr[16];
-          tmem_ld16(tmem_sd + lane_base + sb * 32, sr);
-          tmem_ld16(tmem_sd + lane_base + sb * 32 + 16, dr);
-          tmem_ld_wait(sr);
-          tmem_reg_fence(dr);
+          uint32_t sr[HW], dr[HW];
+          load_sd(sb, sr, dr);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->s_free[sb]);
@@ -598,13 +610,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const int kk = r & 63;
           uint8_t* chunk = dsbuf + db * 2 * kQB + (r >> 6) * kQB + (kk & 7) * 2;
 #pragma unroll
-          for (int h = 0; h < NP; ++h) {
+          for (int hh = 0; hh < HW; ++hh) {
             float ds = 0.f;
             if (valid) {
-              const float pr = fast_exp2(fmaf(__uint_as_float(sr[h]), a.sc2, -lse2[h]));
-              ds = gs[h] * a.scale * pr * (__uint_as_float(dr[h]) - dg[h]);
+              const float pr = fast_exp2(fmaf(__uint_as_float(sr[hh]), a.sc2, -lse2[hh]));
+              ds = gs[hh] * a.scale * pr * (__uint_as_float(dr[hh]) - dg[hh]);
             }
-            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h, kk >> 3)) = __float2bfloat16_rn(ds);
+            *reinterpret_cast<__nv_bfloat16*>(chunk + sw128_offset(h0 + hh, kk >> 3)) = __float2bfloat16_rn(ds);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -614,24 +626,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- epilogue: dq rows of this item (fp32)
+      // ---- epilogue: dq rows of this item (fp32), this warpgroup's heads
       if (!mbar_wait(&bars->dq_full[qq], (uint32_t)((i >> 1) & 1), abort_flag, a.st, 825)) {
         ok = false;
         break;
       }
       tc_fence_after();
       for (int m = 0; m < nm; ++m) {
-        uint32_t rr[16];
-        tmem_ld16(tmem_dq + lane_base + qq * 32 + m * 16, rr);
-        tmem_ld_wait(rr);
+        uint32_t rr[HW];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(rr[0]), "=r"(rr[1]), "=r"(rr[2]), "=r"(rr[3]), "=r"(rr[4]), "=r"(rr[5]), "=r"(rr[6]),
+                       "=r"(rr[7])
+                     : "r"(tmem_dq + lane_base + qq * 32 + m * 16 + h0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;"
+                     : "+r"(rr[0]), "+r"(rr[1]), "+r"(rr[2]), "+r"(rr[3]), "+r"(rr[4]), "+r"(rr[5]), "+r"(rr[6]),
+                       "+r"(rr[7])
+                     :
+                     : "memory");
         const int drow = (m == 0 ? 0 : mchunk1 * 64) + r;
         const bool own = drow < a.dk && (m == 0 || drow >= 128);
         if (own) {
 #pragma unroll
-          for (int h = 0; h < NP; ++h)
-            if (h < a.hpg) {
-              float* o = a.dq + (rowbase + h) * a.dk + drow;
-              const float v = any ? __uint_as_float(rr[h]) : 0.f;
+          for (int hh = 0; hh < HW; ++hh)
+            if (h0 + hh < a.hpg) {
+              float* o = a.dq + (rowbase + h0 + hh) * a.dk + drow;
+              const float v = any ? __uint_as_float(rr[hh]) : 0.f;
               *o = a.acc_dq ? *o + v : v;
             }
         }
@@ -1194,7 +1213,7 @@ struct ColInfo {
   float gs;     // gate of the branch
 };
 
-constexpr int kDkvThreads = 192;   // warps 0-3 softmax / epilogue, 4 producer, 5 MMA
+constexpr int kDkvThreads = 320;   // warps 0-7 softmax / epilogue, 8 producer, 9 MMA
 constexpr int kQChunk = 8192;      // one 64-column chunk of 4 queries x 16 heads
 
 template <int BR>
@@ -1220,14 +1239,14 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->col_full[i], 32);
-      mbar_init(&bars->col_free[i], 4);
+      mbar_init(&bars->col_free[i], 8);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 4);
-    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->s_free, 8);
+    mbar_init(&bars->p_full, 8);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->acc_free, 4);
+    mbar_init(&bars->acc_free, 8);
     mbar_init(&bars->drain, 1);
     bars->abort_flag = prior_error(a.st);
     fence_barrier_init();
@@ -1249,7 +1268,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   const uint32_t tm_dk = tmem + 192, tm_dv = tmem + 192 + a.dk;
 
   if (*abort_flag) {
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ===================================================================== producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
@@ -1344,7 +1363,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         mbar_wait_plain(&bars->q_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
       if (ju > 0) mbar_wait_plain(&bars->kv_full, (uint32_t)((ju - 1) & 1), kWaitLimitNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ===================================================================== MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
@@ -1429,8 +1448,12 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     }
   } else {
     // ===================================================================== softmax + epilogue
-    const int r = warp * 32 + lane;           // TMEM lane = key row of the tile
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // two warpgroups on the same 128 key lanes: warpgroup wg takes score
+    // columns 32 wg .. 32 wg + 31 (queries 2 wg, 2 wg + 1) and, in the
+    // epilogue, half of the dK and dV columns
+    const int wg = warp >> 2, lw = warp & 3;
+    const int r = lw * 32 + lane;             // TMEM lane = key row of the tile
+    const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
     bool ok = true;
     int jc = 0, ju = 0;
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++ju) {
@@ -1451,9 +1474,10 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         }
         tc_fence_after();
         const ColInfo* cc = cols + qb * 64;
-        uint32_t pg[32], dsv[32];
+        uint32_t pg[16], dsv[16];
 #pragma unroll
-        for (int grp = 0; grp < 4; ++grp) {
+        for (int gi = 0; gi < 2; ++gi) {
+          const int grp = 2 * wg + gi;
           uint32_t sr[16], dr[16];
           tmem_ld16(tm_s + lane_base + grp * 16, sr);
           tmem_ld16(tm_dp + lane_base + grp * 16, dr);
@@ -1476,8 +1500,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
               pv[e] = p;
               dv2[e] = d;
             }
-            pg[grp * 8 + h / 2] = pack_bf16x2(pv[0], pv[1]);
-            dsv[grp * 8 + h / 2] = pack_bf16x2(dv2[0], dv2[1]);
+            pg[gi * 8 + h / 2] = pack_bf16x2(pv[0], pv[1]);
+            dsv[gi * 8 + h / 2] = pack_bf16x2(dv2[0], dv2[1]);
           }
         }
         tc_fence_before();
@@ -1491,23 +1515,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           break;
         }
         tc_fence_after();
-        {
-          uint32_t x0[16], x1[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            x0[e] = pg[e];
-            x1[e] = pg[16 + e];
-          }
-          tmem_st16(tm_pg + lane_base, x0);
-          tmem_st16(tm_pg + lane_base + 16, x1);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            x0[e] = dsv[e];
-            x1[e] = dsv[16 + e];
-          }
-          tmem_st16(tm_ds + lane_base, x0);
-          tmem_st16(tm_ds + lane_base + 16, x1);
-        }
+        tmem_st16(tm_pg + lane_base + wg * 16, pg);
+        tmem_st16(tm_ds + lane_base + wg * 16, dsv);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1531,7 +1540,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           dvrow = a.dV + (((size_t)b * a.T + key) * a.G + g) * a.dv;
         }
       }
-      for (int c0 = 0; c0 < a.dk; c0 += 16) {
+      for (int c0 = wg * a.dk / 2; c0 < (wg + 1) * a.dk / 2; c0 += 16) {
         uint32_t rr[16];
         tmem_ld16(tm_dk + lane_base + c0, rr);
         tmem_ld_wait(rr);
@@ -1539,7 +1548,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) atomicAdd(dkrow + c0 + e, __uint_as_float(rr[e]));
       }
-      for (int c0 = 0; c0 < a.dv; c0 += 16) {
+      for (int c0 = wg * a.dv / 2; c0 < (wg + 1) * a.dv / 2; c0 += 16) {
         uint32_t rr[16];
         tmem_ld16(tm_dv + lane_base + c0, rr);
         tmem_ld_wait(rr);
