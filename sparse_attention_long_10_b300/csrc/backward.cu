@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // bwd_dq_kernel.  Writes dq (fp32, overwritten), dgates and the branch rows
 // of lse / dg.
 constexpr int kTileQ = 8;
-constexpr int kTileThreads = 192;     // warps 0-3 rows, 4 producer, 5 MMA
+constexpr int kTileThreads = 320;     // warps 0-7 rows (two warpgroups), 8 producer, 9 MMA
 
 struct TileArgs {
   int T, H, G, dk, dv, w, hpg, Nc;
@@ -690,7 +690,7 @@ struct TileArgs {
   float* lse;                     // [3][B,T,H]
   float* dgw;                     // [3][B,T,H]
   DeviceStatus* st;
-  uint32_t off_do, off_k, off_v, off_bar;
+  uint32_t off_do, off_k, off_v, off_x, off_bar;
 };
 
 struct TileBars {
@@ -700,6 +700,7 @@ struct TileBars {
   uint64_t s_full, s_free;
   uint64_t ds_full, ds_free;
   uint64_t dq_full;
+  uint64_t xbar[2];
   uint64_t drain;
   uint32_t tmem;
   int abort_flag;
@@ -751,8 +752,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     mbar_init(&bars->v_full, 1);
     mbar_init(&bars->v_empty, 1);
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 4);
-    mbar_init(&bars->ds_full, 4);
+    mbar_init(&bars->s_free, 8);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->xbar[0], 8);
+    mbar_init(&bars->xbar[1], 8);
     mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->drain, 1);
@@ -774,7 +777,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const uint32_t tm_s = tmem, tm_dp = tmem + 128, tm_ds = tmem + 256, tm_dq = tmem + 320;
 
   if (*abort_flag) {
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ===================================================================== producer
     if (lane == 0) {
       tma_prefetch_desc(&mapQ);
@@ -837,7 +840,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         if (jv > 0) mbar_wait_plain(&bars->v_full, (uint32_t)((jv - 1) & 1), kWaitLimitNs);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ===================================================================== MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
@@ -913,16 +916,22 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     }
   } else {
     // ===================================================================== rows
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // two warpgroups on the same 128 rows: warpgroup wg takes key columns
+    // 64 wg .. 64 wg + 63 of every tile; a row's statistics are the merge of
+    // the two halves (exchanged through shared memory, one buffer per branch)
+    const int wg = warp >> 2, lw = warp & 3;
+    const int r = lw * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(lw * 32) << 16;
     const int t = t0 + (r >> 4), h = r & 15;
     const bool row_ok = t < a.T && h < a.hpg;
     const size_t row = ((size_t)b * a.T + (row_ok ? t : 0)) * a.H + g * a.hpg + (row_ok ? h : 0);
     const size_t plane = (size_t)gridDim.z * a.T * a.H;
+    float* xchg = reinterpret_cast<float*>(smem + a.off_x);   // [2 branches][2 warpgroups][3][128]
     bool ok = true;
     int jt = 0, jd = 0;
     bool any = false;
     for (int br = kBrCmp; br <= kBrWin && ok; br += kBrWin - kBrCmp) {
+      const int bi = br == kBrCmp ? 0 : 1;
       const TileKeys tk = tile_keys(br, t0, t_last, a.Nc, a.w);
       const float gs = row_ok ? __bfloat162float(a.gates[row * 3 + br]) : 0.f;
       // visible keys of this row, as positions inside the branch's key range
@@ -948,7 +957,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             break;
           }
           const int kb = 128 * kt;
-          for (int grp = 0; grp < 8; ++grp) {
+          for (int gi = 0; gi < 4; ++gi) {
+            const int grp = 4 * wg + gi;
             uint32_t sr[16], dr[16];
             tmem_ld16(tm_s + lane_base + grp * 16, sr);
             tmem_ld16(tm_dp + lane_base + grp * 16, dr);
@@ -1018,9 +1028,30 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         if (!ok) break;
         if (pass == 0) {
-          lse2 = l > 0.f ? m + __log2f(l) : INFINITY;
-          dg = l > 0.f ? __fdividef(s1, l) : 0.f;
-          if (row_ok) {
+          // merge the two warpgroups' halves of the row, in a fixed order
+          float* xb = xchg + bi * 2 * 3 * 128;
+          xb[(wg * 3 + 0) * 128 + r] = m;
+          xb[(wg * 3 + 1) * 128 + r] = l;
+          xb[(wg * 3 + 2) * 128 + r] = s1;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->xbar[bi]);
+          if (!mbar_wait(&bars->xbar[bi], 0, abort_flag, a.st, 884)) {
+            ok = false;
+            break;
+          }
+          const float m0 = xb[0 * 128 + r], l0 = xb[1 * 128 + r], a0 = xb[2 * 128 + r];
+          const float m1 = xb[3 * 128 + r], l1 = xb[4 * 128 + r], a1 = xb[5 * 128 + r];
+          const float mm = fmaxf(m0, m1);
+          float L = 0.f, A = 0.f;
+          if (mm != -INFINITY) {
+            const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm);
+            const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
+            L = fmaf(l0, f0, l1 * f1);
+            A = fmaf(a0, f0, a1 * f1);
+          }
+          lse2 = L > 0.f ? mm + __log2f(L) : INFINITY;
+          dg = L > 0.f ? __fdividef(A, L) : 0.f;
+          if (row_ok && wg == 0) {
             a.dgates[row * 3 + br] = dg;
             a.lse[(size_t)br * plane + row] = lse2;
             a.dgw[(size_t)br * plane + row] = dg;
@@ -1028,10 +1059,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
       }
     }
-    // ---- epilogue: this row's dq (cmp + win), fp32
+    // ---- epilogue: this row's dq (cmp + win), fp32; warpgroup wg writes half the columns
     if (ok && mbar_wait(&bars->dq_full, 0, abort_flag, a.st, 883)) {
       tc_fence_after();
-      for (int c0 = 0; c0 < a.dk; c0 += 16) {
+      for (int c0 = wg * a.dk / 2; c0 < (wg + 1) * a.dk / 2; c0 += 16) {
         uint32_t rr[16];
         tmem_ld16(tm_dq + lane_base + c0, rr);
         tmem_ld_wait(rr);
@@ -1194,10 +1225,12 @@ struct DkvArgs {
   uint32_t off_q, off_col, off_bar;
 };
 
+constexpr int kDkvQBuf = 3;        // query-chunk buffers in flight
+
 struct DkvBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
-  uint64_t col_full[2], col_free[2];
+  uint64_t q_full[kDkvQBuf], q_empty[kDkvQBuf];
+  uint64_t col_full[kDkvQBuf], col_free[kDkvQBuf];
   uint64_t s_full, s_free;
   uint64_t p_full, p_free;
   uint64_t acc_full, acc_free;
@@ -1225,8 +1258,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   const int kcs = a.dk / 64, vcs = a.dv / 64, cs = kcs + vcs;
   uint8_t* kv = smem;                                   // kcs K + vcs V chunks x 16 KB
-  uint8_t* qb_base = smem + a.off_q;                    // 2 x (kcs Q + vcs dout) chunks x 8 KB
-  ColInfo* cols = reinterpret_cast<ColInfo*>(smem + a.off_col);   // [2][64]
+  uint8_t* qb_base = smem + a.off_q;                    // kDkvQBuf x (kcs Q + vcs dout) chunks x 8 KB
+  ColInfo* cols = reinterpret_cast<ColInfo*>(smem + a.off_col);   // [kDkvQBuf][64]
   DkvBars* bars = reinterpret_cast<DkvBars*>(smem + a.off_bar);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = warp_id(), lane = lane_id();
@@ -1235,7 +1268,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     mbar_init(&bars->kv_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDkvQBuf; ++i) {
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->col_full[i], 32);
@@ -1304,8 +1337,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       for (int ci = 0; ci < nch && ok; ++ci, ++jc) {
-        const int qb = jc & 1;
-        const uint32_t par = (uint32_t)(((jc >> 1) & 1) ^ 1);
+        const int qb = jc % kDkvQBuf;
+        const uint32_t par = (uint32_t)(((jc / kDkvQBuf) & 1) ^ 1);
         if (lane == 0) {
           if (!mbar_wait(&bars->q_empty[qb], par, abort_flag, a.st, 832) ||
               !mbar_wait(&bars->col_free[qb], par, abort_flag, a.st, 833))
@@ -1359,8 +1392,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       }
     }
     if (lane == 0 && (!ok || *abort_flag)) {
-      for (int x = (jc > 2 ? jc - 2 : 0); x < jc; ++x)
-        mbar_wait_plain(&bars->q_full[x & 1], (uint32_t)((x >> 1) & 1), kWaitLimitNs);
+      for (int x = (jc > kDkvQBuf ? jc - kDkvQBuf : 0); x < jc; ++x)
+        mbar_wait_plain(&bars->q_full[x % kDkvQBuf], (uint32_t)((x / kDkvQBuf) & 1), kWaitLimitNs);
       if (ju > 0) mbar_wait_plain(&bars->kv_full, (uint32_t)((ju - 1) & 1), kWaitLimitNs);
     }
   } else if (warp == 9) {
@@ -1385,9 +1418,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         // have read chunk j-1's scores, so they run while the rows compute
         // chunk j-1's gP / dS; then dV / dK of chunk j-1
         auto issue_s = [&](int j) -> bool {
-          const int qb = j & 1;
+          const int qb = j % kDkvQBuf;
           const uint32_t qd = q_a + qb * cs * kQChunk;
-          if (!mbar_wait(&bars->q_full[qb], (uint32_t)((j >> 1) & 1), abort_flag, a.st, 843) ||
+          if (!mbar_wait(&bars->q_full[qb], (uint32_t)((j / kDkvQBuf) & 1), abort_flag, a.st, 843) ||
               !mbar_wait(&bars->s_free, (uint32_t)((j & 1) ^ 1), abort_flag, a.st, 844))
             return false;
           tc_fence_after();
@@ -1415,7 +1448,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           break;
         }
         for (int ci = 0; ci < nch; ++ci, ++jc) {
-          const int qb = jc & 1;
+          const int qb = jc % kDkvQBuf;
           const uint32_t qd = q_a + qb * cs * kQChunk;
           if (ci + 1 < nch && !issue_s(jc + 1)) {
             ok = false;
@@ -1465,8 +1498,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       const bool key_ok = BR == kBrCmp ? key < a.Nc : (BR == kBrSlc ? (r < 64 && key < a.T) : key < a.T);
       const int vis_from = BR == kBrCmp ? 16 * key + 31 : key;   // first query that sees the key
       for (int ci = 0; ci < nch; ++ci, ++jc) {
-        const int qb = jc & 1;
-        const uint32_t par = (uint32_t)((jc >> 1) & 1);
+        const int qb = jc % kDkvQBuf;
+        const uint32_t par = (uint32_t)((jc / kDkvQBuf) & 1);
         if (!mbar_wait(&bars->col_full[qb], par, abort_flag, a.st, 851) ||
             !mbar_wait(&bars->s_full, (uint32_t)(jc & 1), abort_flag, a.st, 852)) {
           ok = false;
@@ -1714,14 +1747,15 @@ DqLayout dq_layout(int dk, int dv) {
 }
 
 struct TileLayout {
-  uint32_t off_do, off_k, off_v, off_bar, total;
+  uint32_t off_do, off_k, off_v, off_x, off_bar, total;
 };
 TileLayout tile_layout(int dk, int dv) {
   TileLayout L;
   L.off_do = (uint32_t)(dk / 64 * kChunk);
   L.off_k = L.off_do + (uint32_t)(dv / 64 * kChunk);
   L.off_v = L.off_k + (uint32_t)(2 * (dk / 64) * kChunk);
-  L.off_bar = L.off_v + (uint32_t)(dv / 64 * kChunk);
+  L.off_x = L.off_v + (uint32_t)(dv / 64 * kChunk);
+  L.off_bar = L.off_x + (uint32_t)(2 * 2 * 3 * 128 * sizeof(float));
   L.total = L.off_bar + (uint32_t)align_up(sizeof(TileBars), 256) + 1024;
   return L;
 }
@@ -1733,8 +1767,8 @@ DkvLayout dkv_layout(int dk, int dv) {
   const int cs = dk / 64 + dv / 64;
   DkvLayout L;
   L.off_q = (uint32_t)(cs * kChunk);
-  L.off_col = L.off_q + 2 * cs * kQChunk;
-  L.off_bar = (uint32_t)align_up(L.off_col + 2 * 64 * sizeof(ColInfo), 256);
+  L.off_col = L.off_q + kDkvQBuf * cs * kQChunk;
+  L.off_bar = (uint32_t)align_up(L.off_col + kDkvQBuf * 64 * sizeof(ColInfo), 256);
   L.total = L.off_bar + (uint32_t)align_up(sizeof(DkvBars), 256) + 1024;
   return L;
 }
@@ -1853,6 +1887,7 @@ int launch_prefill_bwd(const nsa_cfg& c, const BwdPtrs& p, uint8_t* ws, const Bw
     a.off_do = L.off_do;
     a.off_k = L.off_k;
     a.off_v = L.off_v;
+    a.off_x = L.off_x;
     a.off_bar = L.off_bar;
     if (int rc = ensure_smem_attr(reinterpret_cast<const void*>(&bwd_dq_tile_kernel), L.total)) return rc;
     dim3 grid((c.T + kTileQ - 1) / kTileQ, c.G, c.B);
