@@ -1169,8 +1169,35 @@ __global__ void __launch_bounds__(1024) build_units_kernel(const UnitArgs a) {
     carry += tot;
   }
   __syncthreads();
-  for (int br = 0; br < 3; ++br) {
-    const int per = br == kBrCmp ? a.ntc : (br == kBrWin ? a.ntw : a.nblk);
+  // compressed branch: every compressed tile is seen by most queries, so its
+  // units are listed query range first (ranges of kRowsPerUnit on a fixed
+  // grid, then every tile that range sees): the CTAs running at one time
+  // share their query rows through L2 instead of each reading them from HBM
+  {
+    const int nqr = (a.T + kRowsPerUnit - 1) / kRowsPerUnit;
+    const int nl = a.B * a.G * nqr;
+    int ucarry = 0;
+    for (int base = 0; base < nl; base += blockDim.x) {
+      const int l = base + threadIdx.x;
+      const int qlo = (l % nqr) * kRowsPerUnit;
+      const int qhi = min(a.T, qlo + kRowsPerUnit);
+      int nu = 0;
+      if (l < nl)
+        for (int tile = 0; tile < a.ntc; ++tile) nu += 16 * 128 * tile + 31 < qhi ? 1 : 0;
+      int tot;
+      const int pre = cta_exclusive_scan(nu, sh, &tot);
+      for (int tile = 0; tile < nu; ++tile) {
+        const int u = ucarry + pre + tile;
+        if (u < a.cap[kBrCmp])
+          a.units[kBrCmp][u] = make_int4(l / nqr, 128 * tile, max(qlo, 16 * 128 * tile + 31), qhi);
+      }
+      ucarry += tot;
+    }
+    if (threadIdx.x == 0) a.nunits[kBrCmp] = min(ucarry, a.cap[kBrCmp]);
+    __syncthreads();
+  }
+  for (int br = kBrSlc; br <= kBrWin; ++br) {
+    const int per = br == kBrWin ? a.ntw : a.nblk;
     const int nl = a.B * a.G * per;
     int ucarry = 0;
     for (int base = 0; base < nl; base += blockDim.x) {
@@ -1178,11 +1205,7 @@ __global__ void __launch_bounds__(1024) build_units_kernel(const UnitArgs a) {
       int key0 = 0, lo = 0, hi = 0;
       if (l < nl) {
         const int tile = l % per;
-        if (br == kBrCmp) {
-          key0 = 128 * tile;
-          lo = min(a.T, 16 * key0 + 31);
-          hi = a.T;
-        } else if (br == kBrWin) {
+        if (br == kBrWin) {
           key0 = 128 * tile;
           lo = key0;
           hi = min(a.T, key0 + 127 + a.w);
@@ -1803,9 +1826,8 @@ BwdWs bwd_ws(const nsa_cfg& c, size_t header) {
   const size_t rows = (size_t)c.B * c.T * c.H;
   const size_t lists = (size_t)c.B * c.G * nblk;
   const int ntc = (Nc + 127) / 128, ntw = (c.T + 127) / 128;
-  const size_t per_list = (size_t)(c.T + kRowsPerUnit - 1) / kRowsPerUnit + 1;
   BwdWs w;
-  w.cap[kBrCmp] = (size_t)c.B * c.G * ntc * per_list;
+  w.cap[kBrCmp] = (size_t)c.B * c.G * ntc * ((c.T + kRowsPerUnit - 1) / kRowsPerUnit);
   w.cap[kBrWin] = (size_t)c.B * c.G * ntw * ((127 + c.w + kRowsPerUnit - 1) / kRowsPerUnit + 1);
   w.cap[kBrSlc] = lists + (size_t)c.B * c.T * c.G * c.n / kRowsPerUnit + 1;
   size_t o = header;
