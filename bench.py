@@ -160,8 +160,8 @@ _CSRC = "sparse_attention_long_10_b300/csrc/"
 NCU_TRAFFIC = {
     "cmp_win": {"files": ["prefill_cmp_win.cu", "common.cuh"], "sha": "e959ad480b14df14",
                 "bytes": (1857.92 + 2115.24) * 1e6, "how": "full-size capture (one pass)"},
-    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "2ebb744aa7a991a6",
-            "bytes": (4453.29 + 1072.77) * 1e6, "how": "full-size capture (one pass)"},
+    "sel": {"files": ["prefill_sel.cu", "common.cuh"], "sha": "10bdbff3281aef65",
+            "bytes": (4423.19 + 1073.58) * 1e6, "how": "full-size capture (one pass)"},
     # both kernels of one decode step
     "decode": {"files": ["decode.cu", "common.cuh"], "sha": "e50108f99388e6fe",
                "bytes": (189.29 + 9.81 + 52.01 + 0.01) * 1e6, "how": "full-size capture, both kernels"},
