@@ -168,6 +168,11 @@ NCU_TRAFFIC = {
     # the four kernels of one DSA step
     "dsa": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "32d048ff48605774",
             "bytes": (134.26 + 4.10 + 4.40 + 36.96 + 8.43) * 1e6, "how": "full-size capture, four kernels"},
+    # the nine largest kernels of one backward step (dq x 2, dK/dV x 3, dx x 2, dw x 2)
+    "backward": {"files": ["backward.cu", "common.cuh"], "sha": "2680b909956a1c8b",
+                 "bytes": (2984.45 + 8892.27 + 3190.17 + 39265.95 + 12238.97 + 217.73 + 118.14 + 143.73 + 77.62) * 1e6 +
+                          (3291.44 + 3293.89 + 42.27 + 492.96 + 323.55 + 140.83 + 0.38 + 73.53 + 0.11) * 1e6,
+                 "how": "full-size capture (one pass), the step's nine largest kernels"},
     "dsa_latent": {"files": ["dsa.cu", "common.cuh", "warp_mma.cuh"], "sha": "32d048ff48605774",
                    "bytes": (134.25 + 4.04 + 4.40 + 20.18 + 8.43) * 1e6,
                    "how": "full-size capture, four kernels"},
@@ -827,8 +832,9 @@ def run_backward_leg(args, ws):
         "useful_tflop_per_step": flops / 1e12,
         "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                      "frac": tf / pk["bf16_sus"], "peak_kind": f"bf16 dense sustained ({pk['src']})",
-                     "traffic": None,
-                     "note": "2.5 x the forward's attention FLOPs + 2 x the compression GEMM over the whole call"},
+                     "traffic": ncu_traffic("backward"), "traffic_how": NCU_TRAFFIC["backward"]["how"],
+                     "note": "2.5 x the forward's attention FLOPs + 2 x the compression GEMM over the whole call; "
+                             "traffic is DRAM bytes per step"},
         "kernels": {k: {"launches_per_step": c / steps, "ms_per_step": t / steps} for k, (c, t) in prof.items()},
         # profiled spans: the list building is 3 kernels, the compression backward 8
         "gpu_launches_per_step": int(sum(c * {"bwd_lists": 3, "bwd_compress": 8}.get(k, 1)
