@@ -32,8 +32,9 @@ docstring.  Parity status per function:
   select_blocks ......... pinned (brute-force stable sort; forced blocks)
   sel / win attention ... pinned (n*l' >= T or w >= T reduces to full causal
                           attention by a textbook formula)
-  combined output ....... parity unpinned beyond the branch pins above (the
-                          pages print no worked example)
+  combined output ....... pinned (an independent torch formulation of the
+                          whole forward on the same kept blocks and cache;
+                          out = sum of gate x branch output)
   dsa_decode ............ pinned (k >= T reduces to full softmax attention;
                           brute-force top-k; 131072/2048 = 64)
   dsa_prefill ........... pinned (topk >= t+1 reduces to textbook causal

@@ -82,6 +82,16 @@ def test_backward_matches_finite_differences(case):
 def _torch_forward_loss(xt, dout, idx):
     """The forward written again in torch fp64 (kept blocks fixed, cache
     unrounded), for torch.autograd."""
+    out = _torch_forward_out(xt, idx)
+    return (torch.as_tensor(dout) * out).sum()
+
+
+def _torch_forward_out(xt, idx, round_cache=False):
+    """out [T, H, dv] of the forward written in torch fp64 from the
+    definition: compression as flatten(X + PE) @ W (rounded to bf16 when
+    ``round_cache``), then per query row softmax attention over the visible
+    compressed entries, over the tokens of the kept blocks ``idx`` up to the
+    row, and over the window, mixed by the gates (cmp, slc, win)."""
     q, k, v, gates = xt["q"], xt["k"], xt["v"], xt["gates"]
     T, H, dk = q.shape
     G, hpg = k.shape[1], H // k.shape[1]
@@ -92,11 +102,15 @@ def _torch_forward_loss(xt, dout, idx):
     def att(qs, Kk, Vk):
         return torch.softmax((qs @ Kk.T) * scale, dim=-1) @ Vk
 
-    total = torch.zeros((), dtype=torch.float64)
+    outs = []
     for g in range(G):
         K, V = k[:, g], v[:, g]
         Kc = torch.stack([(K[d * i: d * i + l] + xt["pe_k"]).reshape(-1) for i in range(Nc)]) @ xt["w_k"]
         Vc = torch.stack([(V[d * i: d * i + l] + xt["pe_v"]).reshape(-1) for i in range(Nc)]) @ xt["w_v"]
+        if round_cache:
+            Kc = Kc.to(torch.bfloat16).to(torch.float64)
+            Vc = Vc.to(torch.bfloat16).to(torch.float64)
+        rows = []
         hs = slice(g * hpg, (g + 1) * hpg)
         for t in range(T):
             qs = q[t, hs]
@@ -108,9 +122,9 @@ def _torch_forward_loss(xt, dout, idx):
             lo = max(0, t - w + 1)
             o_w = att(qs, K[lo:t + 1], V[lo:t + 1])
             gt = gates[t, hs]
-            o = gt[:, 0:1] * o_c + gt[:, 1:2] * o_s + gt[:, 2:3] * o_w
-            total = total + (torch.as_tensor(dout[t, hs]) * o).sum()
-    return total
+            rows.append(gt[:, 0:1] * o_c + gt[:, 1:2] * o_s + gt[:, 2:3] * o_w)
+        outs.append(torch.stack(rows))                  # [T, hpg, dv]
+    return torch.cat(outs, dim=1)
 
 
 def test_backward_matches_torch_autograd(case):
@@ -187,3 +201,19 @@ def test_key_shift_invariance_gives_zero_dpe_k(case):
                                     PARAMS.l, PARAMS.d, g["dkc"][gg])
         direct = g["dk"][:, gg] - dKx
         assert np.abs(direct.sum(axis=0)).max() <= 1e-10 * np.abs(direct).sum(axis=0).max()
+
+
+def test_combined_output_matches_an_independent_formulation(case):
+    """The combined forward output (the three branches and the gates) of the
+    forward oracle against the torch formulation above, on the same kept
+    blocks and the same bf16-rounded cache: a dropped branch, a gate taken
+    from the wrong column or a mis-masked branch would differ by O(1)."""
+    inp, _, idx, x = case
+    ref = O.nsa_prefill_reference(inp, params=PARAMS)
+    xt = {kk: torch.tensor(vv, dtype=torch.float64) for kk, vv in x.items()}
+    got = _torch_forward_out(xt, idx, round_cache=True).numpy()
+    np.testing.assert_allclose(ref["out"], got, rtol=1e-10, atol=1e-12)
+    # the per-branch outputs are mixed by the gates in the order (cmp, slc, win)
+    g = x["gates"][..., None]
+    np.testing.assert_allclose(ref["out"], g[:, :, 0] * ref["o_cmp"] + g[:, :, 1] * ref["o_slc"] +
+                               g[:, :, 2] * ref["o_win"], rtol=1e-12, atol=1e-14)

@@ -145,3 +145,19 @@ def test_selection_band_dropping_forced_blocks_is_caught(monkeypatch):
         return gap, definite - {0, jt - 1}, band | {0, jt - 1, 3}, need
     monkeypatch.setattr(O, "selection_alternatives", no_forced)
     _fails(P.test_selection_set_valid_rejects_planted_invalid_rows)
+
+
+def test_dropped_branch_in_the_combined_output_is_caught(monkeypatch):
+    import tests.test_oracle_backward as BWT
+    real = O.win_attention
+    monkeypatch.setattr(O, "win_attention", lambda *a, **kw: 0.0 * real(*a, **kw))
+    _fails(BWT.test_combined_output_matches_an_independent_formulation, BWT.make_case())
+
+
+def test_selected_branch_scored_with_the_window_gate_is_caught(monkeypatch):
+    # the selected branch's output replaced by the window's: what a gate or
+    # branch mix-up in the combine would produce
+    import tests.test_oracle_backward as BWT
+    monkeypatch.setattr(O, "sel_attention", lambda q, t, K, V, idx, lsel, scale:
+                        O.win_attention(q, t, K, V, BWT.PARAMS.w, scale))
+    _fails(BWT.test_combined_output_matches_an_independent_formulation, BWT.make_case())
